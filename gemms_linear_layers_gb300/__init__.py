@@ -1,0 +1,22 @@
+"""tg: training products of linear layers on GB300 (sm_103a).
+
+The compute lives in ``libtg.so`` (hand-written CUDA behind a C ABI, declared
+in ``include/tg.h``).  This package is a thin ctypes binding with the same
+names as the C entry points; it only marshals torch tensors' device pointers,
+shapes and the current CUDA stream.  Importing the package does not load the
+library; the first call does, and fails loudly if it has not been built.
+"""
+from __future__ import annotations
+
+__all__ = [
+    "tg_gemm_fwd", "tg_gemm_dgrad", "tg_gemm_wgrad", "tg_lora_down", "tg_lora_up",
+    "tg_lora_grad", "tg_bmm_attn", "tg_workspace_size", "tg_stream_status",
+    "tg_status_string", "tg_load_table", "tg_version", "lib", "TGError",
+]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import _binding
+        return getattr(_binding, name)
+    raise AttributeError(name)
