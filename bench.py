@@ -1,0 +1,572 @@
+#!/usr/bin/env python
+"""Benchmark: TFLOP/s of the training products of a linear layer on GB300.
+
+One step = every product of the 135M-class decoder layer set at T = 2,048
+tokens (q, k, v, o, gate, up, down, head; forward, input gradient and weight
+gradient each; bf16 and fp16 with FP32 accumulation): 48 products.  Inputs
+are seeded synthetic tensors resident in HBM; L2 is flushed (a 256 MiB write)
+before every step, outside the timed events.  Each product is one captured
+CUDA graph of the library call; CUDA events on the launching stream bracket
+every product, so per-kernel times come from the same timed region.
+
+Printed: one JSON line (rank 0).  `value` is the whole-job TFLOP/s (all ranks'
+flops / the slowest rank's time).  Also measured: the same step end to end
+through the public API with pinned host inputs and outputs copied each step
+(`e2e`), the oracle's throughput on host cores on a bounded sample
+(`cpu_baseline`), the roofline fraction of the dominant kernel, SM clocks
+sampled during the timed region, and (unless --no-rows) one row per distinct
+product of the other product sets (2B-class layers at 1,024-4,096 tokens,
+rank-16 LoRA at 4,096 tokens, batched attention) against its own roofline.
+
+`--impl reference` times the fp64 CPU oracle on the same workload instead
+(bounded samples per step, host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gemms_linear_layers_gb300 import inputs, workloads  # noqa: E402
+
+METRIC = "TFLOPS per training GEMM (fwd/dgrad/wgrad, bf16/fp16) and % of GB300 dense peak"
+WORKLOAD = "135M-class decoder layer set, T=2048, fwd+dgrad+wgrad, bf16 and fp16 (48 products)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [x for x in sm if x > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ products
+class Product:
+    def __init__(self, layer, op, dtype, T, d_in, d_out):
+        self.layer, self.op, self.dtype = layer, op, dtype
+        self.T, self.d_in, self.d_out = T, d_in, d_out
+        if op == "fwd":
+            self.M, self.N, self.K = T, d_out, d_in
+        elif op == "dgrad":
+            self.M, self.N, self.K = T, d_in, d_out
+        else:
+            self.M, self.N, self.K = d_out, d_in, T
+        self.flops = workloads.flops(self.M, self.N, self.K)
+        self.graph = None
+        self.call = ""
+        self.launches = 1
+
+    @property
+    def name(self):
+        return f"{self.layer}.{self.op}.{str(self.dtype)[6:]}"
+
+
+def build_step(device):
+    """Inputs, outputs and workspaces of every product of the step, on the device."""
+    from gemms_linear_layers_gb300 import _binding as tg
+    cfg = workloads.DECODER_135M
+    T = cfg["T"]
+    prods, tensors = [], {}
+    for dtype in cfg["dtypes"]:
+        for layer, d_in, d_out in cfg["layers"]:
+            X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="bench", device=device)
+            tensors[(layer, dtype)] = {
+                "X": X, "W": W, "dY": dY,
+                "Y": torch.empty(T, d_out, dtype=dtype, device=device),
+                "dX": torch.empty(T, d_in, dtype=dtype, device=device),
+                "dW": torch.empty(d_out, d_in, dtype=dtype, device=device)}
+            for op in ("fwd", "dgrad", "wgrad"):
+                p = Product(layer, op, dtype, T, d_in, d_out)
+                opcode = {"fwd": tg.TG_OP_GEMM_FWD, "dgrad": tg.TG_OP_GEMM_DGRAD, "wgrad": tg.TG_OP_GEMM_WGRAD}[op]
+                n = tg.tg_workspace_size(opcode, T, d_out, d_in, 0, dtype, dtype)
+                p.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
+                p.t = tensors[(layer, dtype)]
+                prods.append(p)
+    return prods
+
+
+def run_product(p):
+    from gemms_linear_layers_gb300 import _binding as tg
+    t = p.t
+    if p.op == "fwd":
+        tg.tg_gemm_fwd(t["X"], t["W"], Y=t["Y"], ws=p.ws)
+    elif p.op == "dgrad":
+        tg.tg_gemm_dgrad(t["dY"], t["W"], dX=t["dX"], ws=p.ws)
+    else:
+        tg.tg_gemm_wgrad(t["dY"], t["X"], dW=t["dW"], ws=p.ws)
+
+
+def kernel_key(call: str) -> str:
+    """'tc nt bn=256' style identity of the kernel a call ran (from tg_last_call)."""
+    f = call.split()
+    path = f[1] if len(f) > 1 else "?"
+    if path != "tc":
+        return f"{path} {f[2] if len(f) > 2 else ''}".strip()
+    bn = next((x for x in f if x.startswith("bn=")), "bn=?")
+    sp = next((x for x in f if x.startswith("splits=")), "splits=1")
+    return f"tc {f[2]} {bn}" + (" +reduce" if sp != "splits=1" else "")
+
+
+def capture(prods, stream):
+    from gemms_linear_layers_gb300 import _binding as tg
+    for p in prods:  # warm-up call: sets kernel attributes, records the plan
+        with torch.cuda.stream(stream):
+            run_product(p)
+        p.call = tg.tg_last_call()
+        p.launches = 2 if ("splits=" in p.call and "splits=1 " not in p.call) else 1
+        p.kernel = kernel_key(p.call)
+    torch.cuda.synchronize()
+    for p in prods:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_product(p)
+        p.graph = g
+    torch.cuda.synchronize()
+
+
+def timed_steps(prods, n_warm, n_steps, stream, flush):
+    """Per step: flush L2 (untimed), then every product between events."""
+    per_step = []
+    per_prod = {p.name: 0.0 for p in prods}
+    with torch.cuda.stream(stream):
+        for s in range(n_warm + n_steps):
+            flush.add_(1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(prods) + 1)]
+            ev[0].record(stream)
+            for i, p in enumerate(prods):
+                p.graph.replay()
+                ev[i + 1].record(stream)
+            if s >= n_warm:
+                per_step.append(ev)
+    torch.cuda.synchronize()
+    total_ms = 0.0
+    for ev in per_step:
+        total_ms += ev[0].elapsed_time(ev[-1])
+        for i, p in enumerate(prods):
+            per_prod[p.name] += ev[i].elapsed_time(ev[i + 1])
+    return total_ms, per_prod
+
+
+# ------------------------------------------------------------------ e2e
+def e2e_steps(prods, n_steps, stream):
+    """The step through the public API with pinned host buffers: every step
+    copies its inputs host->device and its outputs device->host."""
+    host_in, host_out = {}, {}
+    h2d = d2h = 0
+    seen = set()
+    for p in prods:
+        key = (p.layer, p.dtype)
+        if key in seen:
+            continue
+        seen.add(key)
+        for n in ("X", "W", "dY"):
+            host_in[(key, n)] = p.t[n].cpu().pin_memory()
+            h2d += p.t[n].numel() * p.t[n].element_size()
+        for n in ("Y", "dX", "dW"):
+            host_out[(key, n)] = torch.empty(p.t[n].shape, dtype=p.t[n].dtype).pin_memory()
+            d2h += p.t[n].numel() * p.t[n].element_size()
+    times = []
+    with torch.cuda.stream(stream):
+        for s in range(n_steps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for (key, n), h in host_in.items():
+                layer, dtype = key
+                next(p for p in prods if (p.layer, p.dtype) == key).t[n].copy_(h, non_blocking=True)
+            for p in prods:
+                run_product(p)
+            for (key, n), h in host_out.items():
+                h.copy_(next(p for p in prods if (p.layer, p.dtype) == key).t[n], non_blocking=True)
+            b.record(stream)
+            if s > 0:
+                times.append((a, b))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in times)
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(target_s):
+    """The fp64 oracle on the host cores over a bounded sample of the step:
+    the first rows of each of the 48 products (same shapes, same input
+    recipe).  Returns (flops, seconds, rows per product)."""
+    import numpy as np
+
+    import oracle
+    cfg = workloads.DECODER_135M
+    T = cfg["T"]
+    if not hasattr(oracle_sample, "jobs"):
+        jobs = []
+        for dtype in cfg["dtypes"]:
+            for layer, d_in, d_out in cfg["layers"]:
+                X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="bench")
+                for op in ("fwd", "dgrad", "wgrad"):
+                    jobs.append((op, X, W, dY))
+        oracle_sample.jobs = jobs
+        oracle_sample.sec_per_row = None
+
+    def run(rows):
+        flops = 0
+        t0 = time.perf_counter()
+        for op, X, W, dY in oracle_sample.jobs:
+            if op == "fwd":
+                M, N, K = X.shape[0], W.shape[0], X.shape[1]
+            elif op == "dgrad":
+                M, N, K = dY.shape[0], W.shape[1], dY.shape[1]
+            else:
+                M, N, K = dY.shape[1], X.shape[1], dY.shape[0]
+            r = min(rows, M)
+            ii = np.repeat(np.arange(r), N)
+            jj = np.tile(np.arange(N), r)
+            bi = np.zeros_like(ii)
+            if op == "fwd":
+                oracle.gemm_fwd(X, W, sample=(bi, ii, jj))
+            elif op == "dgrad":
+                oracle.gemm_dgrad(dY, W, sample=(bi, ii, jj))
+            else:
+                oracle.gemm_wgrad(dY, X, sample=(bi, ii, jj))
+            flops += 2 * r * N * K
+        return flops, time.perf_counter() - t0
+
+    if oracle_sample.sec_per_row is None:
+        f, t = run(1)  # calibration
+        oracle_sample.sec_per_row = t
+    rows = max(1, int(target_s / max(oracle_sample.sec_per_row, 1e-4)))
+    f, t = run(rows)
+    return f, t, rows
+
+
+def cpu_baseline(target_s=12.0):
+    import oracle
+    f, t, rows = oracle_sample(target_s)
+    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"first {rows} output row(s) of each of the 48 products ({f / 2e9:.2f} GMAC), "
+                      f"fp64 naive loops, {t:.1f} s"}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    steps, warm = args.steps, args.warmup
+    t0 = time.perf_counter()
+    # each step: a sample of the workload, sized so the whole run takes ~2 minutes
+    per_step_s = max(0.5, 120.0 / max(1, steps + warm))
+    total_f = total_t = 0.0
+    rows = 0
+    for s in range(warm + steps):
+        f, t, rows = oracle_sample(per_step_s)
+        if s >= warm:
+            total_f += f
+            total_t += t
+    value = total_f / total_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": round(1000 * total_t / steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "host threads"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+                             "kind": "oracle",
+                             "sample": f"each step: first {rows} output row(s) of all 48 products"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t0, 1)}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ rows
+def measure_rows(stream, pk, budget_s=90.0):
+    """One timing row per distinct product of the other product sets, each
+    alone: CUDA graph of R launches, L2-sized buffer rotation for the
+    HBM-bound ones, median of 5 replays."""
+    from gemms_linear_layers_gb300 import _binding as tg
+    rows = []
+    t_start = time.perf_counter()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+
+    def time_calls(make_call, reps=10, sets=1):
+        calls = [make_call(i) for i in range(sets)]
+        for c in calls:
+            c()
+        torch.cuda.synchronize()
+        call = tg.tg_last_call()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                calls[r % sets]()
+        res = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            res.append(a.elapsed_time(b) / reps)
+        return statistics.median(res), call
+
+    # 2B-class layers
+    for T in workloads.DECODER_2B["T"]:
+        for dtype in workloads.DECODER_2B["dtypes"]:
+            for d_in, d_out, names in ((2304, 2304, "q,k,v,o"), (2304, 5760, "gate,up"), (5760, 2304, "down")):
+                X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="rows", device="cuda")
+                outs = {"fwd": torch.empty(T, d_out, dtype=dtype, device="cuda"),
+                        "dgrad": torch.empty(T, d_in, dtype=dtype, device="cuda"),
+                        "wgrad": torch.empty(d_out, d_in, dtype=dtype, device="cuda")}
+                res = {}
+                ws = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
+                for op in ("fwd", "dgrad", "wgrad"):
+                    fn = {"fwd": lambda i: (lambda: tg.tg_gemm_fwd(X, W, Y=outs["fwd"], ws=ws)),
+                          "dgrad": lambda i: (lambda: tg.tg_gemm_dgrad(dY, W, dX=outs["dgrad"], ws=ws)),
+                          "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws))}[op]
+                    ms, call = time_calls(fn)
+                    M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[op]
+                    tf = workloads.flops(M, N, K) / ms / 1e9
+                    res[op] = tf
+                    rows.append({"set": "2B", "layer": names, "T": T, "op": op, "dtype": str(dtype)[6:],
+                                 "M": M, "N": N, "K": K, "us": round(ms * 1000, 2), "tflops": round(tf, 1),
+                                 "frac_of_peak": round(tf / pk["bf16_tflops"], 3), "bound": "tensor",
+                                 "kernel": kernel_key(call)})
+                rows[-1]["wgrad_over_fwd"] = round(res["wgrad"] / res["fwd"], 3)
+                del X, W, dY, outs
+    # rank-16 LoRA, bf16, T=4096: effective HBM bandwidth
+    cfg = workloads.LORA_2B
+    T, r = cfg["T"], cfg["r"]
+    for name, d_in, d_out in cfg["layers"]:
+        if name in ("k", "v", "o", "up"):
+            continue  # same shapes as q / gate
+        dt = torch.bfloat16
+        big = max(d_in, d_out) * T * 2
+        sets = max(1, int(2 * l2 // big) + 1)
+        data = [inputs.lora_inputs(T, d_in, d_out, r, dt, tag=f"rows{i}", device="cuda") for i in range(sets)]
+        Hs = [torch.empty(T, r, dtype=dt, device="cuda") for _ in range(sets)]
+        Ys = [torch.empty(T, d_out, dtype=dt, device="cuda") for _ in range(sets)]
+        grads = [{"dA": torch.empty(r, d_in, dtype=dt, device="cuda"),
+                  "dB": torch.empty(d_out, r, dtype=dt, device="cuda"),
+                  "dX": torch.empty(T, d_in, dtype=dt, device="cuda")} for _ in range(sets)]
+        wsn = tg.tg_workspace_size(tg.TG_OP_LORA_GRAD, T, d_in, d_out, r, dt, dt)
+        wss = [torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda") for _ in range(sets)]
+        specs = [
+            ("down", lambda i: (lambda: tg.tg_lora_down(data[i][0], data[i][1], H=Hs[i])),
+             (T * d_in + r * d_in + T * r) * 2, 2 * T * d_in * r),
+            ("up", lambda i: (lambda: tg.tg_lora_up(data[i][3], data[i][2], Y=Ys[i])),
+             (T * r + d_out * r + T * d_out) * 2, 2 * T * d_out * r),
+            # reads dY, X, H, A, B; writes dX, dA, dB
+            ("grad", lambda i: (lambda: tg.tg_lora_grad(*data[i], outs=grads[i], ws=wss[i])),
+             (T * d_out + 2 * T * d_in + T * r + 2 * r * d_in + 2 * d_out * r) * 2,
+             4 * T * r * (d_in + d_out)),
+        ]
+        for op, fn, nbytes, fl in specs:
+            ms, call = time_calls(fn, reps=max(10, sets * 2), sets=sets)
+            gbs = nbytes / ms / 1e6
+            rows.append({"set": "LoRA", "layer": name, "T": T, "op": op, "dtype": "bf16", "d_in": d_in,
+                         "d_out": d_out, "us": round(ms * 1000, 2), "gbs": round(gbs, 1),
+                         "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3), "bound": "hbm",
+                         "tflops": round(fl / ms / 1e9, 2), "kernel": call.split(" [")[0][:60]})
+        del data, Hs, Ys, grads, wss
+        if time.perf_counter() - t_start > budget_s:
+            break
+    # attention, s = 1024 / 2048 / 4096, bf16
+    acfg = workloads.ATTENTION
+    for s in acfg["s"]:
+        if time.perf_counter() - t_start > budget_s:
+            break
+        h, d = acfg["heads"], acfg["d"]
+        dt = torch.bfloat16
+        t = inputs.attn_inputs(h, s, d, dt, tag="rows", device="cuda")
+        for op in ("qk", "pv", "do_vt", "pt_do", "ds_k", "dst_q"):
+            a, b = inputs.ATTN_OPERANDS[op]
+            ss_out = op in ("qk", "do_vt")
+            C = torch.empty(h, s, s if ss_out else d, dtype=dt, device="cuda")
+            ms, call = time_calls(lambda i: (lambda: tg.tg_bmm_attn(op, t[a], t[b], C=C)), reps=5)
+            nbytes = (t[a].numel() + t[b].numel() + C.numel()) * 2
+            fl = 2 * h * s * s * d
+            gbs = nbytes / ms / 1e6
+            rows.append({"set": "attention", "s": s, "op": op, "dtype": "bf16", "us": round(ms * 1000, 2),
+                         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3),
+                         "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call)})
+            del C
+        del t
+    return rows
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-product rows of the other sets")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    from gemms_linear_layers_gb300 import _binding as tg
+    tg.tg_load_table(None)
+    table = os.path.join(ROOT, "gemms_linear_layers_gb300", "tables", "gb300.txt")
+    if os.path.exists(table) and not os.environ.get("TG_TABLE"):
+        assert tg.tg_load_table(table) == 0
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    prods = build_step("cuda")
+    capture(prods, stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    step_flops = sum(p.flops for p in prods)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total_ms, per_prod = timed_steps(prods, args.warmup, args.steps, stream, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    st = tg.tg_stream_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after the timed region: {tg.tg_status_string(st)}")
+
+    ms_step = total_ms / args.steps
+    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
+
+    # dominant kernel: largest total time, grouped by kernel identity
+    by_kernel = {}
+    for p in prods:
+        k = by_kernel.setdefault(p.kernel, {"ms": 0.0, "flops": 0, "launches": 0, "products": []})
+        k["ms"] += per_prod[p.name]
+        k["flops"] += p.flops * args.steps
+        k["launches"] += args.steps
+        k["products"].append(p.name)
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+    avg_launch_ms = dom["ms"] / dom["launches"]
+    flops_per_launch = dom["flops"] / dom["launches"]
+    achieved = flops_per_launch / (avg_launch_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+                "kernel": dom_name, "products": dom["products"],
+                "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
+                "share_of_step": round(dom["ms"] / total_ms, 3)}
+
+    launches = sum(p.launches for p in prods) * args.steps
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": 2048, "products_per_step": len(prods),
+                       "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
+                       "l2": "flushed before every step (256 MiB write, untimed)",
+                       "timing": "CUDA events around each product's captured graph, summed over the step"},
+            "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary(),
+            "per_kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in by_kernel.items()}}
+
+    if rank == 0:
+        e2e_n = min(args.steps, 5)
+        ms, h2d, d2h = e2e_steps(prods, e2e_n, stream)
+        line["e2e"] = {"value": round(step_flops * e2e_n / (ms / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(ms / e2e_n, 3)}
+        if world == 1 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline()
+        if not args.no_rows:
+            rows = measure_rows(stream, pk)
+            line["rows"] = rows
+            if args.rows_out:
+                with open(args.rows_out, "w") as f:
+                    json.dump(rows, f, indent=1)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,630 @@
+// api.cu -- the C ABI of libtg.so (include/tg.h): argument checks, the
+// per-device context (SM count, status word, wait limit), the shape-keyed
+// tile table and the dispatch of every product onto its kernels.
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cmath>
+#include <fstream>
+#include <mutex>
+#include <shared_mutex>
+#include <sstream>
+#include <string>
+#include <unordered_map>
+
+#include "ptx.cuh"
+#include "tg.h"
+#include "tg_internal.h"
+
+namespace tg {
+
+// ------------------------------------------------------------ status word
+// One word per device (a module global exists once per device context).
+// Kernels OR a code into it when a bounded wait runs out.
+__device__ unsigned int g_status_word;
+
+__global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: this wait can only end by timing out
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, timeout_ns, &abort_flag, status, 0x7e);
+  __syncthreads();
+}
+
+cudaError_t wait_probe_launch(unsigned long long timeout_ns, unsigned int* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(timeout_ns, status);
+  return cudaGetLastError();
+}
+
+struct DevCtx {
+  bool ready = false;
+  tg_status init_status = TG_OK;
+  int sms = 0;
+  unsigned int* status = nullptr;
+  unsigned long long timeout_ns = 2000000000ull;
+};
+
+static std::mutex g_ctx_mu;
+static DevCtx g_ctx[128];
+
+static tg_status device_ctx(DevCtx** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return TG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_ctx_mu);
+  DevCtx& c = g_ctx[dev];
+  if (!c.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return TG_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      c.init_status = TG_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return TG_ERR_CUDA;
+      c.status = static_cast<unsigned int*>(p);
+      if (const char* e = getenv("TG_WAIT_TIMEOUT_MS")) {
+        long v = strtol(e, nullptr, 10);
+        if (v > 0 && v < 600000) c.timeout_ns = static_cast<unsigned long long>(v) * 1000000ull;
+      }
+    }
+    c.ready = true;
+  }
+  *out = &c;
+  return c.init_status;
+}
+
+// ------------------------------------------------------------- call record
+static thread_local std::string t_last_call;
+static int log_enabled() {
+  static int v = [] {
+    const char* e = getenv("TG_LOG");
+    return (e && *e && strcmp(e, "0") != 0) ? 1 : 0;
+  }();
+  return v;
+}
+static void record(const std::string& s) {
+  t_last_call = s;
+  if (log_enabled()) fprintf(stderr, "[tg] %s\n", s.c_str());
+}
+
+// -------------------------------------------------------------- tile table
+struct TableKey {
+  int layout, in, out;
+  int64_t M, N, K, batch;
+  bool operator==(const TableKey& o) const {
+    return layout == o.layout && in == o.in && out == o.out && M == o.M && N == o.N && K == o.K &&
+           batch == o.batch;
+  }
+};
+struct TableKeyHash {
+  size_t operator()(const TableKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    const int64_t v[7] = {k.layout, k.in, k.out, k.M, k.N, k.K, k.batch};
+    for (int64_t x : v) h = (h ^ static_cast<uint64_t>(x)) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+struct TableVal {
+  int bn, splits;
+};
+static std::shared_mutex g_table_mu;
+static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
+static std::once_flag g_table_env_once;
+
+static const char* layout_name(int l) { return l == LAYOUT_NT ? "nt" : (l == LAYOUT_NN ? "nn" : "tn"); }
+static int parse_layout(const std::string& s) {
+  if (s == "nt" || s == "fwd") return LAYOUT_NT;
+  if (s == "nn" || s == "dgrad") return LAYOUT_NN;
+  if (s == "tn" || s == "wgrad") return LAYOUT_TN;
+  return -1;
+}
+static int parse_dtype(const std::string& s) {
+  if (s == "bf16") return TG_BF16;
+  if (s == "f16" || s == "fp16") return TG_F16;
+  if (s == "f32" || s == "fp32") return TG_F32;
+  return -1;
+}
+
+static tg_status load_table_file(const char* path) {
+  std::unordered_map<TableKey, TableVal, TableKeyHash> t;
+  if (path && *path) {
+    std::ifstream f(path);
+    if (!f) return TG_ERR_TABLE;
+    std::string line;
+    while (std::getline(f, line)) {
+      const size_t h = line.find('#');
+      if (h != std::string::npos) line.resize(h);
+      std::istringstream ss(line);
+      std::string op, din, dout;
+      int64_t M, N, K, batch;
+      int bn, splits;
+      if (!(ss >> op)) continue;  // blank line
+      if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> splits)) return TG_ERR_TABLE;
+      const int l = parse_layout(op), i = parse_dtype(din), o = parse_dtype(dout);
+      if (l < 0 || i < 0 || o < 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return TG_ERR_TABLE;
+      if (!(bn == 64 || bn == 128 || bn == 192 || bn == 256) || splits < 1 || splits > 64) return TG_ERR_TABLE;
+      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits};
+    }
+  }
+  std::unique_lock<std::shared_mutex> lk(g_table_mu);
+  g_table.swap(t);
+  return TG_OK;
+}
+
+static void table_env_init() {
+  std::call_once(g_table_env_once, [] {
+    if (const char* p = getenv("TG_TABLE")) load_table_file(p);
+  });
+}
+
+static bool table_lookup(const TableKey& k, TableVal* v) {
+  table_env_init();
+  std::shared_lock<std::shared_mutex> lk(g_table_mu);
+  auto it = g_table.find(k);
+  if (it == g_table.end()) return false;
+  *v = it->second;
+  return true;
+}
+
+// ----------------------------------------------------------------- planning
+struct Plan {
+  int bn = 256;
+  int splits = 1;
+  bool from_table = false;
+};
+
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Cost model of the persistent tensor-core kernel used when the table has no
+// entry: waves of units x (K blocks per unit x block time, or the epilogue
+// time when that is longer) + the reduction of split partials.
+static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int out_bytes, int sms) {
+  Plan best;
+  double best_t = 1e300;
+  const int64_t kb = cdiv(K, 64);
+  const int bns[4] = {256, 192, 128, 64};
+  for (int bn : bns) {
+    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
+    // one 128 x bn x 64 block: tensor time vs shared-memory operand reads (cycles)
+    const double kb_cyc = 4.0 * fmax(bn / 2.0, 32.0 + bn / 4.0);
+    const double epi_cyc = 128.0 * bn * out_bytes / 48.0;
+    for (int64_t s = 1; s <= 32 && s <= kb; ++s) {
+      const int64_t kps = cdiv(kb, s);
+      const int64_t real = cdiv(kb, kps);
+      if (real != s) continue;
+      const int64_t units = tiles * s;
+      const int64_t waves = cdiv(units, sms);
+      double t = waves * (fmax(kps * kb_cyc, s > 1 ? 128.0 * bn * 4 / 48.0 : epi_cyc) + 600.0);
+      if (s > 1) t += 3000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
+      if (t < best_t * 0.98) {
+        best_t = t;
+        best.bn = bn;
+        best.splits = static_cast<int>(s);
+      }
+    }
+  }
+  return best;
+}
+
+static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in,
+                      tg_dtype out, int sms) {
+  TableVal v;
+  if (table_lookup(TableKey{layout, in, out, M, N, K, batch}, &v)) {
+    Plan p;
+    p.bn = v.bn;
+    const int64_t kb = cdiv(K, 64);
+    const int64_t s = v.splits < kb ? v.splits : kb;
+    const int64_t kps = cdiv(kb, s);
+    p.splits = static_cast<int>(cdiv(kb, kps));
+    p.from_table = true;
+    return p;
+  }
+  return heuristic_plan(M, N, K, batch, out == TG_F32 ? 4 : 2, sms);
+}
+
+static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t batch) {
+  return p.splits > 1 ? static_cast<size_t>(p.splits) * batch * M * N * 4 : 0;
+}
+
+// -------------------------------------------------------------- the GEMMs
+static bool dtype_in_ok(tg_dtype in) { return in == TG_BF16 || in == TG_F16; }
+static bool dtype_out_ok(tg_dtype in, tg_dtype out) { return out == TG_F32 || out == in; }
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static size_t dt_bytes(tg_dtype d) { return d == TG_F32 ? 4 : 2; }
+static const int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+struct GemmCall {
+  int layout;
+  const void* A;
+  const void* B;
+  void* C;
+  int64_t batch, M, N, K;
+  int64_t lda, ldb, a_bs, b_bs;  // elements
+  tg_dtype in, out;
+  int a_kind_override = -1;  // FP32 operand (LoRA dH): CUDA-core path only
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  const char* name;
+};
+
+static bool tc_eligible(const GemmCall& g) {
+  if (g.a_kind_override >= 0) return false;
+  const size_t ob = dt_bytes(g.out);
+  return aligned(g.A, 16) && aligned(g.B, 16) && aligned(g.C, 16) && (g.lda * 2) % 16 == 0 &&
+         (g.ldb * 2) % 16 == 0 && (g.a_bs * 2) % 16 == 0 && (g.b_bs * 2) % 16 == 0 &&
+         (g.N * ob) % 16 == 0 && g.M <= kMaxDim && g.N <= kMaxDim && g.K <= kMaxDim &&
+         g.batch <= 65535;
+}
+
+static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
+  if (g.M == 0 || g.N == 0 || g.batch == 0) {
+    record(std::string(g.name) + " empty output: nothing to do");
+    return TG_OK;
+  }
+  const size_t ob = dt_bytes(g.out);
+  if (g.K == 0) {  // empty sum: zeros (all-zero bits in every output type)
+    record(std::string(g.name) + " empty reduction: zero fill");
+    return cudaMemsetAsync(g.C, 0, static_cast<size_t>(g.batch * g.M * g.N) * ob, g.stream) == cudaSuccess
+               ? TG_OK
+               : TG_ERR_CUDA;
+  }
+  char buf[320];
+  if (tc_eligible(g)) {
+    const Plan p = make_plan(g.layout, g.M, g.N, g.K, g.batch, g.in, g.out, ctx->sms);
+    const size_t need = plan_ws_bytes(p, g.M, g.N, g.batch);
+    if (need > 0 && (g.ws == nullptr || g.ws_bytes < need || !aligned(g.ws, 16))) {
+      snprintf(buf, sizeof buf, "%s tc %s bn=%d splits=%d: workspace %zu bytes needed, %zu given", g.name,
+               layout_name(g.layout), p.bn, p.splits, need, g.ws ? g.ws_bytes : static_cast<size_t>(0));
+      record(buf);
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    TcGemm t;
+    t.layout = g.layout;
+    t.A = g.A;
+    t.B = g.B;
+    t.C = g.C;
+    t.in_kind = g.in == TG_BF16 ? EK_BF16 : EK_F16;
+    t.out_kind = g.out == TG_F32 ? EK_F32 : (g.out == TG_BF16 ? EK_BF16 : EK_F16);
+    t.batch = g.batch;
+    t.M = g.M;
+    t.N = g.N;
+    t.K = g.K;
+    t.lda = g.lda;
+    t.ldb = g.ldb;
+    t.a_bstride = g.a_bs;
+    t.b_bstride = g.b_bs;
+    t.bn = p.bn;
+    t.splits = p.splits;
+    t.ws = g.ws;
+    t.grid = ctx->sms;
+    t.stream = g.stream;
+    t.status = ctx->status;
+    t.timeout_ns = ctx->timeout_ns;
+    cudaError_t e = g.layout == LAYOUT_NT   ? tc_gemm_launch_nt(t)
+                    : g.layout == LAYOUT_NN ? tc_gemm_launch_nn(t)
+                                            : tc_gemm_launch_tn(t);
+    if (e == cudaSuccess && p.splits > 1)
+      e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
+                               g.stream);
+    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d splits=%d table=%s %s", g.name,
+             layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch, p.bn,
+             p.splits, p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+    record(buf);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  // CUDA-core path, same semantics
+  SimtGemm s;
+  s.A = g.A;
+  s.B = g.B;
+  s.C = g.C;
+  s.a_kind = g.a_kind_override >= 0 ? g.a_kind_override : (g.in == TG_BF16 ? EK_BF16 : EK_F16);
+  s.b_kind = g.in == TG_BF16 ? EK_BF16 : EK_F16;
+  s.out_kind = g.out == TG_F32 ? EK_F32 : (g.out == TG_BF16 ? EK_BF16 : EK_F16);
+  s.batch = g.batch;
+  s.M = g.M;
+  s.N = g.N;
+  s.K = g.K;
+  s.stream = g.stream;
+  s.a_bs = g.a_bs;
+  s.b_bs = g.b_bs;
+  if (g.layout == LAYOUT_TN) {
+    s.a_rs = 1;
+    s.a_cs = g.lda;
+  } else {
+    s.a_rs = g.lda;
+    s.a_cs = 1;
+  }
+  if (g.layout == LAYOUT_NT) {
+    s.b_rs = 1;
+    s.b_cs = g.ldb;
+  } else {
+    s.b_rs = g.ldb;
+    s.b_cs = 1;
+  }
+  cudaError_t e = simt_gemm_launch(s);
+  snprintf(buf, sizeof buf, "%s simt %s M=%lld N=%lld K=%lld batch=%lld %s", g.name, layout_name(g.layout),
+           (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
+           e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+  record(buf);
+  return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+static size_t gemm_ws_bytes(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
+                            int sms) {
+  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+  return plan_ws_bytes(make_plan(layout, M, N, K, batch, in, out, sms), M, N, batch);
+}
+
+// Checks shared by the layer products.  Returns TG_OK to proceed.
+static tg_status check_common(tg_dtype in, tg_dtype out, std::initializer_list<int64_t> dims) {
+  if (!dtype_in_ok(in) || !dtype_out_ok(in, out)) return TG_ERR_UNSUPPORTED_DTYPE;
+  for (int64_t d : dims)
+    if (d < 0 || d > kMaxDim) return TG_ERR_INVALID_ARG;
+  return TG_OK;
+}
+
+static tg_status check_ptr(const void* p, int64_t elems, size_t esz) {
+  if (elems == 0) return TG_OK;
+  if (p == nullptr) return TG_ERR_INVALID_ARG;
+  return aligned(p, esz) ? TG_OK : TG_ERR_MISALIGNED;
+}
+
+#define TG_TRY(x)                   \
+  do {                              \
+    tg_status _s = (x);             \
+    if (_s != TG_OK) return _s;     \
+  } while (0)
+
+}  // namespace tg
+
+using namespace tg;
+
+// =================================================================== C ABI
+extern "C" {
+
+int tg_version(void) { return 10000; }
+
+const char* tg_status_string(tg_status s) {
+  switch (s) {
+    case TG_OK: return "ok";
+    case TG_ERR_INVALID_ARG: return "invalid argument";
+    case TG_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case TG_ERR_MISALIGNED: return "misaligned pointer";
+    case TG_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case TG_ERR_CUDA: return "CUDA runtime error";
+    case TG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case TG_ERR_TABLE: return "tile table unreadable";
+    case TG_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+  }
+  return "unknown status";
+}
+
+size_t tg_last_call(char* buf, size_t len) {
+  const std::string& s = t_last_call;
+  if (buf && len) {
+    const size_t n = s.size() < len - 1 ? s.size() : len - 1;
+    memcpy(buf, s.data(), n);
+    buf[n] = '\0';
+  }
+  return s.size();
+}
+
+tg_status tg_load_table(const char* path) {
+  table_env_init();
+  return load_table_file(path);
+}
+
+tg_status tg_stream_status(void* stream) {
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TG_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyAsync(&word, ctx->status, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(ctx->status, 0, sizeof word, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return TG_ERR_CUDA;
+  return (word & TG_DEVSTAT_TIMEOUT) ? TG_ERR_DEVICE_TIMEOUT : TG_OK;
+}
+
+tg_status tg_wait_probe(int64_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return TG_ERR_INVALID_ARG;
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaError_t e = wait_probe_launch(static_cast<unsigned long long>(timeout_us) * 1000ull, ctx->status,
+                                    static_cast<cudaStream_t>(stream));
+  record(std::string("wait_probe ") + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+  return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status tg_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t d_out, int64_t d_in, tg_dtype in,
+                      tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NT, X, W, Y, 1, T, d_out, d_in, d_in, d_in, T * d_in, d_out * d_in, in, out, -1, ws, ws_bytes,
+             static_cast<cudaStream_t>(stream), "fwd"};
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t d_out, int64_t d_in,
+                        tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_ptr(dX, T * d_in, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NN, dY, W, dX, 1, T, d_in, d_out, d_out, d_in, T * d_out, d_out * d_in, in, out, -1, ws,
+             ws_bytes, static_cast<cudaStream_t>(stream), "dgrad"};
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out, int64_t d_in,
+                        tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(dW, d_out * d_in, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_TN, dY, X, dW, 1, d_out, d_in, T, d_out, d_in, T * d_out, T * d_in, in, out, -1, ws,
+             ws_bytes, static_cast<cudaStream_t>(stream), "wgrad"};
+  return run_gemm(g, ctx);
+}
+
+// ------------------------------------------------------------- attention
+static bool attn_call(tg_attn_op op, const void* A, const void* B, void* C, int64_t batch, int64_t s, int64_t d,
+                      tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream, GemmCall* g) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (op) {
+    case TG_ATTN_QK:
+    case TG_ATTN_DO_VT:  // [s,d] x [s,d]^T -> [s,s]
+      *g = GemmCall{LAYOUT_NT, A, B, C, batch, s, s, d, d, d, s * d, s * d, in, out, -1, ws, ws_bytes, st,
+                    op == TG_ATTN_QK ? "attn_qk" : "attn_do_vt"};
+      return true;
+    case TG_ATTN_PV:
+    case TG_ATTN_DS_K:  // [s,s] x [s,d] -> [s,d]
+      *g = GemmCall{LAYOUT_NN, A, B, C, batch, s, d, s, s, d, s * s, s * d, in, out, -1, ws, ws_bytes, st,
+                    op == TG_ATTN_PV ? "attn_pv" : "attn_ds_k"};
+      return true;
+    case TG_ATTN_PT_DO:
+    case TG_ATTN_DST_Q:  // [s,s]^T x [s,d] -> [s,d]
+      *g = GemmCall{LAYOUT_TN, A, B, C, batch, s, d, s, s, d, s * s, s * d, in, out, -1, ws, ws_bytes, st,
+                    op == TG_ATTN_PT_DO ? "attn_pt_do" : "attn_dst_q"};
+      return true;
+  }
+  return false;
+}
+
+tg_status tg_bmm_attn(tg_attn_op op, const void* A, const void* B, void* C, int64_t batch, int64_t s, int64_t d,
+                      tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {batch, s, d}));
+  GemmCall g;
+  if (!attn_call(op, A, B, C, batch, s, d, in, out, ws, ws_bytes, stream, &g)) return TG_ERR_INVALID_ARG;
+  const bool ss_a = op == TG_ATTN_PV || op == TG_ATTN_DS_K || op == TG_ATTN_PT_DO || op == TG_ATTN_DST_Q;
+  const bool ss_c = op == TG_ATTN_QK || op == TG_ATTN_DO_VT;
+  TG_TRY(check_ptr(A, batch * s * (ss_a ? s : d), 2));
+  TG_TRY(check_ptr(B, batch * s * d, 2));
+  TG_TRY(check_ptr(C, batch * s * (ss_c ? s : d), dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  return run_gemm(g, ctx);
+}
+
+// ------------------------------------------------------------------ LoRA
+tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t d_in, int64_t r, tg_dtype in,
+                       tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_in, r}));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(A, r * d_in, 2));
+  TG_TRY(check_ptr(H, T * r, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NT, X, A, H, 1, T, r, d_in, d_in, d_in, T * d_in, r * d_in, in, out, -1, ws, ws_bytes,
+             static_cast<cudaStream_t>(stream), "lora_down"};
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d_out, int64_t r, tg_dtype in,
+                     tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, r}));
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(B, d_out * r, 2));
+  TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, ws, ws_bytes,
+             static_cast<cudaStream_t>(stream), "lora_up"};
+  return run_gemm(g, ctx);
+}
+
+// workspace plan of the composed LoRA gradient: [dH f32 (if not given)] [sub-GEMM ws]
+static size_t lora_grad_sub_ws(int64_t T, int64_t d_in, int64_t d_out, int64_t r, tg_dtype in, tg_dtype out,
+                               int sms) {
+  // dH = dY . B and dB = dY^T . H run one after the other and share the space
+  const size_t a = gemm_ws_bytes(LAYOUT_NN, T, r, d_out, 1, in, TG_F32, sms);
+  const size_t b = gemm_ws_bytes(LAYOUT_TN, d_out, r, T, 1, in, out, sms);
+  (void)d_in;
+  return a > b ? a : b;
+}
+
+tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
+                       void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
+                       tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_in, d_out, r}));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(A, r * d_in, 2));
+  TG_TRY(check_ptr(B, d_out * r, 2));
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(dA, r * d_in, dt_bytes(out)));
+  TG_TRY(check_ptr(dB, d_out * r, dt_bytes(out)));
+  TG_TRY(check_ptr(dX, T * d_in, dt_bytes(out)));
+  if (dH_f32 && !aligned(dH_f32, 4)) return TG_ERR_MISALIGNED;
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t dh_bytes = dH_f32 ? 0 : (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
+  const size_t sub = lora_grad_sub_ws(T, d_in, d_out, r, in, out, ctx->sms);
+  if (dh_bytes + sub > 0 && (ws == nullptr || ws_bytes < dh_bytes + sub || !aligned(ws, 256)))
+    return TG_ERR_WORKSPACE_TOO_SMALL;
+  float* dH = dH_f32 ? dH_f32 : static_cast<float*>(ws);
+  void* sub_ws = static_cast<char*>(ws) + dh_bytes;
+  // dH = dY . B (FP32)
+  GemmCall g1{LAYOUT_NN, dY, B, dH, 1, T, r, d_out, d_out, r, T * d_out, d_out * r, in, TG_F32, -1, sub_ws, sub,
+              st, "lora_grad.dH"};
+  TG_TRY(run_gemm(g1, ctx));
+  // dB = dY^T . H
+  GemmCall g2{LAYOUT_TN, dY, H, dB, 1, d_out, r, T, d_out, r, T * d_out, T * r, in, out, -1, sub_ws, sub, st,
+              "lora_grad.dB"};
+  TG_TRY(run_gemm(g2, ctx));
+  // dA = dH^T . X  and  dX = dH . A  with the FP32 dH operand
+  GemmCall g3{LAYOUT_TN, dH, X, dA, 1, r, d_in, T, r, d_in, T * r, T * d_in, in, out, EK_F32, nullptr, 0, st,
+              "lora_grad.dA"};
+  TG_TRY(run_gemm(g3, ctx));
+  GemmCall g4{LAYOUT_NN, dH, A, dX, 1, T, d_in, r, r, d_in, T * r, r * d_in, in, out, EK_F32, nullptr, 0, st,
+              "lora_grad.dX"};
+  return run_gemm(g4, ctx);
+}
+
+size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in, tg_dtype out) {
+  if (!dtype_in_ok(in) || !dtype_out_ok(in, out)) return SIZE_MAX;
+  if (d0 < 0 || d1 < 0 || d2 < 0 || d3 < 0) return SIZE_MAX;
+  DevCtx* ctx = nullptr;
+  if (device_ctx(&ctx) != TG_OK) return SIZE_MAX;
+  switch (op) {
+    case TG_OP_GEMM_FWD: return gemm_ws_bytes(LAYOUT_NT, d0, d1, d2, 1, in, out, ctx->sms);
+    case TG_OP_GEMM_DGRAD: return gemm_ws_bytes(LAYOUT_NN, d0, d2, d1, 1, in, out, ctx->sms);
+    case TG_OP_GEMM_WGRAD: return gemm_ws_bytes(LAYOUT_TN, d1, d2, d0, 1, in, out, ctx->sms);
+    case TG_OP_LORA_DOWN: return gemm_ws_bytes(LAYOUT_NT, d0, d2, d1, 1, in, out, ctx->sms);
+    case TG_OP_LORA_UP: return gemm_ws_bytes(LAYOUT_NT, d0, d1, d2, 1, in, out, ctx->sms);
+    case TG_OP_LORA_GRAD: {
+      const size_t dh = (static_cast<size_t>(d0 * d3 * 4) + 255) / 256 * 256;
+      return dh + lora_grad_sub_ws(d0, d1, d2, d3, in, out, ctx->sms);
+    }
+    case TG_OP_BMM_ATTN: {
+      GemmCall g;
+      if (!attn_call(static_cast<tg_attn_op>(d0), nullptr, nullptr, nullptr, d1, d2, d3, in, out, nullptr, 0,
+                     nullptr, &g))
+        return SIZE_MAX;
+      return gemm_ws_bytes(g.layout, g.M, g.N, g.K, g.batch, in, out, ctx->sms);
+    }
+  }
+  return SIZE_MAX;
+}
+
+}  // extern "C"

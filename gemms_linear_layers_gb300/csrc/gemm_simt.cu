@@ -1,0 +1,118 @@
+// gemm_simt.cu -- CUDA-core kernels beside the tensor-core path:
+//  * the ordered reduction of FP32 split-K partials (deterministic: split
+//    order fixed, no atomics), with the final cast to the output type;
+//  * a plain strided GEMM for shapes the tensor-core path cannot address
+//    (a row pitch that is not a multiple of 16 bytes, an unaligned base
+//    pointer, an FP32 operand).  It is a GPU path, not a CPU fallback:
+//    FP32 accumulation, k ascending for every output element.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tg_internal.h"
+
+namespace tg {
+
+__device__ __forceinline__ float load_as_float(const void* p, int kind, int64_t i) {
+  if (kind == EK_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  if (kind == EK_F16) return __half2float(static_cast<const __half*>(p)[i]);
+  return static_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void store_from_float(void* p, int kind, int64_t i, float v) {
+  if (kind == EK_BF16)
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  else if (kind == EK_F16)
+    static_cast<__half*>(p)[i] = __float2half_rn(v);
+  else
+    static_cast<float*>(p)[i] = v;
+}
+
+// ---------------------------------------------------------------- split-K
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int out_kind,
+                                     int64_t batch, int64_t splits, int64_t MN) {
+  const int64_t n4 = MN / 4;  // MN is a multiple of 4 on the tensor-core path
+  const int64_t total = batch * n4;
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = v / n4;
+    const int64_t i4 = v - b * n4;
+    const float4* src = reinterpret_cast<const float4*>(ws) + (b * splits) * n4 + i4;
+    float4 s = src[0];
+    for (int64_t k = 1; k < splits; ++k) {
+      const float4 t = src[k * n4];
+      s.x += t.x;
+      s.y += t.y;
+      s.z += t.z;
+      s.w += t.w;
+    }
+    const int64_t o = b * MN + i4 * 4;
+    if (out_kind == EK_F32) {
+      reinterpret_cast<float4*>(C)[o / 4] = s;
+    } else if (out_kind == EK_BF16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(C)[o / 4] = pk;
+    } else {
+      __half2 lo = __floats2half2_rn(s.x, s.y), hi = __floats2half2_rn(s.z, s.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(C)[o / 4] = pk;
+    }
+  }
+}
+
+cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t batch, int64_t splits,
+                                 int64_t MN, cudaStream_t stream) {
+  const int64_t total = batch * (MN / 4);
+  if (total <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  if (blocks > cap) blocks = cap;
+  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, C, out_kind, batch, splits, MN);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- strided
+constexpr int ST = 16;  // 16 x 16 outputs per block, K staged 16 at a time
+
+__global__ void simt_gemm_kernel(SimtGemm g) {
+  __shared__ float As[ST][ST + 1];
+  __shared__ float Bs[ST][ST + 1];
+  const int64_t b = blockIdx.z;
+  const int64_t i = static_cast<int64_t>(blockIdx.y) * ST + threadIdx.y;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * ST + threadIdx.x;
+  float acc = 0.f;
+  for (int64_t k0 = 0; k0 < g.K; k0 += ST) {
+    const int64_t ka = k0 + threadIdx.x;  // A tile: row threadIdx.y, column k
+    const int64_t ia = static_cast<int64_t>(blockIdx.y) * ST + threadIdx.y;
+    As[threadIdx.y][threadIdx.x] =
+        (ia < g.M && ka < g.K) ? load_as_float(g.A, g.a_kind, b * g.a_bs + ia * g.a_rs + ka * g.a_cs) : 0.f;
+    const int64_t kb = k0 + threadIdx.y;  // B tile: row k, column threadIdx.x
+    const int64_t jb = static_cast<int64_t>(blockIdx.x) * ST + threadIdx.x;
+    Bs[threadIdx.y][threadIdx.x] =
+        (kb < g.K && jb < g.N) ? load_as_float(g.B, g.b_kind, b * g.b_bs + kb * g.b_rs + jb * g.b_cs) : 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < ST; ++kk) acc = fmaf(As[threadIdx.y][kk], Bs[kk][threadIdx.x], acc);
+    __syncthreads();
+  }
+  if (i < g.M && j < g.N) store_from_float(g.C, g.out_kind, (b * g.M + i) * g.N + j, acc);
+}
+
+cudaError_t simt_gemm_launch(const SimtGemm& g) {
+  if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
+  dim3 block(ST, ST);
+  dim3 grid(static_cast<unsigned>((g.N + ST - 1) / ST), static_cast<unsigned>((g.M + ST - 1) / ST),
+            static_cast<unsigned>(g.batch));
+  if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
+  simt_gemm_kernel<<<grid, block, 0, g.stream>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace tg

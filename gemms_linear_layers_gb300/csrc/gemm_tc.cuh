@@ -1,0 +1,313 @@
+// gemm_tc.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// The three products of a linear layer in a training step (page "Twice the
+// training speed on a BC-250 from tuned matrix kernels", section "Where the
+// time went") differ only in which operand index is contiguous in memory, so
+// one kernel template covers them, specialised on the major-ness of A and B:
+//   forward   Y  = X W^T   : A = X  K-major,    B = W  K-major
+//   dgrad     dX = dY W    : A = dY K-major,    B = W  MN-major
+//   wgrad     dW = dY^T X  : A = dY MN-major,   B = X  MN-major
+// 16-bit inputs, FP32 accumulation in tensor memory (section "Tuning the
+// kernels": bf16 and fp16 with FP32 accumulation).
+//
+// CTA = 6 warps, one CTA per SM, persistent over output tiles of 128 x BN:
+//   warp 0      TMA producer: 64-deep K blocks of A and B into a STAGES-deep
+//               shared-memory ring (128-byte swizzle), full/empty mbarriers
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
+//               (M=128, N=BN, K=16 per instruction) into one of two TMEM
+//               accumulators, and tcgen05.commit frees smem stages
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, cast (RNE)
+//               to the output type, swizzled staging tile, TMA store; the
+//               accumulator is handed back as soon as it has been read, so
+//               the next tile's MMAs overlap this tile's stores.
+// Split-K: a unit is (tile, K range); partial sums go to an FP32 workspace
+// and a separate kernel adds them in split order (deterministic).
+#pragma once
+#include "ptx.cuh"
+
+namespace tg {
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;  // 128 bytes of 16-bit values: one swizzle row
+constexpr int TC_THREADS = 192;
+constexpr int TC_EPI_WARPS = 4;
+constexpr int TC_A_STAGE = TC_BM * TC_BK * 2;  // 16 KB
+constexpr int TC_EPI_BUF = 32 * 128;           // 32 rows x 128 bytes
+
+template <int BN>
+struct TcCfg {
+  static constexpr int B_STAGE = BN * TC_BK * 2;
+  static constexpr int STAGES = (BN == 256 || BN == 192) ? 4 : (BN == 128) ? 6 : 8;
+  static constexpr int ACC_STRIDE = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
+  static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + STAGES * (TC_A_STAGE + B_STAGE) +
+                              TC_EPI_WARPS * 2 * TC_EPI_BUF + BAR_BYTES;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(BN % 64 == 0 && BN <= 256, "tile width");
+  static_assert(2 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area");
+};
+
+struct TcArgs {
+  int m_tiles, n_tiles;
+  int kb_total;  // K blocks of 64
+  int kps;       // K blocks per split
+  int splits;
+  int units;     // batch * m_tiles * n_tiles * splits
+  uint32_t idesc;
+  int out_f16;   // 16-bit output type: 1 = fp16, 0 = bf16
+  unsigned long long timeout_ns;
+  unsigned int* status;
+};
+
+struct Unit {
+  int b, m0, n0, split, kb0, kb1;
+};
+
+template <int BN>
+__device__ __forceinline__ Unit decode_unit(int u, const TcArgs& a) {
+  Unit c;
+  c.split = u % a.splits;
+  const int t = u / a.splits;
+  const int tiles = a.m_tiles * a.n_tiles;
+  c.b = t / tiles;
+  const int r = t - c.b * tiles;
+  c.m0 = (r % a.m_tiles) * TC_BM;  // consecutive units walk down M: they share B
+  c.n0 = (r / a.m_tiles) * BN;
+  c.kb0 = c.split * a.kps;
+  c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+  return c;
+}
+
+template <bool A_MN, bool B_MN, int BN, bool OUT16>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
+  using Cfg = TcCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * TC_A_STAGE;
+  uint8_t* sE = sB + S * Cfg::B_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + TC_EPI_WARPS * 2 * TC_EPI_BUF);
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), TC_EPI_WARPS);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const unsigned long long tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) issued[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        const Unit c = decode_unit<BN>(u, args);
+        for (int kb = c.kb0; kb < c.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, tmo, abort_flag, args.status, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, TC_A_STAGE + Cfg::B_STAGE);
+          const uint32_t a_dst = smem_u32(sA + stage * TC_A_STAGE);
+          const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_STAGE);
+          const int k0 = kb * TC_BK;
+          if (A_MN) {
+            tma_load_3d(a_dst, &tmA, fb, c.m0, k0, c.b);
+            tma_load_3d(a_dst + 8192, &tmA, fb, c.m0 + 64, k0, c.b);
+          } else {
+            tma_load_3d(a_dst, &tmA, fb, k0, c.m0, c.b);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
+          } else {
+            tma_load_3d(b_dst, &tmB, fb, k0, c.n0, c.b);
+          }
+          issued[stage] = static_cast<int>(phase);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA unwinds
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+          if (issued[s] >= 0)
+            mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>(issued[s]), 200000000ull, nullptr,
+                      args.status, 9);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        const Unit c = decode_unit<BN>(u, args);
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, tmo, abort_flag, args.status, 2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
+        for (int kb = c.kb0; kb < c.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, tmo, abort_flag, args.status, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * TC_A_STAGE);
+          const uint32_t b_base = smem_u32(sB + stage * Cfg::B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a_base + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b_base + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_f16(d_tmem, ad, bd, args.idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&empty[stage]));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[acc]));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // every MMA issued so far must finish before tensor memory is freed
+        umma_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, 200000000ull, nullptr, args.status, 10);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int ew = warp - 2;  // staging buffers owned by this warp
+    const int q = warp & 3;   // TMEM lane quadrant this warp may access
+    uint8_t* ebuf = sE + ew * 2 * TC_EPI_BUF;
+    constexpr int CW = OUT16 ? 64 : 32;  // columns per 128-byte staging row
+    constexpr int NCH = BN / CW;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int nstore = 0;
+    for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
+      const Unit c = decode_unit<BN>(u, args);
+      if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
+      const int zc = c.b * args.splits + c.split;
+#pragma unroll 1
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t r[CW];
+        tmem_ld_32x32b_x32(t_row + ch * CW, r);
+        if (OUT16) tmem_ld_32x32b_x32(t_row + ch * CW + 32, r + 32);
+        tmem_ld_wait();
+        if (ch == NCH - 1) {
+          // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+        uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+        if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* row = buf + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 v;
+          if (OUT16) {
+            const uint32_t* f = r + 8 * j;
+            if (args.out_f16) {
+              v.x = pack_f16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
+              v.y = pack_f16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
+              v.z = pack_f16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
+              v.w = pack_f16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
+            } else {
+              v.x = pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
+              v.y = pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
+              v.z = pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
+              v.w = pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
+            }
+          } else {
+            v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          }
+          // 128-byte swizzle: 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8)
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
+          bulk_commit();
+        }
+        ++nstore;
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace tg

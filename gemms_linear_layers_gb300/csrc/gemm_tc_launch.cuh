@@ -1,0 +1,81 @@
+// gemm_tc_launch.cuh -- host side of one tensor-core GEMM launch: tensor maps,
+// kernel selection by tile width and output width, dynamic shared memory.
+// Included once per layout family (gemm_tc_nt.cu, _nn.cu, _tn.cu) so the
+// three families compile in parallel.
+#pragma once
+#include <cuda.h>
+
+#include "gemm_tc.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+
+template <bool A_MN, bool B_MN, int BN, bool OUT16>
+static cudaError_t tc_launch_one(const TcGemm& g) {
+  using Cfg = TcCfg<BN>;
+  auto kern = tc_gemm_kernel<A_MN, B_MN, BN, OUT16>;
+  // the attribute is per function and per device: set it once per device, so
+  // later calls (including calls under stream capture) make no such call
+  static bool attr_set[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+
+  alignas(64) CUtensorMap tmA, tmB, tmC;
+  const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
+  bool ok;
+  if (A_MN)  // stored [batch][K][M]
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, true);
+  else       // stored [batch][M][K]
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, true);
+  if (!ok) return cudaErrorInvalidValue;
+  if (B_MN)  // stored [batch][K][N]
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, true);
+  else       // stored [batch][N][K]
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, true);
+  if (!ok) return cudaErrorInvalidValue;
+
+  // output (or FP32 split partials): [batch * splits][M][N], dense
+  const int ck = g.splits > 1 ? EK_F32 : g.out_kind;
+  const uint64_t esz = elem_bytes(ck);
+  void* cptr = g.splits > 1 ? g.ws : g.C;
+  ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * g.splits, N * esz, M * N * esz,
+                      OUT16 ? 64 : 32, 32, true);
+  if (!ok) return cudaErrorInvalidValue;
+
+  TcArgs a;
+  a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
+  a.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.splits = g.splits;
+  a.kps = (a.kb_total + g.splits - 1) / g.splits;
+  a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * g.splits;
+  a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC_BM, BN);
+  a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
+  a.timeout_ns = g.timeout_ns;
+  a.status = g.status;
+  const int grid = g.grid < a.units ? g.grid : a.units;
+  kern<<<grid, TC_THREADS, Cfg::SMEM, g.stream>>>(tmA, tmB, tmC, a);
+  return cudaGetLastError();
+}
+
+template <bool A_MN, bool B_MN>
+static cudaError_t tc_launch_layout(const TcGemm& g) {
+  // split partials are FP32; so is an FP32 output
+  const bool out16 = g.splits == 1 && g.out_kind != EK_F32;
+  switch (g.bn) {
+    case 64: return out16 ? tc_launch_one<A_MN, B_MN, 64, true>(g) : tc_launch_one<A_MN, B_MN, 64, false>(g);
+    case 128: return out16 ? tc_launch_one<A_MN, B_MN, 128, true>(g) : tc_launch_one<A_MN, B_MN, 128, false>(g);
+    case 192: return out16 ? tc_launch_one<A_MN, B_MN, 192, true>(g) : tc_launch_one<A_MN, B_MN, 192, false>(g);
+    case 256: return out16 ? tc_launch_one<A_MN, B_MN, 256, true>(g) : tc_launch_one<A_MN, B_MN, 256, false>(g);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tg

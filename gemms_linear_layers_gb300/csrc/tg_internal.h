@@ -1,0 +1,104 @@
+// tg_internal.h -- declarations shared between the translation units of
+// libtg.so (never installed; the public interface is include/tg.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// device status word: bit 31 = a bounded wait timed out; low bits = site id
+#define TG_DEVSTAT_TIMEOUT 0x80000000u
+#define TG_DEVSTAT_SITE_MASK 0x0000FFFFu
+
+namespace tg {
+
+enum ElemKind : int { EK_BF16 = 0, EK_F16 = 1, EK_F32 = 2 };
+
+inline int elem_bytes(int ek) { return ek == EK_F32 ? 4 : 2; }
+
+// Operand layouts of the three kernel families.  "K-major": the reduction
+// index is contiguous; "MN-major": the row (A) or column (B) index is.
+enum Layout : int {
+  LAYOUT_NT = 0,  // A K-major, B K-major   (forward)
+  LAYOUT_NN = 1,  // A K-major, B MN-major  (input gradient)
+  LAYOUT_TN = 2,  // A MN-major, B MN-major (weight gradient)
+};
+
+// One tensor-core GEMM launch: C[b] (MxN) = sum_k A[b](m,k) B[b](k,n).
+//   A K-major : stored [batch][M][K] with row pitch lda;   MN-major: [batch][K][M]
+//   B K-major : stored [batch][N][K] with row pitch ldb;   MN-major: [batch][K][N]
+//   C         : stored [batch][M][N], dense
+struct TcGemm {
+  int layout;
+  const void* A;
+  const void* B;
+  void* C;
+  int in_kind;   // EK_BF16 / EK_F16
+  int out_kind;  // EK_BF16 / EK_F16 / EK_F32
+  int64_t batch, M, N, K;
+  int64_t lda, ldb;           // row pitches in elements
+  int64_t a_bstride, b_bstride;  // batch strides in elements
+  int bn;                     // tile width: 64, 128, 192 or 256
+  int splits;                 // >1: FP32 partials to ws, then an ordered reduction
+  void* ws;
+  int grid;                   // persistent CTAs
+  cudaStream_t stream;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+// per-layout launchers (gemm_tc_{nt,nn,tn}.cu)
+cudaError_t tc_gemm_launch_nt(const TcGemm& g);
+cudaError_t tc_gemm_launch_nn(const TcGemm& g);
+cudaError_t tc_gemm_launch_tn(const TcGemm& g);
+
+// FP32 split partials ws[b*splits + s][M][N] -> C[b][M][N], s ascending
+cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t batch,
+                                 int64_t splits, int64_t MN, cudaStream_t stream);
+
+// Plain strided GEMM on CUDA cores for shapes the tensor-core path cannot take
+// (row pitches that are not 16-byte multiples, unaligned pointers, FP32 operands).
+//   C[b][i][j] = sum_k A[b*a_bs + i*a_rs + k*a_cs] * B[b*b_bs + k*b_rs + j*b_cs]
+struct SimtGemm {
+  const void* A;
+  const void* B;
+  void* C;
+  int a_kind, b_kind, out_kind;
+  int64_t batch, M, N, K;
+  int64_t a_bs, a_rs, a_cs, b_bs, b_rs, b_cs;
+  cudaStream_t stream;
+};
+cudaError_t simt_gemm_launch(const SimtGemm& g);
+
+// Tensor-map encoding through the driver entry point (tmap.cpp).
+bool encode_tmap_3d(void* tmap_out, const void* base, int elem_kind, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                    uint32_t box1, bool swizzle128);
+
+// rank-r LoRA streaming kernels (lora.cu)
+struct LoraArgs {
+  const void* X;   // [T, d_in]
+  const void* A;   // [r, d_in]
+  const void* B;   // [d_out, r]
+  const void* H;   // [T, r]
+  const void* dY;  // [T, d_out]
+  void* out;       // op-dependent output
+  void* out2;
+  void* out3;
+  void* out4;
+  float* ws;
+  int64_t T, d_in, d_out, r;
+  int in_kind, out_kind;
+  int num_sms;
+  cudaStream_t stream;
+};
+size_t lora_down_ws_bytes(int64_t T, int64_t d_in, int64_t r, int num_sms);
+cudaError_t lora_down_launch(const LoraArgs& a);
+cudaError_t lora_up_launch(const LoraArgs& a);
+size_t lora_grad_ws_bytes(int64_t T, int64_t d_in, int64_t d_out, int64_t r, int num_sms);
+cudaError_t lora_grad_launch(const LoraArgs& a);
+
+// wait-timeout probe kernel (api.cu)
+cudaError_t wait_probe_launch(unsigned long long timeout_ns, unsigned int* status,
+                              cudaStream_t stream);
+
+}  // namespace tg

@@ -1,0 +1,176 @@
+/*
+ * tg.h -- training products of linear layers on GB300 (sm_103a): C ABI of libtg.so.
+ *
+ * What the library computes comes from the page "Twice the training speed on a
+ * BC-250 from tuned matrix kernels":
+ *   - section "Where the time went": every linear layer of a training step runs
+ *     three matrix products -- the forward pass, the gradient for its input and
+ *     the gradient for its weight -- each in a different memory layout;
+ *   - section "Tuning the kernels": bf16 and fp16 inputs with FP32 accumulation,
+ *     for every layer of a decoder at 1,024-4,096 tokens, the rank-16 LoRA
+ *     matrices and the batched products inside attention;
+ *   - section "Checking the results are right": all three layouts and the
+ *     batched attention products are checked against a float64 CPU product.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are row-major and dense (no stride arguments).  Names follow the
+ *     page: X[T, d_in] activations, W[d_out, d_in] weight, dY[T, d_out] output
+ *     gradient, T tokens.
+ *   - Pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     reference after the call returns and allocates no device memory for a
+ *     call.  Scratch space, when a call needs it, is the caller's `ws`
+ *     (tg_workspace_size gives the size; `ws` may be NULL when that is 0).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: TG_OK means the work was enqueued.  A device-side failure
+ *     (a bounded wait that timed out) is reported by tg_stream_status.
+ *   - Outputs are overwritten (no alpha/beta).  `in` is TG_BF16 or TG_F16;
+ *     `out` is TG_F32 or the input type.  16-bit outputs are the FP32 result
+ *     rounded to nearest even.
+ *   - Sizes: a negative size is TG_ERR_INVALID_ARG; an empty output (a zero
+ *     row or column count) is TG_OK with nothing done; an empty reduction
+ *     writes zeros.  Every size must be below 2^31.
+ *   - Pointers: each must be aligned to its element size (else
+ *     TG_ERR_MISALIGNED).  Base addresses aligned to 16 bytes with row pitches
+ *     that are multiples of 16 bytes take the tensor-core path; anything else
+ *     takes a slower CUDA-core GPU path with identical semantics.
+ *   - Errors are return codes; nothing aborts, exits or throws across the ABI.
+ *   - Calls on different streams may run concurrently if they do not share a
+ *     workspace or an output.
+ */
+#ifndef TG_H
+#define TG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { TG_BF16 = 0, TG_F16 = 1, TG_F32 = 2 } tg_dtype;
+
+typedef enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1,         /* NULL pointer with a non-empty tensor, bad size, bad enum */
+  TG_ERR_UNSUPPORTED_DTYPE = 2,   /* input not bf16/fp16, or output neither FP32 nor the input type */
+  TG_ERR_MISALIGNED = 3,          /* pointer not aligned to its element size */
+  TG_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below tg_workspace_size() for the call */
+  TG_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, attribute, device query) */
+  TG_ERR_DEVICE_TIMEOUT = 6,      /* a kernel's bounded wait ran out (tg_stream_status) */
+  TG_ERR_TABLE = 7,               /* a tile table could not be read or parsed */
+  TG_ERR_UNSUPPORTED_DEVICE = 8   /* the current device is not sm_103 */
+} tg_status;
+
+/* The six batched products inside attention (no mask, no softmax, no scale).
+ * Tensors are [batch, rows, cols]; batch = heads, s = sequence, d = head dim. */
+typedef enum {
+  TG_ATTN_QK = 0,    /* S  = Q  K^T : A=Q [b,s,d],  B=K [b,s,d]  -> C [b,s,s] */
+  TG_ATTN_PV = 1,    /* O  = P  V   : A=P [b,s,s],  B=V [b,s,d]  -> C [b,s,d] */
+  TG_ATTN_DO_VT = 2, /* dP = dO V^T : A=dO [b,s,d], B=V [b,s,d]  -> C [b,s,s] */
+  TG_ATTN_PT_DO = 3, /* dV = P^T dO : A=P [b,s,s],  B=dO [b,s,d] -> C [b,s,d] */
+  TG_ATTN_DS_K = 4,  /* dQ = dS K   : A=dS [b,s,s], B=K [b,s,d]  -> C [b,s,d] */
+  TG_ATTN_DST_Q = 5  /* dK = dS^T Q : A=dS [b,s,s], B=Q [b,s,d]  -> C [b,s,d] */
+} tg_attn_op;
+
+/* Operation ids for tg_workspace_size. */
+typedef enum {
+  TG_OP_GEMM_FWD = 0,   /* d0=T, d1=d_out, d2=d_in */
+  TG_OP_GEMM_DGRAD = 1, /* d0=T, d1=d_out, d2=d_in */
+  TG_OP_GEMM_WGRAD = 2, /* d0=T, d1=d_out, d2=d_in */
+  TG_OP_LORA_DOWN = 3,  /* d0=T, d1=d_in, d2=r */
+  TG_OP_LORA_UP = 4,    /* d0=T, d1=d_out, d2=r */
+  TG_OP_LORA_GRAD = 5,  /* d0=T, d1=d_in, d2=d_out, d3=r */
+  TG_OP_BMM_ATTN = 6    /* d0=tg_attn_op, d1=batch, d2=s, d3=d */
+} tg_op;
+
+/* Forward product of a linear layer ("Where the time went"):
+ *   Y[T, d_out] = X[T, d_in] . W[d_out, d_in]^T
+ * Both operands have the reduction index (d_in) contiguous. */
+tg_status tg_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t d_out, int64_t d_in,
+                      tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+
+/* Input-gradient product ("Where the time went"):
+ *   dX[T, d_in] = dY[T, d_out] . W[d_out, d_in]
+ * The reduction index (d_out) is contiguous in dY but strided in W. */
+tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t d_out,
+                        int64_t d_in, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Weight-gradient product ("Where the time went"), reduced over tokens:
+ *   dW[d_out, d_in] = dY[T, d_out]^T . X[T, d_in]
+ * The reduction index (T) is strided in both operands.  Long reductions are
+ * split across the GPU with FP32 partials in `ws` and summed in a fixed order,
+ * so results are bitwise reproducible run to run. */
+tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out,
+                        int64_t d_in, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Rank-r LoRA down projection ("Tuning the kernels": the rank-16 LoRA matrices):
+ *   H[T, r] = X[T, d_in] . A[r, d_in]^T
+ * r = 16 takes the streaming kernel (X read once); other ranks are supported
+ * on the general path. */
+tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t d_in, int64_t r,
+                       tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+
+/* Rank-r LoRA up projection:
+ *   Y[T, d_out] = H[T, r] . B[d_out, r]^T        (overwrites Y; no alpha/r scale) */
+tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d_out, int64_t r,
+                     tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+
+/* Gradients of the LoRA branch Y = (X A^T) B^T given dY:
+ *   dH[T, r]     = dY . B          (kept in FP32; written to dH_f32 when non-NULL)
+ *   dB[d_out, r] = dY^T . H
+ *   dA[r, d_in]  = dH^T . X        (uses the FP32 dH)
+ *   dX[T, d_in]  = dH . A          (uses the FP32 dH)
+ * X, A, B, H, dY have type `in`; dA, dB, dX have type `out`; dH_f32 is float. */
+tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY,
+                       void* dA, void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in,
+                       int64_t d_out, int64_t r, tg_dtype in, tg_dtype out, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* One of the batched products inside attention ("Tuning the kernels";
+ * "Checking the results are right": batched attention), see tg_attn_op. */
+tg_status tg_bmm_attn(tg_attn_op op, const void* A, const void* B, void* C, int64_t batch,
+                      int64_t s, int64_t d, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Bytes of `ws` the call with these sizes needs on the current device
+ * (0 when none).  Returns SIZE_MAX for invalid arguments. */
+size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in,
+                         tg_dtype out);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: TG_ERR_DEVICE_TIMEOUT if any kernel's bounded wait ran out since the
+ * last check, TG_ERR_CUDA if the synchronisation failed, else TG_OK. */
+tg_status tg_stream_status(void* stream);
+
+/* Static text for a status code. */
+const char* tg_status_string(tg_status s);
+
+/* Load a tile table (the analogue of tuned logic files; section "Tuning the
+ * kernels").  Lines: "op dtype_in dtype_out M N K batch bn splits", where op
+ * is fwd|dgrad|wgrad|attn_nt|attn_nn|attn_tn and M N K are the GEMM's own
+ * output rows, output columns and reduction length.  Replaces any table
+ * loaded before; NULL or "" clears it.  $TG_TABLE is read at first use. */
+tg_status tg_load_table(const char* path);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int tg_version(void);
+
+/* Writes a one-line description of the last dispatch decision made on the
+ * calling thread (kernel path, tile, splits, whether a table entry was used)
+ * into buf (NUL-terminated, truncated to len).  Returns the full length. */
+size_t tg_last_call(char* buf, size_t len);
+
+/* Diagnostic of the bounded-wait mechanism every pipelined kernel uses: one
+ * CTA waits on a barrier that nothing ever completes, gives up after
+ * timeout_us microseconds and records a timeout in the status word, which
+ * tg_stream_status then reports as TG_ERR_DEVICE_TIMEOUT.  The context stays
+ * usable.  timeout_us must lie in [1, 10,000,000]. */
+tg_status tg_wait_probe(int64_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_H */

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every symbol include/tg.h declares, and rejects bad arguments before
+any device work.  The tile-table reader is host logic and is checked here too."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gemms_linear_layers_gb300 import _binding as B
+from gemms_linear_layers_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tg_gemm_fwd", "tg_gemm_dgrad", "tg_gemm_wgrad", "tg_lora_down", "tg_lora_up",
+              "tg_lora_grad", "tg_bmm_attn", "tg_workspace_size", "tg_stream_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert n in B.SIGNATURES, n
+    assert lib.tg_version() == 10000
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.tg_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.tg_status_string(99) == b"unknown status"
+
+
+NULL = ctypes.c_void_p(0)
+ODD = ctypes.c_void_p(0x1001)   # never dereferenced: checks fail first
+EVEN = ctypes.c_void_p(0x1000)
+
+
+@pytest.mark.parametrize("fn", ["tg_gemm_fwd", "tg_gemm_dgrad", "tg_gemm_wgrad"])
+def test_layer_products_reject_bad_arguments(lib, fn):
+    f = getattr(lib, fn)
+    # negative size
+    assert f(EVEN, EVEN, EVEN, -1, 8, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert f(EVEN, EVEN, EVEN, 8, 8, 1 << 31, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    # unsupported dtypes: FP32 input; 16-bit output of the other type
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_BF16, B.TG_F16, NULL, 0, NULL) == 2
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, 7, B.TG_F32, NULL, 0, NULL) == 2
+    # NULL operand with a non-empty tensor
+    assert f(NULL, EVEN, EVEN, 8, 8, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    # pointer not aligned to its element
+    assert f(ODD, EVEN, EVEN, 8, 8, 8, B.TG_F16, B.TG_F16, NULL, 0, NULL) == 3
+    assert f(EVEN, EVEN, ctypes.c_void_p(0x1002), 8, 8, 8, B.TG_F16, B.TG_F32, NULL, 0, NULL) == 3
+
+
+def test_lora_and_attention_reject_bad_arguments(lib):
+    assert lib.tg_lora_down(EVEN, EVEN, EVEN, 8, -8, 16, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert lib.tg_lora_up(EVEN, EVEN, EVEN, 8, 8, 16, B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
+    assert lib.tg_lora_grad(EVEN, EVEN, EVEN, EVEN, NULL, EVEN, EVEN, EVEN, NULL, 8, 8, 8, 16,
+                            B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert lib.tg_bmm_attn(0, EVEN, EVEN, EVEN, 2, -4, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert lib.tg_bmm_attn(9, EVEN, EVEN, EVEN, 2, 4, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert lib.tg_wait_probe(0, NULL) == 1
+    assert lib.tg_wait_probe(10 ** 8, NULL) == 1
+    assert lib.tg_workspace_size(0, 8, 8, 8, 0, B.TG_F32, B.TG_F32) == B.SIZE_MAX
+    assert lib.tg_workspace_size(0, -8, 8, 8, 0, B.TG_BF16, B.TG_F32) == B.SIZE_MAX
+
+
+def test_tile_table_reader(lib, tmp_path):
+    good = tmp_path / "t.txt"
+    good.write_text("# op in out M N K batch bn splits\n"
+                    "fwd bf16 bf16 2048 576 576 1 192 1\n"
+                    "tn f16 f32 2304 2304 4096 1 256 2   # trailing comment\n\n")
+    assert lib.tg_load_table(str(good).encode()) == 0
+    bad = tmp_path / "bad.txt"
+    bad.write_text("fwd bf16 bf16 2048 576\n")
+    assert lib.tg_load_table(str(bad).encode()) == 7
+    bad.write_text("fwd bf16 bf16 2048 576 576 1 100 1\n")  # tile width not offered
+    assert lib.tg_load_table(str(bad).encode()) == 7
+    bad.write_text("xyz bf16 bf16 2048 576 576 1 128 1\n")
+    assert lib.tg_load_table(str(bad).encode()) == 7
+    assert lib.tg_load_table(str(tmp_path / "missing.txt").encode()) == 7
+    assert lib.tg_load_table(None) == 0
+    # the committed table parses
+    committed = os.path.join(ROOT, "gemms_linear_layers_gb300", "tables", "gb300.txt")
+    if os.path.exists(committed):
+        assert lib.tg_load_table(committed.encode()) == 0
+        assert lib.tg_load_table(None) == 0
+
+
+def test_last_call_buffer(lib):
+    buf = ctypes.create_string_buffer(4)
+    n = lib.tg_last_call(buf, 4)
+    assert n >= 0 and len(buf.value) <= 3

@@ -1,0 +1,107 @@
+"""GPU parity of the batched attention products and the rank-16 LoRA products.
+
+Page "Twice the training speed on a BC-250 from tuned matrix kernels",
+section "Tuning the kernels" (the rank-16 LoRA matrices and the batched
+products inside attention) and section "Checking the results are right"
+(batched attention checked against a float64 CPU product).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemms_linear_layers_gb300 import _binding as tg
+from gemms_linear_layers_gb300 import inputs, workloads
+from parity import assert_close, gather, sample_coords
+
+pytestmark = pytest.mark.gpu
+DT16 = (torch.bfloat16, torch.float16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gemms_linear_layers_gb300 import build
+    build.build()
+    assert tg.tg_load_table(None) == 0
+
+
+# --------------------------------------------------------------- attention
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("op", oracle.ATTN_OPS)
+@pytest.mark.parametrize("hsd", [(3, 256, 64), (2, 200, 64), (1, 136, 16)], ids=lambda t: "x".join(map(str, t)))
+def test_attention_small(hsd, op, dtype, out_kind):
+    h, s, d = hsd
+    t = inputs.attn_inputs(h, s, d, dtype, tag="small")
+    a, b = inputs.ATTN_OPERANDS[op]
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    got = tg.tg_bmm_attn(op, t[a].cuda(), t[b].cuda(), out_dtype=out_dtype)
+    C, S = oracle.bmm_attn(op, t[a], t[b])
+    assert_close(got, C, S, f"attn {op} {hsd} [{tg.tg_last_call()}]", out_dtype)
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("s", workloads.ATTENTION["s"])
+def test_attention_full_size(s, dtype):
+    """36 heads, head_dim 64: all six products, sampled against the oracle."""
+    if s == 4096 and dtype == torch.float16:
+        pytest.skip("s=4096 checked in bf16")
+    h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
+    t = inputs.attn_inputs(h, s, d, dtype, tag="attn")
+    dev = {k: v.cuda() for k, v in t.items()}
+    for op in oracle.ATTN_OPS:
+        a, b = inputs.ATTN_OPERANDS[op]
+        got = tg.tg_bmm_attn(op, dev[a], dev[b])
+        M, N = (s, s) if op in ("qk", "do_vt") else (s, d)
+        co = sample_coords(M, N, batch=h, rows=16, cols=16, rand=2048, seed=s)
+        C, S = oracle.bmm_attn(op, t[a], t[b], sample=co)
+        assert_close(gather(got, co), C, S, f"attn {op} s={s} [{tg.tg_last_call()}]", dtype)
+        del got
+
+
+# -------------------------------------------------------------------- LoRA
+def lora_check(T, d_in, d_out, r, dtype, out_dtype, tag):
+    X, A, B, H, dY = inputs.lora_inputs(T, d_in, d_out, r, dtype, tag=tag)
+    Xc, Ac, Bc, Hc, dYc = (t.cuda() for t in (X, A, B, H, dY))
+    h = tg.tg_lora_down(Xc, Ac, out_dtype=out_dtype)
+    C, S = oracle.lora_down(X, A)
+    assert_close(h, C, S, f"lora_down {T}x{d_in} r={r} [{tg.tg_last_call()}]", out_dtype)
+    y = tg.tg_lora_up(Hc, Bc, out_dtype=out_dtype)
+    C, S = oracle.lora_up(H, B)
+    assert_close(y, C, S, f"lora_up {T}x{d_out} r={r} [{tg.tg_last_call()}]", out_dtype)
+    g = tg.tg_lora_grad(Xc, Ac, Bc, Hc, dYc, out_dtype=out_dtype, want_dH=True)
+    torch.cuda.synchronize()
+    ref = oracle.lora_grad(X, A, B, H, dY)
+    assert_close(g["dH"], *ref["dH"], f"lora dH {T} {d_in}->{d_out} [{tg.tg_last_call()}]", None)
+    for name in ("dB", "dA", "dX"):
+        assert_close(g[name], *ref[name], f"lora {name} {T} {d_in}->{d_out} [{tg.tg_last_call()}]", out_dtype)
+    # without the optional dH output the results are the same bits
+    g2 = tg.tg_lora_grad(Xc, Ac, Bc, Hc, dYc, out_dtype=out_dtype)
+    for name in ("dA", "dB", "dX"):
+        assert torch.equal(g[name], g2[name]), name
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("shape", [(256, 128, 192, 16), (200, 72, 40, 16), (130, 264, 136, 16),
+                                   (64, 64, 64, 8), (33, 24, 40, 4)], ids=lambda t: "x".join(map(str, t)))
+def test_lora_small(shape, dtype, out_kind):
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    lora_check(*shape, dtype, out_dtype, tag="small")
+
+
+@pytest.mark.parametrize("layer", [("q", 2304, 2304), ("gate", 2304, 5760), ("down", 5760, 2304)],
+                         ids=lambda l: l[0])
+def test_lora_2b_T4096(layer):
+    """Rank-16 LoRA on the 2B-class projections at 4,096 tokens, bf16: full check."""
+    _, d_in, d_out = layer
+    lora_check(workloads.LORA_2B["T"], d_in, d_out, 16, torch.bfloat16, torch.bfloat16, tag="lora2b")
+
+
+def test_lora_grad_deterministic():
+    T, d_in, d_out, r = 4096, 2304, 5760, 16
+    t = [x.cuda() for x in inputs.lora_inputs(T, d_in, d_out, r, torch.bfloat16, tag="det")]
+    a = tg.tg_lora_grad(*t, out_dtype=torch.float32, want_dH=True)
+    b = tg.tg_lora_grad(*t, out_dtype=torch.float32, want_dH=True)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
