@@ -136,14 +136,18 @@ class Product:
         return f"{self.layer}.{self.op}.{str(self.dtype)[6:]}"
 
 
-def build_step(device):
-    """Inputs, outputs and workspaces of every product of the step, on the device."""
+def build_step(device, only=None):
+    """Inputs, outputs and workspaces of every product of the step (or of the
+    products named in `only`), on the device."""
     from gemms_linear_layers_gb300 import _binding as tg
     cfg = workloads.DECODER_135M
     T = cfg["T"]
     prods, tensors = [], {}
     for dtype in cfg["dtypes"]:
         for layer, d_in, d_out in cfg["layers"]:
+            names = [Product(layer, op, dtype, T, d_in, d_out).name for op in ("fwd", "dgrad", "wgrad")]
+            if only and not any(n in only for n in names):
+                continue
             X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="bench", device=device)
             tensors[(layer, dtype)] = {
                 "X": X, "W": W, "dY": dY,
@@ -152,6 +156,8 @@ def build_step(device):
                 "dW": torch.empty(d_out, d_in, dtype=dtype, device=device)}
             for op in ("fwd", "dgrad", "wgrad"):
                 p = Product(layer, op, dtype, T, d_in, d_out)
+                if only and p.name not in only:
+                    continue
                 opcode = {"fwd": tg.TG_OP_GEMM_FWD, "dgrad": tg.TG_OP_GEMM_DGRAD, "wgrad": tg.TG_OP_GEMM_WGRAD}[op]
                 n = tg.tg_workspace_size(opcode, T, d_out, d_in, 0, dtype, dtype)
                 p.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
@@ -475,6 +481,9 @@ def main():
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
     ap.add_argument("--no-rows", action="store_true", help="skip the per-product rows of the other sets")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--only", default=None,
+                    help="comma-separated products to run, e.g. head.wgrad.bfloat16 (profiling a single kernel)")
     ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -490,13 +499,15 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from gemms_linear_layers_gb300 import _binding as tg
-    tg.tg_load_table(None)
-    table = os.path.join(ROOT, "gemms_linear_layers_gb300", "tables", "gb300.txt")
-    if os.path.exists(table) and not os.environ.get("TG_TABLE"):
-        assert tg.tg_load_table(table) == 0
+    # the library loads its shipped tile table (or $TG_TABLE) at first use
+    table = os.environ.get("TG_TABLE", tg.DEFAULT_TABLE)
+    table = table if table and os.path.exists(table) else None
     pk = peaks()
     stream = torch.cuda.Stream()
-    prods = build_step("cuda")
+    only = set(args.only.split(",")) if args.only else None
+    prods = build_step("cuda", only)
+    if not prods:
+        raise SystemExit(f"--only {args.only}: no such product")
     capture(prods, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step_flops = sum(p.flops for p in prods)
@@ -541,7 +552,9 @@ def main():
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": 2048, "products_per_step": len(prods),
+            "config": {"workload": WORKLOAD if not only else f"{WORKLOAD}; only {sorted(only)}", "T": 2048,
+                       "products_per_step": len(prods),
+                       "tile_table": os.path.relpath(table, ROOT) if table else None,
                        "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
                        "l2": "flushed before every step (256 MiB write, untimed)",
                        "timing": "CUDA events around each product's captured graph, summed over the step"},
@@ -549,11 +562,12 @@ def main():
             "per_kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in by_kernel.items()}}
 
     if rank == 0:
-        e2e_n = min(args.steps, 5)
-        ms, h2d, d2h = e2e_steps(prods, e2e_n, stream)
-        line["e2e"] = {"value": round(step_flops * e2e_n / (ms / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(ms / e2e_n, 3)}
+        if not args.no_e2e:
+            e2e_n = min(args.steps, 5)
+            ms, h2d, d2h = e2e_steps(prods, e2e_n, stream)
+            line["e2e"] = {"value": round(step_flops * e2e_n / (ms / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                           "ms_per_step": round(ms / e2e_n, 3)}
         if world == 1 and not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline()
         if not args.no_rows:

@@ -16,6 +16,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtg.so")
+DEFAULT_TABLE = os.path.join(_PKG, "tables", "gb300.txt")
 _lock = threading.Lock()
 _lib = None
 

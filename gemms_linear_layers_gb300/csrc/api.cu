@@ -2,6 +2,7 @@
 // per-device context (SM count, status word, wait limit), the shape-keyed
 // tile table and the dispatch of every product onto its kernels.
 #include <cuda_runtime.h>
+#include <dlfcn.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -115,7 +116,7 @@ struct TableKeyHash {
   }
 };
 struct TableVal {
-  int bn, splits;
+  int bn, splits, raster;  // raster: -1 = by operand size, 0 = along M, 1 = along N
 };
 static std::shared_mutex g_table_mu;
 static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
@@ -150,10 +151,17 @@ static tg_status load_table_file(const char* path) {
       int bn, splits;
       if (!(ss >> op)) continue;  // blank line
       if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> splits)) return TG_ERR_TABLE;
+      std::string rs;
+      int raster = -1;
+      if (ss >> rs) {
+        if (rs == "m") raster = 0;
+        else if (rs == "n") raster = 1;
+        else if (rs != "auto") return TG_ERR_TABLE;
+      }
       const int l = parse_layout(op), i = parse_dtype(din), o = parse_dtype(dout);
       if (l < 0 || i < 0 || o < 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return TG_ERR_TABLE;
       if (!(bn == 64 || bn == 128 || bn == 192 || bn == 256) || splits < 1 || splits > 64) return TG_ERR_TABLE;
-      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits};
+      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster};
     }
   }
   std::unique_lock<std::shared_mutex> lk(g_table_mu);
@@ -161,9 +169,22 @@ static tg_status load_table_file(const char* path) {
   return TG_OK;
 }
 
+// At first use: $TG_TABLE if set (empty = no table), else the table shipped
+// next to the library (tables/gb300.txt beside libtg.so), if present.
 static void table_env_init() {
   std::call_once(g_table_env_once, [] {
-    if (const char* p = getenv("TG_TABLE")) load_table_file(p);
+    if (const char* p = getenv("TG_TABLE")) {
+      load_table_file(p);
+      return;
+    }
+    Dl_info info;
+    if (dladdr(reinterpret_cast<void*>(&table_env_init), &info) && info.dli_fname) {
+      std::string path(info.dli_fname);
+      const size_t slash = path.rfind('/');
+      path = (slash == std::string::npos ? std::string(".") : path.substr(0, slash)) + "/tables/gb300.txt";
+      std::ifstream f(path);
+      if (f.good()) load_table_file(path.c_str());
+    }
   });
 }
 
@@ -180,6 +201,7 @@ static bool table_lookup(const TableKey& k, TableVal* v) {
 struct Plan {
   int bn = 256;
   int splits = 1;
+  int raster_n = 0;
   bool from_table = false;
 };
 
@@ -216,6 +238,11 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
   return best;
 }
 
+// Raster: consecutive units should share the operand that would otherwise be
+// re-read from HBM, so walk along N (sharing A tiles) when A is the larger
+// operand and along M (sharing B tiles) otherwise.
+static int auto_raster(int64_t M, int64_t N, int64_t K) { return M * K > N * K ? 1 : 0; }
+
 static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in,
                       tg_dtype out, int sms) {
   TableVal v;
@@ -226,10 +253,13 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
     const int64_t s = v.splits < kb ? v.splits : kb;
     const int64_t kps = cdiv(kb, s);
     p.splits = static_cast<int>(cdiv(kb, kps));
+    p.raster_n = v.raster >= 0 ? v.raster : auto_raster(M, N, K);
     p.from_table = true;
     return p;
   }
-  return heuristic_plan(M, N, K, batch, out == TG_F32 ? 4 : 2, sms);
+  Plan p = heuristic_plan(M, N, K, batch, out == TG_F32 ? 4 : 2, sms);
+  p.raster_n = auto_raster(M, N, K);
+  return p;
 }
 
 static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t batch) {
@@ -306,6 +336,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.b_bstride = g.b_bs;
     t.bn = p.bn;
     t.splits = p.splits;
+    t.raster_n = p.raster_n;
     t.ws = g.ws;
     t.grid = ctx->sms;
     t.stream = g.stream;
@@ -317,9 +348,10 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     if (e == cudaSuccess && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
                                g.stream);
-    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d splits=%d table=%s %s", g.name,
-             layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch, p.bn,
-             p.splits, p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d splits=%d raster=%c table=%s %s",
+             g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
+             p.bn, p.splits, p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss",
+             e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }
@@ -526,6 +558,18 @@ tg_status tg_bmm_attn(tg_attn_op op, const void* A, const void* B, void* C, int6
 }
 
 // ------------------------------------------------------------------ LoRA
+// Rank 16 with 16-byte-aligned rows takes the streaming kernels (lora.cu);
+// anything else is composed from the general products.
+static bool lora_stream_ok(int64_t r, std::initializer_list<int64_t> widths,
+                           std::initializer_list<const void*> ptrs16) {
+  if (r != 16) return false;
+  for (int64_t w : widths)
+    if (w % 8 != 0 || w > (int64_t(1) << 30)) return false;
+  for (const void* p : ptrs16)
+    if (p != nullptr && !aligned(p, 16)) return false;
+  return true;
+}
+
 tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t d_in, int64_t r, tg_dtype in,
                        tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
   TG_TRY(check_common(in, out, {T, d_in, r}));
@@ -534,8 +578,26 @@ tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t
   TG_TRY(check_ptr(H, T * r, dt_bytes(out)));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
-  GemmCall g{LAYOUT_NT, X, A, H, 1, T, r, d_in, d_in, d_in, T * d_in, r * d_in, in, out, -1, ws, ws_bytes,
-             static_cast<cudaStream_t>(stream), "lora_down"};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_in > 0 && lora_stream_ok(r, {d_in}, {X, A})) {
+    LoraArgs a{};
+    a.X = X;
+    a.A = A;
+    a.out = H;
+    a.T = T;
+    a.d_in = d_in;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    cudaError_t e = lora_down_launch(a);
+    record(std::string("lora_down stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  GemmCall g{LAYOUT_NT, X, A, H, 1, T, r, d_in, d_in, d_in, T * d_in, r * d_in, in, out, -1, ws, ws_bytes, st,
+             "lora_down"};
   return run_gemm(g, ctx);
 }
 
@@ -547,19 +609,38 @@ tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d
   TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
-  GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, ws, ws_bytes,
-             static_cast<cudaStream_t>(stream), "lora_up"};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_out > 0 && lora_stream_ok(r, {d_out}, {H, B, Y})) {
+    LoraArgs a{};
+    a.H = H;
+    a.B = B;
+    a.out = Y;
+    a.T = T;
+    a.d_out = d_out;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    cudaError_t e = lora_up_launch(a);
+    record(std::string("lora_up stream T=") + std::to_string(T) + " d_out=" + std::to_string(d_out) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, ws, ws_bytes, st,
+             "lora_up"};
   return run_gemm(g, ctx);
 }
 
-// workspace plan of the composed LoRA gradient: [dH f32 (if not given)] [sub-GEMM ws]
-static size_t lora_grad_sub_ws(int64_t T, int64_t d_in, int64_t d_out, int64_t r, tg_dtype in, tg_dtype out,
-                               int sms) {
+// workspace of the composed LoRA gradient: [dH f32 (if not given)] [sub-GEMM ws]
+static size_t lora_grad_generic_ws(int64_t T, int64_t d_in, int64_t d_out, int64_t r, tg_dtype in, tg_dtype out,
+                                   int sms) {
   // dH = dY . B and dB = dY^T . H run one after the other and share the space
   const size_t a = gemm_ws_bytes(LAYOUT_NN, T, r, d_out, 1, in, TG_F32, sms);
   const size_t b = gemm_ws_bytes(LAYOUT_TN, d_out, r, T, 1, in, out, sms);
   (void)d_in;
-  return a > b ? a : b;
+  const size_t dh = (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
+  return dh + (a > b ? a : b);
 }
 
 tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
@@ -578,8 +659,40 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_in > 0 && d_out > 0 && lora_stream_ok(r, {d_in, d_out}, {X, dY, dX, dH_f32, H})) {
+    const size_t need = lora_grad_ws_bytes(T, d_in, d_out, r, ctx->sms);
+    if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
+      record("lora_grad stream: workspace too small");
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    LoraArgs a{};
+    a.X = X;
+    a.A = A;
+    a.B = B;
+    a.H = H;
+    a.dY = dY;
+    a.out = dA;
+    a.out2 = dB;
+    a.out3 = dX;
+    a.out4 = dH_f32;
+    a.ws = static_cast<float*>(ws);
+    a.T = T;
+    a.d_in = d_in;
+    a.d_out = d_out;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    cudaError_t e = lora_grad_launch(a);
+    record(std::string("lora_grad stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) +
+           " d_out=" + std::to_string(d_out) + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  // general composition (any rank, any alignment)
   const size_t dh_bytes = dH_f32 ? 0 : (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
-  const size_t sub = lora_grad_sub_ws(T, d_in, d_out, r, in, out, ctx->sms);
+  const size_t total = lora_grad_generic_ws(T, d_in, d_out, r, in, out, ctx->sms);
+  const size_t sub = total - (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
   if (dh_bytes + sub > 0 && (ws == nullptr || ws_bytes < dh_bytes + sub || !aligned(ws, 256)))
     return TG_ERR_WORKSPACE_TOO_SMALL;
   float* dH = dH_f32 ? dH_f32 : static_cast<float*>(ws);
@@ -610,11 +723,14 @@ size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d
     case TG_OP_GEMM_FWD: return gemm_ws_bytes(LAYOUT_NT, d0, d1, d2, 1, in, out, ctx->sms);
     case TG_OP_GEMM_DGRAD: return gemm_ws_bytes(LAYOUT_NN, d0, d2, d1, 1, in, out, ctx->sms);
     case TG_OP_GEMM_WGRAD: return gemm_ws_bytes(LAYOUT_TN, d1, d2, d0, 1, in, out, ctx->sms);
+    // LoRA: the larger of the streaming and the general requirement (the
+    // choice between them also depends on pointer alignment)
     case TG_OP_LORA_DOWN: return gemm_ws_bytes(LAYOUT_NT, d0, d2, d1, 1, in, out, ctx->sms);
     case TG_OP_LORA_UP: return gemm_ws_bytes(LAYOUT_NT, d0, d1, d2, 1, in, out, ctx->sms);
     case TG_OP_LORA_GRAD: {
-      const size_t dh = (static_cast<size_t>(d0 * d3 * 4) + 255) / 256 * 256;
-      return dh + lora_grad_sub_ws(d0, d1, d2, d3, in, out, ctx->sms);
+      const size_t a = lora_grad_generic_ws(d0, d1, d2, d3, in, out, ctx->sms);
+      const size_t b = d3 == 16 ? lora_grad_ws_bytes(d0, d1, d2, d3, ctx->sms) : 0;
+      return a > b ? a : b;
     }
     case TG_OP_BMM_ATTN: {
       GemmCall g;

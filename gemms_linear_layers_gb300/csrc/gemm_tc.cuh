@@ -56,6 +56,7 @@ struct TcArgs {
   int units;     // batch * m_tiles * n_tiles * splits
   uint32_t idesc;
   int out_f16;   // 16-bit output type: 1 = fp16, 0 = bf16
+  int raster_n;  // 1: consecutive units walk along N (they share the A tile)
   unsigned long long timeout_ns;
   unsigned int* status;
 };
@@ -72,8 +73,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcArgs& a) {
   const int tiles = a.m_tiles * a.n_tiles;
   c.b = t / tiles;
   const int r = t - c.b * tiles;
-  c.m0 = (r % a.m_tiles) * TC_BM;  // consecutive units walk down M: they share B
-  c.n0 = (r / a.m_tiles) * BN;
+  if (a.raster_n) {  // consecutive units walk along N: they share the A tile
+    c.n0 = (r % a.n_tiles) * BN;
+    c.m0 = (r / a.n_tiles) * TC_BM;
+  } else {           // consecutive units walk down M: they share the B tile
+    c.m0 = (r % a.m_tiles) * TC_BM;
+    c.n0 = (r / a.m_tiles) * BN;
+  }
   c.kb0 = c.split * a.kps;
   c.kb1 = min(a.kb_total, c.kb0 + a.kps);
   return c;

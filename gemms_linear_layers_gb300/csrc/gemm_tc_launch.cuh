@@ -58,6 +58,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * g.splits;
   a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC_BM, BN);
   a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
+  a.raster_n = g.raster_n;
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
   const int grid = g.grid < a.units ? g.grid : a.units;

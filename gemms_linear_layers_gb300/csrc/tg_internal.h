@@ -39,6 +39,7 @@ struct TcGemm {
   int64_t a_bstride, b_bstride;  // batch strides in elements
   int bn;                     // tile width: 64, 128, 192 or 256
   int splits;                 // >1: FP32 partials to ws, then an ordered reduction
+  int raster_n;               // 1: walk output tiles along N first (A tiles reused)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;

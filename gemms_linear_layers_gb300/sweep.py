@@ -1,0 +1,185 @@
+"""On-device sweep that fills the shape-keyed tile table (tables/gb300.txt).
+
+The analogue of the page's tuning run ("Twice the training speed on a BC-250
+from tuned matrix kernels", section "Tuning the kernels": benchmark a set of
+kernel designs for the list of sizes training uses and keep the winners in a
+file the library reads; section "What got in the way": the winners must be
+looked up with the same key they were stored under, and the speed-up has to
+be confirmed through the normal call path).  Here a design is (tile width,
+split count, raster order) of the tensor-core kernel; each candidate is timed
+through the public entry point with a one-line table that forces it, and the
+fastest per shape is written with the same key the library looks up.
+
+Usage (on the GPU): python -m gemms_linear_layers_gb300.sweep [--out PATH] [--sets 2b,135m,attn]
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import statistics
+import sys
+import tempfile
+import time
+
+import torch
+
+from . import _binding as tg
+from . import inputs, workloads
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+DEFAULT_OUT = os.path.join(HERE, "tables", "gb300.txt")
+BNS = (64, 128, 192, 256)
+SPLITS = (1, 2, 3, 4, 6, 8, 12, 16)
+
+
+def shapes(sets):
+    """(layout, M, N, K, batch, make_call) for every distinct product."""
+    out = []
+    seen = set()
+
+    def add(key, make):
+        if key not in seen:
+            seen.add(key)
+            out.append((*key, make))
+
+    if "2b" in sets or "135m" in sets:
+        groups = []
+        if "135m" in sets:
+            groups.append((workloads.DECODER_135M["T"], workloads.LAYERS_135M))
+        if "2b" in sets:
+            for T in workloads.DECODER_2B["T"]:
+                groups.append((T, workloads.LAYERS_2B))
+        for T, layers in groups:
+            for _, d_in, d_out in layers:
+                add(("nt", T, d_out, d_in, 1), lambda T=T, a=d_in, b=d_out: layer_call("fwd", T, a, b))
+                add(("nn", T, d_in, d_out, 1), lambda T=T, a=d_in, b=d_out: layer_call("dgrad", T, a, b))
+                add(("tn", d_out, d_in, T, 1), lambda T=T, a=d_in, b=d_out: layer_call("wgrad", T, a, b))
+    if "attn" in sets:
+        h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
+        for s in workloads.ATTENTION["s"]:
+            add(("nt", s, s, d, h), lambda s=s: attn_call("qk", h, s, d))
+            add(("nn", s, d, s, h), lambda s=s: attn_call("pv", h, s, d))
+            add(("tn", s, d, s, h), lambda s=s: attn_call("pt_do", h, s, d))
+    return out
+
+
+def layer_call(op, T, d_in, d_out, dtype=torch.bfloat16):
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="sweep", device="cuda")
+    ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
+    if op == "fwd":
+        Y = torch.empty(T, d_out, dtype=dtype, device="cuda")
+        return lambda: tg.tg_gemm_fwd(X, W, Y=Y, ws=ws)
+    if op == "dgrad":
+        dX = torch.empty(T, d_in, dtype=dtype, device="cuda")
+        return lambda: tg.tg_gemm_dgrad(dY, W, dX=dX, ws=ws)
+    dW = torch.empty(d_out, d_in, dtype=dtype, device="cuda")
+    return lambda: tg.tg_gemm_wgrad(dY, X, dW=dW, ws=ws)
+
+
+def attn_call(op, h, s, d, dtype=torch.bfloat16):
+    t = inputs.attn_inputs(h, s, d, dtype, tag="sweep", device="cuda")
+    a, b = inputs.ATTN_OPERANDS[op]
+    C = torch.empty(h, s, s if op in ("qk", "do_vt") else d, dtype=dtype, device="cuda")
+    ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
+    return lambda: tg.tg_bmm_attn(op, t[a], t[b], C=C, ws=ws)
+
+
+def time_call(call, stream, reps):
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            call()
+    res = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b) / reps)
+    return statistics.median(res)
+
+
+def candidates(M, N, K, batch, sms):
+    kb = -(-K // 64)
+    for bn in BNS:
+        tiles = batch * -(-M // 128) * -(-N // bn)
+        for s in SPLITS:
+            if s > kb:
+                break
+            kps = -(-kb // s)
+            if -(-kb // kps) != s:
+                continue
+            if s > 1 and tiles * s > 8 * sms:
+                continue
+            for raster in ("m", "n"):
+                yield bn, s, raster
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=DEFAULT_OUT)
+    ap.add_argument("--sets", default="2b,135m,attn")
+    ap.add_argument("--budget-s", type=float, default=900.0)
+    args = ap.parse_args(argv)
+    sets = set(args.sets.split(","))
+    stream = torch.cuda.Stream()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    name = torch.cuda.get_device_name(0)
+    t0 = time.time()
+    lines = []
+    tmpdir = tempfile.mkdtemp()
+    for layout, M, N, K, batch, make in shapes(sets):
+        if time.time() - t0 > args.budget_s:
+            print(f"budget exhausted before {layout} {M}x{N}x{K}x{batch}", flush=True)
+            break
+        call = make()
+        flops = 2 * M * N * K * batch
+        reps = max(3, min(50, int(2e13 / max(flops, 1))))
+        # the heuristic's own choice, for the record
+        tg.tg_load_table(None)
+        base_ms = time_call(call, stream, reps)
+        base_plan = tg.tg_last_call()
+        best = None
+        for bn, s, raster in candidates(M, N, K, batch, sms):
+            path = os.path.join(tmpdir, "one.txt")
+            with open(path, "w") as f:
+                f.write(f"{layout} bf16 bf16 {M} {N} {K} {batch} {bn} {s} {raster}\n")
+            assert tg.tg_load_table(path) == 0
+            try:
+                ms = time_call(call, stream, reps)
+            except Exception as e:  # a candidate that cannot run (e.g. workspace) is skipped
+                print(f"  skip bn={bn} s={s} {raster}: {e}", flush=True)
+                continue
+            plan = tg.tg_last_call()
+            assert "table=hit" in plan, plan
+            if best is None or ms < best[0]:
+                best = (ms, bn, s, raster)
+        tg.tg_load_table(None)
+        ms, bn, s, raster = best
+        tf = flops / ms / 1e9
+        print(f"{layout} {M}x{N}x{K}x{batch}: best bn={bn} splits={s} raster={raster} {ms * 1e3:.1f} us "
+              f"{tf:.0f} TFLOP/s (heuristic {base_ms * 1e3:.1f} us: {base_plan})", flush=True)
+        for din in ("bf16", "f16"):
+            for dout in (din, "f32"):
+                lines.append(f"{layout} {din} {dout} {M} {N} {K} {batch} {bn} {s} {raster}"
+                             f"   # {ms * 1e3:.1f} us, {tf:.0f} TFLOP/s")
+        del call
+        torch.cuda.empty_cache()
+    os.makedirs(os.path.dirname(args.out), exist_ok=True)
+    with open(args.out, "w") as f:
+        f.write("# tile table for the tensor-core kernel: op in out M N K batch bn splits raster\n")
+        f.write(f"# written by `python -m gemms_linear_layers_gb300.sweep --sets {args.sets}` on {name} "
+                f"({sms} SMs); timings are bf16 and apply to fp16 and FP32 outputs too\n")
+        for l in lines:
+            f.write(l + "\n")
+    print(f"wrote {len(lines)} entries to {args.out} in {time.time() - t0:.0f} s", flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -149,9 +149,13 @@ const char* tg_status_string(tg_status s);
 
 /* Load a tile table (the analogue of tuned logic files; section "Tuning the
  * kernels").  Lines: "op dtype_in dtype_out M N K batch bn splits", where op
- * is fwd|dgrad|wgrad|attn_nt|attn_nn|attn_tn and M N K are the GEMM's own
- * output rows, output columns and reduction length.  Replaces any table
- * loaded before; NULL or "" clears it.  $TG_TABLE is read at first use. */
+ * is nt|nn|tn (also accepted: fwd|dgrad|wgrad) -- the operand layout of the
+ * product; attention products use the layout of theirs -- and M N K are the
+ * product's own output rows, output columns and reduction length; an
+ * optional tenth field m|n|auto sets the order in which output tiles are
+ * visited.  Replaces any table loaded before; NULL or "" clears it.  At first
+ * use the library loads $TG_TABLE if set (empty: none), else the table
+ * shipped beside libtg.so (tables/gb300.txt) if present. */
 tg_status tg_load_table(const char* path);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

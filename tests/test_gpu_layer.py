@@ -6,6 +6,8 @@ products, each in its own layout) and section "Checking the results are
 right" (shapes from 1x1x1 up to training sizes, each against a float64 CPU
 product).  Every call goes through the C ABI via the ctypes binding.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -25,7 +27,8 @@ def _lib():
     from gemms_linear_layers_gb300 import build
     build.build()
     tg.lib()
-    assert tg.tg_load_table(None) == 0
+    # the table the library ships (the launch configuration bench.py times)
+    assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
 
 
 def run(op, X, W, dY, out_dtype):
@@ -212,3 +215,21 @@ def test_table_entry_is_used(tmp_path):
         assert tg.tg_load_table(None) == 0
     check_full("fwd", T, d_in, d_out, torch.bfloat16, torch.bfloat16, tag="table")
     assert "table=miss" in tg.tg_last_call()
+    assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_heuristic_plans_without_table(op):
+    """Shapes of the layer sets with no table loaded: the cost-model plans."""
+    assert tg.tg_load_table(None) == 0
+    try:
+        for T, d_in, d_out in ((2048, 576, 49152), (1024, 2304, 5760)):
+            X, W, dY = inputs.layer_inputs(T, d_in, d_out, torch.bfloat16, tag="heur")
+            got = run(op, X.cuda(), W.cuda(), dY.cuda(), torch.bfloat16)
+            assert "table=miss" in tg.tg_last_call()
+            M, N = out_shape(op, T, d_in, d_out)
+            co = sample_coords(M, N, rows=16, cols=16, rand=2048, seed=7)
+            C, S = ref(op, X, W, dY, sample=co)
+            assert_close(gather(got, co), C, S, f"{op} heuristic [{tg.tg_last_call()}]", torch.bfloat16)
+    finally:
+        assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
