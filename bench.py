@@ -205,10 +205,75 @@ def capture(prods, stream):
     torch.cuda.synchronize()
 
 
-def timed_steps(prods, n_warm, n_steps, stream, flush):
-    """Per step: flush L2 (untimed), then every product between events."""
-    per_step = []
+def probe_products(prods, stream, flush, reps=2):
+    """Untimed pass: each product's own graph between events, to find the
+    kernel identity with the largest share of the step."""
     per_prod = {p.name: 0.0 for p in prods}
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush.add_(1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(prods) + 1)]
+            ev[0].record(stream)
+            for i, p in enumerate(prods):
+                p.graph.replay()
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            for i, p in enumerate(prods):
+                per_prod[p.name] += ev[i].elapsed_time(ev[i + 1]) / reps
+    return per_prod
+
+
+def external_event():
+    """A timing event that becomes an event-record node when captured."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def capture_step(prods, stream, dominant):
+    """One graph for the whole step.  External events mark the step's start
+    and end and bracket every launch of the dominant kernel."""
+    e0, e1 = external_event(), external_event()
+    if e0 is None:
+        return None
+    marks = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        e0.record()
+        for p in prods:
+            if p.kernel == dominant:
+                a, b = external_event(), external_event()
+                a.record()
+                run_product(p)
+                b.record()
+                marks.append((p, a, b))
+            else:
+                run_product(p)
+        e1.record()
+    torch.cuda.synchronize()
+    return g, e0, e1, marks
+
+
+def timed_steps(step, n_warm, n_steps, stream, flush):
+    """Per step: flush L2 (untimed), replay the step graph, read its events."""
+    g, e0, e1, marks = step
+    total_ms, dom_ms = 0.0, 0.0
+    for s in range(n_warm + n_steps):
+        with torch.cuda.stream(stream):
+            flush.add_(1)
+            g.replay()
+        torch.cuda.synchronize()
+        if s >= n_warm:
+            total_ms += e0.elapsed_time(e1)
+            dom_ms += sum(a.elapsed_time(b) for _, a, b in marks)
+    return total_ms, dom_ms
+
+
+def timed_steps_per_product(prods, n_warm, n_steps, stream, flush, dominant):
+    """Fallback when events cannot be captured: each product's own graph,
+    events between them on the launching stream."""
+    total_ms, dom_ms = 0.0, 0.0
     with torch.cuda.stream(stream):
         for s in range(n_warm + n_steps):
             flush.add_(1)
@@ -217,15 +282,11 @@ def timed_steps(prods, n_warm, n_steps, stream, flush):
             for i, p in enumerate(prods):
                 p.graph.replay()
                 ev[i + 1].record(stream)
+            torch.cuda.synchronize()
             if s >= n_warm:
-                per_step.append(ev)
-    torch.cuda.synchronize()
-    total_ms = 0.0
-    for ev in per_step:
-        total_ms += ev[0].elapsed_time(ev[-1])
-        for i, p in enumerate(prods):
-            per_prod[p.name] += ev[i].elapsed_time(ev[i + 1])
-    return total_ms, per_prod
+                total_ms += ev[0].elapsed_time(ev[-1])
+                dom_ms += sum(ev[i].elapsed_time(ev[i + 1]) for i, p in enumerate(prods) if p.kernel == dominant)
+    return total_ms, dom_ms
 
 
 # ------------------------------------------------------------------ e2e
@@ -482,6 +543,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-product rows of the other sets")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--per-product-graphs", action="store_true",
+                    help="time with one graph per product instead of one graph per step")
     ap.add_argument("--only", default=None,
                     help="comma-separated products to run, e.g. head.wgrad.bfloat16 (profiling a single kernel)")
     ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
@@ -512,11 +575,28 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step_flops = sum(p.flops for p in prods)
 
+    # untimed probe: per-product times and the dominant kernel identity
+    per_prod = probe_products(prods, stream, flush)
+    by_kernel = {}
+    for p in prods:
+        k = by_kernel.setdefault(p.kernel, {"ms": 0.0, "flops": 0, "n": 0, "products": []})
+        k["ms"] += per_prod[p.name]
+        k["flops"] += p.flops
+        k["n"] += 1
+        k["products"].append(p.name)
+    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+    step = None if args.per_product_graphs else capture_step(prods, stream, dom_name)
+    mode = "one CUDA graph per step; external events inside it bracket the dominant kernel" if step else \
+        "one CUDA graph per product; events between them on the launching stream"
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        total_ms, per_prod = timed_steps(prods, args.warmup, args.steps, stream, flush)
+        if step:
+            total_ms, dom_ms = timed_steps(step, args.warmup, args.steps, stream, flush)
+        else:
+            total_ms, dom_ms = timed_steps_per_product(prods, args.warmup, args.steps, stream, flush, dom_name)
     torch.cuda.synchronize()
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -530,23 +610,15 @@ def main():
     ms_step = total_ms / args.steps
     value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
 
-    # dominant kernel: largest total time, grouped by kernel identity
-    by_kernel = {}
-    for p in prods:
-        k = by_kernel.setdefault(p.kernel, {"ms": 0.0, "flops": 0, "launches": 0, "products": []})
-        k["ms"] += per_prod[p.name]
-        k["flops"] += p.flops * args.steps
-        k["launches"] += args.steps
-        k["products"].append(p.name)
-    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
-    avg_launch_ms = dom["ms"] / dom["launches"]
-    flops_per_launch = dom["flops"] / dom["launches"]
+    dom_launches = dom["n"] * args.steps
+    avg_launch_ms = dom_ms / dom_launches
+    flops_per_launch = dom["flops"] / dom["n"]
     achieved = flops_per_launch / (avg_launch_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
                 "kernel": dom_name, "products": dom["products"],
                 "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
-                "share_of_step": round(dom["ms"] / total_ms, 3)}
+                "share_of_step": round(dom_ms / total_ms, 3)}
 
     launches = sum(p.launches for p in prods) * args.steps
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -557,9 +629,9 @@ def main():
                        "tile_table": os.path.relpath(table, ROOT) if table else None,
                        "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
                        "l2": "flushed before every step (256 MiB write, untimed)",
-                       "timing": "CUDA events around each product's captured graph, summed over the step"},
+                       "timing": mode},
             "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary(),
-            "per_kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in by_kernel.items()}}
+            "per_kernel_ms_per_step_probe": {k: round(v["ms"], 4) for k, v in by_kernel.items()}}
 
     if rank == 0:
         if not args.no_e2e:

@@ -45,6 +45,14 @@ cudaError_t wait_probe_launch(unsigned long long timeout_ns, unsigned int* statu
   return cudaGetLastError();
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("TG_PDL");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
 struct DevCtx {
   bool ready = false;
   tg_status init_status = TG_OK;

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -30,6 +31,8 @@ __device__ __forceinline__ void store_from_float(void* p, int kind, int64_t i, f
 // ---------------------------------------------------------------- split-K
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int out_kind,
                                      int64_t batch, int64_t splits, int64_t MN) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n4 = MN / 4;  // MN is a multiple of 4 on the tensor-core path
   const int64_t total = batch * n4;
   for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
@@ -74,14 +77,16 @@ cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   if (blocks > cap) blocks = cap;
-  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, C, out_kind, batch, splits, MN);
-  return cudaGetLastError();
+  return launch_k(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, ws, C, out_kind,
+                  batch, splits, MN);
 }
 
 // ---------------------------------------------------------------- strided
 constexpr int ST = 16;  // 16 x 16 outputs per block, K staged 16 at a time
 
 __global__ void simt_gemm_kernel(SimtGemm g) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[ST][ST + 1];
   __shared__ float Bs[ST][ST + 1];
   const int64_t b = blockIdx.z;
@@ -111,8 +116,7 @@ cudaError_t simt_gemm_launch(const SimtGemm& g) {
   dim3 grid(static_cast<unsigned>((g.N + ST - 1) / ST), static_cast<unsigned>((g.M + ST - 1) / ST),
             static_cast<unsigned>(g.batch));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-  simt_gemm_kernel<<<grid, block, 0, g.stream>>>(g);
-  return cudaGetLastError();
+  return launch_k(simt_gemm_kernel, grid, block, 0, g.stream, g);
 }
 
 }  // namespace tg

@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const unsigned long long tmo = args.timeout_ns;
+  // the prologue above overlapped the previous kernel; global memory from here
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

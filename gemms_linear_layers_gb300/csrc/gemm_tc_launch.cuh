@@ -62,8 +62,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
   const int grid = g.grid < a.units ? g.grid : a.units;
-  kern<<<grid, TC_THREADS, Cfg::SMEM, g.stream>>>(tmA, tmB, tmC, a);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, a);
 }
 
 template <bool A_MN, bool B_MN>

@@ -388,6 +388,8 @@ __device__ void colred_role(int cta_j, int part, int parts, const uint16_t* __re
 template <bool BF16>
 __global__ void __launch_bounds__(LTHREADS) lora_down_kernel(const uint16_t* X, const uint16_t* A, void* H,
                                                              int out_kind, int T, int d_in) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8 * 16 * 17];
   rowdown_role<BF16>(blockIdx.x, X, A, H, out_kind, T, d_in, red);
 }
@@ -395,12 +397,16 @@ __global__ void __launch_bounds__(LTHREADS) lora_down_kernel(const uint16_t* X, 
 template <bool BF16>
 __global__ void __launch_bounds__(LTHREADS) lora_up_kernel(const uint16_t* H, const uint16_t* B, void* Y,
                                                            int out_kind, int T, int d_out, int n_t) {
+  pdl_wait();
+  pdl_trigger();
   rowup_role<BF16, false>(blockIdx.x, blockIdx.y, n_t, H, B, Y, out_kind, T, d_out);
 }
 
 // prep: Bt[r][o] = B[o][r], At[i][r] = A[r][i]
 __global__ void lora_prep_kernel(const uint16_t* A, const uint16_t* B, uint16_t* At, uint16_t* Bt, int d_in,
                                  int d_out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nA = static_cast<int64_t>(d_in) * LR, nB = static_cast<int64_t>(d_out) * LR;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < nA + nB;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -420,6 +426,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(LTHREADS) lora_grad1_kernel(const uint16_t* dY, const uint16_t* Bt,
                                                               const uint16_t* H, float* dH, float* Pb, int T,
                                                               int d_out, int n_rowdown, int nj_b, int parts_b) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[4 * 64 * 17];
   const int b = blockIdx.x;
   if (b < n_rowdown) {
@@ -437,6 +445,8 @@ __global__ void __launch_bounds__(LTHREADS) lora_grad2_kernel(const uint16_t* X,
                                                               const uint16_t* At, void* dX, int out_kind,
                                                               float* Pa, int T, int d_in, int n_colred, int nj_a,
                                                               int parts_a, int nj_x, int n_tx) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[4 * 64 * 17];
   const int b = blockIdx.x;
   if (b < n_colred) {
@@ -450,6 +460,8 @@ __global__ void __launch_bounds__(LTHREADS) lora_grad2_kernel(const uint16_t* X,
 // pass 3: dB[o][r] = sum_parts Pb ; dA[r][i] = sum_parts Pa[.][i][r] (parts in order)
 __global__ void lora_grad3_kernel(const float* Pb, const float* Pa, void* dB, void* dA, int out_kind, int d_out,
                                   int d_in, int parts_b, int parts_a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nB = static_cast<int64_t>(d_out) * LR, nA = static_cast<int64_t>(d_in) * LR;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < nB + nA;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -487,15 +499,9 @@ size_t lora_down_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
 cudaError_t lora_down_launch(const LoraArgs& a) {
   const int grid = static_cast<int>((a.T + 15) / 16);
   if (grid == 0) return cudaSuccess;
-  if (a.in_kind == EK_BF16)
-    lora_down_kernel<true><<<grid, LTHREADS, 0, a.stream>>>(static_cast<const uint16_t*>(a.X),
-                                                           static_cast<const uint16_t*>(a.A), a.out, a.out_kind,
-                                                           static_cast<int>(a.T), static_cast<int>(a.d_in));
-  else
-    lora_down_kernel<false><<<grid, LTHREADS, 0, a.stream>>>(static_cast<const uint16_t*>(a.X),
-                                                            static_cast<const uint16_t*>(a.A), a.out, a.out_kind,
-                                                            static_cast<int>(a.T), static_cast<int>(a.d_in));
-  return cudaGetLastError();
+  return launch_k(a.in_kind == EK_BF16 ? lora_down_kernel<true> : lora_down_kernel<false>, dim3(grid),
+                  dim3(LTHREADS), 0, a.stream, static_cast<const uint16_t*>(a.X), static_cast<const uint16_t*>(a.A),
+                  a.out, a.out_kind, static_cast<int>(a.T), static_cast<int>(a.d_in));
 }
 
 cudaError_t lora_up_launch(const LoraArgs& a) {
@@ -503,15 +509,9 @@ cudaError_t lora_up_launch(const LoraArgs& a) {
   const int nt = rowup_nt(a.T, a.d_out, a.num_sms);
   if (nj == 0 || a.T == 0) return cudaSuccess;
   dim3 grid(nj, nt);
-  if (a.in_kind == EK_BF16)
-    lora_up_kernel<true><<<grid, LTHREADS, 0, a.stream>>>(static_cast<const uint16_t*>(a.H),
-                                                         static_cast<const uint16_t*>(a.B), a.out, a.out_kind,
-                                                         static_cast<int>(a.T), static_cast<int>(a.d_out), nt);
-  else
-    lora_up_kernel<false><<<grid, LTHREADS, 0, a.stream>>>(static_cast<const uint16_t*>(a.H),
-                                                          static_cast<const uint16_t*>(a.B), a.out, a.out_kind,
-                                                          static_cast<int>(a.T), static_cast<int>(a.d_out), nt);
-  return cudaGetLastError();
+  return launch_k(a.in_kind == EK_BF16 ? lora_up_kernel<true> : lora_up_kernel<false>, grid, dim3(LTHREADS), 0,
+                  a.stream, static_cast<const uint16_t*>(a.H), static_cast<const uint16_t*>(a.B), a.out, a.out_kind,
+                  static_cast<int>(a.T), static_cast<int>(a.d_out), nt);
 }
 
 // workspace: [At d_in*16 x 2B][Bt d_out*16 x 2B][dH T*16 x 4B][Pb][Pa], 256-byte aligned pieces
@@ -555,36 +555,29 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   const uint16_t* dY = static_cast<const uint16_t*>(a.dY);
 
   const int prep_blocks = clampi((static_cast<int64_t>(d_in + d_out) * LR + 255) / 256, 1, 4 * a.num_sms);
-  lora_prep_kernel<<<prep_blocks, 256, 0, a.stream>>>(A, B, At, Bt, d_in, d_out);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(lora_prep_kernel, dim3(prep_blocks), dim3(256), 0, a.stream, A, B, At, Bt, d_in, d_out);
   if (e != cudaSuccess) return e;
 
   const int n_rowdown = (T + 15) / 16;
   const int nj_b = (d_out + 63) / 64;
   const int g1 = n_rowdown + nj_b * w.parts_b;
-  if (bf)
-    lora_grad1_kernel<true><<<g1, LTHREADS, 0, a.stream>>>(dY, Bt, H, dH, Pb, T, d_out, n_rowdown, nj_b, w.parts_b);
-  else
-    lora_grad1_kernel<false><<<g1, LTHREADS, 0, a.stream>>>(dY, Bt, H, dH, Pb, T, d_out, n_rowdown, nj_b, w.parts_b);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_k(bf ? lora_grad1_kernel<true> : lora_grad1_kernel<false>, dim3(g1), dim3(LTHREADS), 0, a.stream, dY,
+               static_cast<const uint16_t*>(Bt), H, dH, Pb, T, d_out, n_rowdown, nj_b, w.parts_b);
+  if (e != cudaSuccess) return e;
 
   const int nj_a = (d_in + 63) / 64;
   const int n_colred = nj_a * w.parts_a;
   const int nj_x = (d_in + 255) / 256;
   const int n_tx = rowup_nt(T, d_in, a.num_sms);
   const int g2 = n_colred + nj_x * n_tx;
-  if (bf)
-    lora_grad2_kernel<true><<<g2, LTHREADS, 0, a.stream>>>(X, dH, At, a.out3, a.out_kind, Pa, T, d_in, n_colred,
-                                                           nj_a, w.parts_a, nj_x, n_tx);
-  else
-    lora_grad2_kernel<false><<<g2, LTHREADS, 0, a.stream>>>(X, dH, At, a.out3, a.out_kind, Pa, T, d_in, n_colred,
-                                                            nj_a, w.parts_a, nj_x, n_tx);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_k(bf ? lora_grad2_kernel<true> : lora_grad2_kernel<false>, dim3(g2), dim3(LTHREADS), 0, a.stream, X,
+               static_cast<const float*>(dH), static_cast<const uint16_t*>(At), a.out3, a.out_kind, Pa, T, d_in,
+               n_colred, nj_a, w.parts_a, nj_x, n_tx);
+  if (e != cudaSuccess) return e;
 
   const int g3 = clampi((static_cast<int64_t>(d_in + d_out) * LR + 255) / 256, 1, 4 * a.num_sms);
-  lora_grad3_kernel<<<g3, 256, 0, a.stream>>>(Pb, Pa, a.out2, a.out, a.out_kind, d_out, d_in, w.parts_b,
-                                              w.parts_a);
-  return cudaGetLastError();
+  return launch_k(lora_grad3_kernel, dim3(g3), dim3(256), 0, a.stream, static_cast<const float*>(Pb),
+                  static_cast<const float*>(Pa), a.out2, a.out, a.out_kind, d_out, d_in, w.parts_b, w.parts_a);
 }
 
 }  // namespace tg

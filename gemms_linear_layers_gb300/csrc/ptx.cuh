@@ -26,6 +26,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------- programmatic launch
+// Kernels are launched with programmatic stream serialization: a kernel may
+// start while the previous one in the stream is finishing.  pdl_wait() blocks
+// until every earlier kernel has completed and its writes are visible; it
+// must come before the first global-memory access.  pdl_trigger() lets the
+// next kernel in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -5,11 +5,35 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 // device status word: bit 31 = a bounded wait timed out; low bits = site id
 #define TG_DEVSTAT_TIMEOUT 0x80000000u
 #define TG_DEVSTAT_SITE_MASK 0x0000FFFFu
 
 namespace tg {
+
+// Programmatic dependent launch on (default) or off ($TG_PDL=0).
+bool pdl_enabled();
+
+// Launch with programmatic stream serialization, so the kernel's prologue
+// overlaps the previous kernel's tail (the kernel calls pdl_wait() before it
+// touches global memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 enum ElemKind : int { EK_BF16 = 0, EK_F16 = 1, EK_F32 = 2 };
 
