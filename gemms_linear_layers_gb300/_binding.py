@@ -34,6 +34,7 @@ SIGNATURES = {
     "tg_gemm_fwd": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_dgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_wgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_gemm_wgrad_noalloc": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
     "tg_lora_down": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_lora_up": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
@@ -165,6 +166,19 @@ def tg_gemm_wgrad(dY, X, dW=None, out_dtype=None, ws=None, stream=None):
     _check(lib().tg_gemm_wgrad(_ptr(dY), _ptr(X), _ptr(dW), T, d_out, d_in, _DT[dY.dtype], _DT[dW.dtype], wp, wn,
                                _stream(stream)), "tg_gemm_wgrad")
     _keep(keep, stream)
+    return dW
+
+
+def tg_gemm_wgrad_noalloc(dY, X, dW, stream=None):
+    """dW = dY^T X without any device allocation by the library (the split-K
+    scratch is the library's own static array); dW must be given."""
+    _need(dY, "dY", 2), _need(X, "X", 2), _need(dW, "dW", 2)
+    T, d_out = dY.shape
+    d_in = X.shape[1]
+    if X.shape[0] != T or X.dtype != dY.dtype or tuple(dW.shape) != (d_out, d_in):
+        raise ValueError("inconsistent shapes or dtypes")
+    _check(lib().tg_gemm_wgrad_noalloc(_ptr(dY), _ptr(X), _ptr(dW), T, d_out, d_in, _DT[dY.dtype], _DT[dW.dtype],
+                                       _stream(stream)), "tg_gemm_wgrad_noalloc")
     return dW
 
 

@@ -105,6 +105,7 @@ static void record(const std::string& s) {
   t_last_call = s;
   if (log_enabled()) fprintf(stderr, "[tg] %s\n", s.c_str());
 }
+void note_last_call(const std::string& s) { record(s); }
 
 // -------------------------------------------------------------- tile table
 struct TableKey {

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
 #include <utility>
 
 // device status word: bit 31 = a bounded wait timed out; low bits = site id
@@ -15,6 +16,9 @@ namespace tg {
 
 // Programmatic dependent launch on (default) or off ($TG_PDL=0).
 bool pdl_enabled();
+
+// Sets the calling thread's tg_last_call() text (and logs it under TG_LOG).
+void note_last_call(const std::string& s);
 
 // Launch with programmatic stream serialization, so the kernel's prologue
 // overlaps the previous kernel's tail (the kernel calls pdl_wait() before it

@@ -105,6 +105,27 @@ tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int6
                         int64_t d_in, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* Weight-gradient product for callers that cannot allocate device memory.
+ * (The page has no counterpart; this is an interface for such callers.)
+ * Some callers may not call cudaMalloc or lend a workspace: code inside a host
+ * framework that owns all device memory through its own pool, or a process
+ * held to a fixed memory budget set at start-up.  This computes exactly what
+ * tg_gemm_wgrad computes, with the same kernels and arguments, minus the
+ * workspace: the split-K scratch is a 32 MiB array inside the library that
+ * every device loading the library holds until the process exits.
+ *   - Nothing is allocated: no cudaMalloc/cudaFree, no library allocator.
+ *   - A shape whose plan needs more than 32 MiB of scratch (see
+ *     tg_workspace_size(TG_OP_GEMM_WGRAD, ...)) is rejected with
+ *     TG_ERR_WORKSPACE_TOO_SMALL and a message in tg_last_call(); nothing runs.
+ *   - All calls share the one array.  Calls that may overlap on the GPU (on
+ *     different streams, or on one stream with no ordering between them)
+ *     race on it and can corrupt each other's results; order them.
+ *   - The first call on a device looks up the array's device address (a CUDA
+ *     runtime query, done once per device with that device current); make
+ *     that first call before any stream capture begins. */
+tg_status tg_gemm_wgrad_noalloc(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out,
+                                int64_t d_in, tg_dtype in, tg_dtype out, void* stream);
+
 /* Rank-r LoRA down projection ("Tuning the kernels": the rank-16 LoRA matrices):
  *   H[T, r] = X[T, d_in] . A[r, d_in]^T
  * r = 16 takes the streaming kernel (X read once); other ranks are supported
