@@ -7,6 +7,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <fstream>
 #include <mutex>
@@ -125,7 +127,7 @@ struct TableKeyHash {
   }
 };
 struct TableVal {
-  int bn, splits, raster;  // raster: -1 = by operand size, 0 = along M, 1 = along N
+  int bn, splits, raster;  // splits 0 = stream-K; raster: -1 = by operand size, 0 = along M, 1 = along N
 };
 static std::shared_mutex g_table_mu;
 static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
@@ -155,11 +157,19 @@ static tg_status load_table_file(const char* path) {
       const size_t h = line.find('#');
       if (h != std::string::npos) line.resize(h);
       std::istringstream ss(line);
-      std::string op, din, dout;
+      std::string op, din, dout, sp;
       int64_t M, N, K, batch;
       int bn, splits;
       if (!(ss >> op)) continue;  // blank line
-      if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> splits)) return TG_ERR_TABLE;
+      if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> sp)) return TG_ERR_TABLE;
+      if (sp == "sk") {
+        splits = 0;
+      } else {
+        char* endp = nullptr;
+        const long v = strtol(sp.c_str(), &endp, 10);
+        if (endp == sp.c_str() || *endp != '\0') return TG_ERR_TABLE;
+        splits = static_cast<int>(v);
+      }
       std::string rs;
       int raster = -1;
       if (ss >> rs) {
@@ -169,7 +179,7 @@ static tg_status load_table_file(const char* path) {
       }
       const int l = parse_layout(op), i = parse_dtype(din), o = parse_dtype(dout);
       if (l < 0 || i < 0 || o < 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return TG_ERR_TABLE;
-      if (!(bn == 64 || bn == 128 || bn == 192 || bn == 256) || splits < 1 || splits > 64) return TG_ERR_TABLE;
+      if (!(bn == 64 || bn == 128 || bn == 192 || bn == 256) || splits < 0 || splits > 64) return TG_ERR_TABLE;
       t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster};
     }
   }
@@ -211,6 +221,7 @@ struct Plan {
   int bn = 256;
   int splits = 1;
   int raster_n = 0;
+  bool sk = false;  // stream-K schedule (splits is then 1)
   bool from_table = false;
 };
 
@@ -244,6 +255,22 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
+  // stream-K: every CTA gets an equal share of the tile x K-block iterations;
+  // a cut tile costs its pieces' FP32 write and the owner's read-back
+  for (int bn : bns) {
+    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
+    const int64_t iters = tiles * kb;
+    if (iters < sms || tiles * 4 < sms) continue;
+    const double kb_cyc = 4.0 * fmax(bn / 2.0, 32.0 + bn / 4.0);
+    const double per_cta = static_cast<double>(cdiv(iters, sms));
+    double t = per_cta * kb_cyc + 600.0 * cdiv(tiles, sms) + 2.0 * 128.0 * bn * 4 / 24.0;
+    if (t < best_t * 0.95) {
+      best_t = t;
+      best.bn = bn;
+      best.splits = 1;
+      best.sk = true;
+    }
+  }
   return best;
 }
 
@@ -259,7 +286,9 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
     Plan p;
     p.bn = v.bn;
     const int64_t kb = cdiv(K, 64);
-    const int64_t s = v.splits < kb ? v.splits : kb;
+    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, p.bn);
+    p.sk = v.splits == 0 && tiles * kb >= 1;
+    const int64_t s = p.sk ? 1 : (v.splits < kb ? v.splits : kb);
     const int64_t kps = cdiv(kb, s);
     p.splits = static_cast<int>(cdiv(kb, kps));
     p.raster_n = v.raster >= 0 ? v.raster : auto_raster(M, N, K);
@@ -271,8 +300,26 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
   return p;
 }
 
-static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t batch) {
+static int sk_grid(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  const int64_t iters = batch * cdiv(M, 128) * cdiv(N, p.bn) * cdiv(K, 64);
+  return static_cast<int>(iters < sms ? iters : sms);
+}
+
+static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  if (p.sk) return sk_ws_bytes(sk_grid(p, M, N, K, batch, sms), p.bn);
   return p.splits > 1 ? static_cast<size_t>(p.splits) * batch * M * N * 4 : 0;
+}
+
+// Stream-K publication flag value for one launch.  Owners clear the flags
+// they consumed, so a workspace that served a completed launch holds zeros; a
+// fresh workspace holds arbitrary bytes, which match a 64-bit value that is
+// never zero with negligible probability.
+static unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> ctr{
+      (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) << 20) ^
+      0x9E3779B97F4A7C15ull};
+  unsigned long long v = ctr.fetch_add(1) + 1;
+  return v ? v : ctr.fetch_add(1) + 1;
 }
 
 // -------------------------------------------------------------- the GEMMs
@@ -321,7 +368,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
   char buf[320];
   if (tc_eligible(g)) {
     const Plan p = make_plan(g.layout, g.M, g.N, g.K, g.batch, g.in, g.out, ctx->sms);
-    const size_t need = plan_ws_bytes(p, g.M, g.N, g.batch);
+    const size_t need = plan_ws_bytes(p, g.M, g.N, g.K, g.batch, ctx->sms);
     if (need > 0 && (g.ws == nullptr || g.ws_bytes < need || !aligned(g.ws, 16))) {
       snprintf(buf, sizeof buf, "%s tc %s bn=%d splits=%d: workspace %zu bytes needed, %zu given", g.name,
                layout_name(g.layout), p.bn, p.splits, need, g.ws ? g.ws_bytes : static_cast<size_t>(0));
@@ -346,6 +393,8 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.bn = p.bn;
     t.splits = p.splits;
     t.raster_n = p.raster_n;
+    t.sk = p.sk ? 1 : 0;
+    t.sk_epoch = p.sk ? next_epoch() : 0;
     t.ws = g.ws;
     t.grid = ctx->sms;
     t.stream = g.stream;
@@ -354,13 +403,13 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     cudaError_t e = g.layout == LAYOUT_NT   ? tc_gemm_launch_nt(t)
                     : g.layout == LAYOUT_NN ? tc_gemm_launch_nn(t)
                                             : tc_gemm_launch_tn(t);
-    if (e == cudaSuccess && p.splits > 1)
+    if (e == cudaSuccess && !p.sk && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
                                g.stream);
-    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d splits=%d raster=%c table=%s %s",
+    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d %s%d raster=%c table=%s %s",
              g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
-             p.bn, p.splits, p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss",
-             e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+             p.bn, p.sk ? "sk grid=" : "splits=", p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits,
+             p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }
@@ -404,7 +453,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
 static size_t gemm_ws_bytes(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
                             int sms) {
   if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
-  return plan_ws_bytes(make_plan(layout, M, N, K, batch, in, out, sms), M, N, batch);
+  return plan_ws_bytes(make_plan(layout, M, N, K, batch, in, out, sms), M, N, K, batch, sms);
 }
 
 // Checks shared by the layer products.  Returns TG_OK to proceed.

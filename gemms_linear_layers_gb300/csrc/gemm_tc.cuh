@@ -22,6 +22,15 @@
 //               the next tile's MMAs overlap this tile's stores.
 // Split-K: a unit is (tile, K range); partial sums go to an FP32 workspace
 // and a separate kernel adds them in split order (deterministic).
+// Stream-K: the (tile x K block) iteration space is cut into gridDim.x equal
+// contiguous ranges, one per CTA.  A tile cut by a range boundary is finished
+// by the CTA holding its first K block (the owner): every later CTA that
+// worked on the tile writes its FP32 partial tile to the workspace and
+// publishes it with a flag; the owner waits for those flags, adds the
+// partials to its accumulator in CTA order, clears their flags and writes the
+// tile.  A flag holds a per-launch value, and is zero between launches.  Waits only
+// ever point to higher-numbered CTAs, which produce their partial first
+// thing, and all CTAs of the persistent grid are resident, so the waits end.
 #pragma once
 #include "ptx.cuh"
 
@@ -57,19 +66,35 @@ struct TcArgs {
   uint32_t idesc;
   int out_f16;   // 16-bit output type: 1 = fp16, 0 = bf16
   int raster_n;  // 1: consecutive units walk along N (they share the A tile)
+  int sk;        // 1: stream-K schedule over batch * m_tiles * n_tiles * kb_total iterations
+  long long sk_iters;
+  float* sk_part;                // [gridDim.x][128][BN] FP32 partial tiles
+  unsigned long long* sk_flags;  // [gridDim.x][4] publication flags, one per 32-row quadrant, 128 B apart
+  unsigned long long sk_epoch;   // this launch's flag value
   unsigned long long timeout_ns;
   unsigned int* status;
+  unsigned long long* trace;  // event timestamps per CTA (only in -DTG_TRACE builds)
 };
+
+#ifdef TG_TRACE
+#define TG_EVENT(ev)                                                                    \
+  do {                                                                                  \
+    if (args.trace) args.trace[blockIdx.x * 16 + (ev)] = globaltimer_ns();             \
+  } while (0)
+#else
+#define TG_EVENT(ev) \
+  do {               \
+  } while (0)
+#endif
 
 struct Unit {
   int b, m0, n0, split, kb0, kb1;
+  int owner;   // this CTA writes the tile (stream-K: it holds the tile's first K block)
+  int c_last;  // stream-K owner: last CTA holding a piece of the tile (> blockIdx.x: wait for partials)
 };
 
 template <int BN>
-__device__ __forceinline__ Unit decode_unit(int u, const TcArgs& a) {
-  Unit c;
-  c.split = u % a.splits;
-  const int t = u / a.splits;
+__device__ __forceinline__ void tile_coords(int t, const TcArgs& a, Unit& c) {
   const int tiles = a.m_tiles * a.n_tiles;
   c.b = t / tiles;
   const int r = t - c.b * tiles;
@@ -80,11 +105,88 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcArgs& a) {
     c.m0 = (r % a.m_tiles) * TC_BM;
     c.n0 = (r / a.m_tiles) * BN;
   }
-  c.kb0 = c.split * a.kps;
-  c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+}
+
+__device__ __forceinline__ long long sk_start(long long cta, const TcArgs& a) {
+  return cta * a.sk_iters / gridDim.x;
+}
+
+// the CTA whose stream-K range holds iteration p
+__device__ __forceinline__ int sk_cta_of(long long p, const TcArgs& a) {
+  int c = static_cast<int>(p * gridDim.x / a.sk_iters);
+  while (c + 1 < static_cast<int>(gridDim.x) && sk_start(c + 1, a) <= p) ++c;
+  while (c > 0 && sk_start(c, a) > p) --c;
   return c;
 }
 
+// The sequence of units one CTA works on; every role walks the same one.
+struct WorkIter {
+  long long pos, end;  // stream-K range, or (unit index, -) for the split schedule
+};
+
+__device__ __forceinline__ WorkIter work_begin(const TcArgs& a) {
+  WorkIter it;
+  if (a.sk) {
+    it.pos = sk_start(blockIdx.x, a);
+    it.end = sk_start(blockIdx.x + 1, a);
+  } else {
+    it.pos = blockIdx.x;
+    it.end = a.units;
+  }
+  return it;
+}
+
+template <int BN>
+__device__ __forceinline__ bool work_next(const TcArgs& a, WorkIter& it, Unit& c) {
+  if (it.pos >= it.end) return false;
+  if (!a.sk) {
+    const int u = static_cast<int>(it.pos);
+    c.split = u % a.splits;
+    tile_coords<BN>(u / a.splits, a, c);
+    c.kb0 = c.split * a.kps;
+    c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+    c.owner = 1;
+    c.c_last = -1;
+    it.pos += gridDim.x;
+    return true;
+  }
+  const long long kb = a.kb_total;
+  const int t = static_cast<int>(it.pos / kb);
+  const long long kt0 = static_cast<long long>(t) * kb;
+  const long long seg_end = min(it.end, kt0 + kb);
+  tile_coords<BN>(t, a, c);
+  c.split = 0;
+  c.kb0 = static_cast<int>(it.pos - kt0);
+  c.kb1 = static_cast<int>(seg_end - kt0);
+  c.owner = it.pos == kt0;
+  c.c_last = (c.owner && seg_end < kt0 + kb) ? sk_cta_of(kt0 + kb - 1, a) : -1;
+  it.pos = seg_end;
+  return true;
+}
+
+// float4 index in the partial-tile area of (CTA, 32-row quadrant q, 32-column
+// block, 4-column group j, lane): lanes innermost, so warp accesses coalesce
+template <int BN>
+__device__ __forceinline__ size_t sk_part_index(int cta, int q, int blk, int j, int lane) {
+  return ((((static_cast<size_t>(cta) * 4 + q) * (BN / 32) + blk) * 8 + j) * 32) + lane;
+}
+
+// flag of (CTA, 32-row quadrant), one per 128-byte line
+__device__ __forceinline__ int sk_flag_index(int cta, int q) { return (cta * 4 + q) * 16; }
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
 template <bool A_MN, bool B_MN, int BN, bool OUT16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -139,6 +241,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // the prologue above overlapped the previous kernel; global memory from here
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) TG_EVENT(0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -149,8 +252,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
       for (int s = 0; s < S; ++s) issued[s] = -1;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit c = decode_unit<BN>(u, args);
+      WorkIter it = work_begin(args);
+      Unit c;
+      while (ok && work_next<BN>(args, it, c)) {
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, tmo, abort_flag, args.status, 1)) {
             ok = false;
@@ -179,7 +283,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             phase ^= 1u;
           }
         }
+        if (it.pos == it.end || c.kb1 - c.kb0 >= 0) TG_EVENT(c.owner ? 9 : 1);
       }
+      TG_EVENT(8);
       if (!ok) {
         // let every copy already issued land before the CTA unwinds
 #pragma unroll
@@ -197,8 +303,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        const Unit c = decode_unit<BN>(u, args);
+      WorkIter it = work_begin(args);
+      Unit c;
+      while (ok && work_next<BN>(args, it, c)) {
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, tmo, abort_flag, args.status, 2)) {
           ok = false;
           break;
@@ -229,6 +336,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!ok) break;
         umma_commit(smem_u32(&tfull[acc]));
+        TG_EVENT(c.owner ? 10 : 2);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -250,58 +358,144 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
-    for (int u = blockIdx.x; u < args.units; u += gridDim.x) {
-      const Unit c = decode_unit<BN>(u, args);
+    WorkIter it = work_begin(args);
+    Unit c;
+    while (work_next<BN>(args, it, c)) {
       if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
-      const int zc = c.b * args.splits + c.split;
+      const int row = q * 32 + lane;  // row of the tile this thread holds
+      if (!c.owner) {
+        // ---- stream-K contributor: FP32 partial tile to this CTA's slot, then publish.
+        // Private layout: for each 32-column block and each 4-column group, the
+        // 32 lanes' float4s are adjacent, so every warp store writes 512
+        // contiguous bytes.
 #pragma unroll 1
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint32_t r[CW];
-        tmem_ld_32x32b_x32(t_row + ch * CW, r);
-        if (OUT16) tmem_ld_32x32b_x32(t_row + ch * CW + 32, r + 32);
-        tmem_ld_wait();
-        if (ch == NCH - 1) {
-          // accumulator fully read: hand it back to the MMA warp
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-        }
-        uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
-        if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
-        __syncwarp();
-        uint8_t* row = buf + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 v;
-          if (OUT16) {
-            const uint32_t* f = r + 8 * j;
-            if (args.out_f16) {
-              v.x = pack_f16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
-              v.y = pack_f16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
-              v.z = pack_f16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
-              v.w = pack_f16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
-            } else {
-              v.x = pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
-              v.y = pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
-              v.z = pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
-              v.w = pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
-            }
-          } else {
-            v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_wait();
+          if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
           }
-          // 128-byte swizzle: 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8)
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = v;
+          float4* dst = reinterpret_cast<float4*>(args.sk_part) + sk_part_index<BN>(blockIdx.x, q, ch, 0, lane);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         }
-        fence_async_smem();
+        // each warp publishes its own 32 rows: no barrier between the epilogue warps
+        __threadfence();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
-          bulk_commit();
+        if (lane == 0) st_release_u64(args.sk_flags + sk_flag_index(blockIdx.x, q), args.sk_epoch);
+        if (warp == 2 && lane == 0) TG_EVENT(3);
+      } else {
+        // ---- tile writer; a stream-K owner first waits for the later pieces
+        // of its own 32 rows (each lane polls the flags itself)
+        const bool fixup = c.c_last > static_cast<int>(blockIdx.x);
+        bool have_parts = true;
+        if (fixup) {
+          // one lane polls, with back-off: flags sit on their own 128-byte lines
+          // and a storm of polls would crowd the L2 slices the TMA loads need
+          int ok = 1;
+          if (warp == 2 && lane == 0) TG_EVENT(4);
+          if (lane == 0) {
+            for (int cc = blockIdx.x + 1; cc <= c.c_last && ok; ++cc) {
+              const unsigned long long* fl = args.sk_flags + sk_flag_index(cc, q);
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_u64(fl) != args.sk_epoch) {
+                __nanosleep(128);
+                if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+                  if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(args.status, TG_DEVSTAT_TIMEOUT | 5u);
+                  }
+                  ok = 0;
+                  break;
+                }
+              }
+            }
+          }
+          have_parts = __shfl_sync(0xffffffffu, ok, 0) != 0;
+          __syncwarp();  // lane 0's acquire orders the other lanes' reads below
+          if (warp == 2 && lane == 0) TG_EVENT(5);
         }
-        ++nstore;
+        const int zc = c.b * args.splits + c.split;
+#pragma unroll 1
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t r[CW];
+          tmem_ld_32x32b_x32(t_row + ch * CW, r);
+          if (OUT16) tmem_ld_32x32b_x32(t_row + ch * CW + 32, r + 32);
+          tmem_ld_wait();
+          if (ch == NCH - 1) {
+            // accumulator fully read: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+          }
+          if (fixup && have_parts) {
+            // add the later CTAs' partials in CTA order
+            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) {
+#pragma unroll
+              for (int sub = 0; sub < CW / 32; ++sub) {
+                const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, ch * (CW / 32) + sub, 0, lane);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 v = ld_cg_f4(src + 4 * 32 * j);
+                  uint32_t* d = r + 32 * sub + 4 * j;
+                  d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
+                  d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
+                  d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
+                  d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+                }
+              }
+            }
+          }
+          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          __syncwarp();
+          uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 v;
+            if (OUT16) {
+              const uint32_t* f = r + 8 * j;
+              if (args.out_f16) {
+                v.x = pack_f16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
+                v.y = pack_f16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
+                v.z = pack_f16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
+                v.w = pack_f16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
+              } else {
+                v.x = pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1]));
+                v.y = pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3]));
+                v.z = pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5]));
+                v.w = pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7]));
+              }
+            } else {
+              v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
+            // 128-byte swizzle: 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = v;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
+            bulk_commit();
+          }
+          ++nstore;
+        }
+        if (fixup && have_parts) {
+          // this warp has read every later piece of its rows: clear their flags,
+          // so flags are zero between launches (a replayed CUDA graph reuses the
+          // same flag value every time)
+          __syncwarp();
+          if (lane == 0)
+            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) st_release_u64(args.sk_flags + sk_flag_index(cc, q), 0ull);
+        }
       }
       if (++acc == 2) {
         acc = 0;
@@ -309,6 +503,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
     if (lane == 0) bulk_wait_all();
+    if (warp == 2 && lane == 0) TG_EVENT(6);
   }
 
   tc_fence_before();

@@ -4,6 +4,7 @@
 // three families compile in parallel.
 #pragma once
 #include <cuda.h>
+#include <stdlib.h>
 
 #include "gemm_tc.cuh"
 #include "tg_internal.h"
@@ -42,10 +43,11 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   if (!ok) return cudaErrorInvalidValue;
 
   // output (or FP32 split partials): [batch * splits][M][N], dense
-  const int ck = g.splits > 1 ? EK_F32 : g.out_kind;
+  const bool split_parts = !g.sk && g.splits > 1;
+  const int ck = split_parts ? EK_F32 : g.out_kind;
   const uint64_t esz = elem_bytes(ck);
-  void* cptr = g.splits > 1 ? g.ws : g.C;
-  ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * g.splits, N * esz, M * N * esz,
+  void* cptr = split_parts ? g.ws : g.C;
+  ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * (split_parts ? g.splits : 1), N * esz, M * N * esz,
                       OUT16 ? 64 : 32, 32, true);
   if (!ok) return cudaErrorInvalidValue;
 
@@ -53,22 +55,38 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
   a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
-  a.splits = g.splits;
-  a.kps = (a.kb_total + g.splits - 1) / g.splits;
-  a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * g.splits;
+  a.splits = g.sk ? 1 : g.splits;
+  a.kps = (a.kb_total + a.splits - 1) / a.splits;
+  a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * a.splits;
   a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC_BM, BN);
   a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
   a.raster_n = g.raster_n;
+  a.sk = g.sk;
+  a.sk_iters = static_cast<long long>(a.units) * a.kb_total;
+  a.sk_part = nullptr;
+  a.sk_flags = nullptr;
+  a.sk_epoch = g.sk_epoch;
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
-  const int grid = g.grid < a.units ? g.grid : a.units;
+  a.trace = nullptr;
+#ifdef TG_TRACE
+  if (const char* e = getenv("TG_TRACE_ADDR")) a.trace = reinterpret_cast<unsigned long long*>(strtoull(e, nullptr, 0));
+#endif
+  int grid = g.grid < a.units ? g.grid : a.units;
+  if (g.sk) {
+    // every CTA gets at least one iteration; the workspace holds grid slots
+    grid = a.sk_iters < g.grid ? static_cast<int>(a.sk_iters) : g.grid;
+    a.sk_part = static_cast<float*>(g.ws);
+    a.sk_flags = reinterpret_cast<unsigned long long*>(static_cast<char*>(g.ws) +
+                                                       static_cast<size_t>(grid) * TC_BM * BN * 4);
+  }
   return launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, a);
 }
 
 template <bool A_MN, bool B_MN>
 static cudaError_t tc_launch_layout(const TcGemm& g) {
   // split partials are FP32; so is an FP32 output
-  const bool out16 = g.splits == 1 && g.out_kind != EK_F32;
+  const bool out16 = (g.sk || g.splits == 1) && g.out_kind != EK_F32;
   switch (g.bn) {
     case 64: return out16 ? tc_launch_one<A_MN, B_MN, 64, true>(g) : tc_launch_one<A_MN, B_MN, 64, false>(g);
     case 128: return out16 ? tc_launch_one<A_MN, B_MN, 128, true>(g) : tc_launch_one<A_MN, B_MN, 128, false>(g);

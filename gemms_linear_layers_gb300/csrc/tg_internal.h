@@ -68,12 +68,20 @@ struct TcGemm {
   int bn;                     // tile width: 64, 128, 192 or 256
   int splits;                 // >1: FP32 partials to ws, then an ordered reduction
   int raster_n;               // 1: walk output tiles along N first (A tiles reused)
+  int sk;                     // 1: stream-K schedule (ws holds per-CTA partial tiles + flags)
+  unsigned long long sk_epoch;  // flag value unique to this launch
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
   unsigned int* status;
   unsigned long long timeout_ns;
 };
+
+// Workspace of a stream-K launch: one FP32 partial tile and four flags per
+// CTA, each flag on its own 128-byte line.
+inline size_t sk_ws_bytes(int grid, int bn) {
+  return static_cast<size_t>(grid) * (128 * static_cast<size_t>(bn) * 4 + 4 * 128);
+}
 
 // per-layout launchers (gemm_tc_{nt,nn,tn}.cu)
 cudaError_t tc_gemm_launch_nt(const TcGemm& g);

@@ -118,6 +118,10 @@ def candidates(M, N, K, batch, sms):
                 continue
             for raster in ("m", "n"):
                 yield bn, s, raster
+        # stream-K: an equal share of tile x K-block iterations per CTA
+        if tiles * kb >= sms and tiles * 4 >= sms:
+            for raster in ("m", "n"):
+                yield bn, "sk", raster
 
 
 def main(argv=None):
@@ -125,6 +129,8 @@ def main(argv=None):
     ap.add_argument("--out", default=DEFAULT_OUT)
     ap.add_argument("--sets", default="2b,135m,attn")
     ap.add_argument("--budget-s", type=float, default=900.0)
+    ap.add_argument("--only", default=None, help="comma-separated layouts or MxNxKxbatch keys to sweep")
+    ap.add_argument("-v", "--verbose", action="store_true", help="print every candidate's time")
     args = ap.parse_args(argv)
     sets = set(args.sets.split(","))
     stream = torch.cuda.Stream()
@@ -133,7 +139,10 @@ def main(argv=None):
     t0 = time.time()
     lines = []
     tmpdir = tempfile.mkdtemp()
+    only = set(args.only.split(",")) if args.only else None
     for layout, M, N, K, batch, make in shapes(sets):
+        if only and layout not in only and f"{M}x{N}x{K}x{batch}" not in only:
+            continue
         if time.time() - t0 > args.budget_s:
             print(f"budget exhausted before {layout} {M}x{N}x{K}x{batch}", flush=True)
             break
@@ -157,6 +166,8 @@ def main(argv=None):
                 continue
             plan = tg.tg_last_call()
             assert "table=hit" in plan, plan
+            if args.verbose:
+                print(f"  bn={bn} splits={s} raster={raster}: {ms * 1e3:.2f} us", flush=True)
             if best is None or ms < best[0]:
                 best = (ms, bn, s, raster)
         tg.tg_load_table(None)

@@ -233,3 +233,113 @@ def test_heuristic_plans_without_table(op):
             assert_close(gather(got, co), C, S, f"{op} heuristic [{tg.tg_last_call()}]", torch.bfloat16)
     finally:
         assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
+
+
+# --------------------------------------------------------------- stream-K
+SK_CASES = [
+    # (op, T, d_in, d_out, bn): tiles vs 152 CTAs: fewer tiles than CTAs (every
+    # tile cut into several pieces), about one tile per CTA, many tiles per CTA
+    ("wgrad", 4096, 2304, 2304, 256),
+    ("wgrad", 16384, 192, 128, 64),
+    ("dgrad", 2048, 576, 49152, 192),
+    ("fwd", 1000, 520, 1000, 128),
+    ("fwd", 2048, 576, 1536, 256),
+]
+
+
+def _with_table(line, fn):
+    import tempfile
+    with tempfile.NamedTemporaryFile("w", suffix=".txt", delete=False) as f:
+        f.write(line + "\n")
+    assert tg.tg_load_table(f.name) == 0
+    try:
+        return fn()
+    finally:
+        os.unlink(f.name)
+        assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("case", SK_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_stream_k_schedule(case, out_kind):
+    op, T, d_in, d_out, bn = case
+    dtype = torch.bfloat16
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    dname = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    line = f"{lay} bf16 {dname[out_dtype]} {M} {N} {K} 1 {bn} sk"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="sk")
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+
+    def go():
+        outs = [run(op, Xc, Wc, dYc, out_dtype) for _ in range(3)]
+        return outs, tg.tg_last_call()
+
+    outs, call = _with_table(line, go)
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert "sk grid=" in call and "table=hit" in call, call
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2]), "stream-K not deterministic"
+    if M * N * K <= 3 * 10 ** 9:
+        C, S = ref(op, X, W, dY)
+        assert_close(outs[0], C, S, f"{op} stream-K [{call}]", out_dtype)
+    else:
+        co = sample_coords(M, N, rows=32, cols=32, rand=4096, seed=3)
+        C, S = ref(op, X, W, dY, sample=co)
+        assert_close(gather(outs[0], co), C, S, f"{op} stream-K sampled [{call}]", out_dtype)
+
+
+def test_stream_k_small_integers_exact():
+    T, d_in, d_out = 8192, 384, 256
+    X = inputs.small_int((T, d_in), -2, 2, torch.float16, 8)
+    dY = inputs.small_int((T, d_out), -2, 2, torch.float16, 9)
+    line = f"tn f16 f32 {d_out} {d_in} {T} 1 128 sk"
+    got = _with_table(line, lambda: tg.tg_gemm_wgrad(dY.cuda(), X.cuda(), out_dtype=torch.float32))
+    C, _ = oracle.gemm_wgrad(dY, X)
+    assert np.array_equal(got.cpu().double().numpy(), C)
+
+
+def test_stream_k_attention_batch():
+    h, s, d = 36, 1024, 64
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="sk")
+    line = f"tn bf16 bf16 {s} {d} {s} {h} 64 sk"
+    got = _with_table(line, lambda: tg.tg_bmm_attn("pt_do", t["P"].cuda(), t["dO"].cuda()))
+    call = tg.tg_last_call()
+    co = sample_coords(s, d, batch=h, rows=16, cols=16, rand=2048, seed=5)
+    C, S = oracle.bmm_attn("pt_do", t["P"], t["dO"], sample=co)
+    assert_close(gather(got, co), C, S, f"attn pt_do stream-K [{call}]", torch.bfloat16)
+
+
+def test_stream_k_in_replayed_cuda_graph():
+    """A captured stream-K launch reuses one flag value on every replay: each
+    replay must still wait for this replay's partial tiles."""
+    T, d_in, d_out = 2048, 2304, 2304
+    line = f"tn bf16 bf16 {d_out} {d_in} {T} 1 256 sk"
+    X, W, dY = (t.cuda() for t in inputs.layer_inputs(T, d_in, d_out, torch.bfloat16, tag="skg"))
+    dW = torch.empty(d_out, d_in, dtype=torch.bfloat16, device="cuda")
+    n = tg.tg_workspace_size(tg.TG_OP_GEMM_WGRAD, T, d_out, d_in, 0, torch.bfloat16, torch.bfloat16)
+
+    def go():
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            tg.tg_gemm_wgrad(dY, X, dW=dW, ws=ws)
+        torch.cuda.synchronize()
+        assert "sk grid=" in tg.tg_last_call()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            tg.tg_gemm_wgrad(dY, X, dW=dW, ws=ws)
+        for i in range(4):
+            # new inputs in place, then replay; compare with a direct call
+            dY.copy_(inputs.normal((T, d_out), 0.01, torch.bfloat16, 100 + i, device="cuda"))
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            want = tg.tg_gemm_wgrad(dY, X, ws=torch.empty(n, dtype=torch.uint8, device="cuda"))
+            torch.cuda.synchronize()
+            assert torch.equal(dW, want), f"replay {i} differs from a direct call"
+        assert tg.tg_stream_status() == 0
+
+    _with_table(line, go)
