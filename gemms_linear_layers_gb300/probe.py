@@ -5,8 +5,9 @@ kind of kernel launch:
 
     python -m gemms_linear_layers_gb300.probe wgrad 2048 2304 2304 [--plan "256 sk n"] [--reps 20]
 
-`op` is fwd|dgrad|wgrad (dims: T d_in d_out) or one of the attention products
-qk|pv|do_vt|pt_do|ds_k|dst_q (dims: heads s d).  --plan "bn splits [raster]"
+`op` is fwd|dgrad|wgrad (dims: T d_in d_out), one of the attention products
+qk|pv|do_vt|pt_do|ds_k|dst_q (dims: heads s d), or lora_down|lora_up|lora_grad
+(dims: T d_in d_out, rank 16).  --plan "bn splits [raster]"
 writes a one-line tile table for this shape and loads it first.
 """
 from __future__ import annotations
@@ -48,6 +49,21 @@ def main(argv=None):
         fn = {"fwd": lambda ws: tg.tg_gemm_fwd(X, W, Y=out, ws=ws),
               "dgrad": lambda ws: tg.tg_gemm_dgrad(dY, W, dX=out, ws=ws),
               "wgrad": lambda ws: tg.tg_gemm_wgrad(dY, X, dW=out, ws=ws)}[a.op]
+    elif a.op.startswith("lora"):
+        T, d_in, d_out = a.dims
+        X, A, B, H, dY = inputs.lora_inputs(T, d_in, d_out, 16, dtype, tag="probe", device=dev)
+        M, N, K, batch = T, 16, d_in, 1
+        outs = {"dA": torch.empty(16, d_in, dtype=out_dtype, device=dev),
+                "dB": torch.empty(d_out, 16, dtype=out_dtype, device=dev),
+                "dX": torch.empty(T, d_in, dtype=out_dtype, device=dev)}
+        Hout = torch.empty(T, 16, dtype=out_dtype, device=dev)
+        Yout = torch.empty(T, d_out, dtype=out_dtype, device=dev)
+        fn = {"lora_down": lambda ws: tg.tg_lora_down(X, A, H=Hout, ws=ws),
+              "lora_up": lambda ws: tg.tg_lora_up(H, B, Y=Yout, ws=ws),
+              "lora_grad": lambda ws: tg.tg_lora_grad(X, A, B, H, dY, outs=outs, ws=ws)}[a.op]
+        nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
+                  "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
+                  "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
     else:
         h, s, d = a.dims
         t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
@@ -83,8 +99,12 @@ def main(argv=None):
         times.append(e0.elapsed_time(e1) / a.reps)
     ms = statistics.median(times)
     st = tg.tg_stream_status(stream)
-    print(f"{a.op} M={M} N={N} K={K} batch={batch}: {ms * 1e3:.2f} us, "
-          f"{workloads.flops(M, N, K, batch) / ms / 1e9:.0f} TFLOP/s, status {st} [{plan}]", flush=True)
+    if a.op.startswith("lora"):
+        print(f"{a.op} T={a.dims[0]} d_in={a.dims[1]} d_out={a.dims[2]}: {ms * 1e3:.2f} us, "
+              f"{nbytes / ms / 1e6:.0f} GB/s, status {st} [{plan}]", flush=True)
+    else:
+        print(f"{a.op} M={M} N={N} K={K} batch={batch}: {ms * 1e3:.2f} us, "
+              f"{workloads.flops(M, N, K, batch) / ms / 1e9:.0f} TFLOP/s, status {st} [{plan}]", flush=True)
     return 0 if st == 0 else 1
 
 
