@@ -649,6 +649,8 @@ tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t
     a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
     a.num_sms = ctx->sms;
     a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
     cudaError_t e = lora_down_launch(a);
     record(std::string("lora_down stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) + " " +
            (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
@@ -680,6 +682,8 @@ tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d
     a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
     a.num_sms = ctx->sms;
     a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
     cudaError_t e = lora_up_launch(a);
     record(std::string("lora_up stream T=") + std::to_string(T) + " d_out=" + std::to_string(d_out) + " " +
            (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
@@ -717,7 +721,7 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (T > 0 && d_in > 0 && d_out > 0 && lora_stream_ok(r, {d_in, d_out}, {X, dY, dX, dH_f32, H})) {
+  if (T > 0 && d_in > 0 && d_out > 0 && lora_stream_ok(r, {d_in, d_out}, {X, B, dY, dX, dH_f32, H})) {
     const size_t need = lora_grad_ws_bytes(T, d_in, d_out, r, ctx->sms);
     if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
       record("lora_grad stream: workspace too small");
@@ -742,6 +746,8 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
     a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
     a.num_sms = ctx->sms;
     a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
     cudaError_t e = lora_grad_launch(a);
     record(std::string("lora_grad stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) +
            " d_out=" + std::to_string(d_out) + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));

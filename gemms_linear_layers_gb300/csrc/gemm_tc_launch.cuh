@@ -32,14 +32,14 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
   bool ok;
   if (A_MN)  // stored [batch][K][M]
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, true);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
   else       // stored [batch][M][K]
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, true);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
   if (!ok) return cudaErrorInvalidValue;
   if (B_MN)  // stored [batch][K][N]
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, true);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
   else       // stored [batch][N][K]
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, true);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
   if (!ok) return cudaErrorInvalidValue;
 
   // output (or FP32 split partials): [batch * splits][M][N], dense
@@ -48,7 +48,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   const uint64_t esz = elem_bytes(ck);
   void* cptr = split_parts ? g.ws : g.C;
   ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * (split_parts ? g.splits : 1), N * esz, M * N * esz,
-                      OUT16 ? 64 : 32, 32, true);
+                      OUT16 ? 64 : 32, 32, 128);
   if (!ok) return cudaErrorInvalidValue;
 
   TcArgs a;

@@ -2,69 +2,111 @@
 //
 // Page "Twice the training speed on a BC-250 from tuned matrix kernels",
 // section "Tuning the kernels": the rank-16 LoRA matrices are among the
-// products a training step runs.  Every one of them reads or writes one
-// [T, d] tensor and touches only small [*, 16] factors otherwise, so they are
-// bound by HBM bandwidth, not by the tensor cores.  Each kernel streams its
-// big operand exactly once with 16-byte vector loads or stores and keeps the
-// rank-16 side in registers; the arithmetic runs on warp-level mma.sync
-// (m16n8k16, FP32 accumulate) because FP32 FFMA alone cannot keep up with
-// ~16 flop per byte at HBM speed.
+// products a training step runs.  Each of them reads or writes one [T, d]
+// tensor and touches only small [*, 16] factors otherwise, so they are bound
+// by HBM bandwidth, not by the tensor cores.  The arithmetic (about 16 flop
+// per streamed byte) still needs the tensor pipe: FP32 FFMA on the CUDA cores
+// cannot keep up with HBM at that intensity, so it runs on warp-level
+// mma.sync (m16n8k16, FP32 accumulate).
 //
-// Register layouts.  mma.sync m16n8k16 splits a warp's lane into g = lane/4
-// and c = lane%4.  A reduction index may be permuted freely as long as both
-// operands use the same permutation, and an output index may be permuted as
-// long as the store undoes it; the kernels use this to feed fragments
-// straight from 16-byte loads:
-//   * a thread that loads 8 consecutive k values of a row feeds two MMAs:
-//     values 0-3 go to MMA 0 (slots 2c,2c+1 <- k 0,1; slots 2c+8,2c+9 <- k 2,3)
-//     and values 4-7 to MMA 1;
-//   * for reductions over tokens, movmatrix.trans turns row-major register
-//     tiles into the (pairs along tokens) layout the fragments need.
-// FP32 operands (the gradient dH) are split into hi + lo 16-bit parts and
-// both parts are multiplied, so dH keeps ~16 significant bits instead of 8.
+// Streaming.  The kernels that read a [T, d] tensor are warp-specialised:
+// one producer warp moves tiles into a ring of shared-memory stages with TMA
+// (cp.async.bulk.tensor, swizzled) and eight consumer warps read fragments
+// from the stages with ldmatrix.  A CTA keeps up to ~150 KB of loads in flight
+// without holding them in registers, and every streamed byte crosses HBM once.
+//   row-down   OUT[t, r] = sum_k IN[t, k] S(r, k)      (H = X A^T, dH = dY B)
+//              CTA = R consecutive rows (R <= 32: about one CTA per SM), all
+//              of K; a warp owns one 64-column chunk of each stage.
+//   col-red    P[j, r] = sum_t IN[t, j] Hm[t, r]        (dB = dY^T H, dA^T = X^T dH)
+//              the (64-column block, 128-token step) space is cut into equal
+//              contiguous ranges, one per CTA (so every CTA streams the same
+//              number of bytes); a column block cut by range boundaries gets
+//              one FP32 partial per CTA, and the last CTA to publish one adds
+//              them in CTA order.  The tiles are read transposed by
+//              ldmatrix.trans, so there is no transposition pass.
+//              Optionally fused with the row-up of the same tile (dX = dH A):
+//              the dH tile in the stage also feeds the [128 x 64] dX tile,
+//              which leaves through a TMA store.
+//   row-up     OUT[t, j] = sum_r Hm[t, r] S2(j, r)      (Y = H B^T)
+//              writes a [T, d] tensor from the small factors, all from
+//              registers (16-byte stores).
+// FP32 operands (the gradient dH) enter the 16-bit MMA as hi + lo, both
+// rounded to the input type (hi = rn(x), lo = rn(x - hi)); both parts are
+// multiplied, so dH keeps about 16 significant bits instead of 8.
+//
+// Every result is a fixed-order sum: a warp adds its chunks in K order, the
+// warps' partial tiles are added in warp order, the CTAs' partials of a column
+// block in CTA order.  Every wait on an mbarrier is bounded (it gives up after
+// the configured limit, raises the device status word and lets the CTA unwind).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "ptx.cuh"
 #include "tg_internal.h"
 
 namespace tg {
 
-constexpr int LR = 16;  // the rank these kernels are written for
-constexpr int LTHREADS = 256;
+constexpr int LR = 16;                    // the rank these kernels are written for
+constexpr int LCW = 8;                    // consumer warps of a TMA-fed role
+constexpr int LGROUP = (LCW + 1) * 32;    // one role: consumers + one producer warp
+constexpr int LGROUP_UP = (2 * LCW + 1) * 32;  // col-red + row-up warps + one producer warp
+constexpr int LMAX_STAGES = 8;
+constexpr int CR_RS = 128;                // tokens per col-red step
+constexpr int RD_RED_BYTES = LCW * 32 * 17 * 4;  // row-down cross-warp partials
+constexpr int BAR_BYTES = 2 * LMAX_STAGES * 8 + 64;  // mbarriers + flags
+constexpr int SMEM_LIMIT = 232448;
+// gradient passes: row-down chunks per stage and smem budget, col-red stages,
+// pass-2 CTAs per SM
+constexpr int G1_RD_CH = 8, G1_RD_BUDGET = 156 * 1024, G1_CR_STAGES = 2, G2_CR_STAGES = 4, G2_CTAS_PER_SM = 1;
 
 // ------------------------------------------------------------------ helpers
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-__device__ __forceinline__ uint4 ld16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// Address of 16-byte chunk `chunk` of row `row` in a tile written by TMA.
+// 128-byte rows with the 128-byte swizzle (tile base 1024-byte aligned): the
+// chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int chunk) {
+  return base + static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+// 32-byte rows with the 32-byte swizzle (tile base 256-byte aligned): the
+// chunk index (0 or 1) is XORed with bit 2 of the row.
+__device__ __forceinline__ uint32_t sw32(uint32_t base, int row, int chunk) {
+  return base + static_cast<uint32_t>(row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4));
+}
+// the consumer warps of one role (named barrier `id`, 256 threads)
+__device__ __forceinline__ void group_bar(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(LCW * 32) : "memory");
+}
+
 __device__ __forceinline__ uint2 ld8(const void* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
-__device__ __forceinline__ float4 ld16f(const void* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 
-__device__ __forceinline__ uint32_t movtrans(uint32_t a) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-  return d;
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
-  return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-}
 template <bool BF16>
 __device__ __forceinline__ float round16(float x) {
   return BF16 ? __bfloat162float(__float2bfloat16_rn(x)) : __half2float(__float2half_rn(x));
 }
-// x = hi + lo + O(2^-16 |x|): both parts as packed pairs
 template <bool BF16>
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const float h0 = round16<BF16>(x0), h1 = round16<BF16>(x1);
-  hi = pack16x2<BF16>(h0, h1);
-  lo = pack16x2<BF16>(x0 - h0, x1 - h1);
+__device__ __forceinline__ uint16_t bits16(float x) {
+  if (BF16) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+  } else {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
 }
 
 __device__ __forceinline__ void store_out(void* out, int kind, size_t i, float v) {
@@ -93,103 +135,531 @@ __device__ __forceinline__ void store8(void* out, int kind, size_t i, const floa
   }
 }
 
-// ===================================================================
-// Role 1: row-down.  OUT[t, r] = sum_k IN[t, k] * S[r, k]   (r < 16)
-//   IN [T, K] 16-bit (the streamed tensor), S [16, K] 16-bit row-major.
-// CTA = 16 rows; its 8 warps take 64-wide K chunks round-robin, two chunks
-// per iteration (16 x 16-byte loads in flight per thread); the 8 partial
-// 16x16 tiles are added in warp order through shared memory.
-// ===================================================================
-struct RdFrag {
-  uint4 xa[2], xb[2], s0[2], s1[2];
+// Producer epilogue after an aborted wait: let every copy already issued
+// land before the CTA unwinds (bounded, without the abort short-cut).
+__device__ __forceinline__ void drain_issued(const uint64_t* full, const int* issued, int stages,
+                                             unsigned int* status) {
+  for (int s = 0; s < stages; ++s)
+    if (issued[s] >= 0)
+      mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>(issued[s]), 200000000ull, nullptr, status, 0x2F);
+}
+
+// Per-CTA event timestamps of a role, only in -DTG_TRACE builds.
+#ifdef TG_TRACE
+#define LORA_EVENT(tr, ev)                                                \
+  do {                                                                    \
+    if (tr) (tr)[blockIdx.x * 16 + (ev)] = globaltimer_ns();             \
+  } while (0)
+#else
+#define LORA_EVENT(tr, ev) \
+  do {                     \
+  } while (0)
+#endif
+
+// The barrier block of a role: full[LMAX_STAGES], empty[LMAX_STAGES], flags.
+struct RoleBars {
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* flags;  // [0] abort, [1] shared decision, [2] last-contributor
+  __device__ RoleBars(uint8_t* p)
+      : full(reinterpret_cast<uint64_t*>(p)),
+        empty(reinterpret_cast<uint64_t*>(p) + LMAX_STAGES),
+        flags(reinterpret_cast<volatile int*>(p + 2 * LMAX_STAGES * 8)) {}
+  __device__ void init(int stages, int consumer_warps = LCW) const {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), static_cast<uint32_t>(consumer_warps));
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+  }
 };
 
-// loads of one 64-wide K chunk (zeros past K or past T)
-__device__ __forceinline__ void rowdown_load(RdFrag& f, const uint16_t* pa, const uint16_t* pb, const uint16_t* S,
-                                             int K, int k0, bool va, bool vb, int g, int c) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int k = k0 + 32 * h + 8 * c;
-    const bool kv = k < K;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    f.xa[h] = (kv && va) ? ld_stream16(pa + k) : z;
-    f.xb[h] = (kv && vb) ? ld_stream16(pb + k) : z;
-    f.s0[h] = kv ? ld16(S + static_cast<size_t>(g) * K + k) : z;
-    f.s1[h] = kv ? ld16(S + static_cast<size_t>(8 + g) * K + k) : z;
+// ===================================================================
+// Role 1: row-down.  OUT[t, r] = sum_k IN[t, k] S(r, k), r < 16.
+// A stage holds CH 64-column chunks of the CTA's R rows and of S, loaded by
+// one 3-D TMA box each: IN viewed as [K/64 chunks][T rows][64], box
+// {64, R, CH}; S viewed as [K/64][16][64] (S_KN = false: S stored [16][K],
+// the LoRA A) or [K/64][64][16] (S_KN = true: S stored [K][16], the LoRA B).
+// Only whole chunks are viewed that way; a last partial chunk (K % 64 != 0)
+// has a stage of its own, loaded through plain 2-D maps whose box reads
+// zeros past K.  Chunks of a 3-D box past the last whole chunk read as zeros.
+// Shared memory per stage: IN [CH][R rows][128 B] (128-byte swizzle, counted
+// in 128-byte rows from the stage base), S [CH][2 KB]; then the cross-warp
+// partials [8][32][17] f32 and the barrier block.
+// ===================================================================
+struct RdArgs {
+  int T, K, R, CH, stages;
+  int nfull;  // whole 64-column chunks
+  int nst3;   // stages of whole chunks (3-D boxes)
+  int tail;   // 1: one more stage with the partial chunk
+  int xs;     // bytes of a stage's IN part
+  void* out;     // [T][16]
+  int out_kind;
+  uint16_t* hi;  // optional hi/lo split of the FP32 result, [T][16] 16-bit each
+  uint16_t* lo;
+  unsigned long long timeout_ns;
+  unsigned int* status;
+  unsigned long long* trace;
+};
+
+__host__ __device__ inline int rd_r16(int R) { return (R + 15) & ~15; }
+// IN part of a stage: the rows a consumer may address (the last chunk's row
+// groups run R16 - R rows past its box), rounded to the 1024-byte swizzle atom
+__host__ __device__ inline int rd_xs(int R, int CH) { return ((CH * R + rd_r16(R) - R) * 128 + 1023) & ~1023; }
+__host__ __device__ inline int rd_ring_bytes(int R, int CH, int stages) { return stages * (rd_xs(R, CH) + CH * 2048); }
+// the role's share of shared memory (1024-byte multiple)
+__host__ __device__ inline int rd_region_bytes(int R, int CH, int stages) {
+  return (rd_ring_bytes(R, CH, stages) + RD_RED_BYTES + BAR_BYTES + 1023) & ~1023;
+}
+// 16-byte chunk `chunk` of 128-byte row `seg` counted from a 1024-aligned base
+__device__ __forceinline__ uint32_t sw128s(uint32_t base, int seg, int chunk) {
+  return base + static_cast<uint32_t>(seg * 128 + ((chunk ^ (seg & 7)) << 4));
+}
+
+struct RdMaps {
+  CUtensorMap x, s, x3, s3;  // 2-D (partial chunk) and 3-D (whole chunks) views
+};
+
+__device__ __forceinline__ RoleBars rd_bars(const RdArgs& a, uint8_t* smem) {
+  return RoleBars(smem + rd_ring_bytes(a.R, a.CH, a.stages) + RD_RED_BYTES);
+}
+
+__device__ __forceinline__ void rowdown_init(const RdArgs& a, const RdMaps* m, uint8_t* smem, int tid) {
+  if (tid == 0) rd_bars(a, smem).init(a.stages);
+  if (tid == LCW * 32) {
+    if (a.nst3 > 0) {
+      prefetch_tmap(&m->x3);
+      prefetch_tmap(&m->s3);
+    }
+    if (a.tail) {
+      prefetch_tmap(&m->x);
+      prefetch_tmap(&m->s);
+    }
   }
 }
 
-template <bool BF16>
-__device__ __forceinline__ void rowdown_mma(const RdFrag& f, float (&acc)[2][4]) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    {
-      const uint32_t a[4] = {f.xa[h].x, f.xb[h].x, f.xa[h].y, f.xb[h].y};
-      const uint32_t b0[2] = {f.s0[h].x, f.s0[h].y}, b1[2] = {f.s1[h].x, f.s1[h].y};
-      mma_16816<BF16>(acc[0], a, b0);
-      mma_16816<BF16>(acc[1], a, b1);
-    }
-    {
-      const uint32_t a[4] = {f.xa[h].z, f.xb[h].z, f.xa[h].w, f.xb[h].w};
-      const uint32_t b0[2] = {f.s0[h].z, f.s0[h].w}, b1[2] = {f.s1[h].z, f.s1[h].w};
-      mma_16816<BF16>(acc[0], a, b0);
-      mma_16816<BF16>(acc[1], a, b1);
-    }
-  }
-}
+template <bool BF16, bool S_KN>
+__device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t* smem, int tid, int bar_id) {
+  const int R16 = rd_r16(a.R);
+  const int stage_bytes = a.xs + a.CH * 2048;
+  const uint32_t sbase = smem_u32(smem);
+  float* red = reinterpret_cast<float*>(smem + rd_ring_bytes(a.R, a.CH, a.stages));
+  const RoleBars rb = rd_bars(a, smem);
+  volatile int* abort_flag = rb.flags;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nst = a.nst3 + a.tail;
+  const int row0 = tile * a.R;
 
-template <bool BF16>
-__device__ void rowdown_role(int cta, const uint16_t* __restrict__ IN, const uint16_t* __restrict__ S,
-                             void* __restrict__ OUT, int out_kind, int T, int K, float* red /* [8][16][17] */) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int t0 = cta * 16;
-  const int ra = t0 + g, rb = t0 + g + 8;
-  const bool va = ra < T, vb = rb < T;
-  const uint16_t* pa = IN + static_cast<size_t>(va ? ra : 0) * K;
-  const uint16_t* pb = IN + static_cast<size_t>(vb ? rb : 0) * K;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  const int nch = (K + 63) / 64;
-  // two chunks per iteration: all 16 loads are issued before the MMAs
-  for (int ch = warp; ch < nch; ch += 16) {
-    RdFrag f0, f1;
-    rowdown_load(f0, pa, pb, S, K, ch * 64, va, vb, g, c);
-    rowdown_load(f1, pa, pb, S, K, (ch + 8) * 64, va, vb, g, c);  // zeros when past K
-    rowdown_mma<BF16>(f0, acc);
-    rowdown_mma<BF16>(f1, acc);
+  if (warp == LCW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    LORA_EVENT(a.trace, 0);
+    int issued[LMAX_STAGES];
+    for (int s = 0; s < LMAX_STAGES; ++s) issued[s] = -1;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % a.stages;
+      const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+      if (!mbar_wait(smem_u32(&rb.empty[slot]), ph ^ 1u, a.timeout_ns, abort_flag, a.status, 0x21)) {
+        drain_issued(rb.full, issued, a.stages, a.status);
+        return;
+      }
+      const uint32_t fb = smem_u32(&rb.full[slot]);
+      const uint32_t xd = sbase + static_cast<uint32_t>(slot * stage_bytes);
+      const uint32_t sd = xd + static_cast<uint32_t>(a.xs);
+      if (s < a.nst3) {
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.CH * (a.R * 128 + 2048)));
+        tma_load_3d(xd, &mp->x3, fb, 0, row0, s * a.CH);
+        tma_load_3d(sd, &mp->s3, fb, 0, 0, s * a.CH);
+      } else {  // the partial last chunk
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.R * 128 + 2048));
+        tma_load_3d(xd, &mp->x, fb, a.nfull * 64, row0, 0);
+        if (S_KN)
+          tma_load_3d(sd, &mp->s, fb, 0, a.nfull * 64, 0);
+        else
+          tma_load_3d(sd, &mp->s, fb, a.nfull * 64, 0, 0);
+      }
+      issued[slot] = static_cast<int>(ph);
+    }
+    return;
   }
-  // acc[nb]: rows g / g+8, columns 8*nb + 2c, +1
-  float* rw = red + warp * (16 * 17);
+
+  // -------------------------------------------------------------- consumers
+  const int m = lane >> 3, i = lane & 7, g = lane >> 2, c = lane & 3;
+  const int cw = warp % a.CH;                     // chunk of each stage this warp takes
+  const int rgs = LCW / a.CH, rg0 = warp / a.CH;  // row groups rg with rg % rgs == rg0
+  const int nrg = R16 / 16;
+  float acc[2][2][4];
 #pragma unroll
-  for (int nb = 0; nb < 2; ++nb) {
-    rw[g * 17 + 8 * nb + 2 * c] = acc[nb][0];
-    rw[g * 17 + 8 * nb + 2 * c + 1] = acc[nb][1];
-    rw[(g + 8) * 17 + 8 * nb + 2 * c] = acc[nb][2];
-    rw[(g + 8) * 17 + 8 * nb + 2 * c + 1] = acc[nb][3];
-  }
-  __syncthreads();
-  {
-    const int o = threadIdx.x;  // 256 threads: one output each
-    const int rr = o >> 4, cc = o & 15;
-    float s = red[rr * 17 + cc];
+  for (int rg = 0; rg < 2; ++rg)
 #pragma unroll
-    for (int w = 1; w < 8; ++w) s += red[w * (16 * 17) + rr * 17 + cc];
-    if (t0 + rr < T) store_out(OUT, out_kind, static_cast<size_t>(t0 + rr) * LR + cc, s);
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[rg][nb][q] = 0.f;
+  for (int s = 0; s < nst; ++s) {
+    const int slot = s % a.stages;
+    const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+    if (!mbar_wait(smem_u32(&rb.full[slot]), ph, a.timeout_ns, abort_flag, a.status, 0x22)) break;
+    if (tid == 0 && s == 0) LORA_EVENT(a.trace, 2);
+    if (tid == 0 && s == nst - 1) LORA_EVENT(a.trace, 3);
+    if (s < a.nst3 || cw == 0) {
+      const uint32_t xb = sbase + static_cast<uint32_t>(slot * stage_bytes);
+      const uint32_t sb = xb + static_cast<uint32_t>(a.xs + cw * 2048);
+      const int seg0 = cw * a.R;  // first 128-byte row of this chunk in the stage
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // b[0..1]: n-block 0 (r 0-7), b[2..3]: n-block 1 (r 8-15)
+        uint32_t b[4];
+        if (S_KN)
+          ldsm_x4_t(sw32(sb, kk * 16 + (m & 1) * 8 + i, m >> 1), b);
+        else
+          ldsm_x4(sw128(sb, (m >> 1) * 8 + i, 2 * kk + (m & 1)), b);
+#pragma unroll
+        for (int rg = 0; rg < 2; ++rg) {
+          if (rg < nrg && rg % rgs == rg0) {
+            uint32_t af[4];
+            ldsm_x4(sw128s(xb, seg0 + rg * 16 + (m & 1) * 8 + i, 2 * kk + (m >> 1)), af);
+            mma_16816<BF16>(acc[rg][0], af, b);
+            mma_16816<BF16>(acc[rg][1], af, b + 2);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));
   }
+  // this warp's partial tile -> red[warp]; rows rg*16 + g (+8), columns nb*8 + 2c (+1)
+  float* rw = red + warp * (32 * 17);
+#pragma unroll
+  for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      const int r0 = rg * 16 + g, col = nb * 8 + 2 * c;
+      rw[r0 * 17 + col] = acc[rg][nb][0];
+      rw[r0 * 17 + col + 1] = acc[rg][nb][1];
+      rw[(r0 + 8) * 17 + col] = acc[rg][nb][2];
+      rw[(r0 + 8) * 17 + col + 1] = acc[rg][nb][3];
+    }
+  group_bar(bar_id);
+  if (*abort_flag) return;  // no barrier follows: a divergent decision is harmless
+  for (int o = tid; o < R16 * LR; o += LCW * 32) {
+    const int row = o >> 4, col = o & 15;
+    float v = red[row * 17 + col];
+#pragma unroll
+    for (int w = 1; w < LCW; ++w) v += red[w * (32 * 17) + row * 17 + col];
+    const int t = row0 + row;
+    if (row < a.R && t < a.T) {
+      const size_t e = static_cast<size_t>(t) * LR + col;
+      store_out(a.out, a.out_kind, e, v);
+      if (a.hi != nullptr) {
+        const float h = round16<BF16>(v);
+        a.hi[e] = bits16<BF16>(h);
+        a.lo[e] = bits16<BF16>(v - h);
+      }
+    }
+  }
+  if (tid == 0) LORA_EVENT(a.trace, 4);
 }
 
 // ===================================================================
-// Role 2: row-up.  OUT[t, j] = sum_r Hm[t, r] * S2[j, r]
-//   Hm [T, 16] 16-bit, or FP32 (HF32: split into hi + lo), S2 [J, 16] 16-bit.
+// Role 2: column reduction over tokens, optionally fused with a row-up.
+//   P[j, r] = sum_t IN[t, j] Hm[t, r]           (Hm 16-bit, or hi + lo parts)
+//   UP:  OUT[t, j] = sum_r Hm[t, r] S2[r, j]    (S2 = the LoRA A, [16][J])
+// Work: steps p = jb * nsteps + s over 128-column blocks jb and 128-token
+// steps s; CTA c takes steps [c*N/G, (c+1)*N/G).  A stage holds the IN tile
+// [128 tokens][128 columns] (two boxes {64, 128}, 128-byte swizzle), the Hm
+// tile(s) [128][16] (box {16, 128}, 32-byte swizzle) and, with UP, the S2
+// tile [16][128 columns] (two boxes {64, 16}).
+// Column reduction: consumer warp w owns the 16-column M-tile w of the block
+// over all 128 tokens of a step; MMA with M = column, K = token;
+// ldmatrix.trans of the [token][column] tile gives the A fragments and of the
+// [token][r] tile the B fragments.  When the CTA's range leaves a column
+// block (or ends) each warp stores its partial to P[c][k] (k-th block of the
+// range); a separate pass adds the partials of a block in CTA order.
+// Row-up (UP): a second group of 8 warps reads the Hm and S2 tiles of the
+// same stages; warp w computes tokens 16w..16w+15 of a step x 128 columns
+// (M = token, N = column, K = r) and stores them straight from registers:
+// the N index is permuted within each 32-column group (n-slot g of N-tile t
+// is column 8*(g/2) + 2t + g%2), so each thread ends with 8 consecutive
+// columns of its two rows, one 16-byte store each.
+// ===================================================================
+constexpr int CR_CB = 128;  // columns per block
+
+struct CrArgs {
+  int T, J, nj, nsteps, stages, G;
+  long long N;   // nj * nsteps
+  int max_segs;  // partial slots per CTA
+  float* P;      // [G][max_segs][128][16]
+  void* out;     // UP: the row-up output [T][J]
+  int out_kind;
+  unsigned long long timeout_ns;
+  unsigned int* status;
+  unsigned long long* trace;
+};
+
+__host__ __device__ inline long long cr_start(long long c, const CrArgs& a) { return c * a.N / a.G; }
+// the CTA whose range holds step p
+__host__ __device__ inline int cr_cta_of(long long p, const CrArgs& a) {
+  int c = static_cast<int>(p * a.G / a.N);
+  while (c + 1 < a.G && cr_start(c + 1, a) <= p) ++c;
+  while (c > 0 && cr_start(c, a) > p) --c;
+  return c;
+}
+
+__host__ __device__ inline int cr_stage_bytes(int nh, bool up) { return 32768 + nh * 4096 + (up ? 4096 : 0); }
+__host__ __device__ inline int cr_region_bytes(int stages, int nh, bool up) {
+  return (stages * cr_stage_bytes(nh, up) + BAR_BYTES + 1023) & ~1023;
+}
+
+struct CrMaps {
+  CUtensorMap in, h, hlo, s2;
+};
+
+__device__ __forceinline__ RoleBars cr_bars(const CrArgs& a, int nh, bool up, uint8_t* smem) {
+  return RoleBars(smem + a.stages * cr_stage_bytes(nh, up));
+}
+
+template <bool HILO, bool UP>
+__device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, uint8_t* smem, int tid) {
+  if (tid == 0) cr_bars(a, HILO ? 2 : 1, UP, smem).init(a.stages, UP ? 2 * LCW : LCW);
+  if (tid == (UP ? 2 * LCW : LCW) * 32) {
+    prefetch_tmap(&m->in);
+    prefetch_tmap(&m->h);
+    if (HILO) prefetch_tmap(&m->hlo);
+    if (UP) prefetch_tmap(&m->s2);
+  }
+}
+
+template <bool BF16, bool HILO, bool UP>
+__device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid) {
+  constexpr int NH = HILO ? 2 : 1;
+  constexpr int SB = 32768 + NH * 4096 + (UP ? 4096 : 0);
+  constexpr int HOFF = 32768, S2OFF = 32768 + NH * 4096;
+  const int cta = blockIdx.x;
+  if (cta >= a.G) return;
+  const long long p0 = cr_start(cta, a), p1 = cr_start(cta + 1, a);
+  const int nst = static_cast<int>(p1 - p0);
+  const uint32_t sbase = smem_u32(smem);
+  const RoleBars rb = cr_bars(a, NH, UP, smem);
+  volatile int* abort_flag = rb.flags;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  if (warp == (UP ? 2 * LCW : LCW)) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    LORA_EVENT(a.trace, 0);
+    int issued[LMAX_STAGES];
+    for (int s = 0; s < LMAX_STAGES; ++s) issued[s] = -1;
+    for (int s = 0; s < nst; ++s) {
+      const long long p = p0 + s;
+      const int jb = static_cast<int>(p / a.nsteps), t0 = static_cast<int>(p % a.nsteps) * CR_RS;
+      const int slot = s % a.stages;
+      const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+      if (!mbar_wait(smem_u32(&rb.empty[slot]), ph ^ 1u, a.timeout_ns, abort_flag, a.status, 0x23)) {
+        drain_issued(rb.full, issued, a.stages, a.status);
+        return;
+      }
+      const uint32_t fb = smem_u32(&rb.full[slot]);
+      const uint32_t dst = sbase + static_cast<uint32_t>(slot * SB);
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(SB));
+      tma_load_3d(dst, &mp->in, fb, jb * CR_CB, t0, 0);
+      tma_load_3d(dst + 16384, &mp->in, fb, jb * CR_CB + 64, t0, 0);
+      tma_load_3d(dst + HOFF, &mp->h, fb, 0, t0, 0);
+      if (HILO) tma_load_3d(dst + HOFF + 4096, &mp->hlo, fb, 0, t0, 0);
+      if (UP) {
+        tma_load_3d(dst + S2OFF, &mp->s2, fb, jb * CR_CB, 0, 0);
+        tma_load_3d(dst + S2OFF + 2048, &mp->s2, fb, jb * CR_CB + 64, 0, 0);
+      }
+      issued[slot] = static_cast<int>(ph);
+    }
+    return;
+  }
+
+  const int m = lane >> 3, i = lane & 7, g = lane >> 2, c = lane & 3;
+  if (UP && warp >= LCW) {
+    // ---------------------------------------------- row-up warps (UP only)
+    // warp LCW + w computes tokens 16w..16w+15 of every step x 128 columns
+    const int w = warp - LCW;
+    uint32_t bup[4][4][2];  // B fragments of the column block (4 groups of 32 columns x 4 N-tiles)
+    bool uok = true;
+    for (int s = 0; s < nst; ++s) {
+      const long long p = p0 + s;
+      const int jb = static_cast<int>(p / a.nsteps), t0 = static_cast<int>(p % a.nsteps) * CR_RS;
+      const int slot = s % a.stages;
+      const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+      if (uok && !mbar_wait(smem_u32(&rb.full[slot]), ph, a.timeout_ns, abort_flag, a.status, 0x25)) uok = false;
+      const uint32_t st = sbase + static_cast<uint32_t>(slot * SB);
+      uint32_t ah[4] = {0u, 0u, 0u, 0u}, al[4] = {0u, 0u, 0u, 0u};
+      if (uok) {
+        if (s == 0 || p % a.nsteps == 0) {
+          // b0 = rows r 2c,2c+1 and b1 = rows 2c+8,2c+9 of the S2 tile at
+          // column 32q + 8(g/2) + 2t + g%2 (S2 tiles: 64 columns each)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int col = 32 * (q & 1) + 8 * (g >> 1) + 2 * t + (g & 1);
+              const uint32_t s2b = st + S2OFF + (q >> 1) * 2048;
+              uint32_t v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int r = (u >> 1) * 8 + 2 * c + (u & 1);
+                uint16_t x;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(x) : "r"(sw128(s2b, r, col >> 3) + (col & 7) * 2));
+                v[u] = x;
+              }
+              bup[q][t][0] = v[0] | (v[1] << 16);
+              bup[q][t][1] = v[2] | (v[3] << 16);
+            }
+        }
+        ldsm_x4(sw32(st + HOFF, w * 16 + (m & 1) * 8 + i, m >> 1), ah);
+        if (HILO) ldsm_x4(sw32(st + HOFF + 4096, w * 16 + (m & 1) * 8 + i, m >> 1), al);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));  // the stage is no longer read
+      if (!uok) continue;
+      const int ra = t0 + w * 16 + g, rb2 = ra + 8;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float d[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+          mma_16816<BF16>(d[t], ah, bup[q][t]);
+          if (HILO) mma_16816<BF16>(d[t], al, bup[q][t]);
+        }
+        const int j = jb * CR_CB + 32 * q + 8 * c;  // this thread's 8 consecutive columns
+        if (j < a.J) {
+          float v[8];
+          if (ra < a.T) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              v[2 * t] = d[t][0];
+              v[2 * t + 1] = d[t][1];
+            }
+            store8(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + j, v);
+          }
+          if (rb2 < a.T) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              v[2 * t] = d[t][2];
+              v[2 * t + 1] = d[t][3];
+            }
+            store8(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + j, v);
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------ col-red consumers
+  // warp w: columns 16w..16w+15 of the block = chunks 2(w%4), 2(w%4)+1 of IN tile w/4
+  float acc[2][4], accl[2][4];  // hi and lo products: two independent chains
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nb][e] = accl[nb][e] = 0.f;
+  int seg = 0;
+  bool ok = true;
+  for (int s = 0; s < nst; ++s) {
+    const long long p = p0 + s;
+    const int slot = s % a.stages;
+    const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+    if (ok && !mbar_wait(smem_u32(&rb.full[slot]), ph, a.timeout_ns, abort_flag, a.status, 0x24)) ok = false;
+    if (tid == 0 && s == 0) LORA_EVENT(a.trace, 2);
+    if (tid == 0 && s == nst - 1) LORA_EVENT(a.trace, 3);
+    const uint32_t st = sbase + static_cast<uint32_t>(slot * SB);
+    const uint32_t inb = st + (warp >> 2) * 16384;
+    if (ok) {
+#pragma unroll
+      for (int ks = 0; ks < CR_RS / 16; ++ks) {
+        uint32_t af[4], bf[4];
+        ldsm_x4_t(sw128(inb, ks * 16 + (m >> 1) * 8 + i, (warp & 3) * 2 + (m & 1)), af);
+        ldsm_x4_t(sw32(st + HOFF, ks * 16 + (m & 1) * 8 + i, m >> 1), bf);
+        mma_16816<BF16>(acc[0], af, bf);
+        mma_16816<BF16>(acc[1], af, bf + 2);
+        if (HILO) {
+          ldsm_x4_t(sw32(st + HOFF + 4096, ks * 16 + (m & 1) * 8 + i, m >> 1), bf);
+          mma_16816<BF16>(accl[0], af, bf);
+          mma_16816<BF16>(accl[1], af, bf + 2);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));
+    // end of this CTA's part of a column block: this warp's 16 columns of the partial
+    if ((p + 1) % a.nsteps == 0 || s == nst - 1) {
+      if (ok) {
+        float* dst = a.P + (static_cast<size_t>(cta) * a.max_segs + seg) * CR_CB * LR;
+        const int jl = warp * 16 + g;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const int r = nb * 8 + 2 * c;
+          *reinterpret_cast<float2*>(dst + jl * LR + r) = make_float2(acc[nb][0] + accl[nb][0], acc[nb][1] + accl[nb][1]);
+          *reinterpret_cast<float2*>(dst + (jl + 8) * LR + r) =
+              make_float2(acc[nb][2] + accl[nb][2], acc[nb][3] + accl[nb][3]);
+        }
+      }
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nb][e] = accl[nb][e] = 0.f;
+      ++seg;
+    }
+  }
+  if (tid == 0) LORA_EVENT(a.trace, 4);
+}
+
+// Finish of a column reduction: out element (j, r) = sum over the CTAs that
+// worked on column block j / 128, in CTA order, of their partials.
+//   transposed = 0: out is [J][16] (dB);  1: out is [16][J] (dA)
+__device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, int transposed, int jb, int e) {
+  const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
+  const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
+  const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);  // slot of c0; every later one uses slot 0
+  constexpr int CB = 8;  // contributors whose loads are in flight together
+  float v = 0.f;
+  for (int cb = c0; cb <= c1; cb += CB) {
+    float x[CB];
+#pragma unroll
+    for (int q = 0; q < CB; ++q) {
+      const int cc = cb + q;
+      x[q] = cc <= c1 ? __ldcg(a.P + (static_cast<size_t>(cc) * a.max_segs + (cc == c0 ? k0 : 0)) * (CR_CB * LR) + e)
+                      : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < CB; ++q) v += x[q];
+  }
+  const int j = jb * CR_CB + (e >> 4), r = e & 15;
+  if (j < a.J) store_out(out, kind, transposed ? static_cast<size_t>(r) * a.J + j : static_cast<size_t>(j) * LR + r, v);
+}
+
+// ===================================================================
+// Role 3: row-up.  OUT[t, j] = sum_r Hm[t, r] S2(j, r), S2 = the LoRA B [J][16].
 // A warp owns 32 output columns of a 256-column CTA slab and walks 16-row
-// blocks.  Output columns are permuted across the four n-blocks so that each
-// thread ends with 8 consecutive columns of its two rows: one 16-byte store
-// per row.  K = 16 is permuted too: slots 2c,2c+1 <- r 4c,4c+1 and slots
-// 2c+8,2c+9 <- r 4c+2,4c+3, so 8 bytes of Hm and of S2 feed a fragment.
+// blocks blk = cta_t, cta_t + n_t, ...; the Hm fragments of RU_PRE blocks are
+// loaded before the first of them is used.  Output columns are permuted
+// across the four n-blocks so that each thread ends with 8 consecutive
+// columns of its two rows (one 16-byte store per row).  K = 16 is permuted
+// too: MMA slots 2c,2c+1 <- r 4c,4c+1 and slots 2c+8,2c+9 <- r 4c+2,4c+3, so
+// 8 bytes of Hm feed a fragment.
 // ===================================================================
-template <bool BF16, bool HF32>
-__device__ void rowup_role(int cta_j, int cta_t, int n_t, const void* __restrict__ Hm,
-                           const uint16_t* __restrict__ S2, void* __restrict__ OUT, int out_kind, int T, int J) {
+constexpr int RU_PRE = 4;
+
+struct RuArgs {
+  const uint16_t* H;
+  const uint16_t* S2;
+  void* out;
+  int out_kind;
+  int T, J, n_t;
+};
+
+template <bool BF16>
+__device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int J = a.J, T = a.T;
   const int j0 = cta_j * 256 + warp * 32;
   if (j0 >= J) return;
   // B fragments for the 4 n-blocks: column of n-slot g in block jb
@@ -197,387 +667,381 @@ __device__ void rowup_role(int cta_j, int cta_t, int n_t, const void* __restrict
 #pragma unroll
   for (int jb = 0; jb < 4; ++jb) {
     const int col = j0 + 8 * (g >> 1) + 2 * jb + (g & 1);
-    const uint2 v = col < J ? ld8(S2 + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0, 0);
+    const uint2 v = col < J ? ld8(a.S2 + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
     bfr[jb][0] = v.x;
     bfr[jb][1] = v.y;
   }
   const bool colv = j0 + 8 * c < J;  // this thread's 8 output columns exist (J % 8 == 0)
   const int nblk = (T + 15) / 16;
-  for (int blk = cta_t; blk < nblk; blk += n_t) {
-    const int ra = blk * 16 + g, rb = ra + 8;
-    const bool va = ra < T, vb = rb < T;
-    float acc[4][4];
+  for (int blk0 = cta_t; blk0 < nblk; blk0 += RU_PRE * a.n_t) {
+    uint2 ha[RU_PRE], hb[RU_PRE];
 #pragma unroll
-    for (int jb = 0; jb < 4; ++jb) acc[jb][0] = acc[jb][1] = acc[jb][2] = acc[jb][3] = 0.f;
-    if (HF32) {
-      const float* H = static_cast<const float*>(Hm);
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 ha = va ? ld16f(H + static_cast<size_t>(ra) * LR + 4 * c) : z;
-      const float4 hb = vb ? ld16f(H + static_cast<size_t>(rb) * LR + 4 * c) : z;
-      uint32_t ah[4], al[4];
-      split2<BF16>(ha.x, ha.y, ah[0], al[0]);
-      split2<BF16>(hb.x, hb.y, ah[1], al[1]);
-      split2<BF16>(ha.z, ha.w, ah[2], al[2]);
-      split2<BF16>(hb.z, hb.w, ah[3], al[3]);
-#pragma unroll
-      for (int jb = 0; jb < 4; ++jb) {
-        mma_16816<BF16>(acc[jb], ah, bfr[jb]);
-        mma_16816<BF16>(acc[jb], al, bfr[jb]);
-      }
-    } else {
-      const uint16_t* H = static_cast<const uint16_t*>(Hm);
-      const uint2 z = make_uint2(0, 0);
-      const uint2 ha = va ? ld8(H + static_cast<size_t>(ra) * LR + 4 * c) : z;
-      const uint2 hb = vb ? ld8(H + static_cast<size_t>(rb) * LR + 4 * c) : z;
-      const uint32_t a[4] = {ha.x, hb.x, ha.y, hb.y};
-#pragma unroll
-      for (int jb = 0; jb < 4; ++jb) mma_16816<BF16>(acc[jb], a, bfr[jb]);
+    for (int u = 0; u < RU_PRE; ++u) {
+      const int ra = (blk0 + u * a.n_t) * 16 + g, rb = ra + 8;
+      const uint2 z = make_uint2(0u, 0u);
+      ha[u] = ra < T ? ld8(a.H + static_cast<size_t>(ra) * LR + 4 * c) : z;
+      hb[u] = rb < T ? ld8(a.H + static_cast<size_t>(rb) * LR + 4 * c) : z;
     }
-    // thread (g, c): rows ra / rb, columns j0 + 8c + 2*jb + {0,1}
-    if (colv) {
-      float v[8];
-      if (va) {
+#pragma unroll
+    for (int u = 0; u < RU_PRE; ++u) {
+      const int blk = blk0 + u * a.n_t;
+      if (blk >= nblk) break;  // warp-uniform: the MMAs below need the whole warp
+      const int ra = blk * 16 + g, rb = ra + 8;
+      float acc[4][4];
+#pragma unroll
+      for (int jb = 0; jb < 4; ++jb) acc[jb][0] = acc[jb][1] = acc[jb][2] = acc[jb][3] = 0.f;
+      const uint32_t ah[4] = {ha[u].x, hb[u].x, ha[u].y, hb[u].y};
+#pragma unroll
+      for (int jb = 0; jb < 4; ++jb) mma_16816<BF16>(acc[jb], ah, bfr[jb]);
+      // thread (g, c): rows ra / rb, columns j0 + 8c + 2*jb + {0,1}
+      if (colv) {
+        float v[8];
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           v[2 * jb] = acc[jb][0];
           v[2 * jb + 1] = acc[jb][1];
         }
-        store8(OUT, out_kind, static_cast<size_t>(ra) * J + j0 + 8 * c, v);
-      }
-      if (vb) {
+        if (ra < T) store8(a.out, a.out_kind, static_cast<size_t>(ra) * J + j0 + 8 * c, v);
+        if (rb < T) {
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          v[2 * jb] = acc[jb][2];
-          v[2 * jb + 1] = acc[jb][3];
+          for (int jb = 0; jb < 4; ++jb) {
+            v[2 * jb] = acc[jb][2];
+            v[2 * jb + 1] = acc[jb][3];
+          }
+          store8(a.out, a.out_kind, static_cast<size_t>(rb) * J + j0 + 8 * c, v);
         }
-        store8(OUT, out_kind, static_cast<size_t>(rb) * J + j0 + 8 * c, v);
       }
     }
-  }
-}
-
-// ===================================================================
-// Role 3: column reduction over tokens.
-//   P[part, j, r] = sum_{t in part} IN[t, j] * Hm[t, r]
-// IN [T, J] 16-bit (streamed), Hm [T, 16] 16-bit or FP32 (hi + lo).
-// A warp owns 32 columns and a row range; per 16-row step each thread loads
-// 8 columns of rows g and g+8 (16 bytes each).  movmatrix.trans turns word w
-// of those loads into (token pairs 2c,2c+1 ; column jcol(g, w)) -- the A
-// fragment of an MMA whose M index is the column (M slot g <- word 2p,
-// slot g+8 <- word 2p+1) and whose K index is the token.  The Hm rows are
-// transposed the same way into B fragments (n slot g <- r = 4(g>>1)+2v+(g&1)).
-// CTA = 8 warps = 2 column groups x 4 row sub-ranges; the 4 sub-range
-// partials are added in order through shared memory.
-// ===================================================================
-template <bool BF16, bool HF32>
-__device__ __forceinline__ void colred_step(const uint16_t* IN, const void* Hm, int T, int J, int t0, int j0,
-                                            int g, int c, float (&acc)[2][2][4], float (&accl)[2][2][4]) {
-  const int ra = t0 + g, rb = t0 + g + 8;
-  const bool va = ra < T, vb = rb < T;
-  const int jc = j0 + 8 * c;
-  const bool jv = jc < J;
-  const uint4 z4 = make_uint4(0, 0, 0, 0);
-  const uint4 xa = (va && jv) ? ld_stream16(IN + static_cast<size_t>(ra) * J + jc) : z4;
-  const uint4 xb = (vb && jv) ? ld_stream16(IN + static_cast<size_t>(rb) * J + jc) : z4;
-  // A fragments: [p][reg]
-  uint32_t a[2][4];
-  a[0][0] = movtrans(xa.x);
-  a[0][1] = movtrans(xa.y);
-  a[0][2] = movtrans(xb.x);
-  a[0][3] = movtrans(xb.y);
-  a[1][0] = movtrans(xa.z);
-  a[1][1] = movtrans(xa.w);
-  a[1][2] = movtrans(xb.z);
-  a[1][3] = movtrans(xb.w);
-  // B fragments: [v][reg]
-  uint32_t b[2][2], bl[2][2];
-  if (HF32) {
-    const float* H = static_cast<const float*>(Hm);
-    const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 ha = va ? ld16f(H + static_cast<size_t>(ra) * LR + 4 * c) : zf;
-    const float4 hb = vb ? ld16f(H + static_cast<size_t>(rb) * LR + 4 * c) : zf;
-    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-    split2<BF16>(ha.x, ha.y, h0, l0);  // row g,   r 4c, 4c+1
-    split2<BF16>(ha.z, ha.w, h1, l1);  // row g,   r 4c+2, 4c+3
-    split2<BF16>(hb.x, hb.y, h2, l2);  // row g+8, r 4c, 4c+1
-    split2<BF16>(hb.z, hb.w, h3, l3);  // row g+8, r 4c+2, 4c+3
-    b[0][0] = movtrans(h0);
-    b[1][0] = movtrans(h1);
-    b[0][1] = movtrans(h2);
-    b[1][1] = movtrans(h3);
-    bl[0][0] = movtrans(l0);
-    bl[1][0] = movtrans(l1);
-    bl[0][1] = movtrans(l2);
-    bl[1][1] = movtrans(l3);
-  } else {
-    const uint16_t* H = static_cast<const uint16_t*>(Hm);
-    const uint2 z2 = make_uint2(0, 0);
-    const uint2 ha = va ? ld8(H + static_cast<size_t>(ra) * LR + 4 * c) : z2;
-    const uint2 hb = vb ? ld8(H + static_cast<size_t>(rb) * LR + 4 * c) : z2;
-    b[0][0] = movtrans(ha.x);
-    b[1][0] = movtrans(ha.y);
-    b[0][1] = movtrans(hb.x);
-    b[1][1] = movtrans(hb.y);
-  }
-#pragma unroll
-  for (int p = 0; p < 2; ++p)
-#pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      mma_16816<BF16>(acc[p][v], a[p], b[v]);
-      if (HF32) mma_16816<BF16>(accl[p][v], a[p], bl[v]);
-    }
-}
-
-template <bool BF16, bool HF32>
-__device__ void colred_role(int cta_j, int part, int parts, const uint16_t* __restrict__ IN,
-                            const void* __restrict__ Hm, float* __restrict__ P, int T, int J,
-                            float* red /* [4][64][17] */) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int cg = warp & 1;   // column group within the CTA
-  const int sub = warp >> 1; // row sub-range
-  const int j0 = cta_j * 64 + cg * 32;
-  // rows of this part, split into 4 sub-ranges of whole 16-row steps
-  const int nsteps = (T + 15) / 16;
-  const int s_begin = static_cast<int>((static_cast<int64_t>(nsteps) * part) / parts);
-  const int s_end = static_cast<int>((static_cast<int64_t>(nsteps) * (part + 1)) / parts);
-  const int per = (s_end - s_begin + 3) / 4;
-  const int my_b = s_begin + sub * per;
-  const int my_e = min(s_end, my_b + per);
-  float acc[2][2][4], accl[2][2][4];
-#pragma unroll
-  for (int p = 0; p < 2; ++p)
-#pragma unroll
-    for (int v = 0; v < 2; ++v)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[p][v][q] = accl[p][v][q] = 0.f;
-  int s = my_b;
-  for (; s + 1 < my_e; s += 2) {
-    colred_step<BF16, HF32>(IN, Hm, T, J, s * 16, j0, g, c, acc, accl);
-    colred_step<BF16, HF32>(IN, Hm, T, J, (s + 1) * 16, j0, g, c, acc, accl);
-  }
-  if (s < my_e) colred_step<BF16, HF32>(IN, Hm, T, J, s * 16, j0, g, c, acc, accl);
-  // acc[p][v]: rows (M slots) g / g+8 -> columns jcol(g, 2p) / jcol(g, 2p+1);
-  // columns (N slots) 2c, 2c+1 -> r = 4c + 2v, 4c + 2v + 1
-  float* rs = red + sub * (64 * 17);
-#pragma unroll
-  for (int p = 0; p < 2; ++p)
-#pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      const int jl0 = cg * 32 + 8 * (g >> 1) + 2 * (2 * p) + (g & 1);
-      const int jl1 = cg * 32 + 8 * (g >> 1) + 2 * (2 * p + 1) + (g & 1);
-      const int r0 = 4 * c + 2 * v;
-      rs[jl0 * 17 + r0] = acc[p][v][0] + accl[p][v][0];
-      rs[jl0 * 17 + r0 + 1] = acc[p][v][1] + accl[p][v][1];
-      rs[jl1 * 17 + r0] = acc[p][v][2] + accl[p][v][2];
-      rs[jl1 * 17 + r0 + 1] = acc[p][v][3] + accl[p][v][3];
-    }
-  __syncthreads();
-  for (int o = threadIdx.x; o < 64 * LR; o += LTHREADS) {
-    const int jl = o >> 4, r = o & 15;
-    float sum = red[jl * 17 + r];
-#pragma unroll
-    for (int w = 1; w < 4; ++w) sum += red[w * (64 * 17) + jl * 17 + r];
-    const int j = cta_j * 64 + jl;
-    if (j < J) P[(static_cast<size_t>(part) * J + j) * LR + r] = sum;
   }
 }
 
 // ===================================================================
 // kernels
 // ===================================================================
-template <bool BF16>
-__global__ void __launch_bounds__(LTHREADS) lora_down_kernel(const uint16_t* X, const uint16_t* A, void* H,
-                                                             int out_kind, int T, int d_in) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float red[8 * 16 * 17];
-  rowdown_role<BF16>(blockIdx.x, X, A, H, out_kind, T, d_in, red);
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
+// H = X A^T
 template <bool BF16>
-__global__ void __launch_bounds__(LTHREADS) lora_up_kernel(const uint16_t* H, const uint16_t* B, void* Y,
-                                                           int out_kind, int T, int d_out, int n_t) {
+__global__ void __launch_bounds__(LGROUP, 1) lora_down_kernel(const __grid_constant__ RdMaps maps, const RdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  if (threadIdx.x == 0) LORA_EVENT(a.trace, 5);
+  rowdown_init(a, &maps, smem, threadIdx.x);
+  fence_mbar_init();
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  rowup_role<BF16, false>(blockIdx.x, blockIdx.y, n_t, H, B, Y, out_kind, T, d_out);
+  rowdown_run<BF16, false>(blockIdx.x, &maps, a, smem, threadIdx.x, 1);
 }
 
-// prep: Bt[r][o] = B[o][r], At[i][r] = A[r][i]
-__global__ void lora_prep_kernel(const uint16_t* A, const uint16_t* B, uint16_t* At, uint16_t* Bt, int d_in,
-                                 int d_out) {
+// Y = H B^T
+template <bool BF16>
+__global__ void __launch_bounds__(256) lora_up_kernel(const RuArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int64_t nA = static_cast<int64_t>(d_in) * LR, nB = static_cast<int64_t>(d_out) * LR;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < nA + nB;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    if (e < nA) {
-      const int64_t i = e / LR, r = e % LR;
-      At[e] = A[r * d_in + i];
-    } else {
-      const int64_t f = e - nA, r = f / d_out, o = f % d_out;
-      Bt[f] = B[o * LR + r];
-    }
-  }
+  rowup_role<BF16>(blockIdx.x, blockIdx.y, a);
 }
 
-// pass 1 over dY: row-down CTAs compute dH = dY B (FP32), column CTAs
-// compute partial dB over token parts
+// Pass 1 over dY, two roles per CTA (threads 0..287 and 288..575):
+// row-down dH = dY B (FP32, and its hi/lo parts) for the CTA's rows, and the
+// column reduction dB = dY^T H over the CTA's share of (column block, step)
+// space (partials only).
 template <bool BF16>
-__global__ void __launch_bounds__(LTHREADS) lora_grad1_kernel(const uint16_t* dY, const uint16_t* Bt,
-                                                              const uint16_t* H, float* dH, float* Pb, int T,
-                                                              int d_out, int n_rowdown, int nj_b, int parts_b) {
+__global__ void __launch_bounds__(2 * LGROUP, 1)
+    lora_grad1_kernel(const __grid_constant__ RdMaps rmaps, const __grid_constant__ CrMaps cmaps, const RdArgs rd,
+                      const CrArgs cr, int rd_region) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  uint8_t* smem_cr = smem + rd_region;
+  const int tid = threadIdx.x;
+  if (tid == 0) LORA_EVENT(rd.trace, 5);
+  if (tid < LGROUP)
+    rowdown_init(rd, &rmaps, smem, tid);
+  else
+    colred_init<false, false>(cr, &cmaps, smem_cr, tid - LGROUP);
+  fence_mbar_init();
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[4 * 64 * 17];
-  const int b = blockIdx.x;
-  if (b < n_rowdown) {
-    rowdown_role<BF16>(b, dY, Bt, dH, EK_F32, T, d_out, red);
+  if (tid < LGROUP) {
+    if (static_cast<int>(blockIdx.x) * rd.R < rd.T) rowdown_run<BF16, true>(blockIdx.x, &rmaps, rd, smem, tid, 1);
   } else {
-    const int q = b - n_rowdown;
-    colred_role<BF16, false>(q % nj_b, q / nj_b, parts_b, dY, H, Pb, T, d_out, red);
+    colred_run<BF16, false, false>(&cmaps, cr, smem_cr, tid - LGROUP);
   }
 }
 
-// pass 2: column CTAs compute partial dA^T over token parts from X and the
-// FP32 dH; row-up CTAs write dX = dH A
+// Pass 2 over X: each step reads an X tile with its dH hi/lo tiles and the
+// matching columns of A; one warp group accumulates dA^T = X^T dH (partials),
+// the other writes the dX = dH A tile.
 template <bool BF16>
-__global__ void __launch_bounds__(LTHREADS) lora_grad2_kernel(const uint16_t* X, const float* dH,
-                                                              const uint16_t* At, void* dX, int out_kind,
-                                                              float* Pa, int T, int d_in, int n_colred, int nj_a,
-                                                              int parts_a, int nj_x, int n_tx) {
+__global__ void __launch_bounds__(LGROUP_UP, 1)
+    lora_grad2_kernel(const __grid_constant__ CrMaps cmaps, const CrArgs cr) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = aligned_smem(smem_raw);
+  const int tid = threadIdx.x;
+  if (tid == 0) LORA_EVENT(cr.trace, 5);
+  colred_init<true, true>(cr, &cmaps, smem, tid);
+  fence_mbar_init();
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[4 * 64 * 17];
-  const int b = blockIdx.x;
-  if (b < n_colred) {
-    colred_role<BF16, true>(b % nj_a, b / nj_a, parts_a, X, dH, Pa, T, d_in, red);
-  } else {
-    const int q = b - n_colred;
-    rowup_role<BF16, true>(q % nj_x, q / nj_x, n_tx, dH, At, dX, out_kind, T, d_in);
-  }
+  colred_run<BF16, true, true>(&cmaps, cr, smem, tid);
 }
 
-// pass 3: dB[o][r] = sum_parts Pb ; dA[r][i] = sum_parts Pa[.][i][r] (parts in order)
-__global__ void lora_grad3_kernel(const float* Pb, const float* Pa, void* dB, void* dA, int out_kind, int d_out,
-                                  int d_in, int parts_b, int parts_a) {
+// Pass 3: dB and dA from the partials of passes 1 and 2.  CTA b takes
+// 256 elements (one per thread) of one column block; blocks of dB first.
+constexpr int FIN_SPLIT = CR_CB * LR / 256;  // CTAs per column block
+__global__ void __launch_bounds__(256) lora_grad3_kernel(const CrArgs crb, const CrArgs cra, void* dB, void* dA,
+                                                         int kind) {
   pdl_wait();
   pdl_trigger();
-  const int64_t nB = static_cast<int64_t>(d_out) * LR, nA = static_cast<int64_t>(d_in) * LR;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < nB + nA;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    if (e < nB) {
-      float s = Pb[e];
-      for (int p = 1; p < parts_b; ++p) s += Pb[static_cast<int64_t>(p) * nB + e];
-      store_out(dB, out_kind, e, s);
-    } else {
-      const int64_t f = e - nB;  // f = r * d_in + i  (dA layout)
-      const int64_t r = f / d_in, i = f % d_in;
-      const int64_t src = i * LR + r;
-      float s = Pa[src];
-      for (int p = 1; p < parts_a; ++p) s += Pa[static_cast<int64_t>(p) * nA + src];
-      store_out(dA, out_kind, f, s);
-    }
-  }
+  const int b = blockIdx.x / FIN_SPLIT, e = (blockIdx.x % FIN_SPLIT) * 256 + threadIdx.x;
+  if (b < crb.nj)
+    cr_finish(crb, dB, kind, 0, b, e);
+  else
+    cr_finish(cra, dA, kind, 1, b - crb.nj, e);
 }
 
 // ===================================================================
-// host launchers
+// host side
 // ===================================================================
 static int clampi(int64_t v, int lo, int hi) { return static_cast<int>(v < lo ? lo : (v > hi ? hi : v)); }
 
-static int rowup_nt(int64_t T, int64_t J, int sms) {
-  const int64_t nj = (J + 255) / 256, nblk = (T + 15) / 16;
-  return clampi((4LL * sms + nj - 1) / nj, 1, static_cast<int>(nblk));
+// Raise a kernel's dynamic shared-memory limit once per device (on first use,
+// so that calls under stream capture make no such call).
+static cudaError_t allow_smem(const void* kern) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({dev, kern})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  if (e == cudaSuccess) done.insert({dev, kern});
+  return e;
 }
-static int colred_parts(int64_t T, int64_t J, int sms) {
-  const int64_t nj = (J + 63) / 64, nsteps = (T + 15) / 16;
-  return clampi((2LL * sms + nj - 1) / nj, 1, static_cast<int>(nsteps < 64 ? nsteps : 64));
+
+static unsigned long long* trace_ptr(int which) {
+#ifdef TG_TRACE
+  if (const char* e = getenv("TG_TRACE_ADDR"))
+    return reinterpret_cast<unsigned long long*>(strtoull(e, nullptr, 0)) + static_cast<size_t>(which) * 8192 * 16;
+#endif
+  (void)which;
+  return nullptr;
+}
+
+// Row-down plan: R rows per CTA (about one CTA per SM, at most 32 rows),
+// CH 64-column chunks per stage, as many stages as fit in smem_budget.
+static RdArgs rd_plan(int64_t T, int64_t K, int sms, int CH, int smem_budget) {
+  RdArgs r{};
+  r.T = static_cast<int>(T);
+  r.K = static_cast<int>(K);
+  r.R = clampi((T + sms - 1) / sms, 1, 32);
+  r.nfull = static_cast<int>(K / 64);
+  r.CH = clampi(CH, 1, r.nfull > 0 ? r.nfull : 1);
+  while (LCW % r.CH) --r.CH;  // CH divides the 8 consumer warps
+  r.nst3 = (r.nfull + r.CH - 1) / r.CH;
+  r.tail = K % 64 != 0 ? 1 : 0;
+  r.xs = rd_xs(r.R, r.CH);
+  const int per_stage = r.xs + r.CH * 2048;
+  r.stages = clampi((smem_budget - RD_RED_BYTES - BAR_BYTES - 1023) / per_stage, 1, LMAX_STAGES);
+  if (r.stages > r.nst3 + r.tail) r.stages = r.nst3 + r.tail;
+  return r;
+}
+
+// 2-D maps (the partial last chunk) and 3-D chunked views (whole chunks) of
+// the streamed tensor IN [T][K] and of the factor S
+static bool rd_maps(RdMaps* m, const void* in, const void* S, int kind, const RdArgs& r, bool s_kn) {
+  const uint64_t T = r.T, K = r.K;
+  if (!encode_tmap_3d(&m->x, in, kind, K, T, 1, K * 2, K * T * 2, 64, r.R, 128)) return false;
+  if (s_kn) {
+    if (!encode_tmap_3d(&m->s, S, kind, LR, K, 1, LR * 2, LR * K * 2, LR, 64, 32)) return false;
+  } else {
+    if (!encode_tmap_3d(&m->s, S, kind, K, LR, 1, K * 2, K * LR * 2, 64, LR, 128)) return false;
+  }
+  if (r.nfull == 0) {  // no whole chunk: the 3-D views are never used
+    m->x3 = m->x;
+    m->s3 = m->s;
+    return true;
+  }
+  const uint64_t nf = r.nfull;
+  {  // IN as [chunk][row][64]
+    const uint64_t d[3] = {64, T, nf}, st[2] = {K * 2, 128};
+    const uint32_t b[3] = {64, static_cast<uint32_t>(r.R), static_cast<uint32_t>(r.CH)};
+    if (!encode_tmap_nd(&m->x3, in, kind, 3, d, st, b, 128)) return false;
+  }
+  if (s_kn) {  // S [K][16] as [chunk][64 k][16]
+    const uint64_t d[3] = {LR, 64, nf}, st[2] = {LR * 2, 64 * LR * 2};
+    const uint32_t b[3] = {LR, 64, static_cast<uint32_t>(r.CH)};
+    return encode_tmap_nd(&m->s3, S, kind, 3, d, st, b, 32);
+  }
+  // S [16][K] as [chunk][16][64]
+  const uint64_t d[3] = {64, LR, nf}, st[2] = {K * 2, 128};
+  const uint32_t b[3] = {64, LR, static_cast<uint32_t>(r.CH)};
+  return encode_tmap_nd(&m->s3, S, kind, 3, d, st, b, 128);
+}
+
+// Column-reduction plan over (at most) G CTAs.
+static CrArgs cr_plan(int64_t T, int64_t J, int G, int stages) {
+  CrArgs c{};
+  c.T = static_cast<int>(T);
+  c.J = static_cast<int>(J);
+  c.nj = static_cast<int>((J + CR_CB - 1) / CR_CB);
+  c.nsteps = static_cast<int>((T + CR_RS - 1) / CR_RS);
+  c.N = static_cast<long long>(c.nj) * c.nsteps;
+  c.G = static_cast<int>(G < c.N ? G : c.N);
+  c.stages = stages;
+  c.max_segs = 1;
+  for (int cc = 0; cc < c.G; ++cc) {
+    const long long s0 = cr_start(cc, c), s1 = cr_start(cc + 1, c);
+    const int segs = static_cast<int>((s1 - 1) / c.nsteps - s0 / c.nsteps + 1);
+    if (segs > c.max_segs) c.max_segs = segs;
+  }
+  return c;
+}
+
+static bool cr_maps(CrMaps* m, const void* in, const void* H, const void* Hlo, const void* S2, int kind, int64_t T,
+                    int64_t J) {
+  if (!encode_tmap_3d(&m->in, in, kind, J, T, 1, J * 2, J * T * 2, 64, CR_RS, 128)) return false;
+  if (!encode_tmap_3d(&m->h, H, kind, LR, T, 1, LR * 2, LR * T * 2, LR, CR_RS, 32)) return false;
+  m->hlo = m->h;
+  m->s2 = m->h;
+  if (Hlo && !encode_tmap_3d(&m->hlo, Hlo, kind, LR, T, 1, LR * 2, LR * T * 2, LR, CR_RS, 32)) return false;
+  if (S2 && !encode_tmap_3d(&m->s2, S2, kind, J, LR, 1, J * 2, J * LR * 2, 64, LR, 128)) return false;
+  return true;
 }
 
 size_t lora_down_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
 
 cudaError_t lora_down_launch(const LoraArgs& a) {
-  const int grid = static_cast<int>((a.T + 15) / 16);
-  if (grid == 0) return cudaSuccess;
-  return launch_k(a.in_kind == EK_BF16 ? lora_down_kernel<true> : lora_down_kernel<false>, dim3(grid),
-                  dim3(LTHREADS), 0, a.stream, static_cast<const uint16_t*>(a.X), static_cast<const uint16_t*>(a.A),
-                  a.out, a.out_kind, static_cast<int>(a.T), static_cast<int>(a.d_in));
+  if (a.T == 0) return cudaSuccess;
+  RdArgs rd = rd_plan(a.T, a.d_in, a.num_sms, 8, 212 * 1024);
+  rd.out = a.out;
+  rd.out_kind = a.out_kind;
+  rd.hi = rd.lo = nullptr;
+  rd.timeout_ns = a.timeout_ns;
+  rd.status = a.status;
+  rd.trace = trace_ptr(0);
+  alignas(64) RdMaps maps;
+  if (!rd_maps(&maps, a.X, a.A, a.in_kind, rd, false)) return cudaErrorInvalidValue;
+  auto kern = a.in_kind == EK_BF16 ? lora_down_kernel<true> : lora_down_kernel<false>;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>((a.T + rd.R - 1) / rd.R);
+  return launch_k(kern, dim3(grid), dim3(LGROUP), rd_region_bytes(rd.R, rd.CH, rd.stages) + 1024, a.stream, maps,
+                  rd);
+}
+
+static int rowup_nt(int64_t T, int64_t J, int ctas) {
+  const int64_t nj = (J + 255) / 256, nblk = (T + 15) / 16;
+  return clampi((ctas + nj - 1) / nj, 1, static_cast<int>(nblk));
 }
 
 cudaError_t lora_up_launch(const LoraArgs& a) {
   const int nj = static_cast<int>((a.d_out + 255) / 256);
-  const int nt = rowup_nt(a.T, a.d_out, a.num_sms);
   if (nj == 0 || a.T == 0) return cudaSuccess;
-  dim3 grid(nj, nt);
-  return launch_k(a.in_kind == EK_BF16 ? lora_up_kernel<true> : lora_up_kernel<false>, grid, dim3(LTHREADS), 0,
-                  a.stream, static_cast<const uint16_t*>(a.H), static_cast<const uint16_t*>(a.B), a.out, a.out_kind,
-                  static_cast<int>(a.T), static_cast<int>(a.d_out), nt);
+  RuArgs ru{};
+  ru.H = static_cast<const uint16_t*>(a.H);
+  ru.S2 = static_cast<const uint16_t*>(a.B);
+  ru.out = a.out;
+  ru.out_kind = a.out_kind;
+  ru.T = static_cast<int>(a.T);
+  ru.J = static_cast<int>(a.d_out);
+  ru.n_t = rowup_nt(a.T, a.d_out, 4 * a.num_sms);
+  return launch_k(a.in_kind == EK_BF16 ? lora_up_kernel<true> : lora_up_kernel<false>, dim3(nj, ru.n_t),
+                  dim3(256), 0, a.stream, ru);
 }
 
-// workspace: [At d_in*16 x 2B][Bt d_out*16 x 2B][dH T*16 x 4B][Pb][Pa], 256-byte aligned pieces
-struct GradWs {
-  size_t at, bt, dh, pb, pa, total;
-  int parts_a, parts_b;
+// ---- gradient: plans and workspace
+
+struct GradPlan {
+  RdArgs rd;   // pass 1 row-down
+  CrArgs crb;  // pass 1 column reduction (dB)
+  CrArgs cra;  // pass 2 column reduction + row-up (dA, dX)
+  int g1;
+  size_t dh, hi, lo, pb, pa, total;  // workspace layout
 };
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
-static GradWs grad_ws(int64_t T, int64_t d_in, int64_t d_out, int sms) {
-  GradWs w;
-  w.parts_b = colred_parts(T, d_out, sms);
-  w.parts_a = colred_parts(T, d_in, sms);
-  w.at = 0;
-  w.bt = w.at + up256(static_cast<size_t>(d_in) * LR * 2);
-  w.dh = w.bt + up256(static_cast<size_t>(d_out) * LR * 2);
-  w.pb = w.dh + up256(static_cast<size_t>(T) * LR * 4);
-  w.pa = w.pb + up256(static_cast<size_t>(w.parts_b) * d_out * LR * 4);
-  w.total = w.pa + up256(static_cast<size_t>(w.parts_a) * d_in * LR * 4);
-  return w;
+
+static GradPlan grad_plan(int64_t T, int64_t d_in, int64_t d_out, int sms, int out_kind) {
+  GradPlan g;
+  g.rd = rd_plan(T, d_out, sms, G1_RD_CH, G1_RD_BUDGET);
+  g.g1 = static_cast<int>((T + g.rd.R - 1) / g.rd.R);
+  g.crb = cr_plan(T, d_out, g.g1, G1_CR_STAGES);
+  g.cra = cr_plan(T, d_in, G2_CTAS_PER_SM * sms, G2_CR_STAGES);
+  g.cra.out_kind = out_kind;
+  g.dh = 0;
+  g.hi = g.dh + up256(static_cast<size_t>(T) * LR * 4);
+  g.lo = g.hi + up256(static_cast<size_t>(T) * LR * 2);
+  g.pb = g.lo + up256(static_cast<size_t>(T) * LR * 2);
+  g.pa = g.pb + up256(static_cast<size_t>(g.crb.G) * g.crb.max_segs * CR_CB * LR * 4);
+  g.total = g.pa + up256(static_cast<size_t>(g.cra.G) * g.cra.max_segs * CR_CB * LR * 4);
+  return g;
 }
 
 size_t lora_grad_ws_bytes(int64_t T, int64_t d_in, int64_t d_out, int64_t, int sms) {
-  return grad_ws(T, d_in, d_out, sms).total;
+  // the partial layout does not depend on the output type
+  return grad_plan(T, d_in, d_out, sms, EK_F32).total;
 }
 
 // a.out = dA, a.out2 = dB, a.out3 = dX, a.out4 = optional dH (FP32)
 cudaError_t lora_grad_launch(const LoraArgs& a) {
-  const GradWs w = grad_ws(a.T, a.d_in, a.d_out, a.num_sms);
+  GradPlan gp = grad_plan(a.T, a.d_in, a.d_out, a.num_sms, a.out_kind);
   char* base = reinterpret_cast<char*>(a.ws);
-  uint16_t* At = reinterpret_cast<uint16_t*>(base + w.at);
-  uint16_t* Bt = reinterpret_cast<uint16_t*>(base + w.bt);
-  float* dH = a.out4 ? static_cast<float*>(a.out4) : reinterpret_cast<float*>(base + w.dh);
-  float* Pb = reinterpret_cast<float*>(base + w.pb);
-  float* Pa = reinterpret_cast<float*>(base + w.pa);
-  const int T = static_cast<int>(a.T), d_in = static_cast<int>(a.d_in), d_out = static_cast<int>(a.d_out);
+  float* dH = a.out4 ? static_cast<float*>(a.out4) : reinterpret_cast<float*>(base + gp.dh);
+  uint16_t* hi = reinterpret_cast<uint16_t*>(base + gp.hi);
+  uint16_t* lo = reinterpret_cast<uint16_t*>(base + gp.lo);
   const bool bf = a.in_kind == EK_BF16;
-  const uint16_t* X = static_cast<const uint16_t*>(a.X);
-  const uint16_t* A = static_cast<const uint16_t*>(a.A);
-  const uint16_t* B = static_cast<const uint16_t*>(a.B);
-  const uint16_t* H = static_cast<const uint16_t*>(a.H);
-  const uint16_t* dY = static_cast<const uint16_t*>(a.dY);
+  const int kind = a.in_kind;
 
-  const int prep_blocks = clampi((static_cast<int64_t>(d_in + d_out) * LR + 255) / 256, 1, 4 * a.num_sms);
-  cudaError_t e = launch_k(lora_prep_kernel, dim3(prep_blocks), dim3(256), 0, a.stream, A, B, At, Bt, d_in, d_out);
+  // ---- pass 1: dH (row-down over dY with B) and dB partials (col-red over dY with H)
+  RdArgs& rd = gp.rd;
+  rd.out = dH;
+  rd.out_kind = EK_F32;
+  rd.hi = hi;
+  rd.lo = lo;
+  rd.timeout_ns = a.timeout_ns;
+  rd.status = a.status;
+  rd.trace = trace_ptr(0);
+  CrArgs& crb = gp.crb;
+  crb.P = reinterpret_cast<float*>(base + gp.pb);
+  crb.timeout_ns = a.timeout_ns;
+  crb.status = a.status;
+  crb.trace = trace_ptr(1);
+  alignas(64) RdMaps rmaps;
+  alignas(64) CrMaps cmaps1;
+  if (!rd_maps(&rmaps, a.dY, a.B, kind, rd, true)) return cudaErrorInvalidValue;
+  if (!cr_maps(&cmaps1, a.dY, a.H, nullptr, nullptr, kind, a.T, a.d_out)) return cudaErrorInvalidValue;
+  const int rd_region = rd_region_bytes(rd.R, rd.CH, rd.stages);
+  const int smem1 = 1024 + rd_region + cr_region_bytes(crb.stages, 1, false);
+  auto k1 = bf ? lora_grad1_kernel<true> : lora_grad1_kernel<false>;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(k1));
+  if (e != cudaSuccess) return e;
+  e = launch_k(k1, dim3(gp.g1), dim3(2 * LGROUP), smem1, a.stream, rmaps, cmaps1, rd, crb, rd_region);
   if (e != cudaSuccess) return e;
 
-  const int n_rowdown = (T + 15) / 16;
-  const int nj_b = (d_out + 63) / 64;
-  const int g1 = n_rowdown + nj_b * w.parts_b;
-  e = launch_k(bf ? lora_grad1_kernel<true> : lora_grad1_kernel<false>, dim3(g1), dim3(LTHREADS), 0, a.stream, dY,
-               static_cast<const uint16_t*>(Bt), H, dH, Pb, T, d_out, n_rowdown, nj_b, w.parts_b);
+  // ---- pass 2: dA partials (col-red over X with dH hi/lo) and dX (row-up of the same tiles)
+  CrArgs& cra = gp.cra;
+  cra.P = reinterpret_cast<float*>(base + gp.pa);
+  cra.out = a.out3;  // dX
+  cra.timeout_ns = a.timeout_ns;
+  cra.status = a.status;
+  cra.trace = trace_ptr(2);
+  alignas(64) CrMaps cmaps2;
+  if (!cr_maps(&cmaps2, a.X, hi, lo, a.A, kind, a.T, a.d_in)) return cudaErrorInvalidValue;
+  auto k2 = bf ? lora_grad2_kernel<true> : lora_grad2_kernel<false>;
+  e = allow_smem(reinterpret_cast<const void*>(k2));
+  if (e != cudaSuccess) return e;
+  e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), 1024 + cr_region_bytes(cra.stages, 2, true), a.stream, cmaps2,
+               cra);
   if (e != cudaSuccess) return e;
 
-  const int nj_a = (d_in + 63) / 64;
-  const int n_colred = nj_a * w.parts_a;
-  const int nj_x = (d_in + 255) / 256;
-  const int n_tx = rowup_nt(T, d_in, a.num_sms);
-  const int g2 = n_colred + nj_x * n_tx;
-  e = launch_k(bf ? lora_grad2_kernel<true> : lora_grad2_kernel<false>, dim3(g2), dim3(LTHREADS), 0, a.stream, X,
-               static_cast<const float*>(dH), static_cast<const uint16_t*>(At), a.out3, a.out_kind, Pa, T, d_in,
-               n_colred, nj_a, w.parts_a, nj_x, n_tx);
-  if (e != cudaSuccess) return e;
-
-  const int g3 = clampi((static_cast<int64_t>(d_in + d_out) * LR + 255) / 256, 1, 4 * a.num_sms);
-  return launch_k(lora_grad3_kernel, dim3(g3), dim3(256), 0, a.stream, static_cast<const float*>(Pb),
-                  static_cast<const float*>(Pa), a.out2, a.out, a.out_kind, d_out, d_in, w.parts_b, w.parts_a);
+  // ---- pass 3: dB and dA from the partials
+  return launch_k(lora_grad3_kernel, dim3((crb.nj + cra.nj) * FIN_SPLIT), dim3(256), 0, a.stream, crb, cra, a.out2,
+                  a.out, a.out_kind);
 }
 
 }  // namespace tg

@@ -109,7 +109,9 @@ cudaError_t simt_gemm_launch(const SimtGemm& g);
 // Tensor-map encoding through the driver entry point (tmap.cpp).
 bool encode_tmap_3d(void* tmap_out, const void* base, int elem_kind, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
-                    uint32_t box1, bool swizzle128);
+                    uint32_t box1, int swizzle_bytes);
+bool encode_tmap_nd(void* tmap_out, const void* base, int elem_kind, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
 
 // rank-r LoRA streaming kernels (lora.cu)
 struct LoraArgs {
@@ -127,6 +129,8 @@ struct LoraArgs {
   int in_kind, out_kind;
   int num_sms;
   cudaStream_t stream;
+  unsigned int* status;          // device status word (bounded waits report here)
+  unsigned long long timeout_ns; // limit of every wait on an mbarrier
 };
 size_t lora_down_ws_bytes(int64_t T, int64_t d_in, int64_t r, int num_sms);
 cudaError_t lora_down_launch(const LoraArgs& a);
