@@ -516,20 +516,28 @@ def measure_rows(stream, pk, budget_s=90.0):
             break
         h, d = acfg["heads"], acfg["d"]
         dt = torch.bfloat16
-        t = inputs.attn_inputs(h, s, d, dt, tag="rows", device="cuda")
+        # operand sets rotated so that the bytes touched between two uses of a
+        # set exceed twice the L2: every launch reads from HBM
+        per_set = 3 * h * s * s * 2 + 6 * h * s * d * 2
+        sets = max(1, int(2 * l2 // per_set) + 1)
+        ts = [inputs.attn_inputs(h, s, d, dt, tag="rows" if i == 0 else f"rows{i}", device="cuda")
+              for i in range(sets)]
         for op in ("qk", "pv", "do_vt", "pt_do", "ds_k", "dst_q"):
             a, b = inputs.ATTN_OPERANDS[op]
             ss_out = op in ("qk", "do_vt")
-            C = torch.empty(h, s, s if ss_out else d, dtype=dt, device="cuda")
-            ms, call = time_calls(lambda i: (lambda: tg.tg_bmm_attn(op, t[a], t[b], C=C)), reps=5)
+            Cs = [torch.empty(h, s, s if ss_out else d, dtype=dt, device="cuda") for _ in range(sets)]
+            ms, call = time_calls(lambda i: (lambda: tg.tg_bmm_attn(op, ts[i][a], ts[i][b], C=Cs[i])),
+                                  reps=max(5, 2 * sets), sets=sets)
+            t, C = ts[0], Cs[0]
             nbytes = (t[a].numel() + t[b].numel() + C.numel()) * 2
             fl = 2 * h * s * s * d
             gbs = nbytes / ms / 1e6
             rows.append({"set": "attention", "s": s, "op": op, "dtype": "bf16", "us": round(ms * 1000, 2),
                          "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3),
-                         "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call)})
-            del C
-        del t
+                         "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call),
+                         "operand_sets": sets})
+            del C, Cs
+        del t, ts
     return rows
 
 

@@ -128,6 +128,7 @@ struct TableKeyHash {
 };
 struct TableVal {
   int bn, splits, raster;  // splits 0 = stream-K; raster: -1 = by operand size, 0 = along M, 1 = along N
+  int tail;                // > 1: tail split of the tiles past the last whole wave
 };
 static std::shared_mutex g_table_mu;
 static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
@@ -159,11 +160,17 @@ static tg_status load_table_file(const char* path) {
       std::istringstream ss(line);
       std::string op, din, dout, sp;
       int64_t M, N, K, batch;
-      int bn, splits;
+      int bn, splits, tail = 0;
       if (!(ss >> op)) continue;  // blank line
       if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> sp)) return TG_ERR_TABLE;
       if (sp == "sk") {
         splits = 0;
+      } else if (sp.size() > 1 && sp[0] == 't') {  // tail split: tN
+        char* endp = nullptr;
+        const long v = strtol(sp.c_str() + 1, &endp, 10);
+        if (*endp != '\0' || v < 2 || v > 64) return TG_ERR_TABLE;
+        splits = 1;
+        tail = static_cast<int>(v);
       } else {
         char* endp = nullptr;
         const long v = strtol(sp.c_str(), &endp, 10);
@@ -179,8 +186,10 @@ static tg_status load_table_file(const char* path) {
       }
       const int l = parse_layout(op), i = parse_dtype(din), o = parse_dtype(dout);
       if (l < 0 || i < 0 || o < 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return TG_ERR_TABLE;
-      if (!(bn == 64 || bn == 128 || bn == 192 || bn == 256) || splits < 0 || splits > 64) return TG_ERR_TABLE;
-      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster};
+      if (!(bn == 64 || bn == 128 || bn == 144 || bn == 192 || bn == 256) || splits < 0 || splits > 64)
+        return TG_ERR_TABLE;
+      if (bn % 64 != 0 && (splits == 0 || tail > 0)) return TG_ERR_TABLE;  // partial tiles: 64-column multiples
+      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail};
     }
   }
   std::unique_lock<std::shared_mutex> lk(g_table_mu);
@@ -222,6 +231,7 @@ struct Plan {
   int splits = 1;
   int raster_n = 0;
   bool sk = false;  // stream-K schedule (splits is then 1)
+  int tail = 0;     // > 1: tail split (splits is then 1)
   bool from_table = false;
 };
 
@@ -234,11 +244,13 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
   Plan best;
   double best_t = 1e300;
   const int64_t kb = cdiv(K, 64);
-  const int bns[4] = {256, 192, 128, 64};
+  const int bns[5] = {256, 192, 144, 128, 64};
+  // one 128 x bn x 64 block: four 128 x bn x 16 MMAs, measured at >= 88 cycles
+  // each and ~0.525 * bn cycles from bn = 192 up (the tensor pipe's full rate)
+  auto kb_cycles = [](int bn) { return 4.0 * fmax(88.0, 0.525 * bn); };
   for (int bn : bns) {
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
-    // one 128 x bn x 64 block: tensor time vs shared-memory operand reads (cycles)
-    const double kb_cyc = 4.0 * fmax(bn / 2.0, 32.0 + bn / 4.0);
+    const double kb_cyc = kb_cycles(bn);
     const double epi_cyc = 128.0 * bn * out_bytes / 48.0;
     for (int64_t s = 1; s <= 32 && s <= kb; ++s) {
       const int64_t kps = cdiv(kb, s);
@@ -257,11 +269,33 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
   }
   // stream-K: every CTA gets an equal share of the tile x K-block iterations;
   // a cut tile costs its pieces' FP32 write and the owner's read-back
+  // tail split: whole tiles in full waves, the last partial wave's tiles cut along K
   for (int bn : bns) {
+    if (bn % 64 != 0) continue;
+    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
+    if (tiles <= sms || tiles % sms == 0) continue;
+    const int64_t rem = tiles % sms;
+    const double kb_cyc = kb_cycles(bn);
+    for (int ts : {2, 3, 4, 6, 8}) {
+      const int64_t kps = cdiv(kb, ts), real = cdiv(kb, kps);
+      if (real < 2) continue;
+      double t = (tiles / sms) * (kb * kb_cyc + 600.0) + cdiv(rem * real, sms) * (kps * kb_cyc + 128.0 * bn * 4 / 48.0 + 600.0);
+      t += 8000.0 + rem * real * 128.0 * bn * 4 / (sms * 24.0);  // + the reduce launch
+      if (t < best_t * 0.97) {
+        best_t = t;
+        best.bn = bn;
+        best.splits = 1;
+        best.sk = false;
+        best.tail = static_cast<int>(ts);
+      }
+    }
+  }
+  for (int bn : bns) {
+    if (bn % 64 != 0) continue;  // stream-K partial tiles are 64-column multiples
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
     const int64_t iters = tiles * kb;
     if (iters < sms || tiles * 4 < sms) continue;
-    const double kb_cyc = 4.0 * fmax(bn / 2.0, 32.0 + bn / 4.0);
+    const double kb_cyc = kb_cycles(bn);
     const double per_cta = static_cast<double>(cdiv(iters, sms));
     double t = per_cta * kb_cyc + 600.0 * cdiv(tiles, sms) + 2.0 * 128.0 * bn * 4 / 24.0;
     if (t < best_t * 0.95) {
@@ -269,6 +303,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       best.bn = bn;
       best.splits = 1;
       best.sk = true;
+      best.tail = 0;
     }
   }
   return best;
@@ -288,6 +323,7 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
     const int64_t kb = cdiv(K, 64);
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, p.bn);
     p.sk = v.splits == 0 && tiles * kb >= 1;
+    p.tail = p.sk ? 0 : v.tail;
     const int64_t s = p.sk ? 1 : (v.splits < kb ? v.splits : kb);
     const int64_t kps = cdiv(kb, s);
     p.splits = static_cast<int>(cdiv(kb, kps));
@@ -307,6 +343,7 @@ static int sk_grid(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch
 
 static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
   if (p.sk) return sk_ws_bytes(sk_grid(p, M, N, K, batch, sms), p.bn);
+  if (p.tail > 1 && p.splits <= 1) return tail_ws_bytes(tail_geo(M, N, K, batch, p.bn, sms, p.tail, p.raster_n));
   return p.splits > 1 ? static_cast<size_t>(p.splits) * batch * M * N * 4 : 0;
 }
 
@@ -395,6 +432,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.raster_n = p.raster_n;
     t.sk = p.sk ? 1 : 0;
     t.sk_epoch = p.sk ? next_epoch() : 0;
+    t.tail_splits = p.tail;
     t.ws = g.ws;
     t.grid = ctx->sms;
     t.stream = g.stream;
@@ -406,10 +444,14 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     if (e == cudaSuccess && !p.sk && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
                                g.stream);
-    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d %s%d raster=%c table=%s %s",
+    const TailGeo tgeo = tail_geo(g.M, g.N, g.K, g.batch, p.bn, ctx->sms, p.sk || p.splits > 1 ? 1 : p.tail,
+                                  p.raster_n);
+    char tail[48] = "";
+    if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
+    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d %s%d%s raster=%c table=%s %s",
              g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
              p.bn, p.sk ? "sk grid=" : "splits=", p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits,
-             p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+             tail, p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }

@@ -28,6 +28,34 @@ __device__ __forceinline__ void store_from_float(void* p, int kind, int64_t i, f
     static_cast<float*>(p)[i] = v;
 }
 
+// ------------------------------------------------------------- tail split
+// C tile dp_tiles + t = sum over s ascending of partial slot t * splits + s
+// (each a dense [128][bn] FP32 tile); rows past M and columns past N skipped.
+__global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int out_kind, TailGeo g) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y;
+  int b, m0, n0;
+  tile_origin(g.dp_tiles + t, g.m_tiles, g.n_tiles, g.raster_n, g.bn, &b, &m0, &n0);
+  const int per = 128 * g.bn;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < per; e += gridDim.x * blockDim.x) {
+    const int r = e / g.bn, col = e - r * g.bn;
+    const int64_t m = m0 + r, n = n0 + col;
+    if (m >= g.M || n >= g.N) continue;
+    const float* src = P + static_cast<size_t>(t) * g.splits * per + e;
+    float v = src[0];
+    for (int s = 1; s < g.splits; ++s) v += src[static_cast<size_t>(s) * per];
+    store_from_float(C, out_kind, (b * g.M + m) * g.N + n, v);
+  }
+}
+
+cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream) {
+  if (t.tail_tiles == 0) return cudaSuccess;
+  const int per = 128 * t.bn;
+  return launch_k(tail_reduce_kernel, dim3((per + 1023) / 1024, t.tail_tiles), dim3(256), 0, stream, P, C, out_kind,
+                  t);
+}
+
 // ---------------------------------------------------------------- split-K
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int out_kind,
                                      int64_t batch, int64_t splits, int64_t MN) {

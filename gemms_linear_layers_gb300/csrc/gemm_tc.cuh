@@ -22,6 +22,10 @@
 //               the next tile's MMAs overlap this tile's stores.
 // Split-K: a unit is (tile, K range); partial sums go to an FP32 workspace
 // and a separate kernel adds them in split order (deterministic).
+// Tail split: when the tiles are not a whole number of waves, the tiles of
+// the last, partial wave are split along K (tail_splits ways) while every
+// other tile runs whole; the split pieces leave as FP32 partial tiles and
+// a small kernel adds them in split order.
 // Stream-K: the (tile x K block) iteration space is cut into gridDim.x equal
 // contiguous ranges, one per CTA.  A tile cut by a range boundary is finished
 // by the CTA holding its first K block (the owner): every later CTA that
@@ -45,15 +49,21 @@ constexpr int TC_EPI_BUF = 32 * 128;           // 32 rows x 128 bytes
 
 template <int BN>
 struct TcCfg {
-  static constexpr int B_STAGE = BN * TC_BK * 2;
-  static constexpr int STAGES = (BN == 256 || BN == 192) ? 4 : (BN == 128) ? 6 : 8;
+  // B tile: BN rows of 128 bytes (K-major) or ceil(BN/64) 64-column chunks
+  // of 8 KB (MN-major; a width that is not a multiple of 64 loads a full last
+  // chunk and the MMA reads only its first columns)
+  static constexpr int B_CHUNKS = (BN + 63) / 64;
+  static constexpr int B_STAGE = B_CHUNKS * 64 * TC_BK * 2;
+  static constexpr int B_BYTES_K = BN * TC_BK * 2;
+  static constexpr int B_BYTES_MN = B_STAGE;
+  static constexpr int STAGES = (BN > 128) ? 4 : (BN == 128) ? 6 : 8;
   static constexpr int ACC_STRIDE = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
   static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + STAGES * (TC_A_STAGE + B_STAGE) +
                               TC_EPI_WARPS * 2 * TC_EPI_BUF + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(BN % 64 == 0 && BN <= 256, "tile width");
+  static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "tile width");
   static_assert(2 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area");
 };
 
@@ -66,6 +76,9 @@ struct TcArgs {
   uint32_t idesc;
   int out_f16;   // 16-bit output type: 1 = fp16, 0 = bf16
   int raster_n;  // 1: consecutive units walk along N (they share the A tile)
+  int dp_tiles;     // tail split: tiles run whole (the first dp_tiles in raster order)
+  int tail_splits;  // > 1: each later tile is split into this many K ranges of tail_kps blocks
+  int tail_kps;
   int sk;        // 1: stream-K schedule over batch * m_tiles * n_tiles * kb_total iterations
   long long sk_iters;
   float* sk_part;                // [gridDim.x][128][BN] FP32 partial tiles
@@ -91,20 +104,13 @@ struct Unit {
   int b, m0, n0, split, kb0, kb1;
   int owner;   // this CTA writes the tile (stream-K: it holds the tile's first K block)
   int c_last;  // stream-K owner: last CTA holding a piece of the tile (> blockIdx.x: wait for partials)
+  int part;    // tail split: this unit writes FP32 partial slot pz instead of the output
+  int pz;
 };
 
 template <int BN>
 __device__ __forceinline__ void tile_coords(int t, const TcArgs& a, Unit& c) {
-  const int tiles = a.m_tiles * a.n_tiles;
-  c.b = t / tiles;
-  const int r = t - c.b * tiles;
-  if (a.raster_n) {  // consecutive units walk along N: they share the A tile
-    c.n0 = (r % a.n_tiles) * BN;
-    c.m0 = (r / a.n_tiles) * TC_BM;
-  } else {           // consecutive units walk down M: they share the B tile
-    c.m0 = (r % a.m_tiles) * TC_BM;
-    c.n0 = (r / a.m_tiles) * BN;
-  }
+  tile_origin(t, a.m_tiles, a.n_tiles, a.raster_n, BN, &c.b, &c.m0, &c.n0);
 }
 
 __device__ __forceinline__ long long sk_start(long long cta, const TcArgs& a) {
@@ -141,12 +147,24 @@ __device__ __forceinline__ bool work_next(const TcArgs& a, WorkIter& it, Unit& c
   if (it.pos >= it.end) return false;
   if (!a.sk) {
     const int u = static_cast<int>(it.pos);
-    c.split = u % a.splits;
-    tile_coords<BN>(u / a.splits, a, c);
-    c.kb0 = c.split * a.kps;
-    c.kb1 = min(a.kb_total, c.kb0 + a.kps);
     c.owner = 1;
     c.c_last = -1;
+    if (a.tail_splits > 1 && u >= a.dp_tiles) {
+      const int v = u - a.dp_tiles;
+      tile_coords<BN>(a.dp_tiles + v / a.tail_splits, a, c);
+      c.split = v % a.tail_splits;
+      c.kb0 = c.split * a.tail_kps;
+      c.kb1 = min(a.kb_total, c.kb0 + a.tail_kps);
+      c.part = 1;
+      c.pz = v;
+    } else {
+      c.split = u % a.splits;
+      tile_coords<BN>(u / a.splits, a, c);
+      c.kb0 = c.split * a.kps;
+      c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+      c.part = 0;
+      c.pz = 0;
+    }
     it.pos += gridDim.x;
     return true;
   }
@@ -160,6 +178,8 @@ __device__ __forceinline__ bool work_next(const TcArgs& a, WorkIter& it, Unit& c
   c.kb1 = static_cast<int>(seg_end - kt0);
   c.owner = it.pos == kt0;
   c.c_last = (c.owner && seg_end < kt0 + kb) ? sk_cta_of(kt0 + kb - 1, a) : -1;
+  c.part = 0;
+  c.pz = 0;
   it.pos = seg_end;
   return true;
 }
@@ -190,7 +210,8 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
 template <bool A_MN, bool B_MN, int BN, bool OUT16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+                   const __grid_constant__ CUtensorMap tmP, const TcArgs args) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -228,6 +249,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
+    if (BN % 64 != 0) prefetch_tmap(&tmC2);
+    if (args.tail_splits > 1) prefetch_tmap(&tmP);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -261,7 +284,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, TC_A_STAGE + Cfg::B_STAGE);
+          mbar_arrive_expect_tx(fb, TC_A_STAGE + (B_MN ? Cfg::B_BYTES_MN : Cfg::B_BYTES_K));
           const uint32_t a_dst = smem_u32(sA + stage * TC_A_STAGE);
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_STAGE);
           const int k0 = kb * TC_BK;
@@ -273,7 +296,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
+            for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
           } else {
             tma_load_3d(b_dst, &tmB, fb, k0, c.n0, c.b);
           }
@@ -355,6 +378,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* ebuf = sE + ew * 2 * TC_EPI_BUF;
     constexpr int CW = OUT16 ? 64 : 32;  // columns per 128-byte staging row
     constexpr int NCH = BN / CW;
+    constexpr int TW = BN % CW;  // a last, narrower chunk (16 columns) for BN = 144
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
@@ -392,6 +416,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         if (lane == 0) st_release_u64(args.sk_flags + sk_flag_index(blockIdx.x, q), args.sk_epoch);
         if (warp == 2 && lane == 0) TG_EVENT(3);
+      } else if (BN % 64 == 0 && c.part) {
+        // ---- tail split piece: FP32 partial tile [128][BN] to slot pz
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_wait();
+          if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+          }
+          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          __syncwarp();
+          uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmP, smem_u32(buf), ch * 32, q * 32, c.pz);
+            bulk_commit();
+          }
+          ++nstore;
+        }
       } else {
         // ---- tile writer; a stream-K owner first waits for the later pieces
         // of its own 32 rows (each lane polls the flags itself)
@@ -430,7 +482,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld_32x32b_x32(t_row + ch * CW, r);
           if (OUT16) tmem_ld_32x32b_x32(t_row + ch * CW + 32, r + 32);
           tmem_ld_wait();
-          if (ch == NCH - 1) {
+          if (ch == NCH - 1 && TW == 0) {
             // accumulator fully read: hand it back to the MMA warp
             tc_fence_before();
             __syncwarp();
@@ -484,6 +536,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
+            bulk_commit();
+          }
+          ++nstore;
+        }
+        if constexpr (TW != 0) {
+          // the last TW columns: staged as dense rows of TW elements (no
+          // swizzle) and stored through a map whose box is TW wide
+          static_assert(TW == 16, "tail width");
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_row + NCH * CW, r);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          __syncwarp();
+          if (OUT16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              w[j] = args.out_f16 ? pack_f16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]))
+                                  : pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 32);
+            rowp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            rowp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rowp[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC2, smem_u32(buf), c.n0 + NCH * CW, c.m0 + q * 32, zc);
             bulk_commit();
           }
           ++nstore;

@@ -28,7 +28,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
     attr_set[dev] = true;
   }
 
-  alignas(64) CUtensorMap tmA, tmB, tmC;
+  alignas(64) CUtensorMap tmA, tmB, tmC, tmC2, tmP;
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
   bool ok;
   if (A_MN)  // stored [batch][K][M]
@@ -50,6 +50,12 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * (split_parts ? g.splits : 1), N * esz, M * N * esz,
                       OUT16 ? 64 : 32, 32, 128);
   if (!ok) return cudaErrorInvalidValue;
+  // the 16-column tail of a tile width that is not a multiple of 64 / 32
+  tmC2 = tmC;
+  if (BN % (OUT16 ? 64 : 32) != 0) {
+    ok = encode_tmap_3d(&tmC2, cptr, ck, N, M, nb * (split_parts ? g.splits : 1), N * esz, M * N * esz, 16, 32, 0);
+    if (!ok) return cudaErrorInvalidValue;
+  }
 
   TcArgs a;
   a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
@@ -62,6 +68,18 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
   a.raster_n = g.raster_n;
   a.sk = g.sk;
+  // tail split (never with stream-K or split partials)
+  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid, (g.sk || g.splits > 1) ? 1 : g.tail_splits, g.raster_n);
+  a.dp_tiles = tg.dp_tiles;
+  a.tail_splits = tg.splits;
+  a.tail_kps = tg.kps;
+  tmP = tmC;
+  if (tg.tail_tiles > 0) {
+    a.units = tg.dp_tiles + tg.tail_tiles * tg.splits;
+    ok = encode_tmap_3d(&tmP, g.ws, EK_F32, BN, 128, static_cast<uint64_t>(tg.tail_tiles) * tg.splits, BN * 4,
+                        128 * BN * 4, 32, 32, 128);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   a.sk_iters = static_cast<long long>(a.units) * a.kb_total;
   a.sk_part = nullptr;
   a.sk_flags = nullptr;
@@ -80,7 +98,9 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
     a.sk_flags = reinterpret_cast<unsigned long long*>(static_cast<char*>(g.ws) +
                                                        static_cast<size_t>(grid) * TC_BM * BN * 4);
   }
-  return launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, a);
+  cudaError_t e2 = launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, tmC2, tmP, a);
+  if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
+  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream);
 }
 
 template <bool A_MN, bool B_MN>
@@ -90,6 +110,7 @@ static cudaError_t tc_launch_layout(const TcGemm& g) {
   switch (g.bn) {
     case 64: return out16 ? tc_launch_one<A_MN, B_MN, 64, true>(g) : tc_launch_one<A_MN, B_MN, 64, false>(g);
     case 128: return out16 ? tc_launch_one<A_MN, B_MN, 128, true>(g) : tc_launch_one<A_MN, B_MN, 128, false>(g);
+    case 144: return out16 ? tc_launch_one<A_MN, B_MN, 144, true>(g) : tc_launch_one<A_MN, B_MN, 144, false>(g);
     case 192: return out16 ? tc_launch_one<A_MN, B_MN, 192, true>(g) : tc_launch_one<A_MN, B_MN, 192, false>(g);
     case 256: return out16 ? tc_launch_one<A_MN, B_MN, 256, true>(g) : tc_launch_one<A_MN, B_MN, 256, false>(g);
     default: return cudaErrorInvalidValue;

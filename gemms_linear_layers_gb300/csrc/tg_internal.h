@@ -70,6 +70,7 @@ struct TcGemm {
   int raster_n;               // 1: walk output tiles along N first (A tiles reused)
   int sk;                     // 1: stream-K schedule (ws holds per-CTA partial tiles + flags)
   unsigned long long sk_epoch;  // flag value unique to this launch
+  int tail_splits;            // >1: tiles past the last whole wave are split along K (ws: partial tiles)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
@@ -82,6 +83,63 @@ struct TcGemm {
 inline size_t sk_ws_bytes(int grid, int bn) {
   return static_cast<size_t>(grid) * (128 * static_cast<size_t>(bn) * 4 + 4 * 128);
 }
+
+// Tail split: the tiles past the last whole wave of `grid` CTAs are each cut
+// into `splits` K ranges whose FP32 partial tiles ([128][bn] each) are added
+// by tail_reduce_kernel in split order.
+struct TailGeo {
+  int dp_tiles, tail_tiles, splits, kps;
+  int m_tiles, n_tiles, raster_n, bn;
+  int64_t M, N;
+};
+inline TailGeo tail_geo(int64_t M, int64_t N, int64_t K, int64_t batch, int bn, int grid, int want_splits,
+                        int raster_n) {
+  TailGeo t{};
+  t.m_tiles = static_cast<int>((M + 127) / 128);
+  t.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  t.raster_n = raster_n;
+  t.bn = bn;
+  t.M = M;
+  t.N = N;
+  const int tiles = static_cast<int>(batch) * t.m_tiles * t.n_tiles;
+  const int kb = static_cast<int>((K + 63) / 64);
+  t.dp_tiles = grid > 0 ? (tiles / grid) * grid : tiles;
+  t.tail_tiles = tiles - t.dp_tiles;
+  if (t.dp_tiles == 0 || t.tail_tiles == 0 || want_splits < 2 || bn % 64 != 0) {
+    t.dp_tiles = tiles;
+    t.tail_tiles = 0;
+    t.splits = 1;
+    t.kps = kb;
+    return t;
+  }
+  t.kps = (kb + want_splits - 1) / want_splits;
+  t.splits = (kb + t.kps - 1) / t.kps;
+  if (t.splits < 2) {
+    t.dp_tiles = tiles;
+    t.tail_tiles = 0;
+    t.splits = 1;
+    t.kps = kb;
+  }
+  return t;
+}
+inline size_t tail_ws_bytes(const TailGeo& t) {
+  return static_cast<size_t>(t.tail_tiles) * t.splits * 128 * static_cast<size_t>(t.bn) * 4;
+}
+// Origin of output tile t (batch-major, then raster order within the batch).
+__host__ __device__ inline void tile_origin(int t, int m_tiles, int n_tiles, int raster_n, int bn, int* b, int* m0,
+                                            int* n0) {
+  const int tiles = m_tiles * n_tiles;
+  *b = t / tiles;
+  const int r = t - *b * tiles;
+  if (raster_n) {  // consecutive units walk along N: they share the A tile
+    *n0 = (r % n_tiles) * bn;
+    *m0 = (r / n_tiles) * 128;
+  } else {  // consecutive units walk down M: they share the B tile
+    *m0 = (r % m_tiles) * 128;
+    *n0 = (r / m_tiles) * bn;
+  }
+}
+cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream);
 
 // per-layout launchers (gemm_tc_{nt,nn,tn}.cu)
 cudaError_t tc_gemm_launch_nt(const TcGemm& g);

@@ -28,7 +28,7 @@ from . import inputs, workloads
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "tables", "gb300.txt")
-BNS = (64, 128, 192, 256)
+BNS = (64, 128, 144, 192, 256)
 SPLITS = (1, 2, 3, 4, 6, 8, 12, 16)
 
 
@@ -118,8 +118,15 @@ def candidates(M, N, K, batch, sms):
                 continue
             for raster in ("m", "n"):
                 yield bn, s, raster
+        # tail split: whole tiles in full waves, the last partial wave cut along K
+        if bn % 64 == 0 and tiles > sms and tiles % sms:
+            for ts in (2, 4, 8):
+                if -(-kb // -(-kb // ts)) >= 2:
+                    for raster in ("m", "n"):
+                        yield bn, f"t{ts}", raster
         # stream-K: an equal share of tile x K-block iterations per CTA
-        if tiles * kb >= sms and tiles * 4 >= sms:
+        # (its partial tiles are 64-column multiples)
+        if bn % 64 == 0 and tiles * kb >= sms and tiles * 4 >= sms:
             for raster in ("m", "n"):
                 yield bn, "sk", raster
 
@@ -182,6 +189,15 @@ def main(argv=None):
         del call
         torch.cuda.empty_cache()
     os.makedirs(os.path.dirname(args.out), exist_ok=True)
+    if only and os.path.exists(args.out):
+        # a partial sweep updates its entries and keeps every other line
+        swept = {" ".join(l.split()[:7]) for l in lines}
+        kept = []
+        for l in open(args.out):
+            body = l.split("#")[0].split()
+            if len(body) >= 7 and " ".join(body[:7]) not in swept:
+                kept.append(l.rstrip("\n"))
+        lines = kept + lines
     with open(args.out, "w") as f:
         f.write("# tile table for the tensor-core kernel: op in out M N K batch bn splits raster\n")
         f.write(f"# written by `python -m gemms_linear_layers_gb300.sweep --sets {args.sets}` on {name} "

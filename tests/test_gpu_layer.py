@@ -343,3 +343,105 @@ def test_stream_k_in_replayed_cuda_graph():
         assert tg.tg_stream_status() == 0
 
     _with_table(line, go)
+
+
+# 144-column tiles (a width that is not a multiple of 64: the last 16 columns
+# of every tile leave through their own store box); ragged N in every layout
+W144_CASES = [("fwd", 300, 200, 520), ("dgrad", 300, 520, 200), ("wgrad", 520, 296, 200),
+              ("fwd", 1000, 1000, 1000)]
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", W144_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_tile_width_144(case, dtype, out_kind, splits):
+    op, T, d_in, d_out = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    dname = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+    line = f"{lay} {dname[dtype]} {dname[out_dtype]} {M} {N} {K} 1 144 {splits}"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="w144")
+    got = _with_table(line, lambda: run(op, X.cuda(), W.cuda(), dY.cuda(), out_dtype))
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert "bn=144" in call and "table=hit" in call, call
+    C, S = ref(op, X, W, dY)
+    assert_close(got, C, S, f"{op} bn=144 [{call}]", out_dtype)
+
+
+def test_tile_width_144_full_size_wgrad():
+    """The square weight gradient of the 2B-class attention projections at
+    2,048 tokens with 144-column tiles (288 tiles: about two waves)."""
+    T, d_in, d_out = 2048, 2304, 2304
+    line = f"tn bf16 bf16 {d_out} {d_in} {T} 1 144 1"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, torch.bfloat16, tag="w144f")
+    got = _with_table(line, lambda: tg.tg_gemm_wgrad(dY.cuda(), X.cuda()))
+    call = tg.tg_last_call()
+    assert "bn=144" in call, call
+    co = sample_coords(d_out, d_in, rows=32, cols=32, rand=4096, seed=144)
+    C, S = oracle.gemm_wgrad(dY, X, sample=co)
+    assert_close(gather(got, co), C, S, f"wgrad bn=144 full size [{call}]", torch.bfloat16)
+
+
+# Tail split: the tiles past the last whole wave of 152 CTAs are cut along K
+# into FP32 partial tiles that a second kernel adds in split order.  Cases
+# with ragged M/N edge tiles in the tail, every layout, a batch.
+TAIL_CASES = [("fwd", 2000, 576, 1528, 64, 4), ("dgrad", 2048, 1536, 576, 64, 3),
+              ("wgrad", 2048, 576, 2304, 64, 4), ("wgrad", 2048, 2304, 2304, 256, 4)]
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", TAIL_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_tail_split_schedule(case, dtype, out_kind):
+    op, T, d_in, d_out, bn, ts = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    dname = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+    line = f"{lay} {dname[dtype]} {dname[out_dtype]} {M} {N} {K} 1 {bn} t{ts}"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="tail")
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+    outs = _with_table(line, lambda: [run(op, Xc, Wc, dYc, out_dtype) for _ in range(2)])
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert " tail=" in call and "table=hit" in call, call
+    assert torch.equal(outs[0], outs[1]), "tail split not deterministic"
+    if M * N * K <= 3 * 10 ** 9:
+        C, S = ref(op, X, W, dY)
+        assert_close(outs[0], C, S, f"{op} tail split [{call}]", out_dtype)
+    else:
+        co = sample_coords(M, N, rows=32, cols=32, rand=4096, seed=7)
+        C, S = ref(op, X, W, dY, sample=co)
+        assert_close(gather(outs[0], co), C, S, f"{op} tail split sampled [{call}]", out_dtype)
+
+
+def test_tail_split_attention_batch():
+    h, s, d = 36, 1024, 64
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="tail")
+    line = f"tn bf16 bf16 {s} {d} {s} {h} 64 t2"
+    got = _with_table(line, lambda: tg.tg_bmm_attn("pt_do", t["P"].cuda(), t["dO"].cuda()))
+    call = tg.tg_last_call()
+    assert " tail=" in call, call
+    co = sample_coords(s, d, batch=h, rows=16, cols=16, rand=2048, seed=9)
+    C, S = oracle.bmm_attn("pt_do", t["P"], t["dO"], sample=co)
+    assert_close(gather(got, co), C, S, f"attn pt_do tail split [{call}]", torch.bfloat16)
+
+
+def test_tail_split_small_integers_exact():
+    """Integer-valued inputs: every split and the reduction are exact, so the
+    result equals the oracle bit for bit."""
+    T, d_in, d_out = 2048, 576, 2304
+    X = inputs.small_int((T, d_in), -2, 2, torch.bfloat16, 21)
+    dY = inputs.small_int((T, d_out), -2, 2, torch.bfloat16, 22)
+    line = f"tn bf16 f32 {d_out} {d_in} {T} 1 64 t4"
+    got = _with_table(line, lambda: tg.tg_gemm_wgrad(dY.cuda(), X.cuda(), out_dtype=torch.float32))
+    assert " tail=" in tg.tg_last_call()
+    C, _ = oracle.gemm_wgrad(dY, X)
+    assert np.array_equal(got.cpu().double().numpy(), C)
