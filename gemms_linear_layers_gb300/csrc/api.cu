@@ -55,6 +55,14 @@ bool pdl_enabled() {
   return on;
 }
 
+bool chunked_mn_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("TG_CHUNKED_MN");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
 struct DevCtx {
   bool ready = false;
   tg_status init_status = TG_OK;

@@ -76,6 +76,7 @@ struct TcArgs {
   uint32_t idesc;
   int out_f16;   // 16-bit output type: 1 = fp16, 0 = bf16
   int raster_n;  // 1: consecutive units walk along N (they share the A tile)
+  int a_chunked, b_chunked;  // MN-major operand loaded by one 4-D box ([batch][chunk][k][64]) per stage
   int dp_tiles;     // tail split: tiles run whole (the first dp_tiles in raster order)
   int tail_splits;  // > 1: each later tile is split into this many K ranges of tail_kps blocks
   int tail_kps;
@@ -289,14 +290,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_STAGE);
           const int k0 = kb * TC_BK;
           if (A_MN) {
-            tma_load_3d(a_dst, &tmA, fb, c.m0, k0, c.b);
-            tma_load_3d(a_dst + 8192, &tmA, fb, c.m0 + 64, k0, c.b);
+            if (args.a_chunked) {  // one box: 2 chunks of 64 columns x 64 k-rows
+              tma_load_4d(a_dst, &tmA, fb, 0, k0, c.m0 / 64, c.b);
+            } else {
+              tma_load_3d(a_dst, &tmA, fb, c.m0, k0, c.b);
+              tma_load_3d(a_dst + 8192, &tmA, fb, c.m0 + 64, k0, c.b);
+            }
           } else {
             tma_load_3d(a_dst, &tmA, fb, k0, c.m0, c.b);
           }
           if (B_MN) {
+            if (args.b_chunked) {
+              tma_load_4d(b_dst, &tmB, fb, 0, k0, c.n0 / 64, c.b);
+            } else {
 #pragma unroll
-            for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
+              for (int j = 0; j < Cfg::B_CHUNKS; ++j)
+                tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
+            }
           } else {
             tma_load_3d(b_dst, &tmB, fb, k0, c.n0, c.b);
           }

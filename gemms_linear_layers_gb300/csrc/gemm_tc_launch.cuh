@@ -31,15 +31,33 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   alignas(64) CUtensorMap tmA, tmB, tmC, tmC2, tmP;
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
   bool ok;
-  if (A_MN)  // stored [batch][K][M]
+  // An MN-major operand whose width is a multiple of 64 is viewed as
+  // [batch][width/64 chunks][K][64], so one box loads all of a stage's chunks
+  // in the layout the MMA reads (chunks 8 KB apart).  Otherwise one 2-D box
+  // per chunk (boxes past the width read zeros).
+  const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
+  const bool b4 = B_MN && N % 64 == 0 && BN % 64 == 0 && chunked_mn_enabled();
+  if (a4) {
+    const uint64_t d[4] = {64, K, M / 64, nb}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
+                                                      static_cast<uint64_t>(g.a_bstride) * 2};
+    const uint32_t b[4] = {64, 64, TC_BM / 64, 1};
+    ok = encode_tmap_nd(&tmA, g.A, g.in_kind, 4, d, st, b, 128);
+  } else if (A_MN) {  // stored [batch][K][M]
     ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
-  else       // stored [batch][M][K]
+  } else {  // stored [batch][M][K]
     ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
+  }
   if (!ok) return cudaErrorInvalidValue;
-  if (B_MN)  // stored [batch][K][N]
+  if (b4) {
+    const uint64_t d[4] = {64, K, N / 64, nb}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
+                                                      static_cast<uint64_t>(g.b_bstride) * 2};
+    const uint32_t b[4] = {64, 64, static_cast<uint32_t>(Cfg::B_CHUNKS), 1};
+    ok = encode_tmap_nd(&tmB, g.B, g.in_kind, 4, d, st, b, 128);
+  } else if (B_MN) {  // stored [batch][K][N]
     ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
-  else       // stored [batch][N][K]
+  } else {  // stored [batch][N][K]
     ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
+  }
   if (!ok) return cudaErrorInvalidValue;
 
   // output (or FP32 split partials): [batch * splits][M][N], dense
@@ -68,6 +86,8 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
   a.raster_n = g.raster_n;
   a.sk = g.sk;
+  a.a_chunked = a4 ? 1 : 0;
+  a.b_chunked = b4 ? 1 : 0;
   // tail split (never with stream-K or split partials)
   const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid, (g.sk || g.splits > 1) ? 1 : g.tail_splits, g.raster_n);
   a.dp_tiles = tg.dp_tiles;

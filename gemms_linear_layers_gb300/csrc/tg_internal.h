@@ -16,6 +16,9 @@ namespace tg {
 
 // Programmatic dependent launch on (default) or off ($TG_PDL=0).
 bool pdl_enabled();
+// MN-major GEMM operands loaded as one chunked 4-D box per stage (default) or
+// one 2-D box per 64-column chunk ($TG_CHUNKED_MN=0).
+bool chunked_mn_enabled();
 
 // Sets the calling thread's tg_last_call() text (and logs it under TG_LOG).
 void note_last_call(const std::string& s);
