@@ -185,7 +185,10 @@ def kernel_key(call: str) -> str:
         return f"{path} {f[2] if len(f) > 2 else ''}".strip()
     bn = next((x for x in f if x.startswith("bn=")), "bn=?")
     sp = next((x for x in f if x.startswith("splits=")), "splits=1")
-    return f"tc {f[2]} {bn}" + (" +reduce" if sp != "splits=1" else "")
+    deep = " deep" if "deep" in f else ""
+    tail = " +tail" if any(x.startswith("tail=") for x in f) else ""
+    sk = " sk" if "sk" in f else ""
+    return f"tc {f[2]} {bn}{deep}{sk}" + (" +reduce" if sp != "splits=1" else "") + tail
 
 
 def capture(prods, stream):

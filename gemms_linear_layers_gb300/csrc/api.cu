@@ -441,6 +441,14 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.sk = p.sk ? 1 : 0;
     t.sk_epoch = p.sk ? next_epoch() : 0;
     t.tail_splits = p.tail;
+    // the deep ring when a CTA streams at least 128 K blocks (its epilogues
+    // hide behind later MMAs); widths 144 and 192 only
+    {
+      const int64_t tiles = g.batch * cdiv(g.M, 128) * cdiv(g.N, p.bn);
+      const int64_t kb = cdiv(g.K, 64);
+      const int64_t per_cta = p.sk ? cdiv(tiles * kb, ctx->sms) : cdiv(tiles * p.splits, ctx->sms) * cdiv(kb, p.splits);
+      t.deep = (p.bn == 192 || p.bn == 144) && per_cta >= 128 ? 1 : 0;
+    }
     t.ws = g.ws;
     t.grid = ctx->sms;
     t.stream = g.stream;
@@ -456,10 +464,11 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
                                   p.raster_n);
     char tail[48] = "";
     if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
-    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d %s%d%s raster=%c table=%s %s",
+    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s %s",
              g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
-             p.bn, p.sk ? "sk grid=" : "splits=", p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits,
-             tail, p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+             p.bn, t.deep ? " deep" : "", p.sk ? "sk grid=" : "splits=",
+             p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits, tail, p.raster_n ? 'n' : 'm',
+             p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }

@@ -47,7 +47,7 @@ constexpr int TC_EPI_WARPS = 4;
 constexpr int TC_A_STAGE = TC_BM * TC_BK * 2;  // 16 KB
 constexpr int TC_EPI_BUF = 32 * 128;           // 32 rows x 128 bytes
 
-template <int BN>
+template <int BN, bool DEEP = false>
 struct TcCfg {
   // B tile: BN rows of 128 bytes (K-major) or ceil(BN/64) 64-column chunks
   // of 8 KB (MN-major; a width that is not a multiple of 64 loads a full last
@@ -56,12 +56,18 @@ struct TcCfg {
   static constexpr int B_STAGE = B_CHUNKS * 64 * TC_BK * 2;
   static constexpr int B_BYTES_K = BN * TC_BK * 2;
   static constexpr int B_BYTES_MN = B_STAGE;
-  static constexpr int STAGES = (BN > 128) ? 4 : (BN == 128) ? 6 : 8;
+  // DEEP (widths 144 and 192 only): each epilogue warp keeps one staging
+  // buffer instead of two, which makes room for a fifth operand stage (more
+  // loads in flight); it pays when a CTA streams many K blocks, so that the
+  // slower epilogue hides behind the next unit's MMAs.
+  static_assert(!DEEP || BN == 192 || BN == 144, "deep ring only for 144 and 192");
+  static constexpr int EPI_BUFS = DEEP ? 1 : 2;
+  static constexpr int STAGES = DEEP ? 5 : (BN > 128) ? 4 : (BN == 128) ? 6 : 8;
   static constexpr int ACC_STRIDE = BN <= 64 ? 64 : (BN <= 128 ? 128 : 256);
   static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + STAGES * (TC_A_STAGE + B_STAGE) +
-                              TC_EPI_WARPS * 2 * TC_EPI_BUF + BAR_BYTES;
+                              TC_EPI_WARPS * EPI_BUFS * TC_EPI_BUF + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "tile width");
   static_assert(2 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area");
@@ -208,12 +214,12 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
   return v;
 }
-template <bool A_MN, bool B_MN, int BN, bool OUT16>
+template <bool A_MN, bool B_MN, int BN, bool OUT16, bool DEEP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                    const __grid_constant__ CUtensorMap tmP, const TcArgs args) {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, DEEP>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * TC_A_STAGE;
   uint8_t* sE = sB + S * Cfg::B_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + TC_EPI_WARPS * 2 * TC_EPI_BUF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + TC_EPI_WARPS * Cfg::EPI_BUFS * TC_EPI_BUF);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ----------------------------------------------------------- epilogue
     const int ew = warp - 2;  // staging buffers owned by this warp
     const int q = warp & 3;   // TMEM lane quadrant this warp may access
-    uint8_t* ebuf = sE + ew * 2 * TC_EPI_BUF;
+    uint8_t* ebuf = sE + ew * Cfg::EPI_BUFS * TC_EPI_BUF;
     constexpr int CW = OUT16 ? 64 : 32;  // columns per 128-byte staging row
     constexpr int NCH = BN / CW;
     constexpr int TW = BN % CW;  // a last, narrower chunk (16 columns) for BN = 144
@@ -438,8 +444,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
           }
-          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
-          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          uint8_t* buf = ebuf + (nstore % Cfg::EPI_BUFS) * TC_EPI_BUF;
+          // the staging buffer's previous store must have read it
+          if (lane == 0 && nstore >= Cfg::EPI_BUFS) bulk_wait_read<Cfg::EPI_BUFS - 1>();
           __syncwarp();
           uint8_t* rowp = buf + lane * 128;
 #pragma unroll
@@ -516,8 +523,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               }
             }
           }
-          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
-          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          uint8_t* buf = ebuf + (nstore % Cfg::EPI_BUFS) * TC_EPI_BUF;
+          // the staging buffer's previous store must have read it
+          if (lane == 0 && nstore >= Cfg::EPI_BUFS) bulk_wait_read<Cfg::EPI_BUFS - 1>();
           __syncwarp();
           uint8_t* rowp = buf + lane * 128;
 #pragma unroll
@@ -560,8 +568,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
-          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          uint8_t* buf = ebuf + (nstore % Cfg::EPI_BUFS) * TC_EPI_BUF;
+          // the staging buffer's previous store must have read it
+          if (lane == 0 && nstore >= Cfg::EPI_BUFS) bulk_wait_read<Cfg::EPI_BUFS - 1>();
           __syncwarp();
           if (OUT16) {
             uint32_t w[8];

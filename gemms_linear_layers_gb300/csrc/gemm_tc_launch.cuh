@@ -11,10 +11,10 @@
 
 namespace tg {
 
-template <bool A_MN, bool B_MN, int BN, bool OUT16>
+template <bool A_MN, bool B_MN, int BN, bool OUT16, bool DEEP = false>
 static cudaError_t tc_launch_one(const TcGemm& g) {
-  using Cfg = TcCfg<BN>;
-  auto kern = tc_gemm_kernel<A_MN, B_MN, BN, OUT16>;
+  using Cfg = TcCfg<BN, DEEP>;
+  auto kern = tc_gemm_kernel<A_MN, B_MN, BN, OUT16, DEEP>;
   // the attribute is per function and per device: set it once per device, so
   // later calls (including calls under stream capture) make no such call
   static bool attr_set[128] = {};
@@ -130,8 +130,12 @@ static cudaError_t tc_launch_layout(const TcGemm& g) {
   switch (g.bn) {
     case 64: return out16 ? tc_launch_one<A_MN, B_MN, 64, true>(g) : tc_launch_one<A_MN, B_MN, 64, false>(g);
     case 128: return out16 ? tc_launch_one<A_MN, B_MN, 128, true>(g) : tc_launch_one<A_MN, B_MN, 128, false>(g);
-    case 144: return out16 ? tc_launch_one<A_MN, B_MN, 144, true>(g) : tc_launch_one<A_MN, B_MN, 144, false>(g);
-    case 192: return out16 ? tc_launch_one<A_MN, B_MN, 192, true>(g) : tc_launch_one<A_MN, B_MN, 192, false>(g);
+    case 144:
+      if (g.deep) return out16 ? tc_launch_one<A_MN, B_MN, 144, true, true>(g) : tc_launch_one<A_MN, B_MN, 144, false, true>(g);
+      return out16 ? tc_launch_one<A_MN, B_MN, 144, true>(g) : tc_launch_one<A_MN, B_MN, 144, false>(g);
+    case 192:
+      if (g.deep) return out16 ? tc_launch_one<A_MN, B_MN, 192, true, true>(g) : tc_launch_one<A_MN, B_MN, 192, false, true>(g);
+      return out16 ? tc_launch_one<A_MN, B_MN, 192, true>(g) : tc_launch_one<A_MN, B_MN, 192, false>(g);
     case 256: return out16 ? tc_launch_one<A_MN, B_MN, 256, true>(g) : tc_launch_one<A_MN, B_MN, 256, false>(g);
     default: return cudaErrorInvalidValue;
   }

@@ -74,6 +74,7 @@ struct TcGemm {
   int sk;                     // 1: stream-K schedule (ws holds per-CTA partial tiles + flags)
   unsigned long long sk_epoch;  // flag value unique to this launch
   int tail_splits;            // >1: tiles past the last whole wave are split along K (ws: partial tiles)
+  int deep;                   // 1: widths 144/192 with a fifth operand stage (one epilogue buffer)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
