@@ -234,25 +234,83 @@ def external_event():
         return None
 
 
-def capture_step(prods, stream, dominant):
-    """One graph for the whole step.  External events mark the step's start
-    and end and bracket every launch of the dominant kernel."""
+# The order of a training step's linear-layer products, as waves of products
+# that have no data dependence on each other: forward q, k, v together, o,
+# gate and up together, down, head; backward from the head down, each
+# layer's input and weight gradients together (both need only dY and the
+# layer's own input or weight), gate/up and q/k/v as groups.
+FWD_WAVES = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"], ["head"]]
+BWD_WAVES = [["head"], ["down"], ["gate", "up"], ["o"], ["q", "k", "v"]]
+
+
+def step_waves(prods):
+    """The step's products as a list of waves (lists of products that may run
+    concurrently), dtype sets one after the other."""
+    by = {(p.layer, p.op, p.dtype): p for p in prods}
+    waves = []
+    for dtype in dict.fromkeys(p.dtype for p in prods):
+        for group in FWD_WAVES:
+            w = [by[(l, "fwd", dtype)] for l in group if (l, "fwd", dtype) in by]
+            if w:
+                waves.append(w)
+        for group in BWD_WAVES:
+            w = [by[(l, op, dtype)] for l in group for op in ("dgrad", "wgrad") if (l, op, dtype) in by]
+            if w:
+                waves.append(w)
+    placed = {id(p) for w in waves for p in w}
+    waves += [[p] for p in prods if id(p) not in placed]
+    return waves
+
+
+def capture_step(prods, stream, dominant, concurrent=True):
+    """One graph for the whole step.  With `concurrent`, the products of a
+    wave run on parallel branches (fork/join through events on side
+    streams).  External events mark the step's start and end and bracket every
+    launch of the dominant kernel."""
     e0, e1 = external_event(), external_event()
     if e0 is None:
         return None
+    waves = step_waves(prods) if concurrent else [[p] for p in prods]
+    # a stream-K launch waits on its own later CTAs, which need every SM it
+    # may occupy: it runs alone in its wave
+    split = []
+    for w in waves:
+        split += [[p] for p in w if " sk" in p.kernel]
+        rest = [p for p in w if " sk" not in p.kernel]
+        if rest:
+            split.append(rest)
+    waves = split
+    width = max(len(w) for w in waves)
+    side = [torch.cuda.Stream() for _ in range(width)]
     marks = []
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         e0.record()
-        for p in prods:
-            if p.kernel == dominant:
-                a, b = external_event(), external_event()
-                a.record()
-                run_product(p)
-                b.record()
-                marks.append((p, a, b))
+        for w in waves:
+            if len(w) == 1:
+                branches = [(stream, w[0])]
             else:
-                run_product(p)
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                branches = []
+                for i, p in enumerate(w):
+                    side[i].wait_event(fork)
+                    branches.append((side[i], p))
+            for st, p in branches:
+                with torch.cuda.stream(st):
+                    if p.kernel == dominant:
+                        a, b = external_event(), external_event()
+                        a.record(st)
+                        run_product(p)
+                        b.record(st)
+                        marks.append((p, a, b))
+                    else:
+                        run_product(p)
+            if len(w) > 1:
+                for st, _ in branches:
+                    j = torch.cuda.Event()
+                    j.record(st)
+                    stream.wait_event(j)
         e1.record()
     torch.cuda.synchronize()
     return g, e0, e1, marks
@@ -556,6 +614,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--per-product-graphs", action="store_true",
                     help="time with one graph per product instead of one graph per step")
+    ap.add_argument("--concurrent-step", action="store_true",
+                    help="one graph per step with the training step's independent products on parallel branches")
     ap.add_argument("--only", default=None,
                     help="comma-separated products to run, e.g. head.wgrad.bfloat16 (profiling a single kernel)")
     ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
@@ -596,9 +656,15 @@ def main():
         k["n"] += 1
         k["products"].append(p.name)
     dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
-    step = None if args.per_product_graphs else capture_step(prods, stream, dom_name)
-    mode = "one CUDA graph per step; external events inside it bracket the dominant kernel" if step else \
-        "one CUDA graph per product; events between them on the launching stream"
+    step = None if args.per_product_graphs else capture_step(prods, stream, dom_name, args.concurrent_step)
+    if step and args.concurrent_step:
+        mode = ("one CUDA graph per step with the training step's independent products on parallel branches "
+                "(forward q|k|v and gate|up; backward each layer's dgrad|wgrad, gate|up and q|k|v as groups); "
+                "external events inside it bracket the dominant kernel")
+    elif step:
+        mode = "one CUDA graph per step, products one after another; external events bracket the dominant kernel"
+    else:
+        mode = "one CUDA graph per product; events between them on the launching stream"
 
     if world > 1:
         torch.distributed.barrier()
