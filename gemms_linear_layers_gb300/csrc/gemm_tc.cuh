@@ -401,6 +401,67 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     WorkIter it = work_begin(args);
     Unit c;
     while (work_next<BN>(args, it, c)) {
+      // A stream-K owner whose tile later CTAs finish: this is the CTA's
+      // last unit, so the other accumulator is idle.  While this unit's MMAs
+      // run, wait for the later pieces of this warp's 32 rows and stage their
+      // sum (in CTA order) there, so the fix-up below reads tensor memory.
+      const bool fixup = c.owner && c.c_last > static_cast<int>(blockIdx.x);
+      bool have_parts = true;
+      const uint32_t t_pre = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>((acc ^ 1) * Cfg::ACC_STRIDE);
+      if (BN % 64 == 0 && fixup) {
+        // one lane polls, with back-off: flags sit on their own 128-byte lines
+        // and a storm of polls would crowd the L2 slices the TMA loads need
+        int ok = 1;
+        if (warp == 2 && lane == 0) TG_EVENT(4);
+        if (lane == 0) {
+          for (int cc = blockIdx.x + 1; cc <= c.c_last && ok; ++cc) {
+            const unsigned long long* fl = args.sk_flags + sk_flag_index(cc, q);
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_u64(fl) != args.sk_epoch) {
+              __nanosleep(128);
+              if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+                if (!*abort_flag) {
+                  *abort_flag = 1;
+                  atomicOr(args.status, TG_DEVSTAT_TIMEOUT | 5u);
+                }
+                ok = 0;
+                break;
+              }
+            }
+          }
+        }
+        have_parts = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        __syncwarp();  // lane 0's acquire orders the other lanes' reads below
+        if (warp == 2 && lane == 0) TG_EVENT(5);
+        if (have_parts) {
+#pragma unroll 1
+          for (int blk = 0; blk < BN / 32; ++blk) {
+            uint32_t sp[32];
+            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) {
+              const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, blk, 0, lane);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 v = ld_cg_f4(src + 4 * 32 * j);
+                uint32_t* d = sp + 4 * j;
+                if (cc == static_cast<int>(blockIdx.x) + 1) {
+                  d[0] = __float_as_uint(v.x);
+                  d[1] = __float_as_uint(v.y);
+                  d[2] = __float_as_uint(v.z);
+                  d[3] = __float_as_uint(v.w);
+                } else {
+                  d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
+                  d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
+                  d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
+                  d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+                }
+              }
+            }
+            tmem_st_32x32b_x32(t_pre + blk * 32, sp);
+          }
+          tmem_st_wait();
+        }
+      }
       if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -462,36 +523,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ++nstore;
         }
       } else {
-        // ---- tile writer; a stream-K owner first waits for the later pieces
-        // of its own 32 rows (each lane polls the flags itself)
-        const bool fixup = c.c_last > static_cast<int>(blockIdx.x);
-        bool have_parts = true;
-        if (fixup) {
-          // one lane polls, with back-off: flags sit on their own 128-byte lines
-          // and a storm of polls would crowd the L2 slices the TMA loads need
-          int ok = 1;
-          if (warp == 2 && lane == 0) TG_EVENT(4);
-          if (lane == 0) {
-            for (int cc = blockIdx.x + 1; cc <= c.c_last && ok; ++cc) {
-              const unsigned long long* fl = args.sk_flags + sk_flag_index(cc, q);
-              const uint64_t t0 = globaltimer_ns();
-              while (ld_acquire_u64(fl) != args.sk_epoch) {
-                __nanosleep(128);
-                if (*abort_flag || globaltimer_ns() - t0 > tmo) {
-                  if (!*abort_flag) {
-                    *abort_flag = 1;
-                    atomicOr(args.status, TG_DEVSTAT_TIMEOUT | 5u);
-                  }
-                  ok = 0;
-                  break;
-                }
-              }
-            }
-          }
-          have_parts = __shfl_sync(0xffffffffu, ok, 0) != 0;
-          __syncwarp();  // lane 0's acquire orders the other lanes' reads below
-          if (warp == 2 && lane == 0) TG_EVENT(5);
-        }
+        // ---- tile writer (a stream-K owner adds the later pieces staged above)
         const int zc = c.b * args.splits + c.split;
 #pragma unroll 1
         for (int ch = 0; ch < NCH; ++ch) {
@@ -505,22 +537,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
           }
-          if (fixup && have_parts) {
-            // add the later CTAs' partials in CTA order
-            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) {
+          if (BN % 64 == 0 && fixup && have_parts) {
+            // add the later CTAs' pieces (their sum, staged in the idle accumulator)
 #pragma unroll
-              for (int sub = 0; sub < CW / 32; ++sub) {
-                const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, ch * (CW / 32) + sub, 0, lane);
+            for (int sub = 0; sub < CW / 32; ++sub) {
+              uint32_t sp[32];
+              tmem_ld_32x32b_x32(t_pre + ch * CW + sub * 32, sp);
+              tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 v = ld_cg_f4(src + 4 * 32 * j);
-                  uint32_t* d = r + 32 * sub + 4 * j;
-                  d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
-                  d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
-                  d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
-                  d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
-                }
-              }
+              for (int j = 0; j < 32; ++j)
+                r[32 * sub + j] = __float_as_uint(__uint_as_float(r[32 * sub + j]) + __uint_as_float(sp[j]));
             }
           }
           uint8_t* buf = ebuf + (nstore % Cfg::EPI_BUFS) * TC_EPI_BUF;
