@@ -353,36 +353,65 @@ def timed_steps_per_product(prods, n_warm, n_steps, stream, flush, dominant):
 # ------------------------------------------------------------------ e2e
 def e2e_steps(prods, n_steps, stream):
     """The step through the public API with pinned host buffers: every step
-    copies its inputs host->device and its outputs device->host."""
-    host_in, host_out = {}, {}
-    h2d = d2h = 0
-    seen = set()
+    copies its inputs host->device and its outputs device->host.  Copies and
+    products form a pipeline: every X and W come in first, so each forward
+    product starts as soon as its own operands have arrived while the dY
+    tensors (the large ones) follow; each result goes out as soon as the
+    product that writes it is done, on a second copy stream.  Steps do not
+    overlap."""
+    groups = {}
     for p in prods:
-        key = (p.layer, p.dtype)
-        if key in seen:
-            continue
-        seen.add(key)
-        for n in ("X", "W", "dY"):
-            host_in[(key, n)] = p.t[n].cpu().pin_memory()
-            h2d += p.t[n].numel() * p.t[n].element_size()
-        for n in ("Y", "dX", "dW"):
-            host_out[(key, n)] = torch.empty(p.t[n].shape, dtype=p.t[n].dtype).pin_memory()
-            d2h += p.t[n].numel() * p.t[n].element_size()
+        groups.setdefault((p.layer, p.dtype), []).append(p)
+    h2d = d2h = 0
+    host = {}
+    for key, ps in groups.items():
+        t = ps[0].t
+        for n in ("X", "W", "dY", "Y", "dX", "dW"):
+            host[(key, n)] = (t[n], torch.empty(t[n].shape, dtype=t[n].dtype).pin_memory())
+            if n in ("X", "W", "dY"):
+                host[(key, n)][1].copy_(t[n].cpu())
+                h2d += t[n].numel() * t[n].element_size()
+            else:
+                d2h += t[n].numel() * t[n].element_size()
+    needs = {"fwd": ("X", "W"), "dgrad": ("dY", "W"), "wgrad": ("dY", "X")}
+    writes = {"fwd": "Y", "dgrad": "dX", "wgrad": "dW"}
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     times = []
-    with torch.cuda.stream(stream):
-        for s in range(n_steps + 1):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for (key, n), h in host_in.items():
-                layer, dtype = key
-                next(p for p in prods if (p.layer, p.dtype) == key).t[n].copy_(h, non_blocking=True)
-            for p in prods:
-                run_product(p)
-            for (key, n), h in host_out.items():
-                h.copy_(next(p for p in prods if (p.layer, p.dtype) == key).t[n], non_blocking=True)
-            b.record(stream)
-            if s > 0:
-                times.append((a, b))
+    for step in range(n_steps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        s_in.wait_event(a)
+        s_out.wait_event(a)
+        arrived = {}
+        for names in (("X", "W"), ("dY",)):  # operands in: X and W of every layer, then dY
+            for key in groups:
+                with torch.cuda.stream(s_in):
+                    for n in names:
+                        dev, h = host[(key, n)]
+                        dev.copy_(h, non_blocking=True)
+                        arrived[(key, n)] = torch.cuda.Event()
+                        arrived[(key, n)].record(s_in)
+        for ops in (("fwd",), ("dgrad", "wgrad")):  # forward products first, as their operands arrive
+            for key, ps in groups.items():
+                for p in ps:
+                    if p.op not in ops:
+                        continue
+                    for n in needs[p.op]:
+                        stream.wait_event(arrived[(key, n)])
+                    with torch.cuda.stream(stream):
+                        run_product(p)
+                    done = torch.cuda.Event()
+                    done.record(stream)
+                    s_out.wait_event(done)
+                    with torch.cuda.stream(s_out):  # its result out
+                        dev, h = host[(key, writes[p.op])]
+                        h.copy_(dev, non_blocking=True)
+        out_done = torch.cuda.Event()
+        out_done.record(s_out)
+        stream.wait_event(out_done)
+        b.record(stream)
+        if step > 0:
+            times.append((a, b))
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in times)
     return ms, h2d, d2h
