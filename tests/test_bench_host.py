@@ -1,0 +1,50 @@
+"""Host logic of bench.py (no GPU): the kernel identity taken from a call
+record, and the waves of the optional concurrent step."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from gemms_linear_layers_gb300 import workloads  # noqa: E402
+
+
+def test_kernel_key():
+    k = bench.kernel_key
+    assert k("fwd tc nt M=2048 N=576 K=576 batch=1 bn=64 splits=1 raster=n table=hit ok") == "tc nt bn=64"
+    assert k("dgrad tc nn M=2048 N=576 K=49152 batch=1 bn=192 deep splits=3 raster=n table=hit ok") == \
+        "tc nn bn=192 deep +reduce"
+    assert k("wgrad tc tn M=2304 N=2304 K=2048 batch=1 bn=256 sk grid=152 raster=n table=hit ok") == "tc tn bn=256 sk"
+    assert k("wgrad tc tn M=2304 N=2304 K=2048 batch=1 bn=256 splits=1 tail=10x4 raster=n table=hit ok") == \
+        "tc tn bn=256 +tail"
+    assert k("wgrad simt tn M=200 N=300 K=520 batch=1 ok") == "simt tn"
+
+
+def _products():
+    prods = []
+    for dt in workloads.DECODER_135M["dtypes"]:
+        for layer, d_in, d_out in workloads.LAYERS_135M:
+            for op in ("fwd", "dgrad", "wgrad"):
+                p = bench.Product(layer, op, dt, 2048, d_in, d_out)
+                p.kernel = "tc nt bn=64"
+                prods.append(p)
+    return prods
+
+
+def test_step_waves_cover_every_product_once_in_training_order():
+    prods = _products()
+    waves = bench.step_waves(prods)
+    flat = [p for w in waves for p in w]
+    assert sorted(map(id, flat)) == sorted(map(id, prods))
+    names = [[p.name for p in w] for w in waves]
+    assert names[0] == ["q.fwd.bfloat16", "k.fwd.bfloat16", "v.fwd.bfloat16"]
+    assert names[5] == ["head.dgrad.bfloat16", "head.wgrad.bfloat16"]
+    # a wave never mixes dtypes, and forward products come before backward ones per dtype
+    for w in waves:
+        assert len({p.dtype for p in w}) == 1
+    order = [(p.dtype, p.op) for w in waves for p in w]
+    bf = [op for dt, op in order if dt == torch.bfloat16]
+    assert bf.index("dgrad") > max(i for i, op in enumerate(bf) if op == "fwd")
