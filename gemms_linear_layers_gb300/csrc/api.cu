@@ -137,6 +137,7 @@ struct TableKeyHash {
 struct TableVal {
   int bn, splits, raster;  // splits 0 = stream-K; raster: -1 = by operand size, 0 = along M, 1 = along N
   int tail;                // > 1: tail split of the tiles past the last whole wave
+  int pair;                // 1: CTA-pair kernel (256-row tiles)
 };
 static std::shared_mutex g_table_mu;
 static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
@@ -166,11 +167,19 @@ static tg_status load_table_file(const char* path) {
       const size_t h = line.find('#');
       if (h != std::string::npos) line.resize(h);
       std::istringstream ss(line);
-      std::string op, din, dout, sp;
+      std::string op, din, dout, bs, sp;
       int64_t M, N, K, batch;
-      int bn, splits, tail = 0;
+      int bn, splits, tail = 0, pair = 0;
       if (!(ss >> op)) continue;  // blank line
-      if (!(ss >> din >> dout >> M >> N >> K >> batch >> bn >> sp)) return TG_ERR_TABLE;
+      if (!(ss >> din >> dout >> M >> N >> K >> batch >> bs >> sp)) return TG_ERR_TABLE;
+      {  // tile width, "p" suffix: CTA pair (256 x bn tiles)
+        char* endp = nullptr;
+        const long v = strtol(bs.c_str(), &endp, 10);
+        if (endp == bs.c_str()) return TG_ERR_TABLE;
+        if (*endp == 'p' && endp[1] == '\0') pair = 1;
+        else if (*endp != '\0') return TG_ERR_TABLE;
+        bn = static_cast<int>(v);
+      }
       if (sp == "sk") {
         splits = 0;
       } else if (sp.size() > 1 && sp[0] == 't') {  // tail split: tN
@@ -197,7 +206,8 @@ static tg_status load_table_file(const char* path) {
       if (!(bn == 64 || bn == 128 || bn == 144 || bn == 192 || bn == 256) || splits < 0 || splits > 64)
         return TG_ERR_TABLE;
       if (bn % 64 != 0 && (splits == 0 || tail > 0)) return TG_ERR_TABLE;  // partial tiles: 64-column multiples
-      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail};
+      if (pair && (bn == 64 || bn == 144 || splits == 0 || tail > 0)) return TG_ERR_TABLE;  // pairs: data-parallel / split
+      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail, pair};
     }
   }
   std::unique_lock<std::shared_mutex> lk(g_table_mu);
@@ -240,6 +250,7 @@ struct Plan {
   int raster_n = 0;
   bool sk = false;  // stream-K schedule (splits is then 1)
   int tail = 0;     // > 1: tail split (splits is then 1)
+  bool pair = false;  // CTA-pair kernel: 256 x bn tiles
   bool from_table = false;
 };
 
@@ -254,8 +265,10 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
   const int64_t kb = cdiv(K, 64);
   const int bns[5] = {256, 192, 144, 128, 64};
   // one 128 x bn x 64 block: four 128 x bn x 16 MMAs, measured at >= 88 cycles
-  // each and ~0.525 * bn cycles from bn = 192 up (the tensor pipe's full rate)
-  auto kb_cycles = [](int bn) { return 4.0 * fmax(88.0, 0.525 * bn); };
+  // each and ~0.525 * bn cycles from bn = 192 up (the tensor pipe's full
+  // rate); from bn = 192 up the single-CTA kernel reaches ~0.89 of that rate,
+  // held back by its operand feed (all bn rows of B per SM)
+  auto kb_cycles = [](int bn) { return 4.0 * fmax(88.0, 0.525 * bn) * (bn >= 192 ? 1.12 : 1.0); };
   for (int bn : bns) {
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
     const double kb_cyc = kb_cycles(bn);
@@ -275,8 +288,6 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
-  // stream-K: every CTA gets an equal share of the tile x K-block iterations;
-  // a cut tile costs its pieces' FP32 write and the owner's read-back
   // tail split: whole tiles in full waves, the last partial wave's tiles cut along K
   for (int bn : bns) {
     if (bn % 64 != 0) continue;
@@ -298,6 +309,32 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
+  // CTA pairs (256 x bn tiles on two SMs, half of B per SM): a pair MMA
+  // costs at least ~125 cycles whatever its width, and runs at the full rate
+  // at bn = 256, measured
+  for (int bn : {256, 192}) {
+    if (M <= 128) break;
+    const int64_t tiles = batch * cdiv(M, 256) * cdiv(N, bn);
+    const double kb_cyc = 4.0 * fmax(125.0, 0.525 * bn);
+    const double epi_cyc = 128.0 * bn * out_bytes / 48.0;
+    for (int64_t s = 1; s <= 8 && s <= kb; ++s) {
+      const int64_t kps = cdiv(kb, s);
+      if (cdiv(kb, kps) != s) continue;
+      const int64_t waves = cdiv(tiles * s, sms / 2);
+      double t = waves * (fmax(kps * kb_cyc, s > 1 ? 128.0 * bn * 4 / 48.0 : epi_cyc) + 600.0);
+      if (s > 1) t += 3000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
+      if (t < best_t * 0.98) {
+        best_t = t;
+        best.bn = bn;
+        best.splits = static_cast<int>(s);
+        best.sk = false;
+        best.tail = 0;
+        best.pair = true;
+      }
+    }
+  }
+  // stream-K: every CTA gets an equal share of the tile x K-block iterations;
+  // a cut tile costs its pieces' FP32 write and the owner's read-back
   for (int bn : bns) {
     if (bn % 64 != 0) continue;  // stream-K partial tiles are 64-column multiples
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
@@ -312,6 +349,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       best.splits = 1;
       best.sk = true;
       best.tail = 0;
+      best.pair = false;
     }
   }
   return best;
@@ -328,6 +366,7 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
   if (table_lookup(TableKey{layout, in, out, M, N, K, batch}, &v)) {
     Plan p;
     p.bn = v.bn;
+    p.pair = v.pair != 0;
     const int64_t kb = cdiv(K, 64);
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, p.bn);
     p.sk = v.splits == 0 && tiles * kb >= 1;
@@ -441,13 +480,14 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.sk = p.sk ? 1 : 0;
     t.sk_epoch = p.sk ? next_epoch() : 0;
     t.tail_splits = p.tail;
+    t.pair = p.pair ? 1 : 0;
     // the deep ring when a CTA streams at least 128 K blocks (its epilogues
     // hide behind later MMAs); widths 144 and 192 only
     {
       const int64_t tiles = g.batch * cdiv(g.M, 128) * cdiv(g.N, p.bn);
       const int64_t kb = cdiv(g.K, 64);
       const int64_t per_cta = p.sk ? cdiv(tiles * kb, ctx->sms) : cdiv(tiles * p.splits, ctx->sms) * cdiv(kb, p.splits);
-      t.deep = (p.bn == 192 || p.bn == 144) && per_cta >= 128 ? 1 : 0;
+      t.deep = !p.pair && (p.bn == 192 || p.bn == 144) && per_cta >= 128 ? 1 : 0;
     }
     t.ws = g.ws;
     t.grid = ctx->sms;
@@ -466,7 +506,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
     snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s %s",
              g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
-             p.bn, t.deep ? " deep" : "", p.sk ? "sk grid=" : "splits=",
+             p.bn, t.deep ? " deep" : (p.pair ? " pair" : ""), p.sk ? "sk grid=" : "splits=",
              p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits, tail, p.raster_n ? 'n' : 'm',
              p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);

@@ -7,6 +7,7 @@
 #include <stdlib.h>
 
 #include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -123,8 +124,117 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream);
 }
 
+// CTA-pair kernel: clusters of two CTAs, one per SM, persistent over
+// 256 x BN tiles (x splits).  The grid is the number of pairs that fit on the
+// device at once (at most half the SMs), times two.
+template <bool A_MN, bool B_MN, int BN, bool OUT16>
+static cudaError_t tc2_launch_one(const TcGemm& g) {
+  using Cfg = Tc2Cfg<BN, B_MN>;
+  auto kern = tc2_gemm_kernel<A_MN, B_MN, BN, OUT16>;
+  static bool attr_set[128] = {};
+  static int max_pairs[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = g.stream;
+  cfg.attrs = attr;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    cfg.gridDim = dim3(2 * (g.grid / 2 > 0 ? g.grid / 2 : 1));
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = n;
+    attr_set[dev] = true;
+  }
+
+  alignas(64) CUtensorMap tmA, tmB, tmC;
+  const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
+  bool ok;
+  const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
+  const bool b4 = B_MN && N % 64 == 0 && Cfg::BH % 64 == 0 && chunked_mn_enabled();
+  if (a4) {
+    const uint64_t d[4] = {64, K, M / 64, nb}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
+                                                      static_cast<uint64_t>(g.a_bstride) * 2};
+    const uint32_t b[4] = {64, 64, TC_BM / 64, 1};
+    ok = encode_tmap_nd(&tmA, g.A, g.in_kind, 4, d, st, b, 128);
+  } else if (A_MN) {
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
+  } else {
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  if (b4) {
+    const uint64_t d[4] = {64, K, N / 64, nb}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
+                                                      static_cast<uint64_t>(g.b_bstride) * 2};
+    const uint32_t b[4] = {64, 64, static_cast<uint32_t>(Cfg::B_CHUNKS), 1};
+    ok = encode_tmap_nd(&tmB, g.B, g.in_kind, 4, d, st, b, 128);
+  } else if (B_MN) {
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
+  } else {
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, Cfg::BH, 128);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const bool split_parts = g.splits > 1;
+  const int ck = split_parts ? EK_F32 : g.out_kind;
+  const uint64_t esz = elem_bytes(ck);
+  void* cptr = split_parts ? g.ws : g.C;
+  ok = encode_tmap_3d(&tmC, cptr, ck, N, M, nb * (split_parts ? g.splits : 1), N * esz, M * N * esz,
+                      OUT16 ? 64 : 32, 32, 128);
+  if (!ok) return cudaErrorInvalidValue;
+
+  TcArgs a = {};
+  a.m_tiles = static_cast<int>((M + TC2_BM - 1) / TC2_BM);
+  a.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.splits = g.splits;
+  a.kps = (a.kb_total + a.splits - 1) / a.splits;
+  a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * a.splits;
+  a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC2_BM, BN);
+  a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
+  a.raster_n = g.raster_n;
+  a.a_chunked = a4 ? 1 : 0;
+  a.b_chunked = b4 ? 1 : 0;
+  a.tail_splits = 1;
+  a.timeout_ns = g.timeout_ns;
+  a.status = g.status;
+  int pairs = g.grid / 2;
+  if (pairs > max_pairs[dev]) pairs = max_pairs[dev];
+  if (pairs > a.units) pairs = a.units;
+  if (pairs < 1) pairs = 1;
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
+}
+
+template <bool A_MN, bool B_MN>
+static cudaError_t tc2_launch_layout(const TcGemm& g) {
+  const bool out16 = g.splits == 1 && g.out_kind != EK_F32;
+  switch (g.bn) {
+    case 128: return out16 ? tc2_launch_one<A_MN, B_MN, 128, true>(g) : tc2_launch_one<A_MN, B_MN, 128, false>(g);
+    case 192: return out16 ? tc2_launch_one<A_MN, B_MN, 192, true>(g) : tc2_launch_one<A_MN, B_MN, 192, false>(g);
+    case 256: return out16 ? tc2_launch_one<A_MN, B_MN, 256, true>(g) : tc2_launch_one<A_MN, B_MN, 256, false>(g);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <bool A_MN, bool B_MN>
 static cudaError_t tc_launch_layout(const TcGemm& g) {
+  if (g.pair) return tc2_launch_layout<A_MN, B_MN>(g);
   // split partials are FP32; so is an FP32 output
   const bool out16 = (g.sk || g.splits == 1) && g.out_kind != EK_F32;
   switch (g.bn) {

@@ -68,13 +68,14 @@ struct TcGemm {
   int64_t batch, M, N, K;
   int64_t lda, ldb;           // row pitches in elements
   int64_t a_bstride, b_bstride;  // batch strides in elements
-  int bn;                     // tile width: 64, 128, 192 or 256
+  int bn;                     // tile width: 64, 128, 144, 192 or 256
   int splits;                 // >1: FP32 partials to ws, then an ordered reduction
   int raster_n;               // 1: walk output tiles along N first (A tiles reused)
   int sk;                     // 1: stream-K schedule (ws holds per-CTA partial tiles + flags)
   unsigned long long sk_epoch;  // flag value unique to this launch
   int tail_splits;            // >1: tiles past the last whole wave are split along K (ws: partial tiles)
   int deep;                   // 1: widths 144/192 with a fifth operand stage (one epilogue buffer)
+  int pair;                   // 1: CTA-pair kernel, 256 x bn tiles (bn 128, 192 or 256; splits only)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;

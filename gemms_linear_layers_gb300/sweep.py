@@ -6,7 +6,8 @@ kernel designs for the list of sizes training uses and keep the winners in a
 file the library reads; section "What got in the way": the winners must be
 looked up with the same key they were stored under, and the speed-up has to
 be confirmed through the normal call path).  Here a design is (tile width,
-split count, raster order) of the tensor-core kernel; each candidate is timed
+single CTA or CTA pair, split count or schedule, raster order) of the
+tensor-core kernel; each candidate is timed
 through the public entry point with a one-line table that forces it, and the
 fastest per shape is written with the same key the library looks up.
 
@@ -29,6 +30,7 @@ from . import inputs, workloads
 HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "tables", "gb300.txt")
 BNS = (64, 128, 144, 192, 256)
+PAIR_BNS = (128, 192, 256)
 SPLITS = (1, 2, 3, 4, 6, 8, 12, 16)
 
 
@@ -129,6 +131,20 @@ def candidates(M, N, K, batch, sms):
         if bn % 64 == 0 and tiles * kb >= sms and tiles * 4 >= sms:
             for raster in ("m", "n"):
                 yield bn, "sk", raster
+    # CTA pairs: 256-row tiles on two SMs, data-parallel or split
+    if M > 128:
+        for bn in PAIR_BNS:
+            tiles = batch * -(-M // 256) * -(-N // bn)
+            for s in SPLITS:
+                if s > kb:
+                    break
+                kps = -(-kb // s)
+                if -(-kb // kps) != s:
+                    continue
+                if s > 1 and tiles * s > 4 * sms:
+                    continue
+                for raster in ("m", "n"):
+                    yield f"{bn}p", s, raster
 
 
 def main(argv=None):

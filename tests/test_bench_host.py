@@ -20,6 +20,10 @@ def test_kernel_key():
     assert k("wgrad tc tn M=2304 N=2304 K=2048 batch=1 bn=256 sk grid=152 raster=n table=hit ok") == "tc tn bn=256 sk"
     assert k("wgrad tc tn M=2304 N=2304 K=2048 batch=1 bn=256 splits=1 tail=10x4 raster=n table=hit ok") == \
         "tc tn bn=256 +tail"
+    assert k("fwd tc nt M=2048 N=49152 K=576 batch=1 bn=256 pair splits=1 raster=m table=hit ok") == \
+        "tc nt bn=256 pair"
+    assert k("dgrad tc nn M=2048 N=576 K=49152 batch=1 bn=192 pair splits=3 raster=n table=hit ok") == \
+        "tc nn bn=192 pair +reduce"
     assert k("wgrad simt tn M=200 N=300 K=520 batch=1 ok") == "simt tn"
 
 

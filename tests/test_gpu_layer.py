@@ -422,6 +422,96 @@ def test_tail_split_schedule(case, dtype, out_kind):
         assert_close(gather(outs[0], co), C, S, f"{op} tail split sampled [{call}]", out_dtype)
 
 
+# CTA pairs: 256-row tiles computed by two CTAs of a cluster (one MMA of
+# M = 256 across both SMs).  Ragged M, N and K; K-major and MN-major B halves
+# of 64, 96 and 128 rows/columns; the 4-D chunked operand views (widths that
+# are multiples of 64) and the per-chunk boxes (other widths); split partials.
+PAIR_CASES = [("fwd", 300, 200, 520, 128, 1), ("dgrad", 300, 520, 200, 192, 1),
+              ("wgrad", 520, 296, 200, 256, 1), ("fwd", 1000, 1000, 1000, 256, 2),
+              ("wgrad", 1024, 512, 768, 256, 1), ("dgrad", 1024, 768, 512, 128, 3),
+              ("wgrad", 1024, 576, 576, 192, 1), ("fwd", 512, 640, 384, 192, 1)]
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_cta_pair_schedule(case, dtype, out_kind):
+    op, T, d_in, d_out, bn, splits = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    dname = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+    line = f"{lay} {dname[dtype]} {dname[out_dtype]} {M} {N} {K} 1 {bn}p {splits}"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="pair")
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+    outs = _with_table(line, lambda: [run(op, Xc, Wc, dYc, out_dtype) for _ in range(2)])
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert f"bn={bn} pair" in call and "table=hit" in call, call
+    assert torch.equal(outs[0], outs[1]), "pair schedule not deterministic"
+    C, S = ref(op, X, W, dY)
+    assert_close(outs[0], C, S, f"{op} pair [{call}]", out_dtype)
+
+
+def test_cta_pair_attention_batch():
+    """Batched scores Q K^T (four heads) on CTA pairs."""
+    h, s, d = 4, 512, 64
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="pair")
+    line = f"nt bf16 bf16 {s} {s} {d} {h} 256p 1"
+    got = _with_table(line, lambda: tg.tg_bmm_attn("qk", t["Q"].cuda(), t["K"].cuda()))
+    call = tg.tg_last_call()
+    assert " pair" in call, call
+    C, S = oracle.bmm_attn("qk", t["Q"], t["K"])
+    assert_close(got, C, S, f"attn qk pair [{call}]", torch.bfloat16)
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_cta_pair_full_size_head(op):
+    """The vocabulary head of the 135M-class model at 2,048 tokens on CTA
+    pairs, sampled against the oracle, and replayed from a CUDA graph."""
+    T, d_in, d_out = 2048, 576, 49152
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    bn, splits = {"fwd": (256, 1), "dgrad": (192, 2), "wgrad": (192, 1)}[op]
+    line = f"{lay} bf16 bf16 {M} {N} {K} 1 {bn}p {splits}"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, torch.bfloat16, tag="pairhead")
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+
+    def go():
+        first = run(op, Xc, Wc, dYc, torch.bfloat16)
+        call = tg.tg_last_call()
+        out = torch.empty_like(first)
+        n = tg.tg_workspace_size({"fwd": tg.TG_OP_GEMM_FWD, "dgrad": tg.TG_OP_GEMM_DGRAD,
+                                  "wgrad": tg.TG_OP_GEMM_WGRAD}[op], T, d_out, d_in, 0,
+                                 torch.bfloat16, torch.bfloat16)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if op == "fwd":
+                tg.tg_gemm_fwd(Xc, Wc, Y=out, ws=ws)
+            elif op == "dgrad":
+                tg.tg_gemm_dgrad(dYc, Wc, dX=out, ws=ws)
+            else:
+                tg.tg_gemm_wgrad(dYc, Xc, dW=out, ws=ws)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        return first, out, call
+
+    first, replayed, call = _with_table(line, go)
+    assert tg.tg_stream_status() == 0
+    assert f"bn={bn} pair" in call, call
+    assert torch.equal(first, replayed), "graph replay differs from the direct call"
+    co = sample_coords(M, N, rows=32, cols=32, rand=4096, seed=256)
+    C, S = ref(op, X, W, dY, sample=co)
+    assert_close(gather(first, co), C, S, f"{op} head pair [{call}]", torch.bfloat16)
+
+
 def test_tail_split_attention_batch():
     h, s, d = 36, 1024, 64
     t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="tail")
