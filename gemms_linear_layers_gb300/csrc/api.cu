@@ -206,7 +206,7 @@ static tg_status load_table_file(const char* path) {
       if (!(bn == 64 || bn == 128 || bn == 144 || bn == 192 || bn == 256) || splits < 0 || splits > 64)
         return TG_ERR_TABLE;
       if (bn % 64 != 0 && (splits == 0 || tail > 0)) return TG_ERR_TABLE;  // partial tiles: 64-column multiples
-      if (pair && (bn == 64 || bn == 144 || splits == 0 || tail > 0)) return TG_ERR_TABLE;  // pairs: data-parallel / split
+      if (pair && (bn == 64 || bn == 144 || tail > 0)) return TG_ERR_TABLE;  // pairs: split counts or stream-K
       t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail, pair};
     }
   }
@@ -352,6 +352,25 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       best.pair = false;
     }
   }
+  // stream-K on CTA pairs (256 x 256 tiles, ranges per pair)
+  if (M > 128) {
+    const int bn = 256, pairs = sms / 2;
+    const int64_t tiles = batch * cdiv(M, 256) * cdiv(N, bn);
+    const int64_t iters = tiles * kb;
+    if (pairs > 0 && iters >= pairs && tiles * 4 >= pairs) {
+      const double kb_cyc = 4.0 * fmax(125.0, 0.525 * bn);
+      const double per_pair = static_cast<double>(cdiv(iters, pairs));
+      const double t = per_pair * kb_cyc + 600.0 * cdiv(tiles, pairs) + 2.0 * 128.0 * bn * 4 / 24.0;
+      if (t < best_t * 0.95) {
+        best_t = t;
+        best.bn = bn;
+        best.splits = 1;
+        best.sk = true;
+        best.tail = 0;
+        best.pair = true;
+      }
+    }
+  }
   return best;
 }
 
@@ -383,7 +402,13 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
   return p;
 }
 
+// CTAs of a stream-K launch (an upper bound for pairs, whose count may be
+// capped further by how many clusters fit at once)
 static int sk_grid(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  if (p.pair) {
+    const int64_t iters = batch * cdiv(M, 256) * cdiv(N, p.bn) * cdiv(K, 64);
+    return 2 * static_cast<int>(iters < sms / 2 ? iters : sms / 2);
+  }
   const int64_t iters = batch * cdiv(M, 128) * cdiv(N, p.bn) * cdiv(K, 64);
   return static_cast<int>(iters < sms ? iters : sms);
 }

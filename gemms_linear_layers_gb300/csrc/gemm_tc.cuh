@@ -214,6 +214,105 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
   return v;
 }
+// ---- stream-K epilogue steps, shared by the single-CTA and CTA-pair kernels.
+// The CTAs holding later pieces of a tile are first, first + step, ..., last
+// (step 2 for pairs: the same rank in each later pair).
+
+// Owner: wait until those CTAs have published their partial of this warp's
+// 32 rows (quadrant q), then stage their sum, in CTA order, in tensor memory
+// at t_pre (the idle accumulator).  False when a wait ran out.
+template <int BN>
+__device__ __forceinline__ bool sk_gather_parts(const TcArgs& args, int first, int last, int step, int q, int lane,
+                                                uint32_t t_pre, volatile int* abort_flag) {
+  // one lane polls, with back-off: flags sit on their own 128-byte lines
+  // and a storm of polls would crowd the L2 slices the TMA loads need
+  int ok = 1;
+  if (lane == 0) {
+    for (int cc = first; cc <= last && ok; cc += step) {
+      const unsigned long long* fl = args.sk_flags + sk_flag_index(cc, q);
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u64(fl) != args.sk_epoch) {
+        __nanosleep(128);
+        if (*abort_flag || globaltimer_ns() - t0 > args.timeout_ns) {
+          if (!*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(args.status, TG_DEVSTAT_TIMEOUT | 5u);
+          }
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  const bool have = __shfl_sync(0xffffffffu, ok, 0) != 0;
+  __syncwarp();  // lane 0's acquire orders the other lanes' reads below
+  if (!have) return false;
+#pragma unroll 1
+  for (int blk = 0; blk < BN / 32; ++blk) {
+    uint32_t sp[32];
+    for (int cc = first; cc <= last; cc += step) {
+      const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, blk, 0, lane);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 v = ld_cg_f4(src + 4 * 32 * j);
+        uint32_t* d = sp + 4 * j;
+        if (cc == first) {
+          d[0] = __float_as_uint(v.x);
+          d[1] = __float_as_uint(v.y);
+          d[2] = __float_as_uint(v.z);
+          d[3] = __float_as_uint(v.w);
+        } else {
+          d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
+          d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
+          d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
+          d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+        }
+      }
+    }
+    tmem_st_32x32b_x32(t_pre + blk * 32, sp);
+  }
+  tmem_st_wait();
+  return true;
+}
+
+// Contributor: this warp's 32 rows of the accumulator at t_row to partial
+// slot `cta`, calling release() once the accumulator has been read (it hands
+// the accumulator back), then publish the slot's quadrant flag.  Private
+// layout: for each 32-column block and each 4-column group, the 32 lanes'
+// float4s are adjacent, so every warp store writes 512 contiguous bytes.
+template <int BN, typename Release>
+__device__ __forceinline__ void sk_put_part(const TcArgs& args, int cta, int q, int lane, uint32_t t_row,
+                                            Release release) {
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + ch * 32, r);
+    tmem_ld_wait();
+    if (ch == BN / 32 - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release();
+    }
+    float4* dst = reinterpret_cast<float4*>(args.sk_part) + sk_part_index<BN>(cta, q, ch, 0, lane);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+  }
+  // each warp publishes its own 32 rows: no barrier between the epilogue warps
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release_u64(args.sk_flags + sk_flag_index(cta, q), args.sk_epoch);
+}
+
+// Owner, after its tile is written: clear the flags it consumed, so flags
+// are zero between launches (a replayed CUDA graph reuses the same value)
+__device__ __forceinline__ void sk_clear_flags(const TcArgs& args, int first, int last, int step, int q, int lane) {
+  __syncwarp();
+  if (lane == 0)
+    for (int cc = first; cc <= last; cc += step) st_release_u64(args.sk_flags + sk_flag_index(cc, q), 0ull);
+}
+
 template <bool A_MN, bool B_MN, int BN, bool OUT16, bool DEEP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -410,57 +509,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t t_pre = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>((acc ^ 1) * Cfg::ACC_STRIDE);
       if (BN % 64 == 0 && fixup) {
-        // one lane polls, with back-off: flags sit on their own 128-byte lines
-        // and a storm of polls would crowd the L2 slices the TMA loads need
-        int ok = 1;
         if (warp == 2 && lane == 0) TG_EVENT(4);
-        if (lane == 0) {
-          for (int cc = blockIdx.x + 1; cc <= c.c_last && ok; ++cc) {
-            const unsigned long long* fl = args.sk_flags + sk_flag_index(cc, q);
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_u64(fl) != args.sk_epoch) {
-              __nanosleep(128);
-              if (*abort_flag || globaltimer_ns() - t0 > tmo) {
-                if (!*abort_flag) {
-                  *abort_flag = 1;
-                  atomicOr(args.status, TG_DEVSTAT_TIMEOUT | 5u);
-                }
-                ok = 0;
-                break;
-              }
-            }
-          }
-        }
-        have_parts = __shfl_sync(0xffffffffu, ok, 0) != 0;
-        __syncwarp();  // lane 0's acquire orders the other lanes' reads below
+        have_parts = sk_gather_parts<BN>(args, blockIdx.x + 1, c.c_last, 1, q, lane, t_pre, abort_flag);
         if (warp == 2 && lane == 0) TG_EVENT(5);
-        if (have_parts) {
-#pragma unroll 1
-          for (int blk = 0; blk < BN / 32; ++blk) {
-            uint32_t sp[32];
-            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) {
-              const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, blk, 0, lane);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 v = ld_cg_f4(src + 4 * 32 * j);
-                uint32_t* d = sp + 4 * j;
-                if (cc == static_cast<int>(blockIdx.x) + 1) {
-                  d[0] = __float_as_uint(v.x);
-                  d[1] = __float_as_uint(v.y);
-                  d[2] = __float_as_uint(v.z);
-                  d[3] = __float_as_uint(v.w);
-                } else {
-                  d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
-                  d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
-                  d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
-                  d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
-                }
-              }
-            }
-            tmem_st_32x32b_x32(t_pre + blk * 32, sp);
-          }
-          tmem_st_wait();
-        }
       }
       if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
       tc_fence_after();
@@ -468,30 +519,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                              static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
       const int row = q * 32 + lane;  // row of the tile this thread holds
       if (!c.owner) {
-        // ---- stream-K contributor: FP32 partial tile to this CTA's slot, then publish.
-        // Private layout: for each 32-column block and each 4-column group, the
-        // 32 lanes' float4s are adjacent, so every warp store writes 512
-        // contiguous bytes.
-#pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + ch * 32, r);
-          tmem_ld_wait();
-          if (ch == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-          }
-          float4* dst = reinterpret_cast<float4*>(args.sk_part) + sk_part_index<BN>(blockIdx.x, q, ch, 0, lane);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j * 32] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
-        // each warp publishes its own 32 rows: no barrier between the epilogue warps
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_u64(args.sk_flags + sk_flag_index(blockIdx.x, q), args.sk_epoch);
+        // ---- stream-K contributor: FP32 partial tile to this CTA's slot, then publish
+        sk_put_part<BN>(args, blockIdx.x, q, lane, t_row, [&] { mbar_arrive(smem_u32(&tempty[acc])); });
         if (warp == 2 && lane == 0) TG_EVENT(3);
       } else if (BN % 64 == 0 && c.part) {
         // ---- tail split piece: FP32 partial tile [128][BN] to slot pz
@@ -620,14 +649,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           ++nstore;
         }
-        if (fixup && have_parts) {
-          // this warp has read every later piece of its rows: clear their flags,
-          // so flags are zero between launches (a replayed CUDA graph reuses the
-          // same flag value every time)
-          __syncwarp();
-          if (lane == 0)
-            for (int cc = blockIdx.x + 1; cc <= c.c_last; ++cc) st_release_u64(args.sk_flags + sk_flag_index(cc, q), 0ull);
-        }
+        if (fixup && have_parts) sk_clear_flags(args, blockIdx.x + 1, c.c_last, 1, q, lane);
       }
       if (++acc == 2) {
         acc = 0;

@@ -51,12 +51,46 @@ struct Tc2Cfg {
 
 struct Unit2 {
   int b, m0, n0, zc, kb0, kb1;
+  int owner;   // this pair writes the tile (stream-K: it holds the tile's first K block)
+  int c_last;  // stream-K owner: last pair holding a piece of the tile (> this pair: gather partials)
 };
 
-__device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, int& u, Unit2& c) {
-  if (u >= a.units) return false;
-  const int split = u % a.splits;
-  const int t = u / a.splits;
+// The sequence of units one pair works on (both CTAs and every role walk
+// the same one): (tile, split) units dealt round-robin to the pairs, or, for
+// stream-K, an equal contiguous range of the (tile x K block) iterations.
+struct PairIter {
+  long long pos, end;
+};
+
+__device__ __forceinline__ int pair_count() { return static_cast<int>(gridDim.x >> 1); }
+__device__ __forceinline__ int pair_index() { return static_cast<int>(blockIdx.x >> 1); }
+
+__device__ __forceinline__ long long pair_sk_start(long long p, const TcArgs& a) {
+  return p * a.sk_iters / pair_count();
+}
+
+// the pair whose stream-K range holds iteration i
+__device__ __forceinline__ int pair_sk_of(long long i, const TcArgs& a) {
+  const int np = pair_count();
+  int p = static_cast<int>(i * np / a.sk_iters);
+  while (p + 1 < np && pair_sk_start(p + 1, a) <= i) ++p;
+  while (p > 0 && pair_sk_start(p, a) > i) --p;
+  return p;
+}
+
+__device__ __forceinline__ PairIter pair_begin(const TcArgs& a) {
+  PairIter it;
+  if (a.sk) {
+    it.pos = pair_sk_start(pair_index(), a);
+    it.end = pair_sk_start(pair_index() + 1, a);
+  } else {
+    it.pos = pair_index();
+    it.end = a.units;
+  }
+  return it;
+}
+
+__device__ __forceinline__ void pair_tile(int t, const TcArgs& a, int bn, Unit2& c) {
   const int tiles = a.m_tiles * a.n_tiles;
   c.b = t / tiles;
   const int r = t - c.b * tiles;
@@ -67,10 +101,33 @@ __device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, int& u, Unit2
     c.m0 = (r % a.m_tiles) * TC2_BM;
     c.n0 = (r / a.m_tiles) * bn;
   }
-  c.zc = c.b * a.splits + split;
-  c.kb0 = split * a.kps;
-  c.kb1 = min(a.kb_total, c.kb0 + a.kps);
-  u += gridDim.x >> 1;
+}
+
+__device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, PairIter& it, Unit2& c) {
+  if (it.pos >= it.end) return false;
+  if (!a.sk) {
+    const int u = static_cast<int>(it.pos);
+    const int split = u % a.splits;
+    pair_tile(u / a.splits, a, bn, c);
+    c.zc = c.b * a.splits + split;
+    c.kb0 = split * a.kps;
+    c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+    c.owner = 1;
+    c.c_last = -1;
+    it.pos += pair_count();
+    return true;
+  }
+  const long long kb = a.kb_total;
+  const int t = static_cast<int>(it.pos / kb);
+  const long long kt0 = static_cast<long long>(t) * kb;
+  const long long seg_end = min(it.end, kt0 + kb);
+  pair_tile(t, a, bn, c);
+  c.zc = c.b;
+  c.kb0 = static_cast<int>(it.pos - kt0);
+  c.kb1 = static_cast<int>(seg_end - kt0);
+  c.owner = it.pos == kt0;
+  c.c_last = (c.owner && seg_end < kt0 + kb) ? pair_sk_of(kt0 + kb - 1, a) : -1;
+  it.pos = seg_end;
   return true;
 }
 
@@ -140,11 +197,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
       for (int s = 0; s < S; ++s) issued[s] = -1;
       bool ok = true;
-      int u = static_cast<int>(blockIdx.x >> 1);
+      PairIter it = pair_begin(args);
       Unit2 c;
-      const int a_row = static_cast<int>(rank) * TC_BM;      // this CTA's rows of the pair tile
-      const int b_off = static_cast<int>(rank) * Cfg::BH;    // this CTA's half of B
-      while (ok && pair_next(args, BN, u, c)) {
+      const int a_row = static_cast<int>(rank) * TC_BM;    // this CTA's rows of the pair tile
+      const int b_off = static_cast<int>(rank) * Cfg::BH;  // this CTA's half of B
+      while (ok && pair_next(args, BN, it, c)) {
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
           if (!mbar_wait<true>(smem_u32(&empty[stage]), phase ^ 1u, tmo, abort_flag, args.status, 1)) {
             ok = false;
@@ -215,9 +272,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      int u = static_cast<int>(blockIdx.x >> 1);
+      PairIter it = pair_begin(args);
       Unit2 c;
-      while (ok && pair_next(args, BN, u, c)) {
+      while (ok && pair_next(args, BN, it, c)) {
         if (!mbar_wait<true>(smem_u32(&tempty[acc]), acc_phase ^ 1u, tmo, abort_flag, args.status, 2)) {
           ok = false;
           break;
@@ -266,16 +323,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr int NCH = BN / CW;
     static_assert(BN % CW == 0, "pair tile width and output width");
     const uint32_t tempty_cl = mapa_shared(smem_u32(&tempty[0]), 0);
+    const int pair = pair_index();
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
-    int u = static_cast<int>(blockIdx.x >> 1);
+    PairIter it = pair_begin(args);
     Unit2 c;
-    while (pair_next(args, BN, u, c)) {
+    while (pair_next(args, BN, it, c)) {
+      // A stream-K owner whose tile later pairs finish: this is the pair's
+      // last unit, so the other accumulator is idle.  While this unit's MMAs
+      // run, gather the later pieces of this warp's 32 rows (from the CTA of
+      // the same rank in each later pair) and stage their sum there.
+      const bool fixup = c.owner && c.c_last > pair;
+      const int first = 2 * (pair + 1) + static_cast<int>(rank);
+      const int last = 2 * c.c_last + static_cast<int>(rank);
+      bool have_parts = true;
+      const uint32_t t_pre = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>((acc ^ 1) * Cfg::ACC_STRIDE);
+      if (fixup) have_parts = sk_gather_parts<BN>(args, first, last, 2, q, lane, t_pre, abort_flag);
       if (!mbar_wait<true>(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
+      if (!c.owner) {
+        // stream-K contributor: FP32 partial of this CTA's 128 rows to its slot
+        const uint32_t te = tempty_cl + static_cast<uint32_t>(acc * 8);
+        sk_put_part<BN>(args, blockIdx.x, q, lane, t_row, [&] { mbar_arrive_cluster(te); });
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       const int row0 = c.m0 + static_cast<int>(rank) * TC_BM + q * 32;
 #pragma unroll 1
       for (int ch = 0; ch < NCH; ++ch) {
@@ -288,6 +367,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty_cl + static_cast<uint32_t>(acc * 8));
+        }
+        if (fixup && have_parts) {
+          // add the later pairs' pieces (their sum, staged in the idle accumulator)
+#pragma unroll
+          for (int sub = 0; sub < CW / 32; ++sub) {
+            uint32_t sp[32];
+            tmem_ld_32x32b_x32(t_pre + ch * CW + sub * 32, sp);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r[32 * sub + j] = __float_as_uint(__uint_as_float(r[32 * sub + j]) + __uint_as_float(sp[j]));
+          }
         }
         uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
         if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
@@ -323,6 +414,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         ++nstore;
       }
+      if (fixup && have_parts) sk_clear_flags(args, first, last, 2, q, lane);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

@@ -125,8 +125,9 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM, persistent over
-// 256 x BN tiles (x splits).  The grid is the number of pairs that fit on the
-// device at once (at most half the SMs), times two.
+// 256 x BN tiles (x splits, or stream-K ranges).  The grid is the number of
+// pairs that fit on the device at once (at most half the SMs), times two:
+// stream-K needs every pair resident.
 template <bool A_MN, bool B_MN, int BN, bool OUT16>
 static cudaError_t tc2_launch_one(const TcGemm& g) {
   using Cfg = Tc2Cfg<BN, B_MN>;
@@ -189,7 +190,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
     ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, Cfg::BH, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const bool split_parts = g.splits > 1;
+  const bool split_parts = !g.sk && g.splits > 1;
   const int ck = split_parts ? EK_F32 : g.out_kind;
   const uint64_t esz = elem_bytes(ck);
   void* cptr = split_parts ? g.ws : g.C;
@@ -201,7 +202,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.m_tiles = static_cast<int>((M + TC2_BM - 1) / TC2_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
   a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
-  a.splits = g.splits;
+  a.splits = g.sk ? 1 : g.splits;
   a.kps = (a.kb_total + a.splits - 1) / a.splits;
   a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * a.splits;
   a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC2_BM, BN);
@@ -212,10 +213,20 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.tail_splits = 1;
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
+  a.sk = g.sk;
+  a.sk_iters = static_cast<long long>(a.units) * a.kb_total;
+  a.sk_epoch = g.sk_epoch;
   int pairs = g.grid / 2;
   if (pairs > max_pairs[dev]) pairs = max_pairs[dev];
-  if (pairs > a.units) pairs = a.units;
+  const long long work = g.sk ? a.sk_iters : a.units;  // every pair gets at least one unit / iteration
+  if (pairs > work) pairs = static_cast<int>(work);
   if (pairs < 1) pairs = 1;
+  if (g.sk) {
+    // stream-K slots: one FP32 partial tile per CTA, then the flags
+    a.sk_part = static_cast<float*>(g.ws);
+    a.sk_flags = reinterpret_cast<unsigned long long*>(static_cast<char*>(g.ws) +
+                                                       static_cast<size_t>(2 * pairs) * TC_BM * BN * 4);
+  }
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
@@ -223,7 +234,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
 
 template <bool A_MN, bool B_MN>
 static cudaError_t tc2_launch_layout(const TcGemm& g) {
-  const bool out16 = g.splits == 1 && g.out_kind != EK_F32;
+  const bool out16 = (g.sk || g.splits == 1) && g.out_kind != EK_F32;
   switch (g.bn) {
     case 128: return out16 ? tc2_launch_one<A_MN, B_MN, 128, true>(g) : tc2_launch_one<A_MN, B_MN, 128, false>(g);
     case 192: return out16 ? tc2_launch_one<A_MN, B_MN, 192, true>(g) : tc2_launch_one<A_MN, B_MN, 192, false>(g);

@@ -145,6 +145,9 @@ def candidates(M, N, K, batch, sms):
                     continue
                 for raster in ("m", "n"):
                     yield f"{bn}p", s, raster
+            if tiles * kb >= sms // 2 and tiles * 4 >= sms // 2:
+                for raster in ("m", "n"):
+                    yield f"{bn}p", "sk", raster
 
 
 def main(argv=None):

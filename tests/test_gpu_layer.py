@@ -244,6 +244,13 @@ SK_CASES = [
     ("dgrad", 2048, 576, 49152, 192),
     ("fwd", 1000, 520, 1000, 128),
     ("fwd", 2048, 576, 1536, 256),
+    # CTA pairs ("p"): a pair's partials come from the CTA of the same rank
+    # in each later pair; ragged edges; one partial per pair and several
+    ("wgrad", 4096, 2304, 2304, "256p"),
+    ("wgrad", 2048, 2304, 2304, "256p"),
+    ("dgrad", 2048, 576, 49152, "192p"),
+    ("fwd", 1000, 520, 1000, "128p"),
+    ("wgrad", 16384, 384, 256, "128p"),
 ]
 
 
@@ -291,11 +298,12 @@ def test_stream_k_schedule(case, out_kind):
         assert_close(gather(outs[0], co), C, S, f"{op} stream-K sampled [{call}]", out_dtype)
 
 
-def test_stream_k_small_integers_exact():
+@pytest.mark.parametrize("bn", ["128", "128p"])
+def test_stream_k_small_integers_exact(bn):
     T, d_in, d_out = 8192, 384, 256
     X = inputs.small_int((T, d_in), -2, 2, torch.float16, 8)
     dY = inputs.small_int((T, d_out), -2, 2, torch.float16, 9)
-    line = f"tn f16 f32 {d_out} {d_in} {T} 1 128 sk"
+    line = f"tn f16 f32 {d_out} {d_in} {T} 1 {bn} sk"
     got = _with_table(line, lambda: tg.tg_gemm_wgrad(dY.cuda(), X.cuda(), out_dtype=torch.float32))
     C, _ = oracle.gemm_wgrad(dY, X)
     assert np.array_equal(got.cpu().double().numpy(), C)
@@ -312,11 +320,12 @@ def test_stream_k_attention_batch():
     assert_close(gather(got, co), C, S, f"attn pt_do stream-K [{call}]", torch.bfloat16)
 
 
-def test_stream_k_in_replayed_cuda_graph():
+@pytest.mark.parametrize("bn", ["256", "256p"])
+def test_stream_k_in_replayed_cuda_graph(bn):
     """A captured stream-K launch reuses one flag value on every replay: each
     replay must still wait for this replay's partial tiles."""
     T, d_in, d_out = 2048, 2304, 2304
-    line = f"tn bf16 bf16 {d_out} {d_in} {T} 1 256 sk"
+    line = f"tn bf16 bf16 {d_out} {d_in} {T} 1 {bn} sk"
     X, W, dY = (t.cuda() for t in inputs.layer_inputs(T, d_in, d_out, torch.bfloat16, tag="skg"))
     dW = torch.empty(d_out, d_in, dtype=torch.bfloat16, device="cuda")
     n = tg.tg_workspace_size(tg.TG_OP_GEMM_WGRAD, T, d_out, d_in, 0, torch.bfloat16, torch.bfloat16)
