@@ -206,7 +206,7 @@ static tg_status load_table_file(const char* path) {
       if (!(bn == 64 || bn == 128 || bn == 144 || bn == 192 || bn == 256) || splits < 0 || splits > 64)
         return TG_ERR_TABLE;
       if (bn % 64 != 0 && (splits == 0 || tail > 0)) return TG_ERR_TABLE;  // partial tiles: 64-column multiples
-      if (pair && (bn == 64 || bn == 144 || tail > 0)) return TG_ERR_TABLE;  // pairs: split counts or stream-K
+      if (pair && (bn == 64 || bn == 144)) return TG_ERR_TABLE;  // pairs: widths 128, 192, 256
       t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail, pair};
     }
   }
@@ -413,9 +413,16 @@ static int sk_grid(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch
   return static_cast<int>(iters < sms ? iters : sms);
 }
 
+// Tail-split geometry of a plan: a wave is every SM (single CTA) or every
+// pair of SMs (256-row tiles)
+static TailGeo plan_tail_geo(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  return tail_geo(M, N, K, batch, p.bn, p.pair ? sms / 2 : sms, p.sk || p.splits > 1 ? 1 : p.tail, p.raster_n,
+                  p.pair ? 256 : 128);
+}
+
 static size_t plan_ws_bytes(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
   if (p.sk) return sk_ws_bytes(sk_grid(p, M, N, K, batch, sms), p.bn);
-  if (p.tail > 1 && p.splits <= 1) return tail_ws_bytes(tail_geo(M, N, K, batch, p.bn, sms, p.tail, p.raster_n));
+  if (p.tail > 1 && p.splits <= 1) return tail_ws_bytes(plan_tail_geo(p, M, N, K, batch, sms));
   return p.splits > 1 ? static_cast<size_t>(p.splits) * batch * M * N * 4 : 0;
 }
 
@@ -525,8 +532,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     if (e == cudaSuccess && !p.sk && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
                                g.stream);
-    const TailGeo tgeo = tail_geo(g.M, g.N, g.K, g.batch, p.bn, ctx->sms, p.sk || p.splits > 1 ? 1 : p.tail,
-                                  p.raster_n);
+    const TailGeo tgeo = plan_tail_geo(p, g.M, g.N, g.K, g.batch, ctx->sms);
     char tail[48] = "";
     if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
     snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s %s",

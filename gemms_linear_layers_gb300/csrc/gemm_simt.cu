@@ -30,29 +30,56 @@ __device__ __forceinline__ void store_from_float(void* p, int kind, int64_t i, f
 
 // ------------------------------------------------------------- tail split
 // C tile dp_tiles + t = sum over s ascending of partial slot t * splits + s
-// (each a dense [128][bn] FP32 tile); rows past M and columns past N skipped.
+// (each a dense [bm][bn] FP32 tile); rows past M and columns past N skipped.
+// One thread per 4 adjacent columns: its loads of every split are issued
+// together (unrolled), so the reduction costs a few L2 round trips rather than
+// one per split.  bn and N are multiples of 4, so 4 columns are all inside or
+// all past N.
 __global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int out_kind, TailGeo g) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
   int b, m0, n0;
-  tile_origin(g.dp_tiles + t, g.m_tiles, g.n_tiles, g.raster_n, g.bn, &b, &m0, &n0);
-  const int per = 128 * g.bn;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < per; e += gridDim.x * blockDim.x) {
-    const int r = e / g.bn, col = e - r * g.bn;
+  tile_origin(g.dp_tiles + t, g.m_tiles, g.n_tiles, g.raster_n, g.bn, &b, &m0, &n0, g.bm);
+  const int per4 = g.bm * g.bn / 4;
+  const float4* tile = reinterpret_cast<const float4*>(P) + static_cast<size_t>(t) * g.splits * per4;
+  for (int e4 = blockIdx.x * blockDim.x + threadIdx.x; e4 < per4; e4 += gridDim.x * blockDim.x) {
+    const int r = (4 * e4) / g.bn, col = 4 * e4 - r * g.bn;
     const int64_t m = m0 + r, n = n0 + col;
     if (m >= g.M || n >= g.N) continue;
-    const float* src = P + static_cast<size_t>(t) * g.splits * per + e;
-    float v = src[0];
-    for (int s = 1; s < g.splits; ++s) v += src[static_cast<size_t>(s) * per];
-    store_from_float(C, out_kind, (b * g.M + m) * g.N + n, v);
+    const float4* src = tile + e4;
+    float4 v = src[0];
+#pragma unroll 8
+    for (int s = 1; s < g.splits; ++s) {
+      const float4 w = src[static_cast<size_t>(s) * per4];
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    const int64_t o = (b * g.M + m) * g.N + n;
+    if (out_kind == EK_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(C) + o) = v;
+    } else if (out_kind == EK_BF16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + o) = pk;
+    } else {
+      __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__half*>(C) + o) = pk;
+    }
   }
 }
 
 cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream) {
   if (t.tail_tiles == 0) return cudaSuccess;
-  const int per = 128 * t.bn;
-  return launch_k(tail_reduce_kernel, dim3((per + 1023) / 1024, t.tail_tiles), dim3(256), 0, stream, P, C, out_kind,
+  const int per4 = t.bm * t.bn / 4;
+  return launch_k(tail_reduce_kernel, dim3((per4 + 255) / 256, t.tail_tiles), dim3(256), 0, stream, P, C, out_kind,
                   t);
 }
 
@@ -69,6 +96,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restr
     const int64_t i4 = v - b * n4;
     const float4* src = reinterpret_cast<const float4*>(ws) + (b * splits) * n4 + i4;
     float4 s = src[0];
+#pragma unroll 8
     for (int64_t k = 1; k < splits; ++k) {
       const float4 t = src[k * n4];
       s.x += t.x;

@@ -247,29 +247,39 @@ __device__ __forceinline__ bool sk_gather_parts(const TcArgs& args, int first, i
   const bool have = __shfl_sync(0xffffffffu, ok, 0) != 0;
   __syncwarp();  // lane 0's acquire orders the other lanes' reads below
   if (!have) return false;
+  // G 32-column blocks per round: their loads are all in flight together, so
+  // the gather costs BN / (32 G) L2 round trips instead of BN / 32 (it runs
+  // after the last piece is published, on the tile's critical path); more
+  // than two blocks per round spill registers
+  constexpr int NB = BN / 32;
+  constexpr int G = NB % 2 == 0 ? 2 : 1;
 #pragma unroll 1
-  for (int blk = 0; blk < BN / 32; ++blk) {
-    uint32_t sp[32];
+  for (int b0 = 0; b0 < NB; b0 += G) {
+    uint32_t sp[G * 32];
     for (int cc = first; cc <= last; cc += step) {
-      const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, blk, 0, lane);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 v = ld_cg_f4(src + 4 * 32 * j);
-        uint32_t* d = sp + 4 * j;
-        if (cc == first) {
-          d[0] = __float_as_uint(v.x);
-          d[1] = __float_as_uint(v.y);
-          d[2] = __float_as_uint(v.z);
-          d[3] = __float_as_uint(v.w);
-        } else {
-          d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
-          d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
-          d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
-          d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+      for (int g = 0; g < G; ++g) {
+        const float* src = args.sk_part + 4 * sk_part_index<BN>(cc, q, b0 + g, 0, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 v = ld_cg_f4(src + 4 * 32 * j);
+          uint32_t* d = sp + 32 * g + 4 * j;
+          if (cc == first) {
+            d[0] = __float_as_uint(v.x);
+            d[1] = __float_as_uint(v.y);
+            d[2] = __float_as_uint(v.z);
+            d[3] = __float_as_uint(v.w);
+          } else {
+            d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
+            d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
+            d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
+            d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+          }
         }
       }
     }
-    tmem_st_32x32b_x32(t_pre + blk * 32, sp);
+#pragma unroll
+    for (int g = 0; g < G; ++g) tmem_st_32x32b_x32(t_pre + (b0 + g) * 32, sp + 32 * g);
   }
   tmem_st_wait();
   return true;

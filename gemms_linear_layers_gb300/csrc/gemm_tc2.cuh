@@ -19,8 +19,10 @@
 // 16 KB of A and BN/2 x 128 bytes of B per 128 x BN x 64 of MMA work, where
 // the single-CTA kernel moves all BN rows of B), and the freed shared
 // memory holds a deeper ring (6 stages at BN = 192/256, 8 at 128).
-// Schedule: data-parallel over (tile, split) units, FP32 split partials to
-// the workspace as in the single-CTA kernel.  Every wait is bounded; an
+// Schedules as in the single-CTA kernel: data-parallel over (tile, split)
+// units with FP32 split partials; the tail split (whole tiles for the full
+// waves, the last wave's tiles cut along K into FP32 partials that a second
+// kernel adds); stream-K over pairs.  Every wait is bounded; an
 // aborting CTA waits at the final cluster barrier, so neither CTA of a pair
 // leaves while the other may still touch its shared or tensor memory.
 #pragma once
@@ -53,6 +55,8 @@ struct Unit2 {
   int b, m0, n0, zc, kb0, kb1;
   int owner;   // this pair writes the tile (stream-K: it holds the tile's first K block)
   int c_last;  // stream-K owner: last pair holding a piece of the tile (> this pair: gather partials)
+  int part;    // tail split: this unit writes FP32 partial slot pz instead of the output
+  int pz;
 };
 
 // The sequence of units one pair works on (both CTAs and every role walk
@@ -107,13 +111,26 @@ __device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, PairIter& it,
   if (it.pos >= it.end) return false;
   if (!a.sk) {
     const int u = static_cast<int>(it.pos);
-    const int split = u % a.splits;
-    pair_tile(u / a.splits, a, bn, c);
-    c.zc = c.b * a.splits + split;
-    c.kb0 = split * a.kps;
-    c.kb1 = min(a.kb_total, c.kb0 + a.kps);
     c.owner = 1;
     c.c_last = -1;
+    if (a.tail_splits > 1 && u >= a.dp_tiles) {
+      // tail split: a K range of one of the tiles past the last whole wave
+      const int v = u - a.dp_tiles;
+      pair_tile(a.dp_tiles + v / a.tail_splits, a, bn, c);
+      c.zc = c.b;
+      c.kb0 = (v % a.tail_splits) * a.tail_kps;
+      c.kb1 = min(a.kb_total, c.kb0 + a.tail_kps);
+      c.part = 1;
+      c.pz = v;
+    } else {
+      const int split = u % a.splits;
+      pair_tile(u / a.splits, a, bn, c);
+      c.zc = c.b * a.splits + split;
+      c.kb0 = split * a.kps;
+      c.kb1 = min(a.kb_total, c.kb0 + a.kps);
+      c.part = 0;
+      c.pz = 0;
+    }
     it.pos += pair_count();
     return true;
   }
@@ -127,6 +144,8 @@ __device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, PairIter& it,
   c.kb1 = static_cast<int>(seg_end - kt0);
   c.owner = it.pos == kt0;
   c.c_last = (c.owner && seg_end < kt0 + kb) ? pair_sk_of(kt0 + kb - 1, a) : -1;
+  c.part = 0;
+  c.pz = 0;
   it.pos = seg_end;
   return true;
 }
@@ -134,7 +153,8 @@ __device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, PairIter& it,
 template <bool A_MN, bool B_MN, int BN, bool OUT16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const TcArgs args) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                    const TcArgs args) {
   using Cfg = Tc2Cfg<BN, B_MN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -173,6 +193,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
+    if (args.tail_splits > 1) prefetch_tmap(&tmP);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -187,6 +208,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const unsigned long long tmo = args.timeout_ns;
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) TG_EVENT(0);
 
   if (warp == 0) {
     // ------------------------------------------------ producer (both CTAs)
@@ -235,6 +257,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           } else {
             tma_load_3d_pair(b_dst, &tmB, fb, k0, n, c.b);
           }
+          if (issued[stage] < 0 && stage == 0) TG_EVENT(1);
           issued[stage] = static_cast<int>(phase);
           if (++stage == S) {
             stage = 0;
@@ -242,6 +265,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       }
+      TG_EVENT(8);
       if (ok) {
         // the last commits of rank 0's MMAs arrive on these barriers: see
         // them all before this CTA can leave
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      int nunit = 0;  // (trace builds) units issued so far
       PairIter it = pair_begin(args);
       Unit2 c;
       while (ok && pair_next(args, BN, it, c)) {
@@ -286,6 +311,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ok = false;
             break;
           }
+          if (kb == c.kb0 && nunit < 3) TG_EVENT(10 + 2 * nunit);
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * TC_A_STAGE);
           const uint32_t b_base = smem_u32(sB + stage * Cfg::B_BYTES);
@@ -305,6 +331,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!ok) break;
         umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+        TG_EVENT(7);
+        if (nunit < 3) TG_EVENT(11 + 2 * nunit);
+        ++nunit;
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -340,8 +369,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       bool have_parts = true;
       const uint32_t t_pre = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>((acc ^ 1) * Cfg::ACC_STRIDE);
-      if (fixup) have_parts = sk_gather_parts<BN>(args, first, last, 2, q, lane, t_pre, abort_flag);
+      if (fixup) {
+        if (warp == 2 && lane == 0) TG_EVENT(4);
+        have_parts = sk_gather_parts<BN>(args, first, last, 2, q, lane, t_pre, abort_flag);
+        if (warp == 2 && lane == 0) TG_EVENT(5);
+      }
       if (!mbar_wait<true>(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
+      if (warp == 2 && lane == 0) TG_EVENT(9);
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
@@ -349,6 +383,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // stream-K contributor: FP32 partial of this CTA's 128 rows to its slot
         const uint32_t te = tempty_cl + static_cast<uint32_t>(acc * 8);
         sk_put_part<BN>(args, blockIdx.x, q, lane, t_row, [&] { mbar_arrive_cluster(te); });
+        if (warp == 2 && lane == 0) TG_EVENT(3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
+      if (c.part) {
+        // tail split piece: this CTA's 128 rows of FP32 partial slot pz
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + ch * 32, r);
+          tmem_ld_wait();
+          if (ch == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_cl + static_cast<uint32_t>(acc * 8));
+          }
+          uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+          if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
+          __syncwarp();
+          uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmP, smem_u32(buf), ch * 32, static_cast<int>(rank) * TC_BM + q * 32, c.pz);
+            bulk_commit();
+          }
+          ++nstore;
+        }
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -421,6 +490,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
     if (lane == 0) bulk_wait_all();
+    if (warp == 2 && lane == 0) TG_EVENT(6);
   }
 
   tc_fence_before();

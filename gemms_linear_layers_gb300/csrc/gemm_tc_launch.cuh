@@ -163,7 +163,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
     attr_set[dev] = true;
   }
 
-  alignas(64) CUtensorMap tmA, tmB, tmC;
+  alignas(64) CUtensorMap tmA, tmB, tmC, tmP;
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
   bool ok;
   const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
@@ -210,12 +210,28 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.raster_n = g.raster_n;
   a.a_chunked = a4 ? 1 : 0;
   a.b_chunked = b4 ? 1 : 0;
-  a.tail_splits = 1;
+  // tail split (never with stream-K or split partials); the geometry is that
+  // of a full wave of grid / 2 pairs, whatever number of pairs runs
+  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid / 2, (g.sk || g.splits > 1) ? 1 : g.tail_splits, g.raster_n,
+                              TC2_BM);
+  a.dp_tiles = tg.dp_tiles;
+  a.tail_splits = tg.splits;
+  a.tail_kps = tg.kps;
+  tmP = tmC;
+  if (tg.tail_tiles > 0) {
+    a.units = tg.dp_tiles + tg.tail_tiles * tg.splits;
+    ok = encode_tmap_3d(&tmP, g.ws, EK_F32, BN, TC2_BM, static_cast<uint64_t>(tg.tail_tiles) * tg.splits, BN * 4,
+                        TC2_BM * BN * 4, 32, 32, 128);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
   a.sk = g.sk;
   a.sk_iters = static_cast<long long>(a.units) * a.kb_total;
   a.sk_epoch = g.sk_epoch;
+#ifdef TG_TRACE
+  if (const char* e = getenv("TG_TRACE_ADDR")) a.trace = reinterpret_cast<unsigned long long*>(strtoull(e, nullptr, 0));
+#endif
   int pairs = g.grid / 2;
   if (pairs > max_pairs[dev]) pairs = max_pairs[dev];
   const long long work = g.sk ? a.sk_iters : a.units;  // every pair gets at least one unit / iteration
@@ -229,7 +245,9 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   }
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, a);
+  cudaError_t e2 = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmP, a);
+  if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
+  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream);
 }
 
 template <bool A_MN, bool B_MN>

@@ -95,12 +95,15 @@ inline size_t sk_ws_bytes(int grid, int bn) {
 struct TailGeo {
   int dp_tiles, tail_tiles, splits, kps;
   int m_tiles, n_tiles, raster_n, bn;
+  int bm;  // tile height: 128 (single CTA) or 256 (CTA pair)
   int64_t M, N;
 };
+// grid: CTAs (single CTA) or pairs (bm = 256) of one wave
 inline TailGeo tail_geo(int64_t M, int64_t N, int64_t K, int64_t batch, int bn, int grid, int want_splits,
-                        int raster_n) {
+                        int raster_n, int bm = 128) {
   TailGeo t{};
-  t.m_tiles = static_cast<int>((M + 127) / 128);
+  t.bm = bm;
+  t.m_tiles = static_cast<int>((M + bm - 1) / bm);
   t.n_tiles = static_cast<int>((N + bn - 1) / bn);
   t.raster_n = raster_n;
   t.bn = bn;
@@ -128,19 +131,20 @@ inline TailGeo tail_geo(int64_t M, int64_t N, int64_t K, int64_t batch, int bn, 
   return t;
 }
 inline size_t tail_ws_bytes(const TailGeo& t) {
-  return static_cast<size_t>(t.tail_tiles) * t.splits * 128 * static_cast<size_t>(t.bn) * 4;
+  return static_cast<size_t>(t.tail_tiles) * t.splits * t.bm * static_cast<size_t>(t.bn) * 4;
 }
-// Origin of output tile t (batch-major, then raster order within the batch).
+// Origin of output tile t (batch-major, then raster order within the batch)
+// for tiles bm rows high.
 __host__ __device__ inline void tile_origin(int t, int m_tiles, int n_tiles, int raster_n, int bn, int* b, int* m0,
-                                            int* n0) {
+                                            int* n0, int bm = 128) {
   const int tiles = m_tiles * n_tiles;
   *b = t / tiles;
   const int r = t - *b * tiles;
   if (raster_n) {  // consecutive units walk along N: they share the A tile
     *n0 = (r % n_tiles) * bn;
-    *m0 = (r / n_tiles) * 128;
+    *m0 = (r / n_tiles) * bm;
   } else {  // consecutive units walk down M: they share the B tile
-    *m0 = (r % m_tiles) * 128;
+    *m0 = (r % m_tiles) * bm;
     *n0 = (r / m_tiles) * bn;
   }
 }

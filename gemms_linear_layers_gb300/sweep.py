@@ -148,6 +148,13 @@ def candidates(M, N, K, batch, sms):
             if tiles * kb >= sms // 2 and tiles * 4 >= sms // 2:
                 for raster in ("m", "n"):
                     yield f"{bn}p", "sk", raster
+            # tail split over the pairs' last partial wave
+            pairs = sms // 2
+            if tiles > pairs and tiles % pairs:
+                for ts in (2, 4, 8, 13, 16):
+                    if -(-kb // -(-kb // ts)) >= 2:
+                        for raster in ("m", "n"):
+                            yield f"{bn}p", f"t{ts}", raster
 
 
 def main(argv=None):

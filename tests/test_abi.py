@@ -113,8 +113,7 @@ def test_last_call_buffer(lib):
 def test_tile_table_schedules(lib, tmp_path):
     """Table tokens for the schedules: stream-K (sk) and tail split (tN) need
     64-column multiples; 144-wide tiles take plain split counts; CTA pairs
-    ("p" after the width) take widths 128, 192 and 256 with split counts or
-    stream-K, not the tail split."""
+    ("p" after the width) take widths 128, 192 and 256 with every schedule."""
     t = tmp_path / "s.txt"
     t.write_text("tn bf16 bf16 2304 2304 2048 1 256 sk n\n"
                  "tn bf16 bf16 2304 2304 4096 1 256 t4 m\n"
@@ -123,13 +122,14 @@ def test_tile_table_schedules(lib, tmp_path):
                  "nt bf16 bf16 2048 49152 576 1 256p 1 m\n"
                  "nn bf16 bf16 2048 576 49152 1 192p 3\n"
                  "tn f16 f32 576 576 2048 1 128p 2 n\n"
-                 "tn bf16 bf16 2304 2304 2048 1 256p sk m\n")
+                 "tn bf16 bf16 2304 2304 2048 1 256p sk m\n"
+                 "tn bf16 bf16 2304 2304 4096 1 256p t13 m\n")
     assert lib.tg_load_table(str(t).encode()) == 0
     for bad in ("tn bf16 bf16 2304 2304 2048 1 144 sk\n", "tn bf16 bf16 2304 2304 2048 1 144 t2\n",
                 "tn bf16 bf16 2304 2304 2048 1 256 t1\n", "tn bf16 bf16 2304 2304 2048 1 256 tx\n",
                 "tn bf16 bf16 2304 2304 2048 1 160 1\n", "tn bf16 bf16 2304 2304 2048 1 64p 1\n",
                 "tn bf16 bf16 2304 2304 2048 1 144p 1\n",
-                "tn bf16 bf16 2304 2304 2048 1 256p t2\n", "tn bf16 bf16 2304 2304 2048 1 256q 1\n",
+                "tn bf16 bf16 2304 2304 2048 1 256q 1\n",
                 "tn bf16 bf16 2304 2304 2048 1 256pp 1\n"):
         t.write_text(bad)
         assert lib.tg_load_table(str(t).encode()) == 7, bad

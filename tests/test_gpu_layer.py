@@ -400,7 +400,10 @@ def test_tile_width_144_full_size_wgrad():
 # into FP32 partial tiles that a second kernel adds in split order.  Cases
 # with ragged M/N edge tiles in the tail, every layout, a batch.
 TAIL_CASES = [("fwd", 2000, 576, 1528, 64, 4), ("dgrad", 2048, 1536, 576, 64, 3),
-              ("wgrad", 2048, 576, 2304, 64, 4), ("wgrad", 2048, 2304, 2304, 256, 4)]
+              ("wgrad", 2048, 576, 2304, 64, 4), ("wgrad", 2048, 2304, 2304, 256, 4),
+              # CTA pairs: 256-row tiles, a wave of 76 pairs
+              ("wgrad", 4096, 2304, 2304, "256p", 13), ("fwd", 2000, 1000, 2304, "128p", 4),
+              ("dgrad", 4096, 1536, 1000, "192p", 3)]
 
 
 @pytest.mark.parametrize("out_kind", ["f32", "same"])
