@@ -150,6 +150,26 @@ __device__ __forceinline__ bool pair_next(const TcArgs& a, int bn, PairIter& it,
   return true;
 }
 
+#ifdef TG_TRACE
+// time spent in a wait, summed per role; written to trace slot `slot`
+#define TG_WAIT_BEGIN(v) const uint64_t v##_t0 = globaltimer_ns()
+#define TG_WAIT_END(acc, v) acc += globaltimer_ns() - v##_t0
+#define TG_WAIT_STORE(slot, acc) \
+  do {                           \
+    if (args.trace) args.trace[blockIdx.x * 16 + (slot)] = (acc); \
+  } while (0)
+#else
+#define TG_WAIT_BEGIN(v) \
+  do {                   \
+  } while (0)
+#define TG_WAIT_END(acc, v) \
+  do {                      \
+  } while (0)
+#define TG_WAIT_STORE(slot, acc) \
+  do {                           \
+  } while (0)
+#endif
+
 template <bool A_MN, bool B_MN, int BN, bool OUT16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -219,16 +239,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
       for (int s = 0; s < S; ++s) issued[s] = -1;
       bool ok = true;
+      unsigned long long w_empty = 0;
+      (void)w_empty;
       PairIter it = pair_begin(args);
       Unit2 c;
       const int a_row = static_cast<int>(rank) * TC_BM;    // this CTA's rows of the pair tile
       const int b_off = static_cast<int>(rank) * Cfg::BH;  // this CTA's half of B
       while (ok && pair_next(args, BN, it, c)) {
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
+          TG_WAIT_BEGIN(we);
           if (!mbar_wait<true>(smem_u32(&empty[stage]), phase ^ 1u, tmo, abort_flag, args.status, 1)) {
             ok = false;
             break;
           }
+          TG_WAIT_END(w_empty, we);
           const uint32_t fb_local = smem_u32(&full[stage]);
           if (rank == 0) mbar_arrive_expect_tx(fb_local, 2 * Cfg::STAGE);
           const uint32_t fb = mapa_shared(fb_local, 0);
@@ -266,6 +290,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
       TG_EVENT(8);
+      TG_WAIT_STORE(10, w_empty);
       if (ok) {
         // the last commits of rank 0's MMAs arrive on these barriers: see
         // them all before this CTA can leave
@@ -296,22 +321,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      int nunit = 0;  // (trace builds) units issued so far
+      unsigned long long w_tempty = 0, w_full = 0;
+      (void)w_tempty;
+      (void)w_full;
       PairIter it = pair_begin(args);
       Unit2 c;
       while (ok && pair_next(args, BN, it, c)) {
+        TG_WAIT_BEGIN(wt);
         if (!mbar_wait<true>(smem_u32(&tempty[acc]), acc_phase ^ 1u, tmo, abort_flag, args.status, 2)) {
           ok = false;
           break;
         }
+        TG_WAIT_END(w_tempty, wt);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
         for (int kb = c.kb0; kb < c.kb1; ++kb) {
+          TG_WAIT_BEGIN(wf);
           if (!mbar_wait<true>(smem_u32(&full[stage]), phase, tmo, abort_flag, args.status, 3)) {
             ok = false;
             break;
           }
-          if (kb == c.kb0 && nunit < 3) TG_EVENT(10 + 2 * nunit);
+          TG_WAIT_END(w_full, wf);
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * TC_A_STAGE);
           const uint32_t b_base = smem_u32(sB + stage * Cfg::B_BYTES);
@@ -332,13 +362,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!ok) break;
         umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
         TG_EVENT(7);
-        if (nunit < 3) TG_EVENT(11 + 2 * nunit);
-        ++nunit;
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
+      TG_WAIT_STORE(11, w_tempty);
+      TG_WAIT_STORE(12, w_full);
       // every MMA issued must finish before either CTA frees tensor memory
       umma_commit_pair(smem_u32(drain), 0x1);
       mbar_wait<true>(smem_u32(drain), 0, ok ? tmo : 200000000ull, nullptr, args.status, 10);
@@ -353,6 +383,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     static_assert(BN % CW == 0, "pair tile width and output width");
     const uint32_t tempty_cl = mapa_shared(smem_u32(&tempty[0]), 0);
     const int pair = pair_index();
+    unsigned long long w_tfull = 0, w_ld = 0, w_bw = 0, w_pack = 0, w_fs = 0, w_chunks = 0, w_unit = 0;
+    (void)w_chunks;
+    (void)w_unit;
+    (void)w_pack;
+    (void)w_fs;
+    (void)w_tfull;
+    (void)w_ld;
+    (void)w_bw;
     int acc = 0;
     uint32_t acc_phase = 0;
     int nstore = 0;
@@ -374,7 +412,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         have_parts = sk_gather_parts<BN>(args, first, last, 2, q, lane, t_pre, abort_flag);
         if (warp == 2 && lane == 0) TG_EVENT(5);
       }
+      TG_WAIT_BEGIN(wtf);
       if (!mbar_wait<true>(smem_u32(&tfull[acc]), acc_phase, tmo, abort_flag, args.status, 4)) break;
+      TG_WAIT_END(w_tfull, wtf);
+      TG_WAIT_BEGIN(wu);
       if (warp == 2 && lane == 0) TG_EVENT(9);
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -425,12 +466,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         continue;
       }
       const int row0 = c.m0 + static_cast<int>(rank) * TC_BM + q * 32;
+      TG_WAIT_BEGIN(wc);
 #pragma unroll 1
       for (int ch = 0; ch < NCH; ++ch) {
         uint32_t r[CW];
+        TG_WAIT_BEGIN(wl);
         tmem_ld_32x32b_x32(t_row + ch * CW, r);
         if (OUT16) tmem_ld_32x32b_x32(t_row + ch * CW + 32, r + 32);
         tmem_ld_wait();
+        TG_WAIT_END(w_ld, wl);
         if (ch == NCH - 1) {
           // accumulator read: hand it back to rank 0's MMA issuer
           tc_fence_before();
@@ -450,9 +494,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
         uint8_t* buf = ebuf + (nstore & 1) * TC_EPI_BUF;
+        TG_WAIT_BEGIN(wb);
         if (lane == 0 && nstore >= 2) bulk_wait_read<1>();
         __syncwarp();
+        TG_WAIT_END(w_bw, wb);
         uint8_t* rowp = buf + lane * 128;
+        TG_WAIT_BEGIN(wp);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint4 v;
@@ -475,22 +522,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // 128-byte swizzle: 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8)
           *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = v;
         }
+        TG_WAIT_END(w_pack, wp);
+        TG_WAIT_BEGIN(wfs);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, row0, c.zc);
           bulk_commit();
         }
+        TG_WAIT_END(w_fs, wfs);
         ++nstore;
       }
+      TG_WAIT_END(w_chunks, wc);
       if (fixup && have_parts) sk_clear_flags(args, first, last, 2, q, lane);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
+      TG_WAIT_END(w_unit, wu);
     }
     if (lane == 0) bulk_wait_all();
     if (warp == 2 && lane == 0) TG_EVENT(6);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(13, w_tfull);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(14, w_ld);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(15, w_bw);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(3, w_pack);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(4, w_fs);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(5, w_chunks);
+    if (warp == 2 && lane == 0) TG_WAIT_STORE(1, w_unit);
   }
 
   tc_fence_before();

@@ -268,9 +268,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// arrive on an mbarrier given by its cluster address (possibly the peer's)
+// arrive on an mbarrier given by its cluster address (possibly the peer's).
+// Default (CTA-scope release) semantics: it hands back tensor memory whose
+// reads have completed (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync),
+// so it needs no cluster-scope ordering of this thread's memory traffic; a
+// cluster-scope release would first wait for the thread's stores in flight
+// (measured: about 1.7 us per output tile).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // every thread of both CTAs
 __device__ __forceinline__ void cluster_sync_all() {
