@@ -186,7 +186,7 @@ def kernel_key(call: str) -> str:
     bn = next((x for x in f if x.startswith("bn=")), "bn=?")
     sp = next((x for x in f if x.startswith("splits=")), "splits=1")
     deep = " deep" if "deep" in f else ""
-    pair = " pair" if "pair" in f else ""
+    pair = " pair" if "pair" in f else (" cs" if "cs" in f else "")
     tail = " +tail" if any(x.startswith("tail=") for x in f) else ""
     sk = " sk" if "sk" in f else ""
     return f"tc {f[2]} {bn}{deep}{pair}{sk}" + (" +reduce" if sp != "splits=1" else "") + tail

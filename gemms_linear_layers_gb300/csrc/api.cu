@@ -138,6 +138,7 @@ struct TableVal {
   int bn, splits, raster;  // splits 0 = stream-K; raster: -1 = by operand size, 0 = along M, 1 = along N
   int tail;                // > 1: tail split of the tiles past the last whole wave
   int pair;                // 1: CTA-pair kernel (256-row tiles)
+  int csplit;              // > 1: split-K across the CTAs of a cluster
 };
 static std::shared_mutex g_table_mu;
 static std::unordered_map<TableKey, TableVal, TableKeyHash> g_table;
@@ -169,7 +170,7 @@ static tg_status load_table_file(const char* path) {
       std::istringstream ss(line);
       std::string op, din, dout, bs, sp;
       int64_t M, N, K, batch;
-      int bn, splits, tail = 0, pair = 0;
+      int bn, splits, tail = 0, pair = 0, csplit = 0;
       if (!(ss >> op)) continue;  // blank line
       if (!(ss >> din >> dout >> M >> N >> K >> batch >> bs >> sp)) return TG_ERR_TABLE;
       {  // tile width, "p" suffix: CTA pair (256 x bn tiles)
@@ -182,6 +183,12 @@ static tg_status load_table_file(const char* path) {
       }
       if (sp == "sk") {
         splits = 0;
+      } else if (sp.size() > 1 && sp[0] == 'c') {  // cluster split-K: cN
+        char* endp = nullptr;
+        const long v = strtol(sp.c_str() + 1, &endp, 10);
+        if (*endp != '\0' || v < 2 || v > 8) return TG_ERR_TABLE;
+        splits = 1;
+        csplit = static_cast<int>(v);
       } else if (sp.size() > 1 && sp[0] == 't') {  // tail split: tN
         char* endp = nullptr;
         const long v = strtol(sp.c_str() + 1, &endp, 10);
@@ -207,7 +214,8 @@ static tg_status load_table_file(const char* path) {
         return TG_ERR_TABLE;
       if (bn % 64 != 0 && (splits == 0 || tail > 0)) return TG_ERR_TABLE;  // partial tiles: 64-column multiples
       if (pair && (bn == 64 || bn == 144)) return TG_ERR_TABLE;  // pairs: widths 128, 192, 256
-      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail, pair};
+      if (csplit && (pair || bn == 144)) return TG_ERR_TABLE;    // cluster split: single CTAs, 64..256
+      t[TableKey{l, i, o, M, N, K, batch}] = TableVal{bn, splits, raster, tail, pair, csplit};
     }
   }
   std::unique_lock<std::shared_mutex> lk(g_table_mu);
@@ -251,6 +259,7 @@ struct Plan {
   bool sk = false;  // stream-K schedule (splits is then 1)
   int tail = 0;     // > 1: tail split (splits is then 1)
   bool pair = false;  // CTA-pair kernel: 256 x bn tiles
+  int csplit = 0;     // > 1: split-K across a cluster of this many CTAs (splits is then 1)
   bool from_table = false;
 };
 
@@ -309,6 +318,26 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
+  // split-K across a cluster (one wave: tiles x S CTAs at most one per SM);
+  // the S partial tiles are added through distributed shared memory
+  for (int bn : {256, 192, 128, 64}) {
+    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
+    const double kb_cyc = kb_cycles(bn);
+    for (int64_t cs = 2; cs <= 8 && cs <= kb; ++cs) {
+      const int64_t kps = cdiv(kb, cs);
+      if (cdiv(kb, kps) != cs || tiles * cs > sms) continue;
+      const double t = kps * kb_cyc + 600.0 + 1500.0 + 128.0 * bn * 4 * (cs - 1) / (cs * 64.0);
+      if (t < best_t * 0.95) {
+        best_t = t;
+        best.bn = bn;
+        best.splits = 1;
+        best.sk = false;
+        best.tail = 0;
+        best.pair = false;
+        best.csplit = static_cast<int>(cs);
+      }
+    }
+  }
   // CTA pairs (256 x bn tiles on two SMs, half of B per SM): a pair MMA
   // costs at least ~125 cycles whatever its width, and runs at the full rate
   // at bn = 256, measured
@@ -330,6 +359,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
         best.sk = false;
         best.tail = 0;
         best.pair = true;
+        best.csplit = 0;
       }
     }
   }
@@ -350,6 +380,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       best.sk = true;
       best.tail = 0;
       best.pair = false;
+      best.csplit = 0;
     }
   }
   // stream-K on CTA pairs (256 x 256 tiles, ranges per pair)
@@ -368,6 +399,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
         best.sk = true;
         best.tail = 0;
         best.pair = true;
+        best.csplit = 0;
       }
     }
   }
@@ -386,6 +418,7 @@ static Plan make_plan(int layout, int64_t M, int64_t N, int64_t K, int64_t batch
     Plan p;
     p.bn = v.bn;
     p.pair = v.pair != 0;
+    p.csplit = v.csplit;
     const int64_t kb = cdiv(K, 64);
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, p.bn);
     p.sk = v.splits == 0 && tiles * kb >= 1;
@@ -513,6 +546,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.sk_epoch = p.sk ? next_epoch() : 0;
     t.tail_splits = p.tail;
     t.pair = p.pair ? 1 : 0;
+    t.csplit = p.csplit;
     // the deep ring when a CTA streams at least 128 K blocks (its epilogues
     // hide behind later MMAs); widths 144 and 192 only
     {
@@ -535,9 +569,10 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     const TailGeo tgeo = plan_tail_geo(p, g.M, g.N, g.K, g.batch, ctx->sms);
     char tail[48] = "";
     if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
+    if (p.csplit > 1) snprintf(tail, sizeof tail, " cluster=%d", p.csplit);
     snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s %s",
              g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
-             p.bn, t.deep ? " deep" : (p.pair ? " pair" : ""), p.sk ? "sk grid=" : "splits=",
+             p.bn, t.deep ? " deep" : (p.pair ? " pair" : (p.csplit > 1 ? " cs" : "")), p.sk ? "sk grid=" : "splits=",
              p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits, tail, p.raster_n ? 'n' : 'm',
              p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     record(buf);

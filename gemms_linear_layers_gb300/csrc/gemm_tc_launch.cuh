@@ -8,6 +8,7 @@
 
 #include "gemm_tc.cuh"
 #include "gemm_tc2.cuh"
+#include "gemm_tc_cs.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -261,8 +262,106 @@ static cudaError_t tc2_launch_layout(const TcGemm& g) {
   }
 }
 
+// Cluster split-K: one 128 x BN tile per cluster of csplit CTAs, every CTA
+// one K range; the grid is tiles x csplit (no persistence, no workspace).
+template <bool A_MN, bool B_MN, int BN, bool OUT16>
+static cudaError_t tcs_launch_one(const TcGemm& g) {
+  using Cfg = TcsCfg<BN>;
+  auto kern = tc_cs_gemm_kernel<A_MN, B_MN, BN, OUT16>;
+  static bool attr_set[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  alignas(64) CUtensorMap tmA, tmB;
+  const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
+  bool ok;
+  const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
+  const bool b4 = B_MN && N % 64 == 0 && BN % 64 == 0 && chunked_mn_enabled();
+  if (a4) {
+    const uint64_t d[4] = {64, K, M / 64, nb}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
+                                                      static_cast<uint64_t>(g.a_bstride) * 2};
+    const uint32_t b[4] = {64, 64, TC_BM / 64, 1};
+    ok = encode_tmap_nd(&tmA, g.A, g.in_kind, 4, d, st, b, 128);
+  } else if (A_MN) {
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
+  } else {
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  if (b4) {
+    const uint64_t d[4] = {64, K, N / 64, nb}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
+                                                      static_cast<uint64_t>(g.b_bstride) * 2};
+    const uint32_t b[4] = {64, 64, static_cast<uint32_t>(Cfg::B_CHUNKS), 1};
+    ok = encode_tmap_nd(&tmB, g.B, g.in_kind, 4, d, st, b, 128);
+  } else if (B_MN) {
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
+  } else {
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+
+  CsArgs a = {};
+  a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
+  a.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  // every rank gets a non-empty K range
+  a.kps = (a.kb_total + g.csplit - 1) / g.csplit;
+  const int ranks = (a.kb_total + a.kps - 1) / a.kps;
+  a.raster_n = g.raster_n;
+  a.idesc = idesc_f16(g.in_kind == EK_BF16, A_MN, B_MN, TC_BM, BN);
+  a.out_f16 = g.out_kind == EK_F16 ? 1 : 0;
+  a.a_chunked = a4 ? 1 : 0;
+  a.b_chunked = b4 ? 1 : 0;
+  a.C = g.C;
+  a.M = static_cast<long long>(M);
+  a.N = static_cast<long long>(N);
+  a.timeout_ns = g.timeout_ns;
+  a.status = g.status;
+  a.trace = nullptr;
+#ifdef TG_TRACE
+  if (const char* e = getenv("TG_TRACE_ADDR")) a.trace = reinterpret_cast<unsigned long long*>(strtoull(e, nullptr, 0));
+#endif
+  const long long tiles = static_cast<long long>(nb) * a.m_tiles * a.n_tiles;
+  if (tiles * ranks > 0x7fffffffLL) return cudaErrorInvalidValue;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ranks);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * ranks));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = g.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
+}
+
+template <bool A_MN, bool B_MN>
+static cudaError_t tcs_launch_layout(const TcGemm& g) {
+  const bool out16 = g.out_kind != EK_F32;
+  switch (g.bn) {
+    case 64: return out16 ? tcs_launch_one<A_MN, B_MN, 64, true>(g) : tcs_launch_one<A_MN, B_MN, 64, false>(g);
+    case 128: return out16 ? tcs_launch_one<A_MN, B_MN, 128, true>(g) : tcs_launch_one<A_MN, B_MN, 128, false>(g);
+    case 192: return out16 ? tcs_launch_one<A_MN, B_MN, 192, true>(g) : tcs_launch_one<A_MN, B_MN, 192, false>(g);
+    case 256: return out16 ? tcs_launch_one<A_MN, B_MN, 256, true>(g) : tcs_launch_one<A_MN, B_MN, 256, false>(g);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <bool A_MN, bool B_MN>
 static cudaError_t tc_launch_layout(const TcGemm& g) {
+  if (g.csplit > 1) return tcs_launch_layout<A_MN, B_MN>(g);
   if (g.pair) return tc2_launch_layout<A_MN, B_MN>(g);
   // split partials are FP32; so is an FP32 output
   const bool out16 = (g.sk || g.splits == 1) && g.out_kind != EK_F32;

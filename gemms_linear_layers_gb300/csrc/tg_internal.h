@@ -75,7 +75,8 @@ struct TcGemm {
   unsigned long long sk_epoch;  // flag value unique to this launch
   int tail_splits;            // >1: tiles past the last whole wave are split along K (ws: partial tiles)
   int deep;                   // 1: widths 144/192 with a fifth operand stage (one epilogue buffer)
-  int pair;                   // 1: CTA-pair kernel, 256 x bn tiles (bn 128, 192 or 256; splits only)
+  int pair;                   // 1: CTA-pair kernel, 256 x bn tiles (bn 128, 192 or 256)
+  int csplit;                 // > 1: split-K across the CTAs of a cluster, added on chip (bn 64..256)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;

@@ -126,6 +126,13 @@ def candidates(M, N, K, batch, sms):
                 if -(-kb // -(-kb // ts)) >= 2:
                     for raster in ("m", "n"):
                         yield bn, f"t{ts}", raster
+        # split-K across a cluster, added on chip: one wave of tiles x N CTAs
+        if bn != 144:
+            for cs in range(2, 9):
+                if cs > kb or tiles * cs > sms or -(-kb // -(-kb // cs)) != cs:
+                    continue
+                for raster in ("m", "n"):
+                    yield bn, f"c{cs}", raster
         # stream-K: an equal share of tile x K-block iterations per CTA
         # (its partial tiles are 64-column multiples)
         if bn % 64 == 0 and tiles * kb >= sms and tiles * 4 >= sms:

@@ -113,7 +113,8 @@ def test_last_call_buffer(lib):
 def test_tile_table_schedules(lib, tmp_path):
     """Table tokens for the schedules: stream-K (sk) and tail split (tN) need
     64-column multiples; 144-wide tiles take plain split counts; CTA pairs
-    ("p" after the width) take widths 128, 192 and 256 with every schedule."""
+    ("p" after the width) take widths 128, 192 and 256 with every schedule;
+    the cluster split-K (cN, 2 <= N <= 8) takes single-CTA widths 64..256."""
     t = tmp_path / "s.txt"
     t.write_text("tn bf16 bf16 2304 2304 2048 1 256 sk n\n"
                  "tn bf16 bf16 2304 2304 4096 1 256 t4 m\n"
@@ -123,13 +124,17 @@ def test_tile_table_schedules(lib, tmp_path):
                  "nn bf16 bf16 2048 576 49152 1 192p 3\n"
                  "tn f16 f32 576 576 2048 1 128p 2 n\n"
                  "tn bf16 bf16 2304 2304 2048 1 256p sk m\n"
-                 "tn bf16 bf16 2304 2304 4096 1 256p t13 m\n")
+                 "tn bf16 bf16 2304 2304 4096 1 256p t13 m\n"
+                 "nt bf16 bf16 2048 576 1536 1 192 c3 m\n"
+                 "tn f16 f32 576 576 2048 1 64 c8\n")
     assert lib.tg_load_table(str(t).encode()) == 0
     for bad in ("tn bf16 bf16 2304 2304 2048 1 144 sk\n", "tn bf16 bf16 2304 2304 2048 1 144 t2\n",
                 "tn bf16 bf16 2304 2304 2048 1 256 t1\n", "tn bf16 bf16 2304 2304 2048 1 256 tx\n",
                 "tn bf16 bf16 2304 2304 2048 1 160 1\n", "tn bf16 bf16 2304 2304 2048 1 64p 1\n",
                 "tn bf16 bf16 2304 2304 2048 1 144p 1\n",
-                "tn bf16 bf16 2304 2304 2048 1 256q 1\n",
+                "tn bf16 bf16 2304 2304 2048 1 256q 1\n", "nt bf16 bf16 2048 576 1536 1 192p c3\n",
+                "nt bf16 bf16 2048 576 1536 1 144 c3\n", "nt bf16 bf16 2048 576 1536 1 192 c1\n",
+                "nt bf16 bf16 2048 576 1536 1 192 c9\n", "nt bf16 bf16 2048 576 1536 1 192 cx\n",
                 "tn bf16 bf16 2304 2304 2048 1 256pp 1\n"):
         t.write_text(bad)
         assert lib.tg_load_table(str(t).encode()) == 7, bad

@@ -24,6 +24,8 @@ def test_kernel_key():
         "tc nt bn=256 pair"
     assert k("dgrad tc nn M=2048 N=576 K=49152 batch=1 bn=192 pair splits=3 raster=n table=hit ok") == \
         "tc nn bn=192 pair +reduce"
+    assert k("fwd tc nt M=2048 N=576 K=1536 batch=1 bn=192 cs splits=1 cluster=3 raster=m table=hit ok") == \
+        "tc nt bn=192 cs"
     assert k("wgrad simt tn M=200 N=300 K=520 batch=1 ok") == "simt tn"
 
 

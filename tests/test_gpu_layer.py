@@ -434,6 +434,81 @@ def test_tail_split_schedule(case, dtype, out_kind):
         assert_close(gather(outs[0], co), C, S, f"{op} tail split sampled [{call}]", out_dtype)
 
 
+# Cluster split-K: the K ranges of one 128 x bn tile on the CTAs of a cluster,
+# their FP32 partial tiles added through distributed shared memory.  Ragged
+# M, N and K (a short last range), every layout, 2 to 8 ranks.
+CLUSTER_CASES = [("fwd", 2048, 1536, 576, 192, 3), ("dgrad", 2048, 576, 1536, 192, 3),
+                 ("wgrad", 2048, 576, 576, 64, 8), ("wgrad", 2048, 576, 192, 64, 8),
+                 ("fwd", 300, 200, 520, 128, 2), ("dgrad", 300, 520, 200, 256, 3),
+                 ("wgrad", 1000, 296, 200, 64, 5), ("fwd", 1000, 1000, 1000, 64, 7)]
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", CLUSTER_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_cluster_split_schedule(case, dtype, out_kind):
+    op, T, d_in, d_out, bn, cs = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    M, N = out_shape(op, T, d_in, d_out)
+    K = {"fwd": d_in, "dgrad": d_out, "wgrad": T}[op]
+    lay = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn"}[op]
+    dname = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+    line = f"{lay} {dname[dtype]} {dname[out_dtype]} {M} {N} {K} 1 {bn} c{cs}"
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="cs")
+    Xc, Wc, dYc = X.cuda(), W.cuda(), dY.cuda()
+    outs = _with_table(line, lambda: [run(op, Xc, Wc, dYc, out_dtype) for _ in range(3)])
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert f"bn={bn} cs" in call and "table=hit" in call, call
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2]), "cluster split not deterministic"
+    C, S = ref(op, X, W, dY)
+    assert_close(outs[0], C, S, f"{op} cluster split [{call}]", out_dtype)
+
+
+def test_cluster_split_small_integers_exact():
+    """FP32 output of small-integer operands is exact whatever the order of
+    the partial sums: the on-chip reduction must equal the oracle bitwise."""
+    T, d_in, d_out = 4096, 576, 192
+    X = inputs.small_int((T, d_in), -2, 2, torch.bfloat16, 21)
+    dY = inputs.small_int((T, d_out), -2, 2, torch.bfloat16, 22)
+    line = f"tn bf16 f32 {d_out} {d_in} {T} 1 64 c8"
+    got = _with_table(line, lambda: tg.tg_gemm_wgrad(dY.cuda(), X.cuda(), out_dtype=torch.float32))
+    assert " cs" in tg.tg_last_call()
+    C, _ = oracle.gemm_wgrad(dY, X)
+    assert np.array_equal(got.cpu().double().numpy(), C)
+
+
+def test_cluster_split_attention_batch_and_graph():
+    """A batch of heads (one cluster per tile of every head), replayed from a
+    CUDA graph with new inputs."""
+    h, s, d = 4, 512, 64
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="cs")
+    line = f"nn bf16 bf16 {s} {d} {s} {h} 64 c4"
+    P, V = t["P"].cuda(), t["V"].cuda()
+
+    def go():
+        out = tg.tg_bmm_attn("pv", P, V)
+        call = tg.tg_last_call()
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        C = torch.empty_like(out)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            tg.tg_bmm_attn("pv", P, V, C=C)
+        V.mul_(2)  # exact in bf16: the replay must see the new values
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        return out, C, call
+
+    out, replayed, call = _with_table(line, go)
+    assert " cs" in call, call
+    C, S = oracle.bmm_attn("pv", t["P"], t["V"])
+    assert_close(out, C, S, f"attn pv cluster split [{call}]", torch.bfloat16)
+    assert_close(replayed, 2 * C, 2 * S, f"attn pv cluster split replay [{call}]", torch.bfloat16)
+
+
 # CTA pairs: 256-row tiles computed by two CTAs of a cluster (one MMA of
 # M = 256 across both SMs).  Ragged M, N and K; K-major and MN-major B halves
 # of 64, 96 and 128 rows/columns; the 4-D chunked operand views (widths that

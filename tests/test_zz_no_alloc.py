@@ -34,24 +34,32 @@ def _call_noalloc(dY, X, dW):
                                           tg._DT[dY.dtype], tg._DT[dW.dtype], stream)
 
 
-def test_noalloc_wgrad_matches_regular_entry_point_twice_in_a_row():
+def test_noalloc_wgrad_matches_regular_entry_point_twice_in_a_row(tmp_path):
+    import os
     from gemms_linear_layers_gb300 import build
     build.build()
-    # two shapes whose plans split the token reduction (so the scratch is used)
+    # two shapes whose plans split the token reduction into FP32 partials (so
+    # the scratch is used): forced by a table, whatever the shipped one picks
     cases = [(2048, 576, 576, torch.bfloat16, torch.bfloat16), (16384, 192, 128, torch.float16, torch.float32)]
-    for T, d_in, d_out, dtype, out_dtype in cases:
-        need = tg.tg_workspace_size(tg.TG_OP_GEMM_WGRAD, T, d_out, d_in, 0, dtype, out_dtype)
-        assert 0 < need <= 32 << 20, need
-        X, _, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="noalloc")
-        Xc, dYc = X.cuda(), dY.cuda()
-        regular = tg.tg_gemm_wgrad(dYc, Xc, out_dtype=out_dtype)
-        dW = torch.full((d_out, d_in), float("nan"), dtype=out_dtype, device="cuda")
-        assert _call_noalloc(dYc, Xc, dW) == 0, tg.tg_last_call()
-        torch.cuda.synchronize()
-        assert tg.tg_stream_status() == 0
-        _, S = oracle.gemm_wgrad(dY, X)
-        ref = regular.double().cpu().numpy()
-        assert_close(dW, ref, S, f"noalloc wgrad {T}x{d_in}->{d_out} vs tg_gemm_wgrad", out_dtype)
+    table = tmp_path / "split.txt"
+    table.write_text("tn bf16 bf16 576 576 2048 1 128 4\ntn f16 f32 128 192 16384 1 64 8\n")
+    assert tg.tg_load_table(str(table)) == 0
+    try:
+        for T, d_in, d_out, dtype, out_dtype in cases:
+            need = tg.tg_workspace_size(tg.TG_OP_GEMM_WGRAD, T, d_out, d_in, 0, dtype, out_dtype)
+            assert 0 < need <= 32 << 20, need
+            X, _, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="noalloc")
+            Xc, dYc = X.cuda(), dY.cuda()
+            regular = tg.tg_gemm_wgrad(dYc, Xc, out_dtype=out_dtype)
+            dW = torch.full((d_out, d_in), float("nan"), dtype=out_dtype, device="cuda")
+            assert _call_noalloc(dYc, Xc, dW) == 0, tg.tg_last_call()
+            torch.cuda.synchronize()
+            assert tg.tg_stream_status() == 0
+            _, S = oracle.gemm_wgrad(dY, X)
+            ref = regular.double().cpu().numpy()
+            assert_close(dW, ref, S, f"noalloc wgrad {T}x{d_in}->{d_out} vs tg_gemm_wgrad", out_dtype)
+    finally:
+        assert tg.tg_load_table(tg.DEFAULT_TABLE if os.path.exists(tg.DEFAULT_TABLE) else None) == 0
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(tmp_path):
