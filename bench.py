@@ -24,8 +24,10 @@ rank-16 LoRA at 4,096 tokens, batched attention) against its own roofline.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,6 +43,47 @@ from gemms_linear_layers_gb300 import inputs, workloads  # noqa: E402
 METRIC = "TFLOPS per training GEMM (fwd/dgrad/wgrad, bf16/fp16) and % of GB300 dense peak"
 WORKLOAD = "135M-class decoder layer set, T=2048, fwd+dgrad+wgrad, bf16 and fp16 (48 products)"
 L2_FLUSH_BYTES = 256 << 20
+PROFILES_DIR = os.path.join(ROOT, "profiles")
+CSRC_DIR = os.path.join(ROOT, "gemms_linear_layers_gb300", "csrc")
+
+
+def kernel_sources_digest(csrc=None) -> str:
+    """SHA-1 over the kernel sources (name and bytes, in name order)."""
+    csrc = csrc or CSRC_DIR
+    h = hashlib.sha1()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel_key: str, profiles=None, digest=None):
+    """DRAM bytes (read + write) per launch of the kernel identity
+    `kernel_key`, from a committed ncu summary that names it and records the
+    digest of the kernel sources it was captured from; None when no summary
+    matches or the kernels changed since the counters were taken."""
+    profiles = profiles or PROFILES_DIR
+    digest = digest or kernel_sources_digest()
+    if not os.path.isdir(profiles):
+        return None
+    pat = re.compile(r"^- (bench_kernel_key|traffic_bytes_per_launch|kernel_sources_sha1): `([^`]*)`")
+    for name in sorted(os.listdir(profiles)):
+        if not name.endswith(".md"):
+            continue
+        fields = {}
+        with open(os.path.join(profiles, name)) as f:
+            for line in f:
+                m = pat.match(line)
+                if m:
+                    fields[m.group(1)] = m.group(2)
+        if fields.get("bench_kernel_key") == kernel_key and fields.get("kernel_sources_sha1") == digest:
+            try:
+                return int(fields["traffic_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
 
 
 def peaks():
@@ -722,7 +765,7 @@ def main():
     flops_per_launch = dom["flops"] / dom["n"]
     achieved = flops_per_launch / (avg_launch_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+                "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": profiled_traffic(dom_name),
                 "kernel": dom_name, "products": dom["products"],
                 "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
                 "share_of_step": round(dom_ms / total_ms, 3)}

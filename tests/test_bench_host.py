@@ -54,3 +54,21 @@ def test_step_waves_cover_every_product_once_in_training_order():
     order = [(p.dtype, p.op) for w in waves for p in w]
     bf = [op for dt, op in order if dt == torch.bfloat16]
     assert bf.index("dgrad") > max(i for i, op in enumerate(bf) if op == "fwd")
+
+
+def test_profiled_traffic_needs_matching_key_and_sources(tmp_path):
+    """The roofline's DRAM traffic comes from a committed ncu summary only if
+    it names the dominant kernel identity and was taken from the current
+    kernel sources."""
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (csrc / "k.cu").write_text("kernel v1\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    digest = bench.kernel_sources_digest(str(csrc))
+    (prof / "k.md").write_text("# capture\n\n- bench_kernel_key: `tc nn bn=192 pair +reduce`\n"
+                               f"- traffic_bytes_per_launch: `275000000`\n- kernel_sources_sha1: `{digest}`\n")
+    assert bench.profiled_traffic("tc nn bn=192 pair +reduce", str(prof), digest) == 275000000
+    assert bench.profiled_traffic("tc nt bn=256 pair", str(prof), digest) is None
+    (csrc / "k.cu").write_text("kernel v2\n")  # the kernel changed since the capture
+    assert bench.profiled_traffic("tc nn bn=192 pair +reduce", str(prof), bench.kernel_sources_digest(str(csrc))) is None
