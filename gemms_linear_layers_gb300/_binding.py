@@ -46,6 +46,7 @@ SIGNATURES = {
     "tg_load_table": (_i, [ctypes.c_char_p]),
     "tg_version": (_i, []),
     "tg_last_call": (_sz, [ctypes.c_char_p, _sz]),
+    "tg_plan_describe": (_sz, [_i, _i64, _i64, _i64, _i64, _i, _i, _i, ctypes.c_char_p, _sz]),
     "tg_wait_probe": (_i, [_i64, _vp]),
 }
 
@@ -275,6 +276,13 @@ def tg_load_table(path) -> int:
 
 def tg_version() -> int:
     return lib().tg_version()
+
+
+def tg_plan_describe(op, M, N, K, batch, din, dout, sms) -> str:
+    """The plan the tensor-core path would use (host only; see include/tg.h)."""
+    buf = ctypes.create_string_buffer(512)
+    n = lib().tg_plan_describe(op, M, N, K, batch, _DT[din], _DT[dout], sms, buf, 512)
+    return buf.value.decode() if n else ""
 
 
 def tg_last_call() -> str:

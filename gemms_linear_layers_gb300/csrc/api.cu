@@ -272,12 +272,20 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
   Plan best;
   double best_t = 1e300;
   const int64_t kb = cdiv(K, 64);
-  const int bns[5] = {256, 192, 144, 128, 64};
+  // narrow first: a wider tile must beat a narrower one by a margin (equal
+  // costs mean the same number of tiles, and then the wider one only wastes
+  // columns)
+  const int bns[5] = {64, 128, 144, 192, 256};
   // one 128 x bn x 64 block: four 128 x bn x 16 MMAs, measured at >= 88 cycles
   // each and ~0.525 * bn cycles from bn = 192 up (the tensor pipe's full
-  // rate); from bn = 192 up the single-CTA kernel reaches ~0.89 of that rate,
-  // held back by its operand feed (all bn rows of B per SM)
-  auto kb_cycles = [](int bn) { return 4.0 * fmax(88.0, 0.525 * bn) * (bn >= 192 ? 1.12 : 1.0); };
+  // rate), or the time the SM's operand feed takes for the block's bytes
+  // (16 KB of A and bn rows of B, whole 64-column chunks), ~75 bytes per
+  // cycle as measured on the single-CTA kernel: ~600 cycles per block at
+  // widths 144 to 256 alike
+  auto kb_cycles = [](int bn) {
+    const double feed = (16384.0 + 128.0 * 64 * ((bn + 63) / 64)) / 75.0;
+    return fmax(4.0 * fmax(88.0, 0.525 * bn), feed);
+  };
   for (int bn : bns) {
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
     const double kb_cyc = kb_cycles(bn);
@@ -289,7 +297,8 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       const int64_t units = tiles * s;
       const int64_t waves = cdiv(units, sms);
       double t = waves * (fmax(kps * kb_cyc, s > 1 ? 128.0 * bn * 4 / 48.0 : epi_cyc) + 600.0);
-      if (s > 1) t += 3000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
+      // the ordered reduction: a second launch plus its pass over the partials
+      if (s > 1) t += 5000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
       if (t < best_t * 0.98) {
         best_t = t;
         best.bn = bn;
@@ -318,15 +327,20 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
-  // split-K across a cluster (one wave: tiles x S CTAs at most one per SM);
-  // the S partial tiles are added through distributed shared memory
-  for (int bn : {256, 192, 128, 64}) {
+  // split-K across a cluster (one wave: tiles x S CTAs at most one per SM,
+  // and no more clusters than fit at once: a cluster lives inside one GPC,
+  // so on 152 SMs only about 74 / 46 / 36 / 28 / 24 / 20 / 16 clusters of
+  // 2..8 are resident together, measured for 3 and 4); the S partial tiles
+  // are added through distributed shared memory at ~16 bytes per cycle per
+  // SM, after two cluster barriers and the accumulator copy
+  for (int bn : {64, 128, 192, 256}) {
     const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
     const double kb_cyc = kb_cycles(bn);
     for (int64_t cs = 2; cs <= 8 && cs <= kb; ++cs) {
+      static const int fit152[9] = {0, 0, 74, 46, 36, 28, 24, 20, 16};
       const int64_t kps = cdiv(kb, cs);
-      if (cdiv(kb, kps) != cs || tiles * cs > sms) continue;
-      const double t = kps * kb_cyc + 600.0 + 1500.0 + 128.0 * bn * 4 * (cs - 1) / (cs * 64.0);
+      if (cdiv(kb, kps) != cs || tiles * cs > sms || tiles > fit152[cs] * sms / 152) continue;
+      const double t = kps * kb_cyc + 600.0 + 3000.0 + 128.0 * bn * 4 * (cs - 1) / (cs * 16.0);
       if (t < best_t * 0.95) {
         best_t = t;
         best.bn = bn;
@@ -335,6 +349,33 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
         best.tail = 0;
         best.pair = false;
         best.csplit = static_cast<int>(cs);
+      }
+    }
+  }
+  // CTA pairs with the tail split: whole 256 x 256 tiles in full waves of
+  // sms / 2 pairs (in lockstep over K), the last partial wave's tiles cut
+  // along K into pieces added by the ordered reduction
+  if (M > 128) {
+    const int bn = 256, pairs = sms / 2;
+    const int64_t tiles = batch * cdiv(M, 256) * cdiv(N, bn);
+    const double kb_cyc = 4.0 * 0.525 * bn;
+    if (pairs > 0 && tiles > pairs && tiles % pairs) {
+      const int64_t rem = tiles % pairs;
+      for (int ts : {2, 4, 8, 13}) {
+        const int64_t kps = cdiv(kb, ts), real = cdiv(kb, kps);
+        if (real < 2) continue;
+        double t = (tiles / pairs) * (kb * kb_cyc + 600.0) +
+                   cdiv(rem * real, pairs) * (kps * kb_cyc + 128.0 * bn * 4 / 48.0 + 600.0);
+        t += 8000.0 + rem * real * 256.0 * bn * 4 / (sms * 24.0);
+        if (t < best_t * 0.97) {
+          best_t = t;
+          best.bn = bn;
+          best.splits = 1;
+          best.sk = false;
+          best.tail = ts;
+          best.pair = true;
+          best.csplit = 0;
+        }
       }
     }
   }
@@ -351,7 +392,7 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       if (cdiv(kb, kps) != s) continue;
       const int64_t waves = cdiv(tiles * s, sms / 2);
       double t = waves * (fmax(kps * kb_cyc, s > 1 ? 128.0 * bn * 4 / 48.0 : epi_cyc) + 600.0);
-      if (s > 1) t += 3000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
+      if (s > 1) t += 5000.0 + (s + 1.0) * M * N * batch * 4.0 / (sms * 24.0);
       if (t < best_t * 0.98) {
         best_t = t;
         best.bn = bn;
@@ -372,7 +413,10 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
     if (iters < sms || tiles * 4 < sms) continue;
     const double kb_cyc = kb_cycles(bn);
     const double per_cta = static_cast<double>(cdiv(iters, sms));
-    double t = per_cta * kb_cyc + 600.0 * cdiv(tiles, sms) + 2.0 * 128.0 * bn * 4 / 24.0;
+    // + the fix-up: flag waits, then the partial tile written and read back
+    // (measured: ~3 us more than the MMAs on small weight gradients)
+    double t = per_cta * kb_cyc + (600.0 + 128.0 * bn * out_bytes / 48.0) * cdiv(tiles, sms) + 6000.0 +
+               2.0 * 128.0 * bn * 4 / 16.0;
     if (t < best_t * 0.95) {
       best_t = t;
       best.bn = bn;
@@ -391,7 +435,8 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
     if (pairs > 0 && iters >= pairs && tiles * 4 >= pairs) {
       const double kb_cyc = 4.0 * fmax(125.0, 0.525 * bn);
       const double per_pair = static_cast<double>(cdiv(iters, pairs));
-      const double t = per_pair * kb_cyc + 600.0 * cdiv(tiles, pairs) + 2.0 * 128.0 * bn * 4 / 24.0;
+      const double t = per_pair * kb_cyc + (600.0 + 128.0 * bn * out_bytes / 48.0) * cdiv(tiles, pairs) + 6000.0 +
+                       2.0 * 128.0 * bn * 4 / 16.0;
       if (t < best_t * 0.95) {
         best_t = t;
         best.bn = bn;
@@ -471,6 +516,32 @@ static unsigned long long next_epoch() {
   return v ? v : ctr.fetch_add(1) + 1;
 }
 
+// The deep ring (widths 144 and 192, single CTA) when a CTA streams at least
+// 128 K blocks: its epilogues hide behind later MMAs.
+static bool plan_deep(const Plan& p, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  if (p.pair || p.csplit > 1 || (p.bn != 192 && p.bn != 144)) return false;
+  const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, p.bn);
+  const int64_t kb = cdiv(K, 64);
+  const int64_t per_cta = p.sk ? cdiv(tiles * kb, sms) : cdiv(tiles * p.splits, sms) * cdiv(kb, p.splits);
+  return per_cta >= 128;
+}
+
+// "tc nt M=.. N=.. K=.. batch=.. bn=.. [deep|pair|cs] splits=..|sk grid=..
+// [tail=AxB|cluster=C] raster=m|n table=hit|miss"
+static std::string plan_text(const Plan& p, int layout, int64_t M, int64_t N, int64_t K, int64_t batch, int sms) {
+  const TailGeo tgeo = plan_tail_geo(p, M, N, K, batch, sms);
+  char tail[48] = "";
+  if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
+  if (p.csplit > 1) snprintf(tail, sizeof tail, " cluster=%d", p.csplit);
+  char buf[256];
+  snprintf(buf, sizeof buf, "tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s",
+           layout_name(layout), (long long)M, (long long)N, (long long)K, (long long)batch, p.bn,
+           plan_deep(p, M, N, K, batch, sms) ? " deep" : (p.pair ? " pair" : (p.csplit > 1 ? " cs" : "")),
+           p.sk ? "sk grid=" : "splits=", p.sk ? sk_grid(p, M, N, K, batch, sms) : p.splits, tail,
+           p.raster_n ? 'n' : 'm', p.from_table ? "hit" : "miss");
+  return buf;
+}
+
 // -------------------------------------------------------------- the GEMMs
 static bool dtype_in_ok(tg_dtype in) { return in == TG_BF16 || in == TG_F16; }
 static bool dtype_out_ok(tg_dtype in, tg_dtype out) { return out == TG_F32 || out == in; }
@@ -547,14 +618,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.tail_splits = p.tail;
     t.pair = p.pair ? 1 : 0;
     t.csplit = p.csplit;
-    // the deep ring when a CTA streams at least 128 K blocks (its epilogues
-    // hide behind later MMAs); widths 144 and 192 only
-    {
-      const int64_t tiles = g.batch * cdiv(g.M, 128) * cdiv(g.N, p.bn);
-      const int64_t kb = cdiv(g.K, 64);
-      const int64_t per_cta = p.sk ? cdiv(tiles * kb, ctx->sms) : cdiv(tiles * p.splits, ctx->sms) * cdiv(kb, p.splits);
-      t.deep = !p.pair && (p.bn == 192 || p.bn == 144) && per_cta >= 128 ? 1 : 0;
-    }
+    t.deep = plan_deep(p, g.M, g.N, g.K, g.batch, ctx->sms) ? 1 : 0;
     t.ws = g.ws;
     t.grid = ctx->sms;
     t.stream = g.stream;
@@ -566,16 +630,8 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     if (e == cudaSuccess && !p.sk && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
                                g.stream);
-    const TailGeo tgeo = plan_tail_geo(p, g.M, g.N, g.K, g.batch, ctx->sms);
-    char tail[48] = "";
-    if (tgeo.tail_tiles > 0) snprintf(tail, sizeof tail, " tail=%dx%d", tgeo.tail_tiles, tgeo.splits);
-    if (p.csplit > 1) snprintf(tail, sizeof tail, " cluster=%d", p.csplit);
-    snprintf(buf, sizeof buf, "%s tc %s M=%lld N=%lld K=%lld batch=%lld bn=%d%s %s%d%s raster=%c table=%s %s",
-             g.name, layout_name(g.layout), (long long)g.M, (long long)g.N, (long long)g.K, (long long)g.batch,
-             p.bn, t.deep ? " deep" : (p.pair ? " pair" : (p.csplit > 1 ? " cs" : "")), p.sk ? "sk grid=" : "splits=",
-             p.sk ? sk_grid(p, g.M, g.N, g.K, g.batch, ctx->sms) : p.splits, tail, p.raster_n ? 'n' : 'm',
-             p.from_table ? "hit" : "miss", e == cudaSuccess ? "ok" : cudaGetErrorString(e));
-    record(buf);
+    record(std::string(g.name) + " " + plan_text(p, g.layout, g.M, g.N, g.K, g.batch, ctx->sms) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }
   // CUDA-core path, same semantics
@@ -667,6 +723,27 @@ const char* tg_status_string(tg_status s) {
 
 size_t tg_last_call(char* buf, size_t len) {
   const std::string& s = t_last_call;
+  if (buf && len) {
+    const size_t n = s.size() < len - 1 ? s.size() : len - 1;
+    memcpy(buf, s.data(), n);
+    buf[n] = '\0';
+  }
+  return s.size();
+}
+
+size_t tg_plan_describe(tg_op op, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
+                        int sms, char* buf, size_t len) {
+  if (op != TG_OP_GEMM_FWD && op != TG_OP_GEMM_DGRAD && op != TG_OP_GEMM_WGRAD) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0 || sms < 2 || !dtype_in_ok(in) || !dtype_out_ok(in, out)) return 0;
+  const int layout = op == TG_OP_GEMM_FWD ? LAYOUT_NT : (op == TG_OP_GEMM_DGRAD ? LAYOUT_NN : LAYOUT_TN);
+  // contiguous operands: the row pitches the tensor-core path needs
+  const int64_t lda = layout == LAYOUT_TN ? M : K, ldb = layout == LAYOUT_NT ? K : N;
+  std::string s;
+  if ((lda * 2) % 16 || (ldb * 2) % 16 || (N * static_cast<int64_t>(dt_bytes(out))) % 16 || batch > 65535) {
+    s = std::string("simt ") + layout_name(layout);
+  } else {
+    s = plan_text(make_plan(layout, M, N, K, batch, in, out, sms), layout, M, N, K, batch, sms);
+  }
   if (buf && len) {
     const size_t n = s.size() < len - 1 ? s.size() : len - 1;
     memcpy(buf, s.data(), n);

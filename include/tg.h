@@ -187,6 +187,19 @@ int tg_version(void);
  * into buf (NUL-terminated, truncated to len).  Returns the full length. */
 size_t tg_last_call(char* buf, size_t len);
 
+/* Host only (no device needed, nothing launched): writes into buf
+ * (NUL-terminated, truncated to len) the plan the tensor-core path would use
+ * for a layer product on a device with `sms` SMs -- tile width, CTA pairs /
+ * deep ring / cluster split, split count or stream-K grid, tail split, tile
+ * order, and whether the tile table or the cost model chose it -- in the
+ * format of tg_last_call, or "simt <layout>" when contiguous operands of
+ * these sizes need the CUDA-core path.  op is TG_OP_GEMM_FWD, _DGRAD or
+ * _WGRAD; M, N, K are the product's output rows, output columns and
+ * reduction length (as in the tile table).  Returns the full length, 0 for
+ * invalid arguments. */
+size_t tg_plan_describe(tg_op op, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
+                        int sms, char* buf, size_t len);
+
 /* Diagnostic of the bounded-wait mechanism every pipelined kernel uses: one
  * CTA waits on a barrier that nothing ever completes, gives up after
  * timeout_us microseconds and records a timeout in the status word, which

@@ -139,3 +139,46 @@ def test_tile_table_schedules(lib, tmp_path):
         t.write_text(bad)
         assert lib.tg_load_table(str(t).encode()) == 7, bad
     assert lib.tg_load_table(None) == 0
+
+
+def _plan(op, M, N, K, batch=1, sms=152):
+    import torch
+    return B.tg_plan_describe(op, M, N, K, batch, torch.bfloat16, torch.bfloat16, sms)
+
+
+def test_plan_describe_reports_table_entries_and_the_cuda_core_path(lib):
+    """tg_plan_describe (host only) gives the plan a call would use: a shipped
+    table entry is reported as a hit; sizes the tensor-core path cannot
+    address go to the CUDA-core path; bad arguments give an empty answer."""
+    assert lib.tg_load_table(B.DEFAULT_TABLE.encode()) == 0
+    try:
+        p = _plan(B.TG_OP_GEMM_FWD, 2048, 49152, 576)
+        assert p.startswith("tc nt M=2048 N=49152 K=576 batch=1 bn=") and "table=hit" in p, p
+        assert _plan(B.TG_OP_GEMM_FWD, 3000, 1000, 700) == "simt nt"  # K = 700: rows of 1,400 bytes
+        assert _plan(B.TG_OP_GEMM_WGRAD, 0, 576, 2048) == ""
+        assert _plan(B.TG_OP_LORA_DOWN, 2048, 576, 16) == ""
+    finally:
+        assert lib.tg_load_table(None) == 0
+
+
+@pytest.mark.parametrize("case", [
+    # (op, M, N, K, batch, must contain, must not contain): choices measured to matter
+    (2, 2304, 2304, 4096, 1, " pair", " bn=144"),   # square weight gradient: pairs, not 144-wide single CTAs
+    (0, 2048, 49152, 576, 1, "bn=256 pair", None),   # the vocabulary head forward
+    (1, 2048, 576, 1536, 1, "bn=64 splits=1", " cs"),  # a cluster split of 3 x 48 tiles would not fit at once
+    (2, 576, 576, 2048, 1, " cs ", " sk"),           # small weight gradient: cluster split, not stream-K
+    (1, 1024, 64, 1024, 36, "bn=64", None),          # 64-wide attention products: no wider tile
+    (0, 2048, 2048, 64, 36, "bn=256 splits=1", " sk"),  # one K block per tile: no stream-K
+])
+def test_cost_model_choices_without_a_table(lib, case):
+    """With no table entry, the cost model must avoid the plans measured to be
+    2x slower than the best (see the sweep's 'heuristic' column)."""
+    op, M, N, K, batch, want, avoid = case
+    assert lib.tg_load_table(b"") == 0
+    try:
+        p = _plan(op, M, N, K, batch)
+        assert "table=miss" in p and want in p, p
+        if avoid:
+            assert avoid not in p, p
+    finally:
+        assert lib.tg_load_table(None) == 0
