@@ -592,22 +592,28 @@ def measure_rows(stream, pk, budget_s=90.0):
                 X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="rows", device="cuda")
                 outs = {"fwd": torch.empty(T, d_out, dtype=dtype, device="cuda"),
                         "dgrad": torch.empty(T, d_in, dtype=dtype, device="cuda"),
-                        "wgrad": torch.empty(d_out, d_in, dtype=dtype, device="cuda")}
+                        "wgrad": torch.empty(d_out, d_in, dtype=dtype, device="cuda"),
+                        "wgrad_acc": torch.zeros(d_out, d_in, dtype=torch.float32, device="cuda")}
                 res = {}
                 ws = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
-                for op in ("fwd", "dgrad", "wgrad"):
+                # wgrad_acc: the weight gradient added into an FP32 gradient buffer
+                for op in ("fwd", "dgrad", "wgrad", "wgrad_acc"):
                     fn = {"fwd": lambda i: (lambda: tg.tg_gemm_fwd(X, W, Y=outs["fwd"], ws=ws)),
                           "dgrad": lambda i: (lambda: tg.tg_gemm_dgrad(dY, W, dX=outs["dgrad"], ws=ws)),
-                          "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws))}[op]
+                          "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws)),
+                          "wgrad_acc": lambda i: (lambda: tg.tg_gemm_wgrad_accumulate(dY, X, outs["wgrad_acc"],
+                                                                                      ws=ws))}[op]
                     ms, call = time_calls(fn)
-                    M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[op]
+                    M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T),
+                               "wgrad_acc": (d_out, d_in, T)}[op]
                     tf = workloads.flops(M, N, K) / ms / 1e9
                     res[op] = tf
                     rows.append({"set": "2B", "layer": names, "T": T, "op": op, "dtype": str(dtype)[6:],
                                  "M": M, "N": N, "K": K, "us": round(ms * 1000, 2), "tflops": round(tf, 1),
                                  "frac_of_peak": round(tf / pk["bf16_tflops"], 3), "bound": "tensor",
                                  "kernel": kernel_key(call)})
-                rows[-1]["wgrad_over_fwd"] = round(res["wgrad"] / res["fwd"], 3)
+                rows[-2]["wgrad_over_fwd"] = round(res["wgrad"] / res["fwd"], 3)
+                rows[-1]["acc_over_wgrad"] = round(res["wgrad_acc"] / res["wgrad"], 3)
                 del X, W, dY, outs
     # rank-16 LoRA, bf16, T=4096: effective HBM bandwidth
     cfg = workloads.LORA_2B

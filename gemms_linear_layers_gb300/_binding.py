@@ -34,6 +34,7 @@ SIGNATURES = {
     "tg_gemm_fwd": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_dgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_wgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_gemm_wgrad_accumulate": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _vp, _sz, _vp]),
     "tg_gemm_wgrad_noalloc": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
     "tg_lora_down": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_lora_up": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -170,6 +171,21 @@ def tg_gemm_wgrad(dY, X, dW=None, out_dtype=None, ws=None, stream=None):
     return dW
 
 
+
+def tg_gemm_wgrad_accumulate(dY, X, dW, ws=None, stream=None):
+    """dW[d_out, d_in] += dY[T, d_out]^T X[T, d_in], dW an FP32 tensor."""
+    _need(dY, "dY", 2), _need(X, "X", 2)
+    T, d_out = dY.shape
+    d_in = X.shape[1]
+    if X.shape[0] != T or X.dtype != dY.dtype:
+        raise ValueError("X must be [T, d_in] with dY's dtype")
+    if dW is None or dW.dtype != torch.float32 or tuple(dW.shape) != (d_out, d_in) or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous FP32 [d_out, d_in] tensor")
+    wp, wn, keep = _workspace(TG_OP_GEMM_WGRAD, (T, d_out, d_in, 0), _DT[dY.dtype], _DT[torch.float32], ws, dY.device)
+    _check(lib().tg_gemm_wgrad_accumulate(_ptr(dY), _ptr(X), _ptr(dW), T, d_out, d_in, _DT[dY.dtype], wp, wn,
+                                          _stream(stream)), "tg_gemm_wgrad_accumulate")
+    _keep(keep, stream)
+    return dW
 def tg_gemm_wgrad_noalloc(dY, X, dW, stream=None):
     """dW = dY^T X without any device allocation by the library (the split-K
     scratch is the library's own static array); dW must be given."""

@@ -562,6 +562,7 @@ struct GemmCall {
   size_t ws_bytes;
   cudaStream_t stream;
   const char* name;
+  int accumulate = 0;  // FP32 C: C += the product (gradient accumulation)
 };
 
 static bool tc_eligible(const GemmCall& g) {
@@ -579,6 +580,10 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     return TG_OK;
   }
   const size_t ob = dt_bytes(g.out);
+  if (g.K == 0 && g.accumulate) {  // adding an empty sum leaves C as it is
+    record(std::string(g.name) + " empty reduction: nothing to add");
+    return TG_OK;
+  }
   if (g.K == 0) {  // empty sum: zeros (all-zero bits in every output type)
     record(std::string(g.name) + " empty reduction: zero fill");
     return cudaMemsetAsync(g.C, 0, static_cast<size_t>(g.batch * g.M * g.N) * ob, g.stream) == cudaSuccess
@@ -618,6 +623,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
     t.tail_splits = p.tail;
     t.pair = p.pair ? 1 : 0;
     t.csplit = p.csplit;
+    t.accumulate = g.accumulate;
     t.deep = plan_deep(p, g.M, g.N, g.K, g.batch, ctx->sms) ? 1 : 0;
     t.ws = g.ws;
     t.grid = ctx->sms;
@@ -629,7 +635,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
                                             : tc_gemm_launch_tn(t);
     if (e == cudaSuccess && !p.sk && p.splits > 1)
       e = splitk_reduce_launch(static_cast<const float*>(g.ws), g.C, t.out_kind, g.batch, p.splits, g.M * g.N,
-                               g.stream);
+                               g.stream, g.accumulate);
     record(std::string(g.name) + " " + plan_text(p, g.layout, g.M, g.N, g.K, g.batch, ctx->sms) + " " +
            (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
@@ -647,6 +653,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
   s.N = g.N;
   s.K = g.K;
   s.stream = g.stream;
+  s.accumulate = g.accumulate;
   s.a_bs = g.a_bs;
   s.b_bs = g.b_bs;
   if (g.layout == LAYOUT_TN) {
@@ -815,6 +822,19 @@ tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int6
   TG_TRY(device_ctx(&ctx));
   GemmCall g{LAYOUT_TN, dY, X, dW, 1, d_out, d_in, T, d_out, d_in, T * d_out, T * d_in, in, out, -1, ws,
              ws_bytes, static_cast<cudaStream_t>(stream), "wgrad"};
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_gemm_wgrad_accumulate(const void* dY, const void* X, float* dW, int64_t T, int64_t d_out,
+                                   int64_t d_in, tg_dtype in, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, TG_F32, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(dW, d_out * d_in, 4));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_TN, dY, X, dW, 1, d_out, d_in, T, d_out, d_in, T * d_out, T * d_in, in, TG_F32, -1, ws,
+             ws_bytes, static_cast<cudaStream_t>(stream), "wgrad_accumulate", 1};
   return run_gemm(g, ctx);
 }
 

@@ -35,7 +35,8 @@ __device__ __forceinline__ void store_from_float(void* p, int kind, int64_t i, f
 // together (unrolled), so the reduction costs a few L2 round trips rather than
 // one per split.  bn and N are multiples of 4, so 4 columns are all inside or
 // all past N.
-__global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int out_kind, TailGeo g) {
+__global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int out_kind, TailGeo g,
+                                   int accumulate) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
@@ -59,7 +60,15 @@ __global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict
     }
     const int64_t o = (b * g.M + m) * g.N + n;
     if (out_kind == EK_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(C) + o) = v;
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(C) + o);
+      if (accumulate) {  // C += the sum of the pieces
+        const float4 c0 = *dst;
+        v.x = c0.x + v.x;
+        v.y = c0.y + v.y;
+        v.z = c0.z + v.z;
+        v.w = c0.w + v.w;
+      }
+      *dst = v;
     } else if (out_kind == EK_BF16) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
       uint2 pk;
@@ -76,16 +85,17 @@ __global__ void tail_reduce_kernel(const float* __restrict__ P, void* __restrict
   }
 }
 
-cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream) {
+cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream,
+                               int accumulate) {
   if (t.tail_tiles == 0) return cudaSuccess;
   const int per4 = t.bm * t.bn / 4;
   return launch_k(tail_reduce_kernel, dim3((per4 + 255) / 256, t.tail_tiles), dim3(256), 0, stream, P, C, out_kind,
-                  t);
+                  t, accumulate);
 }
 
 // ---------------------------------------------------------------- split-K
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restrict__ C, int out_kind,
-                                     int64_t batch, int64_t splits, int64_t MN) {
+                                     int64_t batch, int64_t splits, int64_t MN, int accumulate) {
   pdl_wait();
   pdl_trigger();
   const int64_t n4 = MN / 4;  // MN is a multiple of 4 on the tensor-core path
@@ -106,7 +116,15 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restr
     }
     const int64_t o = b * MN + i4 * 4;
     if (out_kind == EK_F32) {
-      reinterpret_cast<float4*>(C)[o / 4] = s;
+      float4* dst = reinterpret_cast<float4*>(C) + o / 4;
+      if (accumulate) {  // C += the sum of the splits
+        const float4 c0 = *dst;
+        s.x = c0.x + s.x;
+        s.y = c0.y + s.y;
+        s.z = c0.z + s.z;
+        s.w = c0.w + s.w;
+      }
+      *dst = s;
     } else if (out_kind == EK_BF16) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
       uint2 pk;
@@ -124,7 +142,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, void* __restr
 }
 
 cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t batch, int64_t splits,
-                                 int64_t MN, cudaStream_t stream) {
+                                 int64_t MN, cudaStream_t stream, int accumulate) {
   const int64_t total = batch * (MN / 4);
   if (total <= 0) return cudaSuccess;
   int dev = 0, sms = 148;
@@ -134,7 +152,7 @@ cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   if (blocks > cap) blocks = cap;
   return launch_k(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, ws, C, out_kind,
-                  batch, splits, MN);
+                  batch, splits, MN, accumulate);
 }
 
 // ---------------------------------------------------------------- strided
@@ -163,7 +181,11 @@ __global__ void simt_gemm_kernel(SimtGemm g) {
     for (int kk = 0; kk < ST; ++kk) acc = fmaf(As[threadIdx.y][kk], Bs[kk][threadIdx.x], acc);
     __syncthreads();
   }
-  if (i < g.M && j < g.N) store_from_float(g.C, g.out_kind, (b * g.M + i) * g.N + j, acc);
+  if (i < g.M && j < g.N) {
+    const int64_t o = (b * g.M + i) * g.N + j;
+    if (g.accumulate && g.out_kind == EK_F32) acc = static_cast<const float*>(g.C)[o] + acc;  // C += the product
+    store_from_float(g.C, g.out_kind, o, acc);
+  }
 }
 
 cudaError_t simt_gemm_launch(const SimtGemm& g) {

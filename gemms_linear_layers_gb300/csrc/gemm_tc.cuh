@@ -94,6 +94,7 @@ struct TcArgs {
   unsigned long long timeout_ns;
   unsigned int* status;
   unsigned long long* trace;  // event timestamps per CTA (only in -DTG_TRACE builds)
+  int accumulate;             // FP32 output: the tile writer adds its tile into C (C += A B)
 };
 
 #ifdef TG_TRACE
@@ -618,7 +619,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
+            if (!OUT16 && args.accumulate)
+              tma_reduce_add_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
+            else
+              tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, c.m0 + q * 32, zc);
             bulk_commit();
           }
           ++nstore;
@@ -654,7 +658,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmC2, smem_u32(buf), c.n0 + NCH * CW, c.m0 + q * 32, zc);
+            if (!OUT16 && args.accumulate)
+              tma_reduce_add_3d(&tmC2, smem_u32(buf), c.n0 + NCH * CW, c.m0 + q * 32, zc);
+            else
+              tma_store_3d(&tmC2, smem_u32(buf), c.n0 + NCH * CW, c.m0 + q * 32, zc);
             bulk_commit();
           }
           ++nstore;

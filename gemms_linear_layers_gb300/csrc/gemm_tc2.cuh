@@ -527,7 +527,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, row0, c.zc);
+          if (!OUT16 && args.accumulate)
+            tma_reduce_add_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, row0, c.zc);
+          else
+            tma_store_3d(&tmC, smem_u32(buf), c.n0 + ch * CW, row0, c.zc);
           bulk_commit();
         }
         TG_WAIT_END(w_fs, wfs);

@@ -53,6 +53,7 @@ struct CsArgs {
   int a_chunked, b_chunked;
   void* C;  // [batch][M][N], row-major
   long long M, N;
+  int accumulate;  // FP32 output: C += the product
   unsigned long long timeout_ns;
   unsigned int* status;
   unsigned long long* trace;  // event timestamps per CTA (only in -DTG_TRACE builds)
@@ -296,7 +297,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           *reinterpret_cast<uint2*>(static_cast<uint16_t*>(args.C) + o) = pk;
         } else {
-          *reinterpret_cast<float4*>(static_cast<float*>(args.C) + o) = v;
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.C) + o);
+          if (args.accumulate) {
+            const float4 c0 = *dst;  // this thread alone writes these four elements
+            v.x = c0.x + v.x;
+            v.y = c0.y + v.y;
+            v.z = c0.z + v.z;
+            v.w = c0.w + v.w;
+          }
+          *dst = v;
         }
       }
     }

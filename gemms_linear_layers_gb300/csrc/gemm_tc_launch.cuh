@@ -112,6 +112,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
 #ifdef TG_TRACE
   if (const char* e = getenv("TG_TRACE_ADDR")) a.trace = reinterpret_cast<unsigned long long*>(strtoull(e, nullptr, 0));
 #endif
+  a.accumulate = g.accumulate && !split_parts ? 1 : 0;  // split partials: the reduction adds into C
   int grid = g.grid < a.units ? g.grid : a.units;
   if (g.sk) {
     // every CTA gets at least one iteration; the workspace holds grid slots
@@ -122,7 +123,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   }
   cudaError_t e2 = launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, tmC2, tmP, a);
   if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
-  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream);
+  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream, g.accumulate);
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM, persistent over
@@ -227,6 +228,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   }
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
+  a.accumulate = g.accumulate && !split_parts ? 1 : 0;  // split partials: the reduction adds into C
   a.sk = g.sk;
   a.sk_iters = static_cast<long long>(a.units) * a.kb_total;
   a.sk_epoch = g.sk_epoch;
@@ -248,7 +250,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   cudaError_t e2 = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmP, a);
   if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
-  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream);
+  return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream, g.accumulate);
 }
 
 template <bool A_MN, bool B_MN>
@@ -321,6 +323,7 @@ static cudaError_t tcs_launch_one(const TcGemm& g) {
   a.C = g.C;
   a.M = static_cast<long long>(M);
   a.N = static_cast<long long>(N);
+  a.accumulate = g.accumulate;
   a.timeout_ns = g.timeout_ns;
   a.status = g.status;
   a.trace = nullptr;

@@ -125,6 +125,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// element-wise add of a shared-memory tile into global memory (the tensor
+// map's type, here FP32), completed through the bulk group like a store;
+// each element receives one addition per call
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

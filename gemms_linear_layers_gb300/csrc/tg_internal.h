@@ -77,6 +77,7 @@ struct TcGemm {
   int deep;                   // 1: widths 144/192 with a fifth operand stage (one epilogue buffer)
   int pair;                   // 1: CTA-pair kernel, 256 x bn tiles (bn 128, 192 or 256)
   int csplit;                 // > 1: split-K across the CTAs of a cluster, added on chip (bn 64..256)
+  int accumulate;             // FP32 C only: C += the product (gradient accumulation)
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
@@ -149,7 +150,9 @@ __host__ __device__ inline void tile_origin(int t, int m_tiles, int n_tiles, int
     *n0 = (r / m_tiles) * bn;
   }
 }
-cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream);
+// accumulate (FP32 C only): C += the sum instead of C = the sum
+cudaError_t tail_reduce_launch(const float* P, void* C, int out_kind, const TailGeo& t, cudaStream_t stream,
+                               int accumulate);
 
 // per-layout launchers (gemm_tc_{nt,nn,tn}.cu)
 cudaError_t tc_gemm_launch_nt(const TcGemm& g);
@@ -157,8 +160,9 @@ cudaError_t tc_gemm_launch_nn(const TcGemm& g);
 cudaError_t tc_gemm_launch_tn(const TcGemm& g);
 
 // FP32 split partials ws[b*splits + s][M][N] -> C[b][M][N], s ascending
+// (accumulate, FP32 C only: C += the sum)
 cudaError_t splitk_reduce_launch(const float* ws, void* C, int out_kind, int64_t batch,
-                                 int64_t splits, int64_t MN, cudaStream_t stream);
+                                 int64_t splits, int64_t MN, cudaStream_t stream, int accumulate);
 
 // Plain strided GEMM on CUDA cores for shapes the tensor-core path cannot take
 // (row pitches that are not 16-byte multiples, unaligned pointers, FP32 operands).
@@ -170,6 +174,7 @@ struct SimtGemm {
   int a_kind, b_kind, out_kind;
   int64_t batch, M, N, K;
   int64_t a_bs, a_rs, a_cs, b_bs, b_rs, b_cs;
+  int accumulate;  // FP32 C: C += the product
   cudaStream_t stream;
 };
 cudaError_t simt_gemm_launch(const SimtGemm& g);

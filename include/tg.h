@@ -126,6 +126,18 @@ tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int6
 tg_status tg_gemm_wgrad_noalloc(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out,
                                 int64_t d_in, tg_dtype in, tg_dtype out, void* stream);
 
+/* Weight gradient added into an FP32 gradient buffer (gradient accumulation
+ * over micro-batches, a "main grad" kept in FP32 beside 16-bit weights):
+ *   dW[d_out, d_in] += dY[T, d_out]^T . X[T, d_in]          (dW FP32)
+ * Same products, plans and kernels as tg_gemm_wgrad with out = TG_F32 (and
+ * the same workspace, tg_workspace_size(TG_OP_GEMM_WGRAD, ..., TG_F32));
+ * every element of dW receives exactly one FP32 addition of its FP32
+ * product, so repeated calls are bitwise reproducible.  T = 0 leaves dW
+ * unchanged.  16-bit dW is not offered: a rounded product added to a
+ * rounded sum would round twice. */
+tg_status tg_gemm_wgrad_accumulate(const void* dY, const void* X, float* dW, int64_t T, int64_t d_out,
+                                   int64_t d_in, tg_dtype in, void* ws, size_t ws_bytes, void* stream);
+
 /* Rank-r LoRA down projection ("Tuning the kernels": the rank-16 LoRA matrices):
  *   H[T, r] = X[T, d_in] . A[r, d_in]^T
  * r = 16 takes the streaming kernel (X read once); other ranks are supported
