@@ -637,6 +637,9 @@ def measure_rows(stream, pk, budget_s=90.0):
              (T * d_in + r * d_in + T * r) * 2, 2 * T * d_in * r),
             ("up", lambda i: (lambda: tg.tg_lora_up(data[i][3], data[i][2], Y=Ys[i])),
              (T * r + d_out * r + T * d_out) * 2, 2 * T * d_out * r),
+            # the branch added into the base output: Y read and written
+            ("up_add", lambda i: (lambda: tg.tg_lora_up_add(data[i][3], data[i][2], Ys[i], 2.0)),
+             (T * r + d_out * r + 2 * T * d_out) * 2, 2 * T * d_out * r),
             # reads dY, X, H, A, B; writes dX, dA, dB
             ("grad", lambda i: (lambda: tg.tg_lora_grad(*data[i], outs=grads[i], ws=wss[i])),
              (T * d_out + 2 * T * d_in + T * r + 2 * r * d_in + 2 * d_out * r) * 2,

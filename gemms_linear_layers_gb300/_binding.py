@@ -38,6 +38,7 @@ SIGNATURES = {
     "tg_gemm_wgrad_noalloc": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
     "tg_lora_down": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_lora_up": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_lora_up_add": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
                           _vp, _sz, _vp]),
     "tg_bmm_attn": (_i, [_i, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -229,6 +230,21 @@ def tg_lora_up(H, B, Y=None, out_dtype=None, ws=None, stream=None):
     return Y
 
 
+
+def tg_lora_up_add(H, B, Y, scale, ws=None, stream=None):
+    """Y[T, d_out] += scale * H[T, r] B[d_out, r]^T (one rounding to Y's type)."""
+    _need(H, "H", 2), _need(B, "B", 2)
+    T, r = H.shape
+    d_out = B.shape[0]
+    if B.shape[1] != r or B.dtype != H.dtype:
+        raise ValueError("B must be [d_out, r] with H's dtype")
+    if Y is None or tuple(Y.shape) != (T, d_out) or not Y.is_contiguous():
+        raise ValueError("Y must be a contiguous [T, d_out] tensor")
+    wp, wn, keep = _workspace(TG_OP_LORA_UP, (T, d_out, r, 0), _DT[H.dtype], _DT[Y.dtype], ws, H.device)
+    _check(lib().tg_lora_up_add(_ptr(H), _ptr(B), _ptr(Y), T, d_out, r, float(scale), _DT[H.dtype], _DT[Y.dtype],
+                                wp, wn, _stream(stream)), "tg_lora_up_add")
+    _keep(keep, stream)
+    return Y
 def tg_lora_grad(X, A, B, H, dY, out_dtype=None, want_dH=False, outs=None, ws=None, stream=None):
     """Gradients of Y = (X A^T) B^T: returns dict dA, dB, dX (and dH in FP32 when asked)."""
     for t, n in ((X, "X"), (A, "A"), (B, "B"), (H, "H"), (dY, "dY")):

@@ -562,11 +562,15 @@ struct GemmCall {
   size_t ws_bytes;
   cudaStream_t stream;
   const char* name;
-  int accumulate = 0;  // FP32 C: C += the product (gradient accumulation)
+  int accumulate = 0;  // C += scale * the product (gradient accumulation, LoRA branch added to Y)
+  float scale = 1.f;
 };
 
 static bool tc_eligible(const GemmCall& g) {
   if (g.a_kind_override >= 0) return false;
+  // the tensor-core epilogues add only an unscaled FP32 tile (a 16-bit
+  // reduce-add would round twice)
+  if (g.accumulate && (g.out != TG_F32 || g.scale != 1.f)) return false;
   const size_t ob = dt_bytes(g.out);
   return aligned(g.A, 16) && aligned(g.B, 16) && aligned(g.C, 16) && (g.lda * 2) % 16 == 0 &&
          (g.ldb * 2) % 16 == 0 && (g.a_bs * 2) % 16 == 0 && (g.b_bs * 2) % 16 == 0 &&
@@ -654,6 +658,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
   s.K = g.K;
   s.stream = g.stream;
   s.accumulate = g.accumulate;
+  s.scale = g.scale;
   s.a_bs = g.a_bs;
   s.b_bs = g.b_bs;
   if (g.layout == LAYOUT_TN) {
@@ -953,6 +958,42 @@ tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d
   }
   GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, ws, ws_bytes, st,
              "lora_up"};
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_lora_up_add(const void* H, const void* B, void* Y, int64_t T, int64_t d_out, int64_t r, float scale,
+                         tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, r}));
+  if (!std::isfinite(scale)) return TG_ERR_INVALID_ARG;
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(B, d_out * r, 2));
+  TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_out > 0 && lora_stream_ok(r, {d_out}, {H, B, Y})) {
+    LoraArgs a{};
+    a.H = H;
+    a.B = B;
+    a.out = Y;
+    a.T = T;
+    a.d_out = d_out;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
+    a.add = 1;
+    a.scale = scale;
+    cudaError_t e = lora_up_launch(a);
+    record(std::string("lora_up_add stream T=") + std::to_string(T) + " d_out=" + std::to_string(d_out) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, ws, ws_bytes, st,
+             "lora_up_add", 1, scale};
   return run_gemm(g, ctx);
 }
 

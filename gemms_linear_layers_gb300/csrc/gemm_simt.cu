@@ -183,7 +183,7 @@ __global__ void simt_gemm_kernel(SimtGemm g) {
   }
   if (i < g.M && j < g.N) {
     const int64_t o = (b * g.M + i) * g.N + j;
-    if (g.accumulate && g.out_kind == EK_F32) acc = static_cast<const float*>(g.C)[o] + acc;  // C += the product
+    if (g.accumulate) acc = fmaf(g.scale, acc, load_as_float(g.C, g.out_kind, o));  // C += scale * the product
     store_from_float(g.C, g.out_kind, o, acc);
   }
 }

@@ -135,6 +135,28 @@ __device__ __forceinline__ void store8(void* out, int kind, size_t i, const floa
   }
 }
 
+// the 8 consecutive outputs at i, as FP32 (exact: every 16-bit value is one)
+__device__ __forceinline__ void load8(const void* out, int kind, size_t i, float* v) {
+  if (kind == EK_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(out) + i);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + i);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (kind == EK_BF16) {
+        v[2 * k] = __uint_as_float(u[k] << 16);
+        v[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+      } else {
+        v[2 * k] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] & 0xFFFFu)));
+        v[2 * k + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(u[k] >> 16)));
+      }
+    }
+  }
+}
+
 // Producer epilogue after an aborted wait: let every copy already issued
 // land before the CTA unwinds (bounded, without the abort short-cut).
 __device__ __forceinline__ void drain_issued(const uint64_t* full, const int* issued, int stages,
@@ -654,7 +676,20 @@ struct RuArgs {
   void* out;
   int out_kind;
   int T, J, n_t;
+  int add;      // out += scale * H S2^T (one rounding, in FP32) instead of out = H S2^T
+  float scale;
 };
+
+// out[i .. i+8) = v, or out += scale * v
+__device__ __forceinline__ void put8(const RuArgs& a, size_t i, float* v) {
+  if (a.add) {
+    float o[8];
+    load8(a.out, a.out_kind, i, o);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = fmaf(a.scale, v[k], o[k]);
+  }
+  store8(a.out, a.out_kind, i, v);
+}
 
 template <bool BF16>
 __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
@@ -701,14 +736,14 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
           v[2 * jb] = acc[jb][0];
           v[2 * jb + 1] = acc[jb][1];
         }
-        if (ra < T) store8(a.out, a.out_kind, static_cast<size_t>(ra) * J + j0 + 8 * c, v);
+        if (ra < T) put8(a, static_cast<size_t>(ra) * J + j0 + 8 * c, v);
         if (rb < T) {
 #pragma unroll
           for (int jb = 0; jb < 4; ++jb) {
             v[2 * jb] = acc[jb][2];
             v[2 * jb + 1] = acc[jb][3];
           }
-          store8(a.out, a.out_kind, static_cast<size_t>(rb) * J + j0 + 8 * c, v);
+          put8(a, static_cast<size_t>(rb) * J + j0 + 8 * c, v);
         }
       }
     }
@@ -951,6 +986,8 @@ cudaError_t lora_up_launch(const LoraArgs& a) {
   ru.T = static_cast<int>(a.T);
   ru.J = static_cast<int>(a.d_out);
   ru.n_t = rowup_nt(a.T, a.d_out, 4 * a.num_sms);
+  ru.add = a.add;
+  ru.scale = a.scale;
   return launch_k(a.in_kind == EK_BF16 ? lora_up_kernel<true> : lora_up_kernel<false>, dim3(nj, ru.n_t),
                   dim3(256), 0, a.stream, ru);
 }

@@ -174,7 +174,8 @@ struct SimtGemm {
   int a_kind, b_kind, out_kind;
   int64_t batch, M, N, K;
   int64_t a_bs, a_rs, a_cs, b_bs, b_rs, b_cs;
-  int accumulate;  // FP32 C: C += the product
+  int accumulate;  // C += scale * the product (FP32 arithmetic, one rounding to C's type)
+  float scale;
   cudaStream_t stream;
 };
 cudaError_t simt_gemm_launch(const SimtGemm& g);
@@ -204,6 +205,8 @@ struct LoraArgs {
   cudaStream_t stream;
   unsigned int* status;          // device status word (bounded waits report here)
   unsigned long long timeout_ns; // limit of every wait on an mbarrier
+  int add;                       // up projection: out += scale * H B^T
+  float scale;
 };
 size_t lora_down_ws_bytes(int64_t T, int64_t d_in, int64_t r, int num_sms);
 cudaError_t lora_down_launch(const LoraArgs& a);

@@ -150,6 +150,16 @@ tg_status tg_lora_down(const void* X, const void* A, void* H, int64_t T, int64_t
 tg_status tg_lora_up(const void* H, const void* B, void* Y, int64_t T, int64_t d_out, int64_t r,
                      tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
 
+/* The LoRA branch added into the base layer's output with its scale (the
+ * usual alpha / r), one rounding to Y's type:
+ *   Y[T, d_out] += scale . H[T, r] . B[d_out, r]^T
+ * Same kernels as tg_lora_up (r = 16: the streaming kernel, which reads Y's
+ * 8-element groups, adds in FP32 and writes them back; other ranks: the
+ * CUDA-core path).  scale must be finite (TG_ERR_INVALID_ARG otherwise);
+ * r = 0 leaves Y unchanged.  Workspace as tg_lora_up. */
+tg_status tg_lora_up_add(const void* H, const void* B, void* Y, int64_t T, int64_t d_out, int64_t r, float scale,
+                         tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+
 /* Gradients of the LoRA branch Y = (X A^T) B^T given dY:
  *   dH[T, r]     = dY . B          (kept in FP32; written to dH_f32 when non-NULL)
  *   dB[d_out, r] = dY^T . H

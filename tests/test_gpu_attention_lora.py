@@ -108,3 +108,32 @@ def test_lora_grad_deterministic():
     b = tg.tg_lora_grad(*t, out_dtype=torch.float32, want_dH=True)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", [(256, 192, 16, 2.0), (130, 136, 16, -0.5), (4096, 2304, 16, 0.125),
+                                  (64, 64, 8, 2.0), (33, 40, 4, 1.0)], ids=lambda c: "x".join(map(str, c)))
+def test_lora_up_add_into_the_base_output(case, dtype, out_kind):
+    """Y += scale H B^T: the LoRA branch added into the base layer's output
+    (one rounding to Y's type).  Rank 16 takes the streaming kernel, other
+    ranks the CUDA-core path."""
+    import numpy as np
+    T, d_out, r, scale = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    _, _, B, H, _ = inputs.lora_inputs(T, 64, d_out, r, dtype, tag="upadd")
+    Y0 = inputs.normal((T, d_out), 0.05, out_dtype, 555)  # the base layer's output
+    Hc, Bc = H.cuda(), B.cuda()
+    outs = []
+    for _ in range(2):  # the same start twice: the same bits
+        Y = Y0.cuda()
+        tg.tg_lora_up_add(Hc, Bc, Y, scale)
+        outs.append(Y)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    assert ("lora_up_add stream" in call) == (r == 16), call
+    C, S = oracle.lora_up(H, B)
+    base = Y0.double().numpy()
+    assert_close(outs[0], base + scale * C, np.abs(base) + abs(scale) * S, f"lora_up_add {T}x{d_out} r={r} [{call}]",
+                 out_dtype)
