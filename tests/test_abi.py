@@ -82,6 +82,20 @@ def test_lora_and_attention_reject_bad_arguments(lib):
     assert lib.tg_workspace_size(0, -8, 8, 8, 0, B.TG_BF16, B.TG_F32) == B.SIZE_MAX
 
 
+def test_accumulating_entry_points_reject_bad_arguments(lib):
+    """Both are checked before any device work: the accumulating weight
+    gradient takes 16-bit operands and an aligned FP32 buffer; the LoRA
+    up-add takes a finite scale."""
+    f = lib.tg_gemm_wgrad_accumulate
+    assert f(EVEN, EVEN, EVEN, 8, -8, 8, B.TG_BF16, NULL, 0, NULL) == 1
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, NULL, 0, NULL) == 2
+    assert f(EVEN, EVEN, ctypes.c_void_p(0x1002), 8, 8, 8, B.TG_BF16, NULL, 0, NULL) == 3  # dW not 4-aligned
+    g = lib.tg_lora_up_add
+    assert g(EVEN, EVEN, EVEN, 8, 8, 16, float("nan"), B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert g(EVEN, EVEN, EVEN, 8, 8, 16, float("inf"), B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert g(EVEN, EVEN, EVEN, 8, 8, 16, 2.0, B.TG_BF16, B.TG_F16, NULL, 0, NULL) == 2
+
+
 def test_tile_table_reader(lib, tmp_path):
     good = tmp_path / "t.txt"
     good.write_text("# op in out M N K batch bn splits\n"
