@@ -135,15 +135,26 @@ __device__ __forceinline__ void store8(void* out, int kind, size_t i, const floa
   }
 }
 
-// the 8 consecutive outputs at i, as FP32 (exact: every 16-bit value is one)
-__device__ __forceinline__ void load8(const void* out, int kind, size_t i, float* v) {
+// the bits of the 8 consecutive outputs at i: two 16-byte words for FP32,
+// one (w[0]) for the 16-bit kinds
+__device__ __forceinline__ void load8_raw(const void* out, int kind, size_t i, uint4* w) {
   if (kind == EK_F32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(out) + i);
-    const float4 a = p[0], b = p[1];
-    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(out) + i);
+    w[0] = p[0];
+    w[1] = p[1];
   } else {
-    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + i);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    w[0] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + i);
+  }
+}
+
+// those 8 outputs as FP32 (exact: every 16-bit value is one)
+__device__ __forceinline__ void raw8_to_float(int kind, const uint4* w, float* v) {
+  if (kind == EK_F32) {
+    const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(u[k]);
+  } else {
+    const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (kind == EK_BF16) {
@@ -680,18 +691,23 @@ struct RuArgs {
   float scale;
 };
 
-// out[i .. i+8) = v, or out += scale * v
-__device__ __forceinline__ void put8(const RuArgs& a, size_t i, float* v) {
-  if (a.add) {
+// out[i .. i+8) = v, or (ADD) out = old + scale * v with old the bits read
+// earlier from the same place
+template <bool ADD>
+__device__ __forceinline__ void put8(const RuArgs& a, size_t i, float* v, const uint4* old) {
+  if (ADD) {
     float o[8];
-    load8(a.out, a.out_kind, i, o);
+    raw8_to_float(a.out_kind, old, o);
 #pragma unroll
     for (int k = 0; k < 8; ++k) v[k] = fmaf(a.scale, v[k], o[k]);
   }
   store8(a.out, a.out_kind, i, v);
 }
 
-template <bool BF16>
+// ADD: the old outputs of the RU_PRE blocks are read together with their Hm
+// fragments, so that every thread has all of its reads in flight at once
+// instead of one 16-byte read ahead of each store.
+template <bool BF16, bool ADD>
 __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int J = a.J, T = a.T;
@@ -710,12 +726,17 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
   const int nblk = (T + 15) / 16;
   for (int blk0 = cta_t; blk0 < nblk; blk0 += RU_PRE * a.n_t) {
     uint2 ha[RU_PRE], hb[RU_PRE];
+    uint4 oa[ADD ? RU_PRE : 1][2], ob[ADD ? RU_PRE : 1][2];
 #pragma unroll
     for (int u = 0; u < RU_PRE; ++u) {
       const int ra = (blk0 + u * a.n_t) * 16 + g, rb = ra + 8;
       const uint2 z = make_uint2(0u, 0u);
       ha[u] = ra < T ? ld8(a.H + static_cast<size_t>(ra) * LR + 4 * c) : z;
       hb[u] = rb < T ? ld8(a.H + static_cast<size_t>(rb) * LR + 4 * c) : z;
+      if (ADD && colv) {
+        if (ra < T) load8_raw(a.out, a.out_kind, static_cast<size_t>(ra) * J + j0 + 8 * c, oa[u]);
+        if (rb < T) load8_raw(a.out, a.out_kind, static_cast<size_t>(rb) * J + j0 + 8 * c, ob[u]);
+      }
     }
 #pragma unroll
     for (int u = 0; u < RU_PRE; ++u) {
@@ -736,14 +757,14 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
           v[2 * jb] = acc[jb][0];
           v[2 * jb + 1] = acc[jb][1];
         }
-        if (ra < T) put8(a, static_cast<size_t>(ra) * J + j0 + 8 * c, v);
+        if (ra < T) put8<ADD>(a, static_cast<size_t>(ra) * J + j0 + 8 * c, v, oa[ADD ? u : 0]);
         if (rb < T) {
 #pragma unroll
           for (int jb = 0; jb < 4; ++jb) {
             v[2 * jb] = acc[jb][2];
             v[2 * jb + 1] = acc[jb][3];
           }
-          put8(a, static_cast<size_t>(rb) * J + j0 + 8 * c, v);
+          put8<ADD>(a, static_cast<size_t>(rb) * J + j0 + 8 * c, v, ob[ADD ? u : 0]);
         }
       }
     }
@@ -772,11 +793,11 @@ __global__ void __launch_bounds__(LGROUP, 1) lora_down_kernel(const __grid_const
 }
 
 // Y = H B^T
-template <bool BF16>
+template <bool BF16, bool ADD>
 __global__ void __launch_bounds__(256) lora_up_kernel(const RuArgs a) {
   pdl_wait();
   pdl_trigger();
-  rowup_role<BF16>(blockIdx.x, blockIdx.y, a);
+  rowup_role<BF16, ADD>(blockIdx.x, blockIdx.y, a);
 }
 
 // Pass 1 over dY, two roles per CTA (threads 0..287 and 288..575):
@@ -985,11 +1006,14 @@ cudaError_t lora_up_launch(const LoraArgs& a) {
   ru.out_kind = a.out_kind;
   ru.T = static_cast<int>(a.T);
   ru.J = static_cast<int>(a.d_out);
-  ru.n_t = rowup_nt(a.T, a.d_out, 4 * a.num_sms);
+  // one wave: 4 CTAs per SM fit the plain kernel's registers, 2 the adding one's
+  ru.n_t = rowup_nt(a.T, a.d_out, (a.add ? 2 : 4) * a.num_sms);
   ru.add = a.add;
   ru.scale = a.scale;
-  return launch_k(a.in_kind == EK_BF16 ? lora_up_kernel<true> : lora_up_kernel<false>, dim3(nj, ru.n_t),
-                  dim3(256), 0, a.stream, ru);
+  const bool bf = a.in_kind == EK_BF16;
+  auto k = a.add ? (bf ? lora_up_kernel<true, true> : lora_up_kernel<false, true>)
+                 : (bf ? lora_up_kernel<true, false> : lora_up_kernel<false, false>);
+  return launch_k(k, dim3(nj, ru.n_t), dim3(256), 0, a.stream, ru);
 }
 
 // ---- gradient: plans and workspace
