@@ -645,6 +645,12 @@ def measure_rows(stream, pk, budget_s=90.0):
             ("grad", lambda i: (lambda: tg.tg_lora_grad(*data[i], outs=grads[i], ws=wss[i])),
              (T * d_out + 2 * T * d_in + T * r + 2 * r * d_in + 2 * d_out * r) * 2,
              4 * T * r * (d_in + d_out)),
+            # the same with dX added into the base layer's input gradient: dX also read
+            ("grad_add", lambda i: (lambda: tg.tg_lora_grad_add(*data[i], grads[i]["dX"], 2.0,
+                                                                 outs={"dA": grads[i]["dA"], "dB": grads[i]["dB"]},
+                                                                 ws=wss[i])),
+             (T * d_out + 3 * T * d_in + T * r + 2 * r * d_in + 2 * d_out * r) * 2,
+             4 * T * r * (d_in + d_out)),
         ]
         for op, fn, nbytes, fl in specs:
             ms, call = time_calls(fn, reps=max(10, sets * 2), sets=sets)

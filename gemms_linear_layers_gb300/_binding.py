@@ -41,6 +41,8 @@ SIGNATURES = {
     "tg_lora_up_add": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
                           _vp, _sz, _vp]),
+    "tg_lora_grad_add": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float,
+                              _i, _i, _vp, _sz, _vp]),
     "tg_bmm_attn": (_i, [_i, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_workspace_size": (_sz, [_i, _i64, _i64, _i64, _i64, _i, _i]),
     "tg_stream_status": (_i, [_vp]),
@@ -264,6 +266,37 @@ def tg_lora_grad(X, A, B, H, dY, out_dtype=None, want_dH=False, outs=None, ws=No
     wp, wn, keep = _workspace(TG_OP_LORA_GRAD, (T, d_in, d_out, r), din, _DT[od], ws, X.device)
     _check(lib().tg_lora_grad(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(dY), _ptr(dA), _ptr(dB), _ptr(dX),
                               _ptr(dH), T, d_in, d_out, r, din, _DT[od], wp, wn, _stream(stream)), "tg_lora_grad")
+    _keep(keep, stream)
+    res = {"dA": dA, "dB": dB, "dX": dX}
+    if dH is not None:
+        res["dH"] = dH
+    return res
+
+
+def tg_lora_grad_add(X, A, B, H, dY, dX, scale, want_dH=False, outs=None, ws=None, stream=None):
+    """Gradients of Y = X W^T + scale (X A^T) B^T with the LoRA part added into
+    dX (the base layer's dgrad on entry): returns dict dA, dB (scaled), dX (the
+    same tensor, updated) and dH (FP32, unscaled) when asked.  dA and dB take
+    dX's dtype."""
+    for t, n in ((X, "X"), (A, "A"), (B, "B"), (H, "H"), (dY, "dY")):
+        _need(t, n, 2)
+    T, d_in = X.shape
+    r = A.shape[0]
+    d_out = B.shape[0]
+    if A.shape[1] != d_in or B.shape[1] != r or H.shape != (T, r) or dY.shape != (T, d_out):
+        raise ValueError("inconsistent LoRA shapes")
+    if dX is None or tuple(dX.shape) != (T, d_in) or not dX.is_contiguous():
+        raise ValueError("dX must be a contiguous [T, d_in] tensor")
+    od = dX.dtype
+    outs = dict(outs or {})
+    dA = _out(outs.get("dA"), (r, d_in), od, X.device, "dA")
+    dB = _out(outs.get("dB"), (d_out, r), od, X.device, "dB")
+    dH = _out(outs.get("dH"), (T, r), torch.float32, X.device, "dH") if (want_dH or "dH" in outs) else None
+    din = _DT[X.dtype]
+    wp, wn, keep = _workspace(TG_OP_LORA_GRAD, (T, d_in, d_out, r), din, _DT[od], ws, X.device)
+    _check(lib().tg_lora_grad_add(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(dY), _ptr(dA), _ptr(dB), _ptr(dX),
+                                  _ptr(dH), T, d_in, d_out, r, float(scale), din, _DT[od], wp, wn, _stream(stream)),
+           "tg_lora_grad_add")
     _keep(keep, stream)
     res = {"dA": dA, "dB": dB, "dX": dX}
     if dH is not None:

@@ -563,14 +563,14 @@ struct GemmCall {
   cudaStream_t stream;
   const char* name;
   int accumulate = 0;  // C += scale * the product (gradient accumulation, LoRA branch added to Y)
-  float scale = 1.f;
+  float scale = 1.f;   // without accumulate: C = scale * the product (scaled LoRA gradients)
 };
 
 static bool tc_eligible(const GemmCall& g) {
   if (g.a_kind_override >= 0) return false;
-  // the tensor-core epilogues add only an unscaled FP32 tile (a 16-bit
-  // reduce-add would round twice)
-  if (g.accumulate && (g.out != TG_F32 || g.scale != 1.f)) return false;
+  // the tensor-core epilogues neither scale nor add anything but an
+  // unscaled FP32 tile (a 16-bit reduce-add would round twice)
+  if (g.scale != 1.f || (g.accumulate && g.out != TG_F32)) return false;
   const size_t ob = dt_bytes(g.out);
   return aligned(g.A, 16) && aligned(g.B, 16) && aligned(g.C, 16) && (g.lda * 2) % 16 == 0 &&
          (g.ldb * 2) % 16 == 0 && (g.a_bs * 2) % 16 == 0 && (g.b_bs * 2) % 16 == 0 &&
@@ -1008,10 +1008,14 @@ static size_t lora_grad_generic_ws(int64_t T, int64_t d_in, int64_t d_out, int64
   return dh + (a > b ? a : b);
 }
 
-tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
-                       void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
-                       tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+// add = 0: the plain gradients; add = 1: dX += scale dH A, dA and dB scaled
+static tg_status lora_grad_impl(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
+                                void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
+                                tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream, int add,
+                                float scale) {
+  const std::string name = add ? "lora_grad_add" : "lora_grad";
   TG_TRY(check_common(in, out, {T, d_in, d_out, r}));
+  if (!std::isfinite(scale)) return TG_ERR_INVALID_ARG;
   TG_TRY(check_ptr(X, T * d_in, 2));
   TG_TRY(check_ptr(A, r * d_in, 2));
   TG_TRY(check_ptr(B, d_out * r, 2));
@@ -1027,7 +1031,7 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
   if (T > 0 && d_in > 0 && d_out > 0 && lora_stream_ok(r, {d_in, d_out}, {X, B, dY, dX, dH_f32, H})) {
     const size_t need = lora_grad_ws_bytes(T, d_in, d_out, r, ctx->sms);
     if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
-      record("lora_grad stream: workspace too small");
+      record(name + " stream: workspace too small");
       return TG_ERR_WORKSPACE_TOO_SMALL;
     }
     LoraArgs a{};
@@ -1051,8 +1055,10 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
     a.stream = st;
     a.status = ctx->status;
     a.timeout_ns = ctx->timeout_ns;
+    a.add = add;
+    a.scale = scale;
     cudaError_t e = lora_grad_launch(a);
-    record(std::string("lora_grad stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) +
+    record(name + " stream T=" + std::to_string(T) + " d_in=" + std::to_string(d_in) +
            " d_out=" + std::to_string(d_out) + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }
@@ -1068,17 +1074,31 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
   GemmCall g1{LAYOUT_NN, dY, B, dH, 1, T, r, d_out, d_out, r, T * d_out, d_out * r, in, TG_F32, -1, sub_ws, sub,
               st, "lora_grad.dH"};
   TG_TRY(run_gemm(g1, ctx));
-  // dB = dY^T . H
+  // dB = dY^T . H  (scaled)
   GemmCall g2{LAYOUT_TN, dY, H, dB, 1, d_out, r, T, d_out, r, T * d_out, T * r, in, out, -1, sub_ws, sub, st,
-              "lora_grad.dB"};
+              add ? "lora_grad_add.dB" : "lora_grad.dB", 0, add ? scale : 1.f};
   TG_TRY(run_gemm(g2, ctx));
-  // dA = dH^T . X  and  dX = dH . A  with the FP32 dH operand
+  // dA = dH^T . X (scaled)  and  dX = dH . A (or dX += scale dH . A)  with the FP32 dH operand
   GemmCall g3{LAYOUT_TN, dH, X, dA, 1, r, d_in, T, r, d_in, T * r, T * d_in, in, out, EK_F32, nullptr, 0, st,
-              "lora_grad.dA"};
+              add ? "lora_grad_add.dA" : "lora_grad.dA", 0, add ? scale : 1.f};
   TG_TRY(run_gemm(g3, ctx));
   GemmCall g4{LAYOUT_NN, dH, A, dX, 1, T, d_in, r, r, d_in, T * r, r * d_in, in, out, EK_F32, nullptr, 0, st,
-              "lora_grad.dX"};
+              add ? "lora_grad_add.dX" : "lora_grad.dX", add, add ? scale : 1.f};
   return run_gemm(g4, ctx);
+}
+
+tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
+                       void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
+                       tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  return lora_grad_impl(X, A, B, H, dY, dA, dB, dX, dH_f32, T, d_in, d_out, r, in, out, ws, ws_bytes, stream, 0,
+                        1.f);
+}
+
+tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const void* H, const void* dY, void* dA,
+                           void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
+                           float scale, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  return lora_grad_impl(X, A, B, H, dY, dA, dB, dX, dH_f32, T, d_in, d_out, r, in, out, ws, ws_bytes, stream, 1,
+                        scale);
 }
 
 size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in, tg_dtype out) {

@@ -183,7 +183,10 @@ __global__ void simt_gemm_kernel(SimtGemm g) {
   }
   if (i < g.M && j < g.N) {
     const int64_t o = (b * g.M + i) * g.N + j;
-    if (g.accumulate) acc = fmaf(g.scale, acc, load_as_float(g.C, g.out_kind, o));  // C += scale * the product
+    if (g.accumulate)
+      acc = fmaf(g.scale, acc, load_as_float(g.C, g.out_kind, o));  // C += scale * the product
+    else
+      acc *= g.scale;  // C = scale * the product (exact for scale 1)
     store_from_float(g.C, g.out_kind, o, acc);
   }
 }

@@ -147,6 +147,12 @@ __device__ __forceinline__ void load8_raw(const void* out, int kind, size_t i, u
   }
 }
 
+// ask for the line of the 8 outputs at i to be brought into L2
+__device__ __forceinline__ void prefetch_l2_out(const void* out, int kind, size_t i) {
+  const char* p = static_cast<const char*>(out) + i * (kind == EK_F32 ? 4 : 2);
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // those 8 outputs as FP32 (exact: every 16-bit value is one)
 __device__ __forceinline__ void raw8_to_float(int kind, const uint4* w, float* v) {
   if (kind == EK_F32) {
@@ -426,12 +432,23 @@ struct CrArgs {
   float* P;      // [G][max_segs][128][16]
   void* out;     // UP: the row-up output [T][J]
   int out_kind;
+  int add;       // UP: out += scale * the row-up (one rounding) instead of out = the row-up (the kernel's
+                 // ADD instance)
+  float scale;   // also multiplies the ordered sums of the partials (1: unchanged bits)
   unsigned long long timeout_ns;
   unsigned int* status;
   unsigned long long* trace;
 };
 
 __host__ __device__ inline long long cr_start(long long c, const CrArgs& a) { return c * a.N / a.G; }
+
+// v = old + scale * v, with old the bits read from the output
+__device__ __forceinline__ void add8(const CrArgs& a, const uint4* old, float* v) {
+  float o[8];
+  raw8_to_float(a.out_kind, old, o);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = fmaf(a.scale, v[k], o[k]);
+}
 // the CTA whose range holds step p
 __host__ __device__ inline int cr_cta_of(long long p, const CrArgs& a) {
   int c = static_cast<int>(p * a.G / a.N);
@@ -464,7 +481,7 @@ __device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, ui
   }
 }
 
-template <bool BF16, bool HILO, bool UP>
+template <bool BF16, bool HILO, bool UP, bool ADD = false>
 __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid) {
   constexpr int NH = HILO ? 2 : 1;
   constexpr int SB = 32768 + NH * 4096 + (UP ? 4096 : 0);
@@ -521,6 +538,18 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
       const int jb = static_cast<int>(p / a.nsteps), t0 = static_cast<int>(p % a.nsteps) * CR_RS;
       const int slot = s % a.stages;
       const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+      if (ADD) {
+        // pull this step's old outputs into L2 while the stage is still loading
+        const int ra = t0 + w * 16 + g, rb2 = ra + 8;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int jq = jb * CR_CB + 32 * q + 8 * c;
+          if (jq < a.J) {
+            if (ra < a.T) prefetch_l2_out(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + jq);
+            if (rb2 < a.T) prefetch_l2_out(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + jq);
+          }
+        }
+      }
       if (uok && !mbar_wait(smem_u32(&rb.full[slot]), ph, a.timeout_ns, abort_flag, a.status, 0x25)) uok = false;
       const uint32_t st = sbase + static_cast<uint32_t>(slot * SB);
       uint32_t ah[4] = {0u, 0u, 0u, 0u}, al[4] = {0u, 0u, 0u, 0u};
@@ -565,12 +594,18 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         const int j = jb * CR_CB + 32 * q + 8 * c;  // this thread's 8 consecutive columns
         if (j < a.J) {
           float v[8];
+          uint4 oa[2], ob[2];  // add: the old outputs (L2 hits after the prefetch)
+          if (ADD) {
+            if (ra < a.T) load8_raw(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + j, oa);
+            if (rb2 < a.T) load8_raw(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + j, ob);
+          }
           if (ra < a.T) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               v[2 * t] = d[t][0];
               v[2 * t + 1] = d[t][1];
             }
+            if (ADD) add8(a, oa, v);
             store8(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + j, v);
           }
           if (rb2 < a.T) {
@@ -579,6 +614,7 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
               v[2 * t] = d[t][2];
               v[2 * t + 1] = d[t][3];
             }
+            if (ADD) add8(a, ob, v);
             store8(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + j, v);
           }
         }
@@ -665,6 +701,7 @@ __device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, 
 #pragma unroll
     for (int q = 0; q < CB; ++q) v += x[q];
   }
+  v *= a.scale;  // exact for scale 1
   const int j = jb * CR_CB + (e >> 4), r = e & 15;
   if (j < a.J) store_out(out, kind, transposed ? static_cast<size_t>(r) * a.J + j : static_cast<size_t>(j) * LR + r, v);
 }
@@ -831,7 +868,7 @@ __global__ void __launch_bounds__(2 * LGROUP, 1)
 // Pass 2 over X: each step reads an X tile with its dH hi/lo tiles and the
 // matching columns of A; one warp group accumulates dA^T = X^T dH (partials),
 // the other writes the dX = dH A tile.
-template <bool BF16>
+template <bool BF16, bool ADD>
 __global__ void __launch_bounds__(LGROUP_UP, 1)
     lora_grad2_kernel(const __grid_constant__ CrMaps cmaps, const CrArgs cr) {
   extern __shared__ uint8_t smem_raw[];
@@ -843,7 +880,7 @@ __global__ void __launch_bounds__(LGROUP_UP, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  colred_run<BF16, true, true>(&cmaps, cr, smem, tid);
+  colred_run<BF16, true, true, ADD>(&cmaps, cr, smem, tid);
 }
 
 // Pass 3: dB and dA from the partials of passes 1 and 2.  CTA b takes
@@ -950,6 +987,7 @@ static CrArgs cr_plan(int64_t T, int64_t J, int G, int stages) {
   c.N = static_cast<long long>(c.nj) * c.nsteps;
   c.G = static_cast<int>(G < c.N ? G : c.N);
   c.stages = stages;
+  c.scale = 1.f;
   c.max_segs = 1;
   for (int cc = 0; cc < c.G; ++cc) {
     const long long s0 = cr_start(cc, c), s1 = cr_start(cc + 1, c);
@@ -1069,6 +1107,7 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   rd.trace = trace_ptr(0);
   CrArgs& crb = gp.crb;
   crb.P = reinterpret_cast<float*>(base + gp.pb);
+  crb.scale = a.add ? a.scale : 1.f;
   crb.timeout_ns = a.timeout_ns;
   crb.status = a.status;
   crb.trace = trace_ptr(1);
@@ -1088,12 +1127,15 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   CrArgs& cra = gp.cra;
   cra.P = reinterpret_cast<float*>(base + gp.pa);
   cra.out = a.out3;  // dX
+  cra.add = a.add;   // dX += scale * dH A
+  cra.scale = a.add ? a.scale : 1.f;
   cra.timeout_ns = a.timeout_ns;
   cra.status = a.status;
   cra.trace = trace_ptr(2);
   alignas(64) CrMaps cmaps2;
   if (!cr_maps(&cmaps2, a.X, hi, lo, a.A, kind, a.T, a.d_in)) return cudaErrorInvalidValue;
-  auto k2 = bf ? lora_grad2_kernel<true> : lora_grad2_kernel<false>;
+  auto k2 = a.add ? (bf ? lora_grad2_kernel<true, true> : lora_grad2_kernel<false, true>)
+                  : (bf ? lora_grad2_kernel<true, false> : lora_grad2_kernel<false, false>);
   e = allow_smem(reinterpret_cast<const void*>(k2));
   if (e != cudaSuccess) return e;
   e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), 1024 + cr_region_bytes(cra.stages, 2, true), a.stream, cmaps2,

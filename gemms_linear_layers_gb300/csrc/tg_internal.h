@@ -175,7 +175,7 @@ struct SimtGemm {
   int64_t batch, M, N, K;
   int64_t a_bs, a_rs, a_cs, b_bs, b_rs, b_cs;
   int accumulate;  // C += scale * the product (FP32 arithmetic, one rounding to C's type)
-  float scale;
+  float scale;     // without accumulate: C = scale * the product
   cudaStream_t stream;
 };
 cudaError_t simt_gemm_launch(const SimtGemm& g);
@@ -205,7 +205,8 @@ struct LoraArgs {
   cudaStream_t stream;
   unsigned int* status;          // device status word (bounded waits report here)
   unsigned long long timeout_ns; // limit of every wait on an mbarrier
-  int add;                       // up projection: out += scale * H B^T
+  int add;                       // up projection: out += scale * H B^T; gradient: dX += scale * dH A,
+                                 // dA and dB scaled
   float scale;
 };
 size_t lora_down_ws_bytes(int64_t T, int64_t d_in, int64_t r, int num_sms);

@@ -171,6 +171,24 @@ tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* 
                        int64_t d_out, int64_t r, tg_dtype in, tg_dtype out, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* Gradients of a LoRA branch added into its base layer with a scale (the
+ * usual alpha / r), Y = X W^T + scale . (X A^T) B^T, given dY: the LoRA part
+ * of the layer's input gradient is added into dX, which holds the base
+ * layer's dgrad (dY . W) on entry.
+ *   dH[T, r]      = dY . B               (FP32, unscaled as in tg_lora_grad;
+ *                                          written to dH_f32 when non-NULL)
+ *   dB[d_out, r]  = scale . dY^T . H     (overwritten)
+ *   dA[r, d_in]   = scale . dH^T . X     (overwritten)
+ *   dX[T, d_in]  += scale . dH . A       (read and rewritten, one rounding)
+ * The scale multiplies the FP32 sums before the one rounding to `out`, so
+ * scale = 1 with dX = 0 gives tg_lora_grad's bits.  Same kernels, workspace
+ * and arguments as tg_lora_grad; scale must be finite (TG_ERR_INVALID_ARG
+ * otherwise).  r = 0 leaves dX unchanged. */
+tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const void* H, const void* dY,
+                           void* dA, void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in,
+                           int64_t d_out, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
+                           size_t ws_bytes, void* stream);
+
 /* One of the batched products inside attention ("Tuning the kernels";
  * "Checking the results are right": batched attention), see tg_attn_op. */
 tg_status tg_bmm_attn(tg_attn_op op, const void* A, const void* B, void* C, int64_t batch,

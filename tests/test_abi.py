@@ -83,9 +83,9 @@ def test_lora_and_attention_reject_bad_arguments(lib):
 
 
 def test_accumulating_entry_points_reject_bad_arguments(lib):
-    """Both are checked before any device work: the accumulating weight
+    """All are checked before any device work: the accumulating weight
     gradient takes 16-bit operands and an aligned FP32 buffer; the LoRA
-    up-add takes a finite scale."""
+    up-add and gradient-add take a finite scale."""
     f = lib.tg_gemm_wgrad_accumulate
     assert f(EVEN, EVEN, EVEN, 8, -8, 8, B.TG_BF16, NULL, 0, NULL) == 1
     assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, NULL, 0, NULL) == 2
@@ -94,6 +94,14 @@ def test_accumulating_entry_points_reject_bad_arguments(lib):
     assert g(EVEN, EVEN, EVEN, 8, 8, 16, float("nan"), B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
     assert g(EVEN, EVEN, EVEN, 8, 8, 16, float("inf"), B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
     assert g(EVEN, EVEN, EVEN, 8, 8, 16, 2.0, B.TG_BF16, B.TG_F16, NULL, 0, NULL) == 2
+    h = lib.tg_lora_grad_add
+    for bad in (float("nan"), float("-inf")):
+        assert h(EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, NULL, 8, 8, 8, 16, bad,
+                 B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert h(EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, NULL, 8, -8, 8, 16, 1.0,
+             B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
+    assert h(EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, EVEN, NULL, 8, 8, 8, 16, 1.0,
+             B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
 
 
 def test_tile_table_reader(lib, tmp_path):

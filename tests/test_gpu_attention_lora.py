@@ -137,3 +137,66 @@ def test_lora_up_add_into_the_base_output(case, dtype, out_kind):
     base = Y0.double().numpy()
     assert_close(outs[0], base + scale * C, np.abs(base) + abs(scale) * S, f"lora_up_add {T}x{d_out} r={r} [{call}]",
                  out_dtype)
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("case", [(256, 128, 192, 16, 2.0), (130, 264, 136, 16, -0.5),
+                                  (4096, 2304, 5760, 16, 0.125), (64, 64, 64, 8, 2.0), (33, 24, 40, 4, 1.0)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_lora_grad_add_into_the_base_dgrad(case, dtype, out_kind):
+    """dX += scale dH A on top of the base layer's input gradient, dA and dB
+    scaled, dH unscaled (one rounding of each FP32 result).  Rank 16 takes
+    the streaming kernels, other ranks the CUDA-core path."""
+    import numpy as np
+    T, d_in, d_out, r, scale = case
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    X, A, B, H, dY = inputs.lora_inputs(T, d_in, d_out, r, dtype, tag="gradadd")
+    dX0 = inputs.normal((T, d_in), 0.002, out_dtype, 556)  # the base layer's input gradient
+    dev = [t.cuda() for t in (X, A, B, H, dY)]
+    outs = []
+    for _ in range(2):  # the same start twice: the same bits
+        outs.append(tg.tg_lora_grad_add(*dev, dX0.cuda(), scale, want_dH=True))
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    for k in outs[0]:
+        assert torch.equal(outs[0][k], outs[1][k]), k
+    assert ("lora_grad_add stream" in call) == (r == 16), call
+    ref = oracle.lora_grad(X, A, B, H, dY)
+    what = f"{T} {d_in}->{d_out} r={r} scale={scale} [{call}]"
+    assert_close(outs[0]["dH"], *ref["dH"], f"lora_grad_add dH {what}", None)
+    for name in ("dA", "dB"):
+        C, S = ref[name]
+        assert_close(outs[0][name], scale * C, abs(scale) * S, f"lora_grad_add {name} {what}", out_dtype)
+    C, S = ref["dX"]
+    base = dX0.double().numpy()
+    assert_close(outs[0]["dX"], base + scale * C, np.abs(base) + abs(scale) * S, f"lora_grad_add dX {what}",
+                 out_dtype)
+
+
+@pytest.mark.parametrize("shape", [(1000, 576, 1536, 16), (100, 40, 24, 8)], ids=lambda t: "x".join(map(str, t)))
+def test_lora_grad_add_unit_scale_on_zero_is_the_plain_gradient(shape):
+    """scale 1 added into a zero dX multiplies and adds exactly: the bits of
+    tg_lora_grad, on the streaming kernels and on the CUDA-core path."""
+    dev = [t.cuda() for t in inputs.lora_inputs(*shape, torch.bfloat16, tag="unit")]
+    g = tg.tg_lora_grad(*dev, want_dH=True)
+    dX = torch.zeros_like(g["dX"])
+    h = tg.tg_lora_grad_add(*dev, dX, 1.0, want_dH=True)
+    torch.cuda.synchronize()
+    for k in ("dA", "dB", "dX", "dH"):
+        assert torch.equal(g[k], h[k]), k
+
+
+def test_lora_grad_add_rank_zero_leaves_dX():
+    T, d_in, d_out = 64, 32, 48
+    X = torch.randn(T, d_in, device="cuda").to(torch.bfloat16)
+    dY = torch.randn(T, d_out, device="cuda").to(torch.bfloat16)
+    A = torch.empty(0, d_in, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(d_out, 0, dtype=torch.bfloat16, device="cuda")
+    H = torch.empty(T, 0, dtype=torch.bfloat16, device="cuda")
+    dX0 = torch.randn(T, d_in, device="cuda").to(torch.bfloat16)
+    dX = dX0.clone()
+    tg.tg_lora_grad_add(X, A, B, H, dY, dX, 3.0)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, dX0)
