@@ -147,10 +147,22 @@ __device__ __forceinline__ void load8_raw(const void* out, int kind, size_t i, u
   }
 }
 
-// ask for the line of the 8 outputs at i to be brought into L2
-__device__ __forceinline__ void prefetch_l2_out(const void* out, int kind, size_t i) {
-  const char* p = static_cast<const char*>(out) + i * (kind == EK_F32 ? 4 : 2);
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+// 16 bytes global -> shared without a register round trip (completion per
+// thread: cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// all but the most recent commit group are complete
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // those 8 outputs as FP32 (exact: every 16-bit value is one)
@@ -481,6 +493,13 @@ __device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, ui
   }
 }
 
+// ADD staging of the old outputs a row-up warp rewrites in a step, double
+// buffered (the copies of step s + 1 fly during step s): per warp and buffer
+// [4 column groups q][2 rows][W words][32 lanes] 16-byte chunks (W = 2 for
+// FP32 outputs, else 1); lane-major so that a warp's accesses are conflict-free
+__host__ __device__ inline int ru_old_buf(int out_kind) { return 8 * (out_kind == EK_F32 ? 2 : 1) * 512; }
+__host__ __device__ inline int ru_old_bytes(int out_kind) { return LCW * 2 * ru_old_buf(out_kind); }
+
 template <bool BF16, bool HILO, bool UP, bool ADD = false>
 __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid) {
   constexpr int NH = HILO ? 2 : 1;
@@ -533,22 +552,41 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
     const int w = warp - LCW;
     uint32_t bup[4][4][2];  // B fragments of the column block (4 groups of 32 columns x 4 N-tiles)
     bool uok = true;
+    const int ow = a.out_kind == EK_F32 ? 2 : 1, esz = a.out_kind == EK_F32 ? 4 : 2;  // ADD staging words, bytes
+    const uint32_t obase0 = sbase + static_cast<uint32_t>(cr_region_bytes(a.stages, NH, UP) +
+                                                          w * 2 * ru_old_buf(a.out_kind));
+    // ADD: copy the old outputs of step sp into staging buffer sp & 1 (one commit group)
+    auto stage_old = [&](int sp) {
+      const long long pp = p0 + sp;
+      const int jbp = static_cast<int>(pp / a.nsteps);
+      const int ra = static_cast<int>(pp % a.nsteps) * CR_RS + w * 16 + g;
+      const uint32_t ob = obase0 + static_cast<uint32_t>((sp & 1) * ru_old_buf(a.out_kind));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jq = jbp * CR_CB + 32 * q + 8 * c;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = ra + 8 * h;
+          if (jq < a.J && row < a.T) {
+            const char* src = static_cast<const char*>(a.out) + (static_cast<size_t>(row) * a.J + jq) * esz;
+            for (int wd = 0; wd < ow; ++wd) cp_async16(ob + ((q * 2 + h) * ow + wd) * 512 + lane * 16, src + 16 * wd);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+    if (ADD && nst > 0) stage_old(0);
     for (int s = 0; s < nst; ++s) {
       const long long p = p0 + s;
       const int jb = static_cast<int>(p / a.nsteps), t0 = static_cast<int>(p % a.nsteps) * CR_RS;
       const int slot = s % a.stages;
       const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
+      // ADD: the next step's old outputs start moving (an empty group at the end)
       if (ADD) {
-        // pull this step's old outputs into L2 while the stage is still loading
-        const int ra = t0 + w * 16 + g, rb2 = ra + 8;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int jq = jb * CR_CB + 32 * q + 8 * c;
-          if (jq < a.J) {
-            if (ra < a.T) prefetch_l2_out(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + jq);
-            if (rb2 < a.T) prefetch_l2_out(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + jq);
-          }
-        }
+        if (uok && s + 1 < nst)
+          stage_old(s + 1);
+        else
+          cp_async_commit();
       }
       if (uok && !mbar_wait(smem_u32(&rb.full[slot]), ph, a.timeout_ns, abort_flag, a.status, 0x25)) uok = false;
       const uint32_t st = sbase + static_cast<uint32_t>(slot * SB);
@@ -592,12 +630,18 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
           if (HILO) mma_16816<BF16>(d[t], al, bup[q][t]);
         }
         const int j = jb * CR_CB + 32 * q + 8 * c;  // this thread's 8 consecutive columns
+        if (ADD && q == 0) cp_async_wait_group1();  // this step's staged old outputs have landed
         if (j < a.J) {
           float v[8];
-          uint4 oa[2], ob[2];  // add: the old outputs (L2 hits after the prefetch)
+          uint4 oa[2], ob[2];  // add: the old outputs, from the staging
           if (ADD) {
-            if (ra < a.T) load8_raw(a.out, a.out_kind, static_cast<size_t>(ra) * a.J + j, oa);
-            if (rb2 < a.T) load8_raw(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + j, ob);
+            const uint32_t obs = obase0 + static_cast<uint32_t>((s & 1) * ru_old_buf(a.out_kind));
+#pragma unroll
+            for (int wd = 0; wd < 2; ++wd)
+              if (wd < ow) {
+                oa[wd] = ld_shared_v4(obs + ((q * 2) * ow + wd) * 512 + lane * 16);
+                ob[wd] = ld_shared_v4(obs + ((q * 2 + 1) * ow + wd) * 512 + lane * 16);
+              }
           }
           if (ra < a.T) {
 #pragma unroll
@@ -620,6 +664,7 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         }
       }
     }
+    if (ADD) cp_async_wait_all();  // no copy outlives the kernel (a step given up after a failed wait)
     return;
   }
 
@@ -1138,7 +1183,11 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
                   : (bf ? lora_grad2_kernel<true, false> : lora_grad2_kernel<false, false>);
   e = allow_smem(reinterpret_cast<const void*>(k2));
   if (e != cudaSuccess) return e;
-  e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), 1024 + cr_region_bytes(cra.stages, 2, true), a.stream, cmaps2,
+  // the adding instance stages the old dX of two steps: one operand stage
+  // fewer for 16-bit dX, two for FP32
+  if (a.add) cra.stages = G2_CR_STAGES - (a.out_kind == EK_F32 ? 2 : 1);
+  const int smem2 = 1024 + cr_region_bytes(cra.stages, 2, true) + (a.add ? ru_old_bytes(a.out_kind) : 0);
+  e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), smem2, a.stream, cmaps2,
                cra);
   if (e != cudaSuccess) return e;
 
