@@ -228,6 +228,8 @@ def kernel_key(call: str) -> str:
     """'tc nt bn=256' style identity of the kernel a call ran (from tg_last_call)."""
     f = call.split()
     path = f[1] if len(f) > 1 else "?"
+    if path == "ffma":
+        return f"ffma {f[2]}" + (" +reduce" if any(x.startswith("splits=") and x != "splits=1" for x in f) else "")
     if path != "tc":
         return f"{path} {f[2] if len(f) > 2 else ''}".strip()
     bn = next((x for x in f if x.startswith("bn=")), "bn=?")
@@ -556,6 +558,24 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------ rows
+FP32_LANES_PER_SM = 128  # FP32 FMA units per SM (4 sub-partitions x 32)
+
+
+def fp32_peak_tflops(sms=None, mhz=None):
+    """FP32 CUDA-core peak: SMs x FMA units x 2 flop x the maximum SM clock
+    (152 x 128 x 2 x 2,070 MHz = 80.5 TFLOP/s on a GB300)."""
+    if sms is None:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if mhz is None:
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits", "-i", "0"],
+                                 capture_output=True, text=True, timeout=20).stdout.split()
+            mhz = float(out[0])
+        except Exception:
+            mhz = 2070.0
+    return sms * FP32_LANES_PER_SM * 2 * mhz / 1e6
+
+
 def measure_rows(stream, pk, budget_s=90.0):
     """One timing row per distinct product of the other product sets, each
     alone: CUDA graph of R launches, L2-sized buffer rotation for the
@@ -616,6 +636,29 @@ def measure_rows(stream, pk, budget_s=90.0):
                 rows[-2]["wgrad_over_fwd"] = round(res["wgrad"] / res["fwd"], 3)
                 rows[-1]["acc_over_wgrad"] = round(res["wgrad_acc"] / res["wgrad"], 3)
                 del X, W, dY, outs
+    # FP32 operands (the CUDA-core FFMA kernel): the 2B-class layers at T=2048
+    # and the 135M-class head, against the FP32 CUDA-core peak
+    f32_peak = fp32_peak_tflops()
+    for names, T, d_in, d_out in (("q,k,v,o", 2048, 2304, 2304), ("gate,up", 2048, 2304, 5760),
+                                  ("down", 2048, 5760, 2304), ("head", 2048, 576, 49152)):
+        dt = torch.float32
+        X, W, dY = inputs.layer_inputs(T, d_in, d_out, dt, tag="rows32", device="cuda")
+        outs = {"fwd": torch.empty(T, d_out, dtype=dt, device="cuda"),
+                "dgrad": torch.empty(T, d_in, dtype=dt, device="cuda"),
+                "wgrad": torch.empty(d_out, d_in, dtype=dt, device="cuda")}
+        ws = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
+        for op in ("fwd", "dgrad", "wgrad"):
+            fn = {"fwd": lambda i: (lambda: tg.tg_gemm_fwd(X, W, Y=outs["fwd"], ws=ws)),
+                  "dgrad": lambda i: (lambda: tg.tg_gemm_dgrad(dY, W, dX=outs["dgrad"], ws=ws)),
+                  "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws))}[op]
+            ms, call = time_calls(fn, reps=5)
+            M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[op]
+            tf = workloads.flops(M, N, K) / ms / 1e9
+            rows.append({"set": "FP32", "layer": names, "T": T, "op": op, "dtype": "fp32", "M": M, "N": N, "K": K,
+                         "us": round(ms * 1000, 2), "tflops": round(tf, 2),
+                         "frac_of_peak": round(tf / f32_peak, 3), "bound": "alu",
+                         "peak_tflops": round(f32_peak, 1), "kernel": kernel_key(call)})
+        del X, W, dY, outs, ws
     # rank-16 LoRA, bf16, T=4096: effective HBM bandwidth
     cfg = workloads.LORA_2B
     T, r = cfg["T"], cfg["r"]

@@ -544,6 +544,8 @@ static std::string plan_text(const Plan& p, int layout, int64_t M, int64_t N, in
 
 // -------------------------------------------------------------- the GEMMs
 static bool dtype_in_ok(tg_dtype in) { return in == TG_BF16 || in == TG_F16; }
+// the layer products also take FP32 operands (FP32 output only)
+static bool dtype_in_ok_layer(tg_dtype in) { return dtype_in_ok(in) || in == TG_F32; }
 static bool dtype_out_ok(tg_dtype in, tg_dtype out) { return out == TG_F32 || out == in; }
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 static size_t dt_bytes(tg_dtype d) { return d == TG_F32 ? 4 : 2; }
@@ -595,6 +597,34 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
                : TG_ERR_CUDA;
   }
   char buf[320];
+  if (g.in == TG_F32) {  // FP32 operands: the CUDA-core FFMA kernel
+    FfmaGemm f;
+    f.layout = g.layout;
+    f.A = static_cast<const float*>(g.A);
+    f.B = static_cast<const float*>(g.B);
+    f.C = static_cast<float*>(g.C);
+    f.M = g.M;
+    f.N = g.N;
+    f.K = g.K;
+    f.lda = g.lda;
+    f.ldb = g.ldb;
+    f.splits = ffma_splits(g.M, g.N, g.K, ctx->sms);
+    f.accumulate = g.accumulate;
+    f.stream = g.stream;
+    const size_t need = ffma_ws_bytes(g.M, g.N, g.K, ctx->sms);
+    if (need > 0 && (g.ws == nullptr || g.ws_bytes < need || !aligned(g.ws, 16))) {
+      snprintf(buf, sizeof buf, "%s ffma %s splits=%d: workspace %zu bytes needed, %zu given", g.name,
+               layout_name(g.layout), f.splits, need, g.ws ? g.ws_bytes : static_cast<size_t>(0));
+      record(buf);
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    f.ws = static_cast<float*>(g.ws);
+    cudaError_t e = ffma_gemm_launch(f);
+    snprintf(buf, sizeof buf, "%s ffma %s M=%lld N=%lld K=%lld splits=%d %s", g.name, layout_name(g.layout),
+             (long long)g.M, (long long)g.N, (long long)g.K, f.splits, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+    record(buf);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
   if (tc_eligible(g)) {
     const Plan p = make_plan(g.layout, g.M, g.N, g.K, g.batch, g.in, g.out, ctx->sms);
     const size_t need = plan_ws_bytes(p, g.M, g.N, g.K, g.batch, ctx->sms);
@@ -686,12 +716,21 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
 static size_t gemm_ws_bytes(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
                             int sms) {
   if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+  if (in == TG_F32) return batch == 1 ? ffma_ws_bytes(M, N, K, sms) : 0;
   return plan_ws_bytes(make_plan(layout, M, N, K, batch, in, out, sms), M, N, K, batch, sms);
 }
 
-// Checks shared by the layer products.  Returns TG_OK to proceed.
+// Checks shared by the LoRA and attention products.  Returns TG_OK to proceed.
 static tg_status check_common(tg_dtype in, tg_dtype out, std::initializer_list<int64_t> dims) {
   if (!dtype_in_ok(in) || !dtype_out_ok(in, out)) return TG_ERR_UNSUPPORTED_DTYPE;
+  for (int64_t d : dims)
+    if (d < 0 || d > kMaxDim) return TG_ERR_INVALID_ARG;
+  return TG_OK;
+}
+
+// The same for the layer products, which also take FP32 operands.
+static tg_status check_layer(tg_dtype in, tg_dtype out, std::initializer_list<int64_t> dims) {
+  if (!dtype_in_ok_layer(in) || !dtype_out_ok(in, out)) return TG_ERR_UNSUPPORTED_DTYPE;
   for (int64_t d : dims)
     if (d < 0 || d > kMaxDim) return TG_ERR_INVALID_ARG;
   return TG_OK;
@@ -746,12 +785,15 @@ size_t tg_last_call(char* buf, size_t len) {
 size_t tg_plan_describe(tg_op op, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
                         int sms, char* buf, size_t len) {
   if (op != TG_OP_GEMM_FWD && op != TG_OP_GEMM_DGRAD && op != TG_OP_GEMM_WGRAD) return 0;
-  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0 || sms < 2 || !dtype_in_ok(in) || !dtype_out_ok(in, out)) return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0 || sms < 2 || !dtype_in_ok_layer(in) || !dtype_out_ok(in, out))
+    return 0;
   const int layout = op == TG_OP_GEMM_FWD ? LAYOUT_NT : (op == TG_OP_GEMM_DGRAD ? LAYOUT_NN : LAYOUT_TN);
   // contiguous operands: the row pitches the tensor-core path needs
   const int64_t lda = layout == LAYOUT_TN ? M : K, ldb = layout == LAYOUT_NT ? K : N;
   std::string s;
-  if ((lda * 2) % 16 || (ldb * 2) % 16 || (N * static_cast<int64_t>(dt_bytes(out))) % 16 || batch > 65535) {
+  if (in == TG_F32) {
+    s = std::string("ffma ") + layout_name(layout) + " splits=" + std::to_string(ffma_splits(M, N, K, sms));
+  } else if ((lda * 2) % 16 || (ldb * 2) % 16 || (N * static_cast<int64_t>(dt_bytes(out))) % 16 || batch > 65535) {
     s = std::string("simt ") + layout_name(layout);
   } else {
     s = plan_text(make_plan(layout, M, N, K, batch, in, out, sms), layout, M, N, K, batch, sms);
@@ -793,9 +835,9 @@ tg_status tg_wait_probe(int64_t timeout_us, void* stream) {
 
 tg_status tg_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t d_out, int64_t d_in, tg_dtype in,
                       tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
-  TG_TRY(check_common(in, out, {T, d_out, d_in}));
-  TG_TRY(check_ptr(X, T * d_in, 2));
-  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_layer(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(X, T * d_in, dt_bytes(in)));
+  TG_TRY(check_ptr(W, d_out * d_in, dt_bytes(in)));
   TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
@@ -806,9 +848,9 @@ tg_status tg_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t 
 
 tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t d_out, int64_t d_in,
                         tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
-  TG_TRY(check_common(in, out, {T, d_out, d_in}));
-  TG_TRY(check_ptr(dY, T * d_out, 2));
-  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_layer(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, dt_bytes(in)));
+  TG_TRY(check_ptr(W, d_out * d_in, dt_bytes(in)));
   TG_TRY(check_ptr(dX, T * d_in, dt_bytes(out)));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
@@ -819,9 +861,9 @@ tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int6
 
 tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out, int64_t d_in,
                         tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
-  TG_TRY(check_common(in, out, {T, d_out, d_in}));
-  TG_TRY(check_ptr(dY, T * d_out, 2));
-  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_layer(in, out, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, dt_bytes(in)));
+  TG_TRY(check_ptr(X, T * d_in, dt_bytes(in)));
   TG_TRY(check_ptr(dW, d_out * d_in, dt_bytes(out)));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
@@ -832,9 +874,9 @@ tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int6
 
 tg_status tg_gemm_wgrad_accumulate(const void* dY, const void* X, float* dW, int64_t T, int64_t d_out,
                                    int64_t d_in, tg_dtype in, void* ws, size_t ws_bytes, void* stream) {
-  TG_TRY(check_common(in, TG_F32, {T, d_out, d_in}));
-  TG_TRY(check_ptr(dY, T * d_out, 2));
-  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_layer(in, TG_F32, {T, d_out, d_in}));
+  TG_TRY(check_ptr(dY, T * d_out, dt_bytes(in)));
+  TG_TRY(check_ptr(X, T * d_in, dt_bytes(in)));
   TG_TRY(check_ptr(dW, d_out * d_in, 4));
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
@@ -1102,7 +1144,8 @@ tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const vo
 }
 
 size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in, tg_dtype out) {
-  if (!dtype_in_ok(in) || !dtype_out_ok(in, out)) return SIZE_MAX;
+  const bool layer = op == TG_OP_GEMM_FWD || op == TG_OP_GEMM_DGRAD || op == TG_OP_GEMM_WGRAD;
+  if (!(layer ? dtype_in_ok_layer(in) : dtype_in_ok(in)) || !dtype_out_ok(in, out)) return SIZE_MAX;
   if (d0 < 0 || d1 < 0 || d2 < 0 || d3 < 0) return SIZE_MAX;
   DevCtx* ctx = nullptr;
   if (device_ctx(&ctx) != TG_OK) return SIZE_MAX;

@@ -180,6 +180,23 @@ struct SimtGemm {
 };
 cudaError_t simt_gemm_launch(const SimtGemm& g);
 
+// FP32-input layer product on the CUDA cores (gemm_ffma.cu), batch 1, dense
+// row-major operands in the layouts above; C FP32 with row pitch N.
+struct FfmaGemm {
+  int layout;
+  const float* A;
+  const float* B;
+  float* C;
+  int64_t M, N, K, lda, ldb;
+  int splits;      // > 1: FP32 partials in ws[split][M][N], added in split order afterwards
+  float* ws;
+  int accumulate;  // C += the product
+  cudaStream_t stream;
+};
+int ffma_splits(int64_t M, int64_t N, int64_t K, int sms);
+size_t ffma_ws_bytes(int64_t M, int64_t N, int64_t K, int sms);
+cudaError_t ffma_gemm_launch(const FfmaGemm& g);
+
 // Tensor-map encoding through the driver entry point (tmap.cpp).
 bool encode_tmap_3d(void* tmap_out, const void* base, int elem_kind, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,

@@ -58,9 +58,11 @@ def test_layer_products_reject_bad_arguments(lib, fn):
     # negative size
     assert f(EVEN, EVEN, EVEN, -1, 8, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
     assert f(EVEN, EVEN, EVEN, 8, 8, 1 << 31, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
-    # unsupported dtypes: FP32 input; 16-bit output of the other type
-    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
+    # unsupported dtypes: a 16-bit output of FP32 inputs or of the other 16-bit type
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, B.TG_BF16, NULL, 0, NULL) == 2
     assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_BF16, B.TG_F16, NULL, 0, NULL) == 2
+    # FP32 operands are 4-byte elements
+    assert f(ctypes.c_void_p(0x1002), EVEN, EVEN, 8, 8, 8, B.TG_F32, B.TG_F32, NULL, 0, NULL) == 3
     assert f(EVEN, EVEN, EVEN, 8, 8, 8, 7, B.TG_F32, NULL, 0, NULL) == 2
     # NULL operand with a non-empty tensor
     assert f(NULL, EVEN, EVEN, 8, 8, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
@@ -78,7 +80,8 @@ def test_lora_and_attention_reject_bad_arguments(lib):
     assert lib.tg_bmm_attn(9, EVEN, EVEN, EVEN, 2, 4, 8, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
     assert lib.tg_wait_probe(0, NULL) == 1
     assert lib.tg_wait_probe(10 ** 8, NULL) == 1
-    assert lib.tg_workspace_size(0, 8, 8, 8, 0, B.TG_F32, B.TG_F32) == B.SIZE_MAX
+    assert lib.tg_workspace_size(B.TG_OP_LORA_UP, 8, 8, 8, 0, B.TG_F32, B.TG_F32) == B.SIZE_MAX  # FP32: layers only
+    assert lib.tg_workspace_size(B.TG_OP_GEMM_FWD, 8, 8, 8, 0, B.TG_F32, B.TG_BF16) == B.SIZE_MAX
     assert lib.tg_workspace_size(0, -8, 8, 8, 0, B.TG_BF16, B.TG_F32) == B.SIZE_MAX
 
 
@@ -88,7 +91,8 @@ def test_accumulating_entry_points_reject_bad_arguments(lib):
     up-add and gradient-add take a finite scale."""
     f = lib.tg_gemm_wgrad_accumulate
     assert f(EVEN, EVEN, EVEN, 8, -8, 8, B.TG_BF16, NULL, 0, NULL) == 1
-    assert f(EVEN, EVEN, EVEN, 8, 8, 8, B.TG_F32, NULL, 0, NULL) == 2
+    assert f(EVEN, EVEN, EVEN, 8, 8, 8, 7, NULL, 0, NULL) == 2
+    assert f(ctypes.c_void_p(0x1002), EVEN, EVEN, 8, 8, 8, B.TG_F32, NULL, 0, NULL) == 3  # FP32 dY not 4-aligned
     assert f(EVEN, EVEN, ctypes.c_void_p(0x1002), 8, 8, 8, B.TG_BF16, NULL, 0, NULL) == 3  # dW not 4-aligned
     g = lib.tg_lora_up_add
     assert g(EVEN, EVEN, EVEN, 8, 8, 16, float("nan"), B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 1
@@ -169,6 +173,7 @@ def _plan(op, M, N, K, batch=1, sms=152):
 
 
 def test_plan_describe_reports_table_entries_and_the_cuda_core_path(lib):
+    import torch
     """tg_plan_describe (host only) gives the plan a call would use: a shipped
     table entry is reported as a hit; sizes the tensor-core path cannot
     address go to the CUDA-core path; bad arguments give an empty answer."""
@@ -179,6 +184,12 @@ def test_plan_describe_reports_table_entries_and_the_cuda_core_path(lib):
         assert _plan(B.TG_OP_GEMM_FWD, 3000, 1000, 700) == "simt nt"  # K = 700: rows of 1,400 bytes
         assert _plan(B.TG_OP_GEMM_WGRAD, 0, 576, 2048) == ""
         assert _plan(B.TG_OP_LORA_DOWN, 2048, 576, 16) == ""
+        # FP32 operands: the FFMA kernel, split along K when few tiles would occupy the SMs
+        f32 = lambda op, M, N, K: B.tg_plan_describe(op, M, N, K, 1, torch.float32, torch.float32, 152)
+        assert f32(B.TG_OP_GEMM_FWD, 4096, 5760, 2304) == "ffma nt splits=1"
+        assert f32(B.TG_OP_GEMM_DGRAD, 2048, 576, 49152) == "ffma nn splits=3"
+        assert f32(B.TG_OP_GEMM_WGRAD, 576, 576, 2048) == "ffma tn splits=4"
+        assert B.tg_plan_describe(B.TG_OP_GEMM_FWD, 64, 64, 64, 1, torch.float32, torch.bfloat16, 152) == ""
     finally:
         assert lib.tg_load_table(None) == 0
 

@@ -14,6 +14,8 @@ from gemms_linear_layers_gb300 import workloads  # noqa: E402
 
 def test_kernel_key():
     k = bench.kernel_key
+    assert k("fwd ffma nt M=2048 N=2304 K=2304 splits=1 ok") == "ffma nt"
+    assert k("dgrad ffma nn M=2048 N=576 K=49152 splits=3 ok") == "ffma nn +reduce"
     assert k("fwd tc nt M=2048 N=576 K=576 batch=1 bn=64 splits=1 raster=n table=hit ok") == "tc nt bn=64"
     assert k("dgrad tc nn M=2048 N=576 K=49152 batch=1 bn=192 deep splits=3 raster=n table=hit ok") == \
         "tc nn bn=192 deep +reduce"
@@ -72,3 +74,8 @@ def test_profiled_traffic_needs_matching_key_and_sources(tmp_path):
     assert bench.profiled_traffic("tc nt bn=256 pair", str(prof), digest) is None
     (csrc / "k.cu").write_text("kernel v2\n")  # the kernel changed since the capture
     assert bench.profiled_traffic("tc nn bn=192 pair +reduce", str(prof), bench.kernel_sources_digest(str(csrc))) is None
+
+
+def test_fp32_peak_from_units_and_clock():
+    """152 SMs x 128 FP32 FMA units x 2 flop x 2,070 MHz."""
+    assert abs(bench.fp32_peak_tflops(152, 2070.0) - 80.5478) < 1e-3
