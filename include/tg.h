@@ -25,7 +25,10 @@
  *     (a bounded wait that timed out) is reported by tg_stream_status.
  *   - Outputs are overwritten (no alpha/beta).  `in` is TG_BF16 or TG_F16;
  *     `out` is TG_F32 or the input type.  16-bit outputs are the FP32 result
- *     rounded to nearest even.
+ *     rounded to nearest even.  The layer products (tg_gemm_fwd, _dgrad,
+ *     _wgrad and their _noalloc / _accumulate forms) also take in = TG_F32
+ *     with out = TG_F32: FP32 operands, every product fused into its FP32 sum
+ *     on the CUDA cores (FFMA), no tensor-core rounding of the operands.
  *   - Sizes: a negative size is TG_ERR_INVALID_ARG; an empty output (a zero
  *     row or column count) is TG_OK with nothing done; an empty reduction
  *     writes zeros.  Every size must be below 2^31.
@@ -52,7 +55,8 @@ typedef enum { TG_BF16 = 0, TG_F16 = 1, TG_F32 = 2 } tg_dtype;
 typedef enum {
   TG_OK = 0,
   TG_ERR_INVALID_ARG = 1,         /* NULL pointer with a non-empty tensor, bad size, bad enum */
-  TG_ERR_UNSUPPORTED_DTYPE = 2,   /* input not bf16/fp16, or output neither FP32 nor the input type */
+  TG_ERR_UNSUPPORTED_DTYPE = 2,   /* input not bf16/fp16 (or FP32 for a layer product), or output
+                                     neither FP32 nor the input type */
   TG_ERR_MISALIGNED = 3,          /* pointer not aligned to its element size */
   TG_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below tg_workspace_size() for the call */
   TG_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, attribute, device query) */
