@@ -20,6 +20,7 @@ from gemms_linear_layers_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 DT16 = (torch.bfloat16, torch.float16)
+DTIN = DT16 + (torch.float32,)  # the layer products also take FP32 operands
 U = 2.0 ** -53
 
 
@@ -150,7 +151,7 @@ def _operands(op, T, d_in, d_out, dtype, seed):
 ORACLE_OP = {"fwd": oracle.gemm_fwd, "dgrad": oracle.gemm_dgrad, "wgrad": oracle.gemm_wgrad}
 
 
-@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("dtype", DTIN)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 def test_bruteforce_rational_all_tiny_shapes(op, dtype):
     for T, d_in, d_out in itertools.product(range(1, 5), repeat=3):
@@ -168,7 +169,7 @@ def test_bruteforce_rational_all_tiny_shapes(op, dtype):
 LADDER = [(1, 1, 1), (1, 8, 8), (7, 5, 13), (16, 16, 16), (64, 64, 64), (33, 129, 65), (200, 96, 300)]
 
 
-@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("dtype", DTIN)
 @pytest.mark.parametrize("T,d_in,d_out", LADDER)
 def test_numpy_float64_matmul(T, d_in, d_out, dtype):
     X = rand16((T, d_in), dtype, 1)
@@ -183,7 +184,7 @@ def test_numpy_float64_matmul(T, d_in, d_out, dtype):
         assert np.all(np.abs(C - ref) <= 2 * K * U * S + 1e-300), op
 
 
-@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("dtype", DTIN)
 def test_small_integer_inputs_are_exact(dtype):
     T, d_in, d_out = 96, 700, 40
     X = inputs.small_int((T, d_in), -2, 2, dtype, 5)
