@@ -676,6 +676,16 @@ def measure_rows(stream, pk, budget_s=90.0):
                   "dX": torch.empty(T, d_in, dtype=dt, device="cuda")} for _ in range(sets)]
         wsn = tg.tg_workspace_size(tg.TG_OP_LORA_GRAD, T, d_in, d_out, r, dt, dt)
         wss = [torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda") for _ in range(sets)]
+        # FP32 factors (as an optimizer keeps them) with the same bf16 activations
+        f32 = [inputs.lora_inputs(T, d_in, d_out, r, torch.float32, tag=f"rows{i}", device="cuda")[1:3]
+               for i in range(sets)]
+        grads32 = [{"dA": torch.empty(r, d_in, dtype=torch.float32, device="cuda"),
+                    "dB": torch.empty(d_out, r, dtype=torch.float32, device="cuda"),
+                    "dX": torch.empty(T, d_in, dtype=dt, device="cuda")} for _ in range(sets)]
+        wsn32 = max(tg.tg_workspace_size(op, *dims, dt, dt) for op, dims in (
+            (tg.TG_OP_LORA_DOWN_F32W, (T, d_in, r, 0)), (tg.TG_OP_LORA_UP_F32W, (T, d_out, r, 0)),
+            (tg.TG_OP_LORA_GRAD_F32W, (T, d_in, d_out, r))))
+        wss32 = [torch.empty(max(wsn32, 16), dtype=torch.uint8, device="cuda") for _ in range(sets)]
         specs = [
             ("down", lambda i: (lambda: tg.tg_lora_down(data[i][0], data[i][1], H=Hs[i])),
              (T * d_in + r * d_in + T * r) * 2, 2 * T * d_in * r),
@@ -694,6 +704,15 @@ def measure_rows(stream, pk, budget_s=90.0):
                                                                  ws=wss[i])),
              (T * d_out + 3 * T * d_in + T * r + 2 * r * d_in + 2 * d_out * r) * 2,
              4 * T * r * (d_in + d_out)),
+            # FP32 factors: 4-byte A and B, read once by a split into 16-bit parts
+            ("down_f32w", lambda i: (lambda: tg.tg_lora_down_f32w(data[i][0], f32[i][0], H=Hs[i], ws=wss32[i])),
+             (T * d_in + T * r) * 2 + r * d_in * 4, 2 * T * d_in * r),
+            ("up_f32w", lambda i: (lambda: tg.tg_lora_up_f32w(data[i][3], f32[i][1], Y=Ys[i], ws=wss32[i])),
+             (T * r + T * d_out) * 2 + d_out * r * 4, 2 * T * d_out * r),
+            ("grad_f32w", lambda i: (lambda: tg.tg_lora_grad_f32w(data[i][0], f32[i][0], f32[i][1], data[i][3],
+                                                                  data[i][4], outs=grads32[i], ws=wss32[i])),
+             (T * d_out + 2 * T * d_in + T * r) * 2 + (2 * r * d_in + 2 * d_out * r) * 4,
+             4 * T * r * (d_in + d_out)),
         ]
         for op, fn, nbytes, fl in specs:
             ms, call = time_calls(fn, reps=max(10, sets * 2), sets=sets)
@@ -702,7 +721,7 @@ def measure_rows(stream, pk, budget_s=90.0):
                          "d_out": d_out, "us": round(ms * 1000, 2), "gbs": round(gbs, 1),
                          "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3), "bound": "hbm",
                          "tflops": round(fl / ms / 1e9, 2), "kernel": call.split(" [")[0][:60]})
-        del data, Hs, Ys, grads, wss
+        del data, Hs, Ys, grads, wss, f32, grads32, wss32
         if time.perf_counter() - t_start > budget_s:
             break
     # attention, s = 1024 / 2048 / 4096, bf16

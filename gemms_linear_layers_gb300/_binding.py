@@ -25,6 +25,7 @@ _DT = {torch.bfloat16: TG_BF16, torch.float16: TG_F16, torch.float32: TG_F32}
 
 TG_OP_GEMM_FWD, TG_OP_GEMM_DGRAD, TG_OP_GEMM_WGRAD = 0, 1, 2
 TG_OP_LORA_DOWN, TG_OP_LORA_UP, TG_OP_LORA_GRAD, TG_OP_BMM_ATTN = 3, 4, 5, 6
+TG_OP_LORA_DOWN_F32W, TG_OP_LORA_UP_F32W, TG_OP_LORA_GRAD_F32W = 7, 8, 9
 ATTN_OPS = {"qk": 0, "pv": 1, "do_vt": 2, "pt_do": 3, "ds_k": 4, "dst_q": 5}
 SIZE_MAX = (1 << 64) - 1
 
@@ -41,6 +42,10 @@ SIGNATURES = {
     "tg_lora_up_add": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
                           _vp, _sz, _vp]),
+    "tg_lora_down_f32w": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_lora_up_f32w": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_lora_grad_f32w": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
+                               _vp, _sz, _vp]),
     "tg_lora_grad_add": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float,
                               _i, _i, _vp, _sz, _vp]),
     "tg_bmm_attn": (_i, [_i, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -297,6 +302,70 @@ def tg_lora_grad_add(X, A, B, H, dY, dX, scale, want_dH=False, outs=None, ws=Non
     _check(lib().tg_lora_grad_add(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(dY), _ptr(dA), _ptr(dB), _ptr(dX),
                                   _ptr(dH), T, d_in, d_out, r, float(scale), din, _DT[od], wp, wn, _stream(stream)),
            "tg_lora_grad_add")
+    _keep(keep, stream)
+    res = {"dA": dA, "dB": dB, "dX": dX}
+    if dH is not None:
+        res["dH"] = dH
+    return res
+
+
+def _need_f32(t, name, shape):
+    _need(t, name, len(shape))
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be an FP32 {tuple(shape)} tensor, got {t.dtype} {tuple(t.shape)}")
+
+
+def tg_lora_down_f32w(X, A, H=None, out_dtype=None, ws=None, stream=None):
+    """H[T, r] = X[T, d_in] A[r, d_in]^T with an FP32 factor A and 16-bit X."""
+    _need(X, "X", 2)
+    T, d_in = X.shape
+    r = A.shape[0]
+    _need_f32(A, "A", (r, d_in))
+    H = _out(H, (T, r), out_dtype or X.dtype, X.device, "H")
+    wp, wn, keep = _workspace(TG_OP_LORA_DOWN_F32W, (T, d_in, r, 0), _DT[X.dtype], _DT[H.dtype], ws, X.device)
+    _check(lib().tg_lora_down_f32w(_ptr(X), _ptr(A), _ptr(H), T, d_in, r, _DT[X.dtype], _DT[H.dtype], wp, wn,
+                                   _stream(stream)), "tg_lora_down_f32w")
+    _keep(keep, stream)
+    return H
+
+
+def tg_lora_up_f32w(H, B, Y=None, out_dtype=None, ws=None, stream=None):
+    """Y[T, d_out] = H[T, r] B[d_out, r]^T with an FP32 factor B and 16-bit H."""
+    _need(H, "H", 2)
+    T, r = H.shape
+    d_out = B.shape[0]
+    _need_f32(B, "B", (d_out, r))
+    Y = _out(Y, (T, d_out), out_dtype or H.dtype, H.device, "Y")
+    wp, wn, keep = _workspace(TG_OP_LORA_UP_F32W, (T, d_out, r, 0), _DT[H.dtype], _DT[Y.dtype], ws, H.device)
+    _check(lib().tg_lora_up_f32w(_ptr(H), _ptr(B), _ptr(Y), T, d_out, r, _DT[H.dtype], _DT[Y.dtype], wp, wn,
+                                 _stream(stream)), "tg_lora_up_f32w")
+    _keep(keep, stream)
+    return Y
+
+
+def tg_lora_grad_f32w(X, A, B, H, dY, out_dtype=None, want_dH=False, outs=None, ws=None, stream=None):
+    """Gradients of Y = (X A^T) B^T with FP32 factors A, B and 16-bit X, H, dY:
+    dict dA, dB (FP32), dX (out_dtype, default X's) and dH (FP32) when asked."""
+    for t, n in ((X, "X"), (H, "H"), (dY, "dY")):
+        _need(t, n, 2)
+    T, d_in = X.shape
+    r = A.shape[0]
+    d_out = B.shape[0]
+    _need_f32(A, "A", (r, d_in))
+    _need_f32(B, "B", (d_out, r))
+    if H.shape != (T, r) or dY.shape != (T, d_out):
+        raise ValueError("inconsistent LoRA shapes")
+    od = out_dtype or X.dtype
+    outs = dict(outs or {})
+    dA = _out(outs.get("dA"), (r, d_in), torch.float32, X.device, "dA")
+    dB = _out(outs.get("dB"), (d_out, r), torch.float32, X.device, "dB")
+    dX = _out(outs.get("dX"), (T, d_in), od, X.device, "dX")
+    dH = _out(outs.get("dH"), (T, r), torch.float32, X.device, "dH") if (want_dH or "dH" in outs) else None
+    din = _DT[X.dtype]
+    wp, wn, keep = _workspace(TG_OP_LORA_GRAD_F32W, (T, d_in, d_out, r), din, _DT[od], ws, X.device)
+    _check(lib().tg_lora_grad_f32w(_ptr(X), _ptr(A), _ptr(B), _ptr(H), _ptr(dY), _ptr(dA), _ptr(dB), _ptr(dX),
+                                   _ptr(dH), T, d_in, d_out, r, din, _DT[od], wp, wn, _stream(stream)),
+           "tg_lora_grad_f32w")
     _keep(keep, stream)
     res = {"dA": dA, "dB": dB, "dX": dX}
     if dH is not None:

@@ -566,10 +566,11 @@ struct GemmCall {
   const char* name;
   int accumulate = 0;  // C += scale * the product (gradient accumulation, LoRA branch added to Y)
   float scale = 1.f;   // without accumulate: C = scale * the product (scaled LoRA gradients)
+  int b_kind_override = -1;  // FP32 B operand (an FP32 LoRA factor): CUDA-core path only
 };
 
 static bool tc_eligible(const GemmCall& g) {
-  if (g.a_kind_override >= 0) return false;
+  if (g.a_kind_override >= 0 || g.b_kind_override >= 0) return false;
   // the tensor-core epilogues neither scale nor add anything but an
   // unscaled FP32 tile (a 16-bit reduce-add would round twice)
   if (g.scale != 1.f || (g.accumulate && g.out != TG_F32)) return false;
@@ -680,7 +681,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
   s.B = g.B;
   s.C = g.C;
   s.a_kind = g.a_kind_override >= 0 ? g.a_kind_override : (g.in == TG_BF16 ? EK_BF16 : EK_F16);
-  s.b_kind = g.in == TG_BF16 ? EK_BF16 : EK_F16;
+  s.b_kind = g.b_kind_override >= 0 ? g.b_kind_override : (g.in == TG_BF16 ? EK_BF16 : EK_F16);
   s.out_kind = g.out == TG_F32 ? EK_F32 : (g.out == TG_BF16 ? EK_BF16 : EK_F16);
   s.batch = g.batch;
   s.M = g.M;
@@ -1143,6 +1144,180 @@ tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const vo
                         scale);
 }
 
+// ---- LoRA with FP32 factors (the factors as an optimizer keeps them; activations 16-bit)
+
+static size_t w32_generic_grad_ws(int64_t T, int64_t d_in, int64_t d_out, int64_t r, tg_dtype in, int sms) {
+  // dH = dY . B (FP32, CUDA cores) and dB = dY^T . H (FP32 out) run one after the other
+  const size_t b = gemm_ws_bytes(LAYOUT_TN, d_out, r, T, 1, in, TG_F32, sms);
+  (void)d_in;
+  return (static_cast<size_t>(T * r * 4) + 255) / 256 * 256 + b;
+}
+
+static size_t w32_ws(int which, int64_t T, int64_t d_in, int64_t d_out, int64_t r, tg_dtype in, int sms) {
+  const size_t stream = r == 16 ? lora_w32_ws_bytes(which, T, d_in, d_out, sms) : 0;
+  const size_t generic = which == 2 ? w32_generic_grad_ws(T, d_in, d_out, r, in, sms) : 0;
+  return stream > generic ? stream : generic;
+}
+
+tg_status tg_lora_down_f32w(const void* X, const float* A, void* H, int64_t T, int64_t d_in, int64_t r, tg_dtype in,
+                            tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_in, r}));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(A, r * d_in, 4));
+  TG_TRY(check_ptr(H, T * r, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_in > 0 && lora_stream_ok(r, {d_in}, {X})) {
+    const size_t need = lora_w32_ws_bytes(0, T, d_in, 0, ctx->sms);
+    if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
+      record("lora_down_f32w stream: workspace too small");
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    LoraArgs a{};
+    a.X = X;
+    a.A = A;
+    a.out = H;
+    a.ws = static_cast<float*>(ws);
+    a.T = T;
+    a.d_in = d_in;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
+    a.w32 = 1;
+    cudaError_t e = lora_down_launch(a);
+    record(std::string("lora_down_f32w stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  GemmCall g{LAYOUT_NT, X, A, H, 1, T, r, d_in, d_in, d_in, T * d_in, r * d_in, in, out, -1, nullptr, 0, st,
+             "lora_down_f32w"};
+  g.b_kind_override = EK_F32;
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_lora_up_f32w(const void* H, const float* B, void* Y, int64_t T, int64_t d_out, int64_t r, tg_dtype in,
+                          tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, r}));
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(B, d_out * r, 4));
+  TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_out > 0 && lora_stream_ok(r, {d_out}, {H, Y})) {
+    const size_t need = lora_w32_ws_bytes(1, T, 0, d_out, ctx->sms);
+    if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
+      record("lora_up_f32w stream: workspace too small");
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    LoraArgs a{};
+    a.H = H;
+    a.B = B;
+    a.out = Y;
+    a.ws = static_cast<float*>(ws);
+    a.T = T;
+    a.d_out = d_out;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
+    a.w32 = 1;
+    cudaError_t e = lora_up_launch(a);
+    record(std::string("lora_up_f32w stream T=") + std::to_string(T) + " d_out=" + std::to_string(d_out) + " " +
+           (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  GemmCall g{LAYOUT_NT, H, B, Y, 1, T, d_out, r, r, r, T * r, d_out * r, in, out, -1, nullptr, 0, st,
+             "lora_up_f32w"};
+  g.b_kind_override = EK_F32;
+  return run_gemm(g, ctx);
+}
+
+tg_status tg_lora_grad_f32w(const void* X, const float* A, const float* B, const void* H, const void* dY, float* dA,
+                            float* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in, int64_t d_out, int64_t r,
+                            tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_in, d_out, r}));
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(A, r * d_in, 4));
+  TG_TRY(check_ptr(B, d_out * r, 4));
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(dA, r * d_in, 4));
+  TG_TRY(check_ptr(dB, d_out * r, 4));
+  TG_TRY(check_ptr(dX, T * d_in, dt_bytes(out)));
+  if (dH_f32 && !aligned(dH_f32, 4)) return TG_ERR_MISALIGNED;
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T > 0 && d_in > 0 && d_out > 0 && lora_stream_ok(r, {d_in, d_out}, {X, dY, dX, dH_f32, H})) {
+    const size_t need = lora_w32_ws_bytes(2, T, d_in, d_out, ctx->sms);
+    if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
+      record("lora_grad_f32w stream: workspace too small");
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    LoraArgs a{};
+    a.X = X;
+    a.A = A;
+    a.B = B;
+    a.H = H;
+    a.dY = dY;
+    a.out = dA;
+    a.out2 = dB;
+    a.out3 = dX;
+    a.out4 = dH_f32;
+    a.ws = static_cast<float*>(ws);
+    a.T = T;
+    a.d_in = d_in;
+    a.d_out = d_out;
+    a.r = r;
+    a.in_kind = in == TG_BF16 ? EK_BF16 : EK_F16;
+    a.out_kind = out == TG_F32 ? EK_F32 : a.in_kind;
+    a.num_sms = ctx->sms;
+    a.stream = st;
+    a.status = ctx->status;
+    a.timeout_ns = ctx->timeout_ns;
+    a.scale = 1.f;
+    a.w32 = 1;
+    cudaError_t e = lora_grad_launch(a);
+    record(std::string("lora_grad_f32w stream T=") + std::to_string(T) + " d_in=" + std::to_string(d_in) +
+           " d_out=" + std::to_string(d_out) + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  // general composition on the CUDA cores for the FP32 factor operands
+  const size_t dh_bytes = dH_f32 ? 0 : (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
+  const size_t total = w32_generic_grad_ws(T, d_in, d_out, r, in, ctx->sms);
+  const size_t sub = total - (static_cast<size_t>(T * r * 4) + 255) / 256 * 256;
+  if (dh_bytes + sub > 0 && (ws == nullptr || ws_bytes < dh_bytes + sub || !aligned(ws, 256)))
+    return TG_ERR_WORKSPACE_TOO_SMALL;
+  float* dH = dH_f32 ? dH_f32 : static_cast<float*>(ws);
+  void* sub_ws = static_cast<char*>(ws) + dh_bytes;
+  // dH = dY . B (FP32)
+  GemmCall g1{LAYOUT_NN, dY, B, dH, 1, T, r, d_out, d_out, r, T * d_out, d_out * r, in, TG_F32, -1, nullptr, 0, st,
+              "lora_grad_f32w.dH"};
+  g1.b_kind_override = EK_F32;
+  TG_TRY(run_gemm(g1, ctx));
+  // dB = dY^T . H (FP32)
+  GemmCall g2{LAYOUT_TN, dY, H, dB, 1, d_out, r, T, d_out, r, T * d_out, T * r, in, TG_F32, -1, sub_ws, sub, st,
+              "lora_grad_f32w.dB"};
+  TG_TRY(run_gemm(g2, ctx));
+  // dA = dH^T . X (FP32)  and  dX = dH . A
+  GemmCall g3{LAYOUT_TN, dH, X, dA, 1, r, d_in, T, r, d_in, T * r, T * d_in, in, TG_F32, EK_F32, nullptr, 0, st,
+              "lora_grad_f32w.dA"};
+  TG_TRY(run_gemm(g3, ctx));
+  GemmCall g4{LAYOUT_NN, dH, A, dX, 1, T, d_in, r, r, d_in, T * r, r * d_in, in, out, EK_F32, nullptr, 0, st,
+              "lora_grad_f32w.dX"};
+  g4.b_kind_override = EK_F32;
+  return run_gemm(g4, ctx);
+}
+
 size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in, tg_dtype out) {
   const bool layer = op == TG_OP_GEMM_FWD || op == TG_OP_GEMM_DGRAD || op == TG_OP_GEMM_WGRAD;
   if (!(layer ? dtype_in_ok_layer(in) : dtype_in_ok(in)) || !dtype_out_ok(in, out)) return SIZE_MAX;
@@ -1162,6 +1337,9 @@ size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d
       const size_t b = d3 == 16 ? lora_grad_ws_bytes(d0, d1, d2, d3, ctx->sms) : 0;
       return a > b ? a : b;
     }
+    case TG_OP_LORA_DOWN_F32W: return w32_ws(0, d0, d1, 0, d2, in, ctx->sms);
+    case TG_OP_LORA_UP_F32W: return w32_ws(1, d0, 0, d1, d2, in, ctx->sms);
+    case TG_OP_LORA_GRAD_F32W: return w32_ws(2, d0, d1, d2, d3, in, ctx->sms);
     case TG_OP_BMM_ATTN: {
       GemmCall g;
       if (!attn_call(static_cast<tg_attn_op>(d0), nullptr, nullptr, nullptr, d1, d2, d3, in, out, nullptr, 0,

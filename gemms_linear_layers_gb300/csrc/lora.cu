@@ -242,6 +242,7 @@ struct RoleBars {
 // ===================================================================
 struct RdArgs {
   int T, K, R, CH, stages;
+  int sparts;  // factor parts per chunk: 1, or 2 (hi and lo 16-bit parts of an FP32 factor)
   int nfull;  // whole 64-column chunks
   int nst3;   // stages of whole chunks (3-D boxes)
   int tail;   // 1: one more stage with the partial chunk
@@ -259,10 +260,12 @@ __host__ __device__ inline int rd_r16(int R) { return (R + 15) & ~15; }
 // IN part of a stage: the rows a consumer may address (the last chunk's row
 // groups run R16 - R rows past its box), rounded to the 1024-byte swizzle atom
 __host__ __device__ inline int rd_xs(int R, int CH) { return ((CH * R + rd_r16(R) - R) * 128 + 1023) & ~1023; }
-__host__ __device__ inline int rd_ring_bytes(int R, int CH, int stages) { return stages * (rd_xs(R, CH) + CH * 2048); }
+__host__ __device__ inline int rd_ring_bytes(int R, int CH, int stages, int sparts) {
+  return stages * (rd_xs(R, CH) + CH * 2048 * sparts);
+}
 // the role's share of shared memory (1024-byte multiple)
-__host__ __device__ inline int rd_region_bytes(int R, int CH, int stages) {
-  return (rd_ring_bytes(R, CH, stages) + RD_RED_BYTES + BAR_BYTES + 1023) & ~1023;
+__host__ __device__ inline int rd_region_bytes(int R, int CH, int stages, int sparts) {
+  return (rd_ring_bytes(R, CH, stages, sparts) + RD_RED_BYTES + BAR_BYTES + 1023) & ~1023;
 }
 // 16-byte chunk `chunk` of 128-byte row `seg` counted from a 1024-aligned base
 __device__ __forceinline__ uint32_t sw128s(uint32_t base, int seg, int chunk) {
@@ -271,10 +274,11 @@ __device__ __forceinline__ uint32_t sw128s(uint32_t base, int seg, int chunk) {
 
 struct RdMaps {
   CUtensorMap x, s, x3, s3;  // 2-D (partial chunk) and 3-D (whole chunks) views
+  CUtensorMap slo, s3lo;     // the same views of the factor's lo part (sparts = 2)
 };
 
 __device__ __forceinline__ RoleBars rd_bars(const RdArgs& a, uint8_t* smem) {
-  return RoleBars(smem + rd_ring_bytes(a.R, a.CH, a.stages) + RD_RED_BYTES);
+  return RoleBars(smem + rd_ring_bytes(a.R, a.CH, a.stages, a.sparts) + RD_RED_BYTES);
 }
 
 __device__ __forceinline__ void rowdown_init(const RdArgs& a, const RdMaps* m, uint8_t* smem, int tid) {
@@ -283,20 +287,25 @@ __device__ __forceinline__ void rowdown_init(const RdArgs& a, const RdMaps* m, u
     if (a.nst3 > 0) {
       prefetch_tmap(&m->x3);
       prefetch_tmap(&m->s3);
+      if (a.sparts == 2) prefetch_tmap(&m->s3lo);
     }
     if (a.tail) {
       prefetch_tmap(&m->x);
       prefetch_tmap(&m->s);
+      if (a.sparts == 2) prefetch_tmap(&m->slo);
     }
   }
 }
 
-template <bool BF16, bool S_KN>
+// SLO: the factor is an FP32 one given as hi + lo 16-bit parts (sparts = 2):
+// each stage also holds the lo chunks, after the hi ones, and every MMA with
+// the factor is issued for both parts into the same FP32 accumulators.
+template <bool BF16, bool S_KN, bool SLO = false>
 __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t* smem, int tid, int bar_id) {
   const int R16 = rd_r16(a.R);
-  const int stage_bytes = a.xs + a.CH * 2048;
+  const int stage_bytes = a.xs + a.CH * 2048 * (SLO ? 2 : 1);
   const uint32_t sbase = smem_u32(smem);
-  float* red = reinterpret_cast<float*>(smem + rd_ring_bytes(a.R, a.CH, a.stages));
+  float* red = reinterpret_cast<float*>(smem + rd_ring_bytes(a.R, a.CH, a.stages, SLO ? 2 : 1));
   const RoleBars rb = rd_bars(a, smem);
   volatile int* abort_flag = rb.flags;
   const int warp = tid >> 5, lane = tid & 31;
@@ -319,17 +328,22 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
       const uint32_t fb = smem_u32(&rb.full[slot]);
       const uint32_t xd = sbase + static_cast<uint32_t>(slot * stage_bytes);
       const uint32_t sd = xd + static_cast<uint32_t>(a.xs);
+      const uint32_t sdl = sd + static_cast<uint32_t>(a.CH * 2048);  // SLO: the lo chunks
       if (s < a.nst3) {
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.CH * (a.R * 128 + 2048)));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.CH * (a.R * 128 + 2048 * (SLO ? 2 : 1))));
         tma_load_3d(xd, &mp->x3, fb, 0, row0, s * a.CH);
         tma_load_3d(sd, &mp->s3, fb, 0, 0, s * a.CH);
+        if (SLO) tma_load_3d(sdl, &mp->s3lo, fb, 0, 0, s * a.CH);
       } else {  // the partial last chunk
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.R * 128 + 2048));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.R * 128 + 2048 * (SLO ? 2 : 1)));
         tma_load_3d(xd, &mp->x, fb, a.nfull * 64, row0, 0);
-        if (S_KN)
+        if (S_KN) {
           tma_load_3d(sd, &mp->s, fb, 0, a.nfull * 64, 0);
-        else
+          if (SLO) tma_load_3d(sdl, &mp->slo, fb, 0, a.nfull * 64, 0);
+        } else {
           tma_load_3d(sd, &mp->s, fb, a.nfull * 64, 0, 0);
+          if (SLO) tma_load_3d(sdl, &mp->slo, fb, a.nfull * 64, 0, 0);
+        }
       }
       issued[slot] = static_cast<int>(ph);
     }
@@ -357,15 +371,22 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
     if (s < a.nst3 || cw == 0) {
       const uint32_t xb = sbase + static_cast<uint32_t>(slot * stage_bytes);
       const uint32_t sb = xb + static_cast<uint32_t>(a.xs + cw * 2048);
+      const uint32_t sbl = sb + static_cast<uint32_t>(a.CH * 2048);  // SLO: this chunk's lo part
       const int seg0 = cw * a.R;  // first 128-byte row of this chunk in the stage
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         // b[0..1]: n-block 0 (r 0-7), b[2..3]: n-block 1 (r 8-15)
-        uint32_t b[4];
+        uint32_t b[4], bl[4];
         if (S_KN)
           ldsm_x4_t(sw32(sb, kk * 16 + (m & 1) * 8 + i, m >> 1), b);
         else
           ldsm_x4(sw128(sb, (m >> 1) * 8 + i, 2 * kk + (m & 1)), b);
+        if (SLO) {
+          if (S_KN)
+            ldsm_x4_t(sw32(sbl, kk * 16 + (m & 1) * 8 + i, m >> 1), bl);
+          else
+            ldsm_x4(sw128(sbl, (m >> 1) * 8 + i, 2 * kk + (m & 1)), bl);
+        }
 #pragma unroll
         for (int rg = 0; rg < 2; ++rg) {
           if (rg < nrg && rg % rgs == rg0) {
@@ -373,6 +394,10 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
             ldsm_x4(sw128s(xb, seg0 + rg * 16 + (m & 1) * 8 + i, 2 * kk + (m >> 1)), af);
             mma_16816<BF16>(acc[rg][0], af, b);
             mma_16816<BF16>(acc[rg][1], af, b + 2);
+            if (SLO) {
+              mma_16816<BF16>(acc[rg][0], af, bl);
+              mma_16816<BF16>(acc[rg][1], af, bl + 2);
+            }
           }
         }
       }
@@ -446,6 +471,7 @@ struct CrArgs {
   int out_kind;
   int add;       // UP: out += scale * the row-up (one rounding) instead of out = the row-up (the kernel's
                  // ADD instance)
+  int s2parts;   // UP: parts of the S2 tile, 1, or 2 (hi and lo 16-bit parts of an FP32 factor)
   float scale;   // also multiplies the ordered sums of the partials (1: unchanged bits)
   unsigned long long timeout_ns;
   unsigned int* status;
@@ -469,17 +495,19 @@ __host__ __device__ inline int cr_cta_of(long long p, const CrArgs& a) {
   return c;
 }
 
-__host__ __device__ inline int cr_stage_bytes(int nh, bool up) { return 32768 + nh * 4096 + (up ? 4096 : 0); }
-__host__ __device__ inline int cr_region_bytes(int stages, int nh, bool up) {
-  return (stages * cr_stage_bytes(nh, up) + BAR_BYTES + 1023) & ~1023;
+__host__ __device__ inline int cr_stage_bytes(int nh, bool up, bool s2lo = false) {
+  return 32768 + nh * 4096 + (up ? 4096 : 0) + (up && s2lo ? 4096 : 0);
+}
+__host__ __device__ inline int cr_region_bytes(int stages, int nh, bool up, bool s2lo = false) {
+  return (stages * cr_stage_bytes(nh, up, s2lo) + BAR_BYTES + 1023) & ~1023;
 }
 
 struct CrMaps {
-  CUtensorMap in, h, hlo, s2;
+  CUtensorMap in, h, hlo, s2, s2lo;
 };
 
 __device__ __forceinline__ RoleBars cr_bars(const CrArgs& a, int nh, bool up, uint8_t* smem) {
-  return RoleBars(smem + a.stages * cr_stage_bytes(nh, up));
+  return RoleBars(smem + a.stages * cr_stage_bytes(nh, up, a.s2parts == 2));
 }
 
 template <bool HILO, bool UP>
@@ -490,6 +518,7 @@ __device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, ui
     prefetch_tmap(&m->h);
     if (HILO) prefetch_tmap(&m->hlo);
     if (UP) prefetch_tmap(&m->s2);
+    if (UP && a.s2parts == 2) prefetch_tmap(&m->s2lo);
   }
 }
 
@@ -500,10 +529,12 @@ __device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, ui
 __host__ __device__ inline int ru_old_buf(int out_kind) { return 8 * (out_kind == EK_F32 ? 2 : 1) * 512; }
 __host__ __device__ inline int ru_old_bytes(int out_kind) { return LCW * 2 * ru_old_buf(out_kind); }
 
-template <bool BF16, bool HILO, bool UP, bool ADD = false>
+// SLO (with UP): S2 is an FP32 factor given as hi + lo 16-bit parts; the lo
+// tile follows the hi one in each stage and the row-up adds its products too.
+template <bool BF16, bool HILO, bool UP, bool ADD = false, bool SLO = false>
 __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid) {
   constexpr int NH = HILO ? 2 : 1;
-  constexpr int SB = 32768 + NH * 4096 + (UP ? 4096 : 0);
+  constexpr int SB = 32768 + NH * 4096 + (UP ? 4096 : 0) + (UP && SLO ? 4096 : 0);
   constexpr int HOFF = 32768, S2OFF = 32768 + NH * 4096;
   const int cta = blockIdx.x;
   if (cta >= a.G) return;
@@ -540,6 +571,10 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         tma_load_3d(dst + S2OFF, &mp->s2, fb, jb * CR_CB, 0, 0);
         tma_load_3d(dst + S2OFF + 2048, &mp->s2, fb, jb * CR_CB + 64, 0, 0);
       }
+      if (UP && SLO) {
+        tma_load_3d(dst + S2OFF + 4096, &mp->s2lo, fb, jb * CR_CB, 0, 0);
+        tma_load_3d(dst + S2OFF + 6144, &mp->s2lo, fb, jb * CR_CB + 64, 0, 0);
+      }
       issued[slot] = static_cast<int>(ph);
     }
     return;
@@ -553,7 +588,7 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
     uint32_t bup[4][4][2];  // B fragments of the column block (4 groups of 32 columns x 4 N-tiles)
     bool uok = true;
     const int ow = a.out_kind == EK_F32 ? 2 : 1, esz = a.out_kind == EK_F32 ? 4 : 2;  // ADD staging words, bytes
-    const uint32_t obase0 = sbase + static_cast<uint32_t>(cr_region_bytes(a.stages, NH, UP) +
+    const uint32_t obase0 = sbase + static_cast<uint32_t>(cr_region_bytes(a.stages, NH, UP, SLO) +
                                                           w * 2 * ru_old_buf(a.out_kind));
     // ADD: copy the old outputs of step sp into staging buffer sp & 1 (one commit group)
     auto stage_old = [&](int sp) {
@@ -616,8 +651,10 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         ldsm_x4(sw32(st + HOFF, w * 16 + (m & 1) * 8 + i, m >> 1), ah);
         if (HILO) ldsm_x4(sw32(st + HOFF + 4096, w * 16 + (m & 1) * 8 + i, m >> 1), al);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));  // the stage is no longer read
+      if (!SLO || !uok) {  // SLO reads the stage's lo tile below: it frees the stage after that
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));  // the stage is no longer read
+      }
       if (!uok) continue;
       const int ra = t0 + w * 16 + g, rb2 = ra + 8;
 #pragma unroll
@@ -628,6 +665,22 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
           d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
           mma_16816<BF16>(d[t], ah, bup[q][t]);
           if (HILO) mma_16816<BF16>(d[t], al, bup[q][t]);
+          if (SLO) {
+            // the lo fragment, read from this stage as bup was (the lo part times
+            // the lo part of Hm is below FP32 resolution and is left out)
+            const int col = 32 * (q & 1) + 8 * (g >> 1) + 2 * t + (g & 1);
+            const uint32_t s2l = st + S2OFF + 4096 + (q >> 1) * 2048;
+            uint32_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = (u >> 1) * 8 + 2 * c + (u & 1);
+              uint16_t x;
+              asm volatile("ld.shared.u16 %0, [%1];" : "=h"(x) : "r"(sw128(s2l, r, col >> 3) + (col & 7) * 2));
+              v[u] = x;
+            }
+            const uint32_t bl[2] = {v[0] | (v[1] << 16), v[2] | (v[3] << 16)};
+            mma_16816<BF16>(d[t], ah, bl);
+          }
         }
         const int j = jb * CR_CB + 32 * q + 8 * c;  // this thread's 8 consecutive columns
         if (ADD && q == 0) cp_async_wait_group1();  // this step's staged old outputs have landed
@@ -662,6 +715,10 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
             store8(a.out, a.out_kind, static_cast<size_t>(rb2) * a.J + j, v);
           }
         }
+      }
+      if (SLO) {  // the lo tile has been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));
       }
     }
     if (ADD) cp_async_wait_all();  // no copy outlives the kernel (a step given up after a failed wait)
@@ -766,6 +823,7 @@ constexpr int RU_PRE = 4;
 struct RuArgs {
   const uint16_t* H;
   const uint16_t* S2;
+  const uint16_t* S2lo;  // SLO: lo part of an FP32 factor given as hi (S2) + lo
   void* out;
   int out_kind;
   int T, J, n_t;
@@ -789,20 +847,25 @@ __device__ __forceinline__ void put8(const RuArgs& a, size_t i, float* v, const 
 // ADD: the old outputs of the RU_PRE blocks are read together with their Hm
 // fragments, so that every thread has all of its reads in flight at once
 // instead of one 16-byte read ahead of each store.
-template <bool BF16, bool ADD>
+template <bool BF16, bool ADD, bool SLO = false>
 __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int J = a.J, T = a.T;
   const int j0 = cta_j * 256 + warp * 32;
   if (j0 >= J) return;
   // B fragments for the 4 n-blocks: column of n-slot g in block jb
-  uint32_t bfr[4][2];
+  uint32_t bfr[4][2], bfl[SLO ? 4 : 1][2];
 #pragma unroll
   for (int jb = 0; jb < 4; ++jb) {
     const int col = j0 + 8 * (g >> 1) + 2 * jb + (g & 1);
     const uint2 v = col < J ? ld8(a.S2 + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
     bfr[jb][0] = v.x;
     bfr[jb][1] = v.y;
+    if (SLO) {
+      const uint2 w = col < J ? ld8(a.S2lo + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
+      bfl[SLO ? jb : 0][0] = w.x;
+      bfl[SLO ? jb : 0][1] = w.y;
+    }
   }
   const bool colv = j0 + 8 * c < J;  // this thread's 8 output columns exist (J % 8 == 0)
   const int nblk = (T + 15) / 16;
@@ -830,7 +893,10 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
       for (int jb = 0; jb < 4; ++jb) acc[jb][0] = acc[jb][1] = acc[jb][2] = acc[jb][3] = 0.f;
       const uint32_t ah[4] = {ha[u].x, hb[u].x, ha[u].y, hb[u].y};
 #pragma unroll
-      for (int jb = 0; jb < 4; ++jb) mma_16816<BF16>(acc[jb], ah, bfr[jb]);
+      for (int jb = 0; jb < 4; ++jb) {
+        mma_16816<BF16>(acc[jb], ah, bfr[jb]);
+        if (SLO) mma_16816<BF16>(acc[jb], ah, bfl[SLO ? jb : 0]);
+      }
       // thread (g, c): rows ra / rb, columns j0 + 8c + 2*jb + {0,1}
       if (colv) {
         float v[8];
@@ -861,7 +927,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 }
 
 // H = X A^T
-template <bool BF16>
+template <bool BF16, bool SLO>
 __global__ void __launch_bounds__(LGROUP, 1) lora_down_kernel(const __grid_constant__ RdMaps maps, const RdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
@@ -871,22 +937,22 @@ __global__ void __launch_bounds__(LGROUP, 1) lora_down_kernel(const __grid_const
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  rowdown_run<BF16, false>(blockIdx.x, &maps, a, smem, threadIdx.x, 1);
+  rowdown_run<BF16, false, SLO>(blockIdx.x, &maps, a, smem, threadIdx.x, 1);
 }
 
 // Y = H B^T
-template <bool BF16, bool ADD>
+template <bool BF16, bool ADD, bool SLO>
 __global__ void __launch_bounds__(256) lora_up_kernel(const RuArgs a) {
   pdl_wait();
   pdl_trigger();
-  rowup_role<BF16, ADD>(blockIdx.x, blockIdx.y, a);
+  rowup_role<BF16, ADD, SLO>(blockIdx.x, blockIdx.y, a);
 }
 
 // Pass 1 over dY, two roles per CTA (threads 0..287 and 288..575):
 // row-down dH = dY B (FP32, and its hi/lo parts) for the CTA's rows, and the
 // column reduction dB = dY^T H over the CTA's share of (column block, step)
 // space (partials only).
-template <bool BF16>
+template <bool BF16, bool SLO>
 __global__ void __launch_bounds__(2 * LGROUP, 1)
     lora_grad1_kernel(const __grid_constant__ RdMaps rmaps, const __grid_constant__ CrMaps cmaps, const RdArgs rd,
                       const CrArgs cr, int rd_region) {
@@ -904,7 +970,7 @@ __global__ void __launch_bounds__(2 * LGROUP, 1)
   pdl_wait();
   pdl_trigger();
   if (tid < LGROUP) {
-    if (static_cast<int>(blockIdx.x) * rd.R < rd.T) rowdown_run<BF16, true>(blockIdx.x, &rmaps, rd, smem, tid, 1);
+    if (static_cast<int>(blockIdx.x) * rd.R < rd.T) rowdown_run<BF16, true, SLO>(blockIdx.x, &rmaps, rd, smem, tid, 1);
   } else {
     colred_run<BF16, false, false>(&cmaps, cr, smem_cr, tid - LGROUP);
   }
@@ -913,7 +979,7 @@ __global__ void __launch_bounds__(2 * LGROUP, 1)
 // Pass 2 over X: each step reads an X tile with its dH hi/lo tiles and the
 // matching columns of A; one warp group accumulates dA^T = X^T dH (partials),
 // the other writes the dX = dH A tile.
-template <bool BF16, bool ADD>
+template <bool BF16, bool ADD, bool SLO>
 __global__ void __launch_bounds__(LGROUP_UP, 1)
     lora_grad2_kernel(const __grid_constant__ CrMaps cmaps, const CrArgs cr) {
   extern __shared__ uint8_t smem_raw[];
@@ -925,7 +991,7 @@ __global__ void __launch_bounds__(LGROUP_UP, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  colred_run<BF16, true, true, ADD>(&cmaps, cr, smem, tid);
+  colred_run<BF16, true, true, ADD, SLO>(&cmaps, cr, smem, tid);
 }
 
 // Pass 3: dB and dA from the partials of passes 1 and 2.  CTA b takes
@@ -973,8 +1039,9 @@ static unsigned long long* trace_ptr(int which) {
 
 // Row-down plan: R rows per CTA (about one CTA per SM, at most 32 rows),
 // CH 64-column chunks per stage, as many stages as fit in smem_budget.
-static RdArgs rd_plan(int64_t T, int64_t K, int sms, int CH, int smem_budget) {
+static RdArgs rd_plan(int64_t T, int64_t K, int sms, int CH, int smem_budget, int sparts = 1) {
   RdArgs r{};
+  r.sparts = sparts;
   r.T = static_cast<int>(T);
   r.K = static_cast<int>(K);
   r.R = clampi((T + sms - 1) / sms, 1, 32);
@@ -984,42 +1051,56 @@ static RdArgs rd_plan(int64_t T, int64_t K, int sms, int CH, int smem_budget) {
   r.nst3 = (r.nfull + r.CH - 1) / r.CH;
   r.tail = K % 64 != 0 ? 1 : 0;
   r.xs = rd_xs(r.R, r.CH);
-  const int per_stage = r.xs + r.CH * 2048;
+  const int per_stage = r.xs + r.CH * 2048 * sparts;
   r.stages = clampi((smem_budget - RD_RED_BYTES - BAR_BYTES - 1023) / per_stage, 1, LMAX_STAGES);
   if (r.stages > r.nst3 + r.tail) r.stages = r.nst3 + r.tail;
   return r;
 }
 
 // 2-D maps (the partial last chunk) and 3-D chunked views (whole chunks) of
-// the streamed tensor IN [T][K] and of the factor S
-static bool rd_maps(RdMaps* m, const void* in, const void* S, int kind, const RdArgs& r, bool s_kn) {
-  const uint64_t T = r.T, K = r.K;
-  if (!encode_tmap_3d(&m->x, in, kind, K, T, 1, K * 2, K * T * 2, 64, r.R, 128)) return false;
+// the streamed tensor IN [T][K] and of the factor S (and of its lo part Slo,
+// when the factor is an FP32 one split into two 16-bit parts)
+static bool rd_factor_maps(CUtensorMap* s2d, CUtensorMap* s3d, const void* S, int kind, const RdArgs& r, bool s_kn) {
+  const uint64_t K = r.K;
   if (s_kn) {
-    if (!encode_tmap_3d(&m->s, S, kind, LR, K, 1, LR * 2, LR * K * 2, LR, 64, 32)) return false;
+    if (!encode_tmap_3d(s2d, S, kind, LR, K, 1, LR * 2, LR * K * 2, LR, 64, 32)) return false;
   } else {
-    if (!encode_tmap_3d(&m->s, S, kind, K, LR, 1, K * 2, K * LR * 2, 64, LR, 128)) return false;
+    if (!encode_tmap_3d(s2d, S, kind, K, LR, 1, K * 2, K * LR * 2, 64, LR, 128)) return false;
   }
-  if (r.nfull == 0) {  // no whole chunk: the 3-D views are never used
-    m->x3 = m->x;
-    m->s3 = m->s;
+  if (r.nfull == 0) {  // no whole chunk: the 3-D view is never used
+    *s3d = *s2d;
     return true;
   }
   const uint64_t nf = r.nfull;
-  {  // IN as [chunk][row][64]
-    const uint64_t d[3] = {64, T, nf}, st[2] = {K * 2, 128};
-    const uint32_t b[3] = {64, static_cast<uint32_t>(r.R), static_cast<uint32_t>(r.CH)};
-    if (!encode_tmap_nd(&m->x3, in, kind, 3, d, st, b, 128)) return false;
-  }
   if (s_kn) {  // S [K][16] as [chunk][64 k][16]
     const uint64_t d[3] = {LR, 64, nf}, st[2] = {LR * 2, 64 * LR * 2};
     const uint32_t b[3] = {LR, 64, static_cast<uint32_t>(r.CH)};
-    return encode_tmap_nd(&m->s3, S, kind, 3, d, st, b, 32);
+    return encode_tmap_nd(s3d, S, kind, 3, d, st, b, 32);
   }
   // S [16][K] as [chunk][16][64]
   const uint64_t d[3] = {64, LR, nf}, st[2] = {K * 2, 128};
   const uint32_t b[3] = {64, LR, static_cast<uint32_t>(r.CH)};
-  return encode_tmap_nd(&m->s3, S, kind, 3, d, st, b, 128);
+  return encode_tmap_nd(s3d, S, kind, 3, d, st, b, 128);
+}
+
+static bool rd_maps(RdMaps* m, const void* in, const void* S, const void* Slo, int kind, const RdArgs& r, bool s_kn) {
+  const uint64_t T = r.T, K = r.K;
+  if (!encode_tmap_3d(&m->x, in, kind, K, T, 1, K * 2, K * T * 2, 64, r.R, 128)) return false;
+  if (!rd_factor_maps(&m->s, &m->s3, S, kind, r, s_kn)) return false;
+  if (Slo) {
+    if (!rd_factor_maps(&m->slo, &m->s3lo, Slo, kind, r, s_kn)) return false;
+  } else {
+    m->slo = m->s;
+    m->s3lo = m->s3;
+  }
+  if (r.nfull == 0) {  // no whole chunk: the 3-D view is never used
+    m->x3 = m->x;
+    return true;
+  }
+  // IN as [chunk][row][64]
+  const uint64_t d[3] = {64, T, static_cast<uint64_t>(r.nfull)}, st[2] = {K * 2, 128};
+  const uint32_t b[3] = {64, static_cast<uint32_t>(r.R), static_cast<uint32_t>(r.CH)};
+  return encode_tmap_nd(&m->x3, in, kind, 3, d, st, b, 128);
 }
 
 // Column-reduction plan over (at most) G CTAs.
@@ -1043,35 +1124,82 @@ static CrArgs cr_plan(int64_t T, int64_t J, int G, int stages) {
 }
 
 static bool cr_maps(CrMaps* m, const void* in, const void* H, const void* Hlo, const void* S2, int kind, int64_t T,
-                    int64_t J) {
+                    int64_t J, const void* S2lo = nullptr) {
   if (!encode_tmap_3d(&m->in, in, kind, J, T, 1, J * 2, J * T * 2, 64, CR_RS, 128)) return false;
   if (!encode_tmap_3d(&m->h, H, kind, LR, T, 1, LR * 2, LR * T * 2, LR, CR_RS, 32)) return false;
   m->hlo = m->h;
   m->s2 = m->h;
+  m->s2lo = m->h;
   if (Hlo && !encode_tmap_3d(&m->hlo, Hlo, kind, LR, T, 1, LR * 2, LR * T * 2, LR, CR_RS, 32)) return false;
   if (S2 && !encode_tmap_3d(&m->s2, S2, kind, J, LR, 1, J * 2, J * LR * 2, 64, LR, 128)) return false;
+  if (S2lo && !encode_tmap_3d(&m->s2lo, S2lo, kind, J, LR, 1, J * 2, J * LR * 2, 64, LR, 128)) return false;
   return true;
 }
 
 size_t lora_down_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
 
+// ---- FP32 factors: each is split once per call into 16-bit hi and lo parts
+// (hi = RNE(w), lo = RNE(w - hi), so hi + lo is w to within 2^-18 of |w| in
+// bf16), which the streaming kernels multiply in turn into the same FP32 sums.
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) lora_split_kernel(const float* w, uint16_t* hi, uint16_t* lo, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = w[i];
+    const float h = round16<BF16>(v);
+    hi[i] = bits16<BF16>(h);
+    lo[i] = bits16<BF16>(v - h);
+  }
+}
+
+// bytes of the hi and lo parts of an FP32 factor of n elements (256-byte multiple)
+static size_t parts_bytes(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) / 256 * 256; }
+
+static cudaError_t split_factor(const float* w, uint16_t* hi, int64_t n, int in_kind, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  return launch_k(in_kind == EK_BF16 ? lora_split_kernel<true> : lora_split_kernel<false>, dim3(blocks), dim3(256), 0,
+                  st, w, hi, hi + n, n);
+}
+
+size_t lora_w32_ws_bytes(int op, int64_t T, int64_t d_in, int64_t d_out, int sms) {
+  if (op == 0) return parts_bytes(LR * d_in);   // down: A
+  if (op == 1) return parts_bytes(LR * d_out);  // up: B
+  return lora_grad_ws_bytes(T, d_in, d_out, LR, sms) + parts_bytes(LR * d_in) + parts_bytes(LR * d_out);
+}
+
 cudaError_t lora_down_launch(const LoraArgs& a) {
   if (a.T == 0) return cudaSuccess;
-  RdArgs rd = rd_plan(a.T, a.d_in, a.num_sms, 8, 212 * 1024);
+  const int sp = a.w32 ? 2 : 1;
+  RdArgs rd = rd_plan(a.T, a.d_in, a.num_sms, 8, 212 * 1024, sp);
   rd.out = a.out;
   rd.out_kind = a.out_kind;
   rd.hi = rd.lo = nullptr;
   rd.timeout_ns = a.timeout_ns;
   rd.status = a.status;
   rd.trace = trace_ptr(0);
+  const void* S = a.A;
+  const void* Slo = nullptr;
+  if (a.w32) {  // A is FP32: its hi and lo parts in the workspace
+    uint16_t* hi = reinterpret_cast<uint16_t*>(a.ws);
+    cudaError_t e = split_factor(static_cast<const float*>(a.A), hi, LR * a.d_in, a.in_kind, a.stream);
+    if (e != cudaSuccess) return e;
+    S = hi;
+    Slo = hi + LR * a.d_in;
+  }
   alignas(64) RdMaps maps;
-  if (!rd_maps(&maps, a.X, a.A, a.in_kind, rd, false)) return cudaErrorInvalidValue;
-  auto kern = a.in_kind == EK_BF16 ? lora_down_kernel<true> : lora_down_kernel<false>;
+  if (!rd_maps(&maps, a.X, S, Slo, a.in_kind, rd, false)) return cudaErrorInvalidValue;
+  const bool bf = a.in_kind == EK_BF16;
+  auto kern = a.w32 ? (bf ? lora_down_kernel<true, true> : lora_down_kernel<false, true>)
+                    : (bf ? lora_down_kernel<true, false> : lora_down_kernel<false, false>);
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>((a.T + rd.R - 1) / rd.R);
-  return launch_k(kern, dim3(grid), dim3(LGROUP), rd_region_bytes(rd.R, rd.CH, rd.stages) + 1024, a.stream, maps,
-                  rd);
+  return launch_k(kern, dim3(grid), dim3(LGROUP), rd_region_bytes(rd.R, rd.CH, rd.stages, sp) + 1024, a.stream,
+                  maps, rd);
 }
 
 static int rowup_nt(int64_t T, int64_t J, int ctas) {
@@ -1085,17 +1213,25 @@ cudaError_t lora_up_launch(const LoraArgs& a) {
   RuArgs ru{};
   ru.H = static_cast<const uint16_t*>(a.H);
   ru.S2 = static_cast<const uint16_t*>(a.B);
+  if (a.w32) {  // B is FP32: its hi and lo parts in the workspace
+    uint16_t* hi = reinterpret_cast<uint16_t*>(a.ws);
+    cudaError_t e = split_factor(static_cast<const float*>(a.B), hi, a.d_out * LR, a.in_kind, a.stream);
+    if (e != cudaSuccess) return e;
+    ru.S2 = hi;
+    ru.S2lo = hi + a.d_out * LR;
+  }
   ru.out = a.out;
   ru.out_kind = a.out_kind;
   ru.T = static_cast<int>(a.T);
   ru.J = static_cast<int>(a.d_out);
-  // one wave: 4 CTAs per SM fit the plain kernel's registers, 2 the adding one's
-  ru.n_t = rowup_nt(a.T, a.d_out, (a.add ? 2 : 4) * a.num_sms);
+  // one wave: 4 CTAs per SM fit the plain kernel's registers, 3 the FP32-factor one's, 2 the adding one's
+  ru.n_t = rowup_nt(a.T, a.d_out, (a.add ? 2 : a.w32 ? 3 : 4) * a.num_sms);
   ru.add = a.add;
   ru.scale = a.scale;
   const bool bf = a.in_kind == EK_BF16;
-  auto k = a.add ? (bf ? lora_up_kernel<true, true> : lora_up_kernel<false, true>)
-                 : (bf ? lora_up_kernel<true, false> : lora_up_kernel<false, false>);
+  auto k = a.w32 ? (bf ? lora_up_kernel<true, false, true> : lora_up_kernel<false, false, true>)
+           : a.add ? (bf ? lora_up_kernel<true, true, false> : lora_up_kernel<false, true, false>)
+                   : (bf ? lora_up_kernel<true, false, false> : lora_up_kernel<false, false, false>);
   return launch_k(k, dim3(nj, ru.n_t), dim3(256), 0, a.stream, ru);
 }
 
@@ -1110,9 +1246,9 @@ struct GradPlan {
 };
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-static GradPlan grad_plan(int64_t T, int64_t d_in, int64_t d_out, int sms, int out_kind) {
+static GradPlan grad_plan(int64_t T, int64_t d_in, int64_t d_out, int sms, int out_kind, int sparts = 1) {
   GradPlan g;
-  g.rd = rd_plan(T, d_out, sms, G1_RD_CH, G1_RD_BUDGET);
+  g.rd = rd_plan(T, d_out, sms, G1_RD_CH, G1_RD_BUDGET, sparts);
   g.g1 = static_cast<int>((T + g.rd.R - 1) / g.rd.R);
   g.crb = cr_plan(T, d_out, g.g1, G1_CR_STAGES);
   g.cra = cr_plan(T, d_in, G2_CTAS_PER_SM * sms, G2_CR_STAGES);
@@ -1133,13 +1269,30 @@ size_t lora_grad_ws_bytes(int64_t T, int64_t d_in, int64_t d_out, int64_t, int s
 
 // a.out = dA, a.out2 = dB, a.out3 = dX, a.out4 = optional dH (FP32)
 cudaError_t lora_grad_launch(const LoraArgs& a) {
-  GradPlan gp = grad_plan(a.T, a.d_in, a.d_out, a.num_sms, a.out_kind);
+  const int sp = a.w32 ? 2 : 1;
+  GradPlan gp = grad_plan(a.T, a.d_in, a.d_out, a.num_sms, a.out_kind, sp);
   char* base = reinterpret_cast<char*>(a.ws);
   float* dH = a.out4 ? static_cast<float*>(a.out4) : reinterpret_cast<float*>(base + gp.dh);
   uint16_t* hi = reinterpret_cast<uint16_t*>(base + gp.hi);
   uint16_t* lo = reinterpret_cast<uint16_t*>(base + gp.lo);
   const bool bf = a.in_kind == EK_BF16;
   const int kind = a.in_kind;
+  // factors: 16-bit as given, or (FP32) their hi and lo parts after the plan's workspace
+  const void* Ahi = a.A;
+  const void* Bhi = a.B;
+  const void* Alo = nullptr;
+  const void* Blo = nullptr;
+  if (a.w32) {
+    uint16_t* pa = reinterpret_cast<uint16_t*>(base + gp.total);
+    uint16_t* pb = reinterpret_cast<uint16_t*>(base + gp.total + parts_bytes(LR * a.d_in));
+    cudaError_t e = split_factor(static_cast<const float*>(a.A), pa, LR * a.d_in, kind, a.stream);
+    if (e == cudaSuccess) e = split_factor(static_cast<const float*>(a.B), pb, a.d_out * LR, kind, a.stream);
+    if (e != cudaSuccess) return e;
+    Ahi = pa;
+    Alo = pa + LR * a.d_in;
+    Bhi = pb;
+    Blo = pb + a.d_out * LR;
+  }
 
   // ---- pass 1: dH (row-down over dY with B) and dB partials (col-red over dY with H)
   RdArgs& rd = gp.rd;
@@ -1158,11 +1311,16 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   crb.trace = trace_ptr(1);
   alignas(64) RdMaps rmaps;
   alignas(64) CrMaps cmaps1;
-  if (!rd_maps(&rmaps, a.dY, a.B, kind, rd, true)) return cudaErrorInvalidValue;
+  if (!rd_maps(&rmaps, a.dY, Bhi, Blo, kind, rd, true)) return cudaErrorInvalidValue;
   if (!cr_maps(&cmaps1, a.dY, a.H, nullptr, nullptr, kind, a.T, a.d_out)) return cudaErrorInvalidValue;
-  const int rd_region = rd_region_bytes(rd.R, rd.CH, rd.stages);
+  // the two roles share the SM's shared memory: fewer row-down stages if they do not fit
+  while (rd.stages > 1 &&
+         1024 + rd_region_bytes(rd.R, rd.CH, rd.stages, sp) + cr_region_bytes(crb.stages, 1, false) > SMEM_LIMIT)
+    --rd.stages;
+  const int rd_region = rd_region_bytes(rd.R, rd.CH, rd.stages, sp);
   const int smem1 = 1024 + rd_region + cr_region_bytes(crb.stages, 1, false);
-  auto k1 = bf ? lora_grad1_kernel<true> : lora_grad1_kernel<false>;
+  auto k1 = a.w32 ? (bf ? lora_grad1_kernel<true, true> : lora_grad1_kernel<false, true>)
+                  : (bf ? lora_grad1_kernel<true, false> : lora_grad1_kernel<false, false>);
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(k1));
   if (e != cudaSuccess) return e;
   e = launch_k(k1, dim3(gp.g1), dim3(2 * LGROUP), smem1, a.stream, rmaps, cmaps1, rd, crb, rd_region);
@@ -1178,22 +1336,26 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   cra.status = a.status;
   cra.trace = trace_ptr(2);
   alignas(64) CrMaps cmaps2;
-  if (!cr_maps(&cmaps2, a.X, hi, lo, a.A, kind, a.T, a.d_in)) return cudaErrorInvalidValue;
-  auto k2 = a.add ? (bf ? lora_grad2_kernel<true, true> : lora_grad2_kernel<false, true>)
-                  : (bf ? lora_grad2_kernel<true, false> : lora_grad2_kernel<false, false>);
+  cra.s2parts = sp;
+  if (!cr_maps(&cmaps2, a.X, hi, lo, Ahi, kind, a.T, a.d_in, Alo)) return cudaErrorInvalidValue;
+  auto k2 = a.w32 ? (bf ? lora_grad2_kernel<true, false, true> : lora_grad2_kernel<false, false, true>)
+            : a.add ? (bf ? lora_grad2_kernel<true, true, false> : lora_grad2_kernel<false, true, false>)
+                    : (bf ? lora_grad2_kernel<true, false, false> : lora_grad2_kernel<false, false, false>);
   e = allow_smem(reinterpret_cast<const void*>(k2));
   if (e != cudaSuccess) return e;
   // the adding instance stages the old dX of two steps: one operand stage
   // fewer for 16-bit dX, two for FP32
   if (a.add) cra.stages = G2_CR_STAGES - (a.out_kind == EK_F32 ? 2 : 1);
-  const int smem2 = 1024 + cr_region_bytes(cra.stages, 2, true) + (a.add ? ru_old_bytes(a.out_kind) : 0);
+  const int smem2 =
+      1024 + cr_region_bytes(cra.stages, 2, true, a.w32 != 0) + (a.add ? ru_old_bytes(a.out_kind) : 0);
   e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), smem2, a.stream, cmaps2,
                cra);
   if (e != cudaSuccess) return e;
 
   // ---- pass 3: dB and dA from the partials
+  // dA and dB: FP32 for FP32 factors (the gradients of FP32 weights), else the output type
   return launch_k(lora_grad3_kernel, dim3((crb.nj + cra.nj) * FIN_SPLIT), dim3(256), 0, a.stream, crb, cra, a.out2,
-                  a.out, a.out_kind);
+                  a.out, a.w32 ? static_cast<int>(EK_F32) : a.out_kind);
 }
 
 }  // namespace tg

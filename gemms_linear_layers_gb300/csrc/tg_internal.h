@@ -225,12 +225,16 @@ struct LoraArgs {
   int add;                       // up projection: out += scale * H B^T; gradient: dX += scale * dH A,
                                  // dA and dB scaled
   float scale;
+  int w32;                       // A and B are FP32 (split into 16-bit hi + lo parts in ws); dA, dB FP32
 };
 size_t lora_down_ws_bytes(int64_t T, int64_t d_in, int64_t r, int num_sms);
 cudaError_t lora_down_launch(const LoraArgs& a);
 cudaError_t lora_up_launch(const LoraArgs& a);
 size_t lora_grad_ws_bytes(int64_t T, int64_t d_in, int64_t d_out, int64_t r, int num_sms);
 cudaError_t lora_grad_launch(const LoraArgs& a);
+// workspace of the FP32-factor calls (op 0 down, 1 up, 2 gradient): the
+// factors' hi/lo parts, after the gradient's own workspace
+size_t lora_w32_ws_bytes(int op, int64_t T, int64_t d_in, int64_t d_out, int sms);
 
 // wait-timeout probe kernel (api.cu)
 cudaError_t wait_probe_launch(unsigned long long timeout_ns, unsigned int* status,

@@ -84,7 +84,10 @@ typedef enum {
   TG_OP_LORA_DOWN = 3,  /* d0=T, d1=d_in, d2=r */
   TG_OP_LORA_UP = 4,    /* d0=T, d1=d_out, d2=r */
   TG_OP_LORA_GRAD = 5,  /* d0=T, d1=d_in, d2=d_out, d3=r */
-  TG_OP_BMM_ATTN = 6    /* d0=tg_attn_op, d1=batch, d2=s, d3=d */
+  TG_OP_BMM_ATTN = 6,   /* d0=tg_attn_op, d1=batch, d2=s, d3=d */
+  TG_OP_LORA_DOWN_F32W = 7,  /* d0=T, d1=d_in, d2=r */
+  TG_OP_LORA_UP_F32W = 8,    /* d0=T, d1=d_out, d2=r */
+  TG_OP_LORA_GRAD_F32W = 9   /* d0=T, d1=d_in, d2=d_out, d3=r */
 } tg_op;
 
 /* Forward product of a linear layer ("Where the time went"):
@@ -192,6 +195,31 @@ tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const vo
                            void* dA, void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in,
                            int64_t d_out, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
                            size_t ws_bytes, void* stream);
+
+/* The LoRA products with FP32 factors, as an optimizer keeps the LoRA
+ * weights, and 16-bit activations ("Tuning the kernels": the rank-16 LoRA
+ * matrices; the FP32 LoRA weights otherwise cost a conversion of every
+ * activation to FP32 or of the weights to 16 bits per call):
+ *   tg_lora_down_f32w:  H[T, r]      = X[T, d_in] . A[r, d_in]^T
+ *   tg_lora_up_f32w:    Y[T, d_out]  = H[T, r] . B[d_out, r]^T
+ *   tg_lora_grad_f32w:  dH = dY . B (FP32, optional out), dB = dY^T . H,
+ *                       dA = dH^T . X, dX = dH . A;  dA and dB FP32
+ * X, H, dY have type `in` (bf16 or fp16); A, B are FP32 and are not rounded
+ * to `in`: r = 16 splits each factor into 16-bit parts hi = RNE(w) and
+ * lo = RNE(w - hi) in `ws` (one small launch per factor) and the streaming
+ * kernels multiply both parts into the same FP32 sums, so hi + lo stands for
+ * w to within 2^-18 |w| (bf16); other ranks run on the CUDA cores with the
+ * FP32 factors as they are.  H, Y, dX have type `out`.  Workspace:
+ * tg_workspace_size(TG_OP_LORA_*_F32W, ...); arguments and errors otherwise
+ * as tg_lora_down / _up / _grad. */
+tg_status tg_lora_down_f32w(const void* X, const float* A, void* H, int64_t T, int64_t d_in, int64_t r,
+                            tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+tg_status tg_lora_up_f32w(const void* H, const float* B, void* Y, int64_t T, int64_t d_out, int64_t r,
+                          tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
+tg_status tg_lora_grad_f32w(const void* X, const float* A, const float* B, const void* H, const void* dY,
+                            float* dA, float* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in,
+                            int64_t d_out, int64_t r, tg_dtype in, tg_dtype out, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /* One of the batched products inside attention ("Tuning the kernels";
  * "Checking the results are right": batched attention), see tg_attn_op. */

@@ -108,6 +108,22 @@ def test_accumulating_entry_points_reject_bad_arguments(lib):
              B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
 
 
+def test_fp32_factor_lora_rejects_bad_arguments(lib):
+    """The FP32 factors are 4-byte elements; the activations stay 16-bit."""
+    A2 = ctypes.c_void_p(0x1002)  # aligned for 16-bit, not for FP32
+    assert lib.tg_lora_down_f32w(EVEN, A2, EVEN, 8, 8, 16, B.TG_BF16, B.TG_BF16, NULL, 0, NULL) == 3
+    assert lib.tg_lora_down_f32w(EVEN, EVEN, EVEN, 8, 8, 16, B.TG_F32, B.TG_F32, NULL, 0, NULL) == 2
+    assert lib.tg_lora_up_f32w(EVEN, A2, EVEN, 8, 8, 16, B.TG_F16, B.TG_F32, NULL, 0, NULL) == 3
+    assert lib.tg_lora_up_f32w(EVEN, EVEN, EVEN, -8, 8, 16, B.TG_F16, B.TG_F32, NULL, 0, NULL) == 1
+    f = lib.tg_lora_grad_f32w
+    assert f(EVEN, EVEN, A2, EVEN, EVEN, EVEN, EVEN, EVEN, NULL, 8, 8, 8, 16, B.TG_BF16, B.TG_BF16,
+             NULL, 0, NULL) == 3  # B
+    assert f(EVEN, EVEN, EVEN, EVEN, EVEN, A2, EVEN, EVEN, NULL, 8, 8, 8, 16, B.TG_BF16, B.TG_BF16,
+             NULL, 0, NULL) == 3  # dA is FP32
+    assert f(EVEN, EVEN, EVEN, EVEN, NULL, EVEN, EVEN, EVEN, NULL, 8, 8, 8, 16, B.TG_BF16, B.TG_BF16,
+             NULL, 0, NULL) == 1  # no dY
+
+
 def test_tile_table_reader(lib, tmp_path):
     good = tmp_path / "t.txt"
     good.write_text("# op in out M N K batch bn splits\n"

@@ -200,3 +200,62 @@ def test_lora_grad_add_rank_zero_leaves_dX():
     tg.tg_lora_grad_add(X, A, B, H, dY, dX, 3.0)
     torch.cuda.synchronize()
     assert torch.equal(dX, dX0)
+
+
+# ------------------------------------------------------- FP32 LoRA factors
+F32_SHAPES = [(256, 128, 192, 16), (130, 264, 136, 16), (4096, 2304, 5760, 16), (64, 64, 64, 8), (33, 24, 40, 4)]
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("shape", F32_SHAPES, ids=lambda t: "x".join(map(str, t)))
+def test_lora_fp32_factors(shape, dtype, out_kind):
+    """16-bit activations with FP32 A and B (not rounded to 16 bits): the
+    down, up and gradient products against the oracle on the FP32 factors;
+    dA and dB come out in FP32.  Rank 16 takes the streaming kernels with
+    the factors split into hi + lo parts, other ranks the CUDA cores."""
+    T, d_in, d_out, r = shape
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    X, _, _, H, dY = inputs.lora_inputs(T, d_in, d_out, r, dtype, tag="w32")
+    _, A, B, _, _ = inputs.lora_inputs(T, d_in, d_out, r, torch.float32, tag="w32")
+    Xc, Ac, Bc, Hc, dYc = (t.cuda() for t in (X, A, B, H, dY))
+    stream_path = r == 16
+    h = tg.tg_lora_down_f32w(Xc, Ac, out_dtype=out_dtype)
+    call = tg.tg_last_call()
+    assert ("lora_down_f32w stream" in call) == stream_path, call
+    C, S = oracle.lora_down(X, A)
+    assert_close(h, C, S, f"lora_down_f32w {shape} [{call}]", out_dtype)
+    y = tg.tg_lora_up_f32w(Hc, Bc, out_dtype=out_dtype)
+    call = tg.tg_last_call()
+    assert ("lora_up_f32w stream" in call) == stream_path, call
+    C, S = oracle.lora_up(H, B)
+    assert_close(y, C, S, f"lora_up_f32w {shape} [{call}]", out_dtype)
+    g = tg.tg_lora_grad_f32w(Xc, Ac, Bc, Hc, dYc, out_dtype=out_dtype, want_dH=True)
+    g2 = tg.tg_lora_grad_f32w(Xc, Ac, Bc, Hc, dYc, out_dtype=out_dtype, want_dH=True)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert ("lora_grad_f32w stream" in call) == stream_path, call
+    ref = oracle.lora_grad(X, A, B, H, dY)
+    assert_close(g["dH"], *ref["dH"], f"lora_grad_f32w dH {shape} [{call}]", None)
+    for name in ("dA", "dB"):
+        assert g[name].dtype == torch.float32
+        assert_close(g[name], *ref[name], f"lora_grad_f32w {name} {shape} [{call}]", torch.float32)
+    assert_close(g["dX"], *ref["dX"], f"lora_grad_f32w dX {shape} [{call}]", out_dtype)
+    for k in g:
+        assert torch.equal(g[k], g2[k]), k
+
+
+def test_lora_fp32_factors_use_the_low_part():
+    """With FP32 outputs the error against the FP32 factors is far below what
+    rounding the factors to bf16 first would give: the lo parts are used."""
+    T, d_in, d_out, r = 4096, 2304, 2304, 16
+    X, _, _, H, dY = inputs.lora_inputs(T, d_in, d_out, r, torch.bfloat16, tag="w32lo")
+    _, A, B, _, _ = inputs.lora_inputs(T, d_in, d_out, r, torch.float32, tag="w32lo")
+    h = tg.tg_lora_down_f32w(X.cuda(), A.cuda(), out_dtype=torch.float32).cpu().double().numpy()
+    y = tg.tg_lora_up_f32w(H.cuda(), B.cuda(), out_dtype=torch.float32).cpu().double().numpy()
+    for got, exact, rounded in ((h, oracle.lora_down(X, A)[0], oracle.lora_down(X, A.to(torch.bfloat16))[0]),
+                                (y, oracle.lora_up(H, B)[0], oracle.lora_up(H, B.to(torch.bfloat16))[0])):
+        err = np.abs(got - exact).max()
+        err_rounded = np.abs(rounded - exact).max()
+        assert err < 0.02 * err_rounded, (err, err_rounded)
