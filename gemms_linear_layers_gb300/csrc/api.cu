@@ -1209,9 +1209,9 @@ tg_status tg_lora_up_f32w(const void* H, const float* B, void* Y, int64_t T, int
   DevCtx* ctx = nullptr;
   TG_TRY(device_ctx(&ctx));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (T > 0 && d_out > 0 && lora_stream_ok(r, {d_out}, {H, Y})) {
+  if (T > 0 && d_out > 0 && lora_stream_ok(r, {d_out}, {H, Y, B})) {  // B: 16-byte loads of FP32 rows
     const size_t need = lora_w32_ws_bytes(1, T, 0, d_out, ctx->sms);
-    if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) {
+    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) {
       record("lora_up_f32w stream: workspace too small");
       return TG_ERR_WORKSPACE_TOO_SMALL;
     }

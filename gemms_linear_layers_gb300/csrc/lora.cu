@@ -823,7 +823,7 @@ constexpr int RU_PRE = 4;
 struct RuArgs {
   const uint16_t* H;
   const uint16_t* S2;
-  const uint16_t* S2lo;  // SLO: lo part of an FP32 factor given as hi (S2) + lo
+  const float* S2f;      // SLO: the factor in FP32, split into 16-bit hi + lo fragments in registers
   void* out;
   int out_kind;
   int T, J, n_t;
@@ -858,13 +858,25 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
 #pragma unroll
   for (int jb = 0; jb < 4; ++jb) {
     const int col = j0 + 8 * (g >> 1) + 2 * jb + (g & 1);
-    const uint2 v = col < J ? ld8(a.S2 + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
-    bfr[jb][0] = v.x;
-    bfr[jb][1] = v.y;
-    if (SLO) {
-      const uint2 w = col < J ? ld8(a.S2lo + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
-      bfl[SLO ? jb : 0][0] = w.x;
-      bfl[SLO ? jb : 0][1] = w.y;
+    if (SLO) {  // r = 4c .. 4c+3 of the FP32 factor: hi = RNE(w), lo = RNE(w - hi), packed in pairs
+      const float4 w = col < J ? *reinterpret_cast<const float4*>(a.S2f + static_cast<size_t>(col) * LR + 4 * c)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float wv[4] = {w.x, w.y, w.z, w.w};
+      uint32_t hb[4], lb[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float h = round16<BF16>(wv[e]);
+        hb[e] = bits16<BF16>(h);
+        lb[e] = bits16<BF16>(wv[e] - h);
+      }
+      bfr[jb][0] = hb[0] | (hb[1] << 16);
+      bfr[jb][1] = hb[2] | (hb[3] << 16);
+      bfl[SLO ? jb : 0][0] = lb[0] | (lb[1] << 16);
+      bfl[SLO ? jb : 0][1] = lb[2] | (lb[3] << 16);
+    } else {
+      const uint2 v = col < J ? ld8(a.S2 + static_cast<size_t>(col) * LR + 4 * c) : make_uint2(0u, 0u);
+      bfr[jb][0] = v.x;
+      bfr[jb][1] = v.y;
     }
   }
   const bool colv = j0 + 8 * c < J;  // this thread's 8 output columns exist (J % 8 == 0)
@@ -1142,32 +1154,41 @@ size_t lora_down_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
 // (hi = RNE(w), lo = RNE(w - hi), so hi + lo is w to within 2^-18 of |w| in
 // bf16), which the streaming kernels multiply in turn into the same FP32 sums.
 
+// one or two factors in one launch: element i < n1 of w1 -> (hi1, hi1 + n1),
+// element n1 + i of the index space -> element i of w2 -> (hi2, hi2 + n2)
 template <bool BF16>
-__global__ void __launch_bounds__(256) lora_split_kernel(const float* w, uint16_t* hi, uint16_t* lo, int64_t n) {
+__global__ void __launch_bounds__(256)
+    lora_split_kernel(const float* w1, uint16_t* hi1, int64_t n1, const float* w2, uint16_t* hi2, int64_t n2) {
   pdl_wait();
   pdl_trigger();
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n1 + n2;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float v = w[i];
+    const bool first = i < n1;
+    const int64_t k = first ? i : i - n1, n = first ? n1 : n2;
+    uint16_t* hi = first ? hi1 : hi2;
+    const float v = (first ? w1 : w2)[k];
     const float h = round16<BF16>(v);
-    hi[i] = bits16<BF16>(h);
-    lo[i] = bits16<BF16>(v - h);
+    hi[k] = bits16<BF16>(h);
+    hi[n + k] = bits16<BF16>(v - h);
   }
 }
 
 // bytes of the hi and lo parts of an FP32 factor of n elements (256-byte multiple)
 static size_t parts_bytes(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) / 256 * 256; }
 
-static cudaError_t split_factor(const float* w, uint16_t* hi, int64_t n, int in_kind, cudaStream_t st) {
+// parts of w1 [n1] at hi1 (hi, then lo) and, if n2 > 0, of w2 [n2] at hi2
+static cudaError_t split_factors(const float* w1, uint16_t* hi1, int64_t n1, const float* w2, uint16_t* hi2, int64_t n2,
+                                 int in_kind, cudaStream_t st) {
+  const int64_t n = n1 + n2;
   if (n == 0) return cudaSuccess;
   const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
   return launch_k(in_kind == EK_BF16 ? lora_split_kernel<true> : lora_split_kernel<false>, dim3(blocks), dim3(256), 0,
-                  st, w, hi, hi + n, n);
+                  st, w1, hi1, n1, w2, hi2, n2);
 }
 
 size_t lora_w32_ws_bytes(int op, int64_t T, int64_t d_in, int64_t d_out, int sms) {
   if (op == 0) return parts_bytes(LR * d_in);   // down: A
-  if (op == 1) return parts_bytes(LR * d_out);  // up: B
+  if (op == 1) return 0;                         // up: B is split in registers
   return lora_grad_ws_bytes(T, d_in, d_out, LR, sms) + parts_bytes(LR * d_in) + parts_bytes(LR * d_out);
 }
 
@@ -1185,7 +1206,8 @@ cudaError_t lora_down_launch(const LoraArgs& a) {
   const void* Slo = nullptr;
   if (a.w32) {  // A is FP32: its hi and lo parts in the workspace
     uint16_t* hi = reinterpret_cast<uint16_t*>(a.ws);
-    cudaError_t e = split_factor(static_cast<const float*>(a.A), hi, LR * a.d_in, a.in_kind, a.stream);
+    cudaError_t e =
+        split_factors(static_cast<const float*>(a.A), hi, LR * a.d_in, nullptr, nullptr, 0, a.in_kind, a.stream);
     if (e != cudaSuccess) return e;
     S = hi;
     Slo = hi + LR * a.d_in;
@@ -1213,13 +1235,7 @@ cudaError_t lora_up_launch(const LoraArgs& a) {
   RuArgs ru{};
   ru.H = static_cast<const uint16_t*>(a.H);
   ru.S2 = static_cast<const uint16_t*>(a.B);
-  if (a.w32) {  // B is FP32: its hi and lo parts in the workspace
-    uint16_t* hi = reinterpret_cast<uint16_t*>(a.ws);
-    cudaError_t e = split_factor(static_cast<const float*>(a.B), hi, a.d_out * LR, a.in_kind, a.stream);
-    if (e != cudaSuccess) return e;
-    ru.S2 = hi;
-    ru.S2lo = hi + a.d_out * LR;
-  }
+  if (a.w32) ru.S2f = static_cast<const float*>(a.B);  // split into hi + lo in the kernel
   ru.out = a.out;
   ru.out_kind = a.out_kind;
   ru.T = static_cast<int>(a.T);
@@ -1285,8 +1301,8 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   if (a.w32) {
     uint16_t* pa = reinterpret_cast<uint16_t*>(base + gp.total);
     uint16_t* pb = reinterpret_cast<uint16_t*>(base + gp.total + parts_bytes(LR * a.d_in));
-    cudaError_t e = split_factor(static_cast<const float*>(a.A), pa, LR * a.d_in, kind, a.stream);
-    if (e == cudaSuccess) e = split_factor(static_cast<const float*>(a.B), pb, a.d_out * LR, kind, a.stream);
+    cudaError_t e = split_factors(static_cast<const float*>(a.A), pa, LR * a.d_in, static_cast<const float*>(a.B), pb,
+                                  a.d_out * LR, kind, a.stream);
     if (e != cudaSuccess) return e;
     Ahi = pa;
     Alo = pa + LR * a.d_in;

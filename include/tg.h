@@ -206,7 +206,8 @@ tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const vo
  *                       dA = dH^T . X, dX = dH . A;  dA and dB FP32
  * X, H, dY have type `in` (bf16 or fp16); A, B are FP32 and are not rounded
  * to `in`: r = 16 splits each factor into 16-bit parts hi = RNE(w) and
- * lo = RNE(w - hi) in `ws` (one small launch per factor) and the streaming
+ * lo = RNE(w - hi) (in `ws` by one small launch, or in registers for the up
+ * product, whose B must then be 16-byte aligned) and the streaming
  * kernels multiply both parts into the same FP32 sums, so hi + lo stands for
  * w to within 2^-18 |w| (bf16); other ranks run on the CUDA cores with the
  * FP32 factors as they are.  H, Y, dX have type `out`.  Workspace:
