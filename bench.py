@@ -557,6 +557,23 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (a replicated job takes as long as its
+    slowest replica); x itself when no process group with several ranks is
+    up."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every replica's work over the slowest replica's time."""
+    return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
+
+
 # ------------------------------------------------------------------ rows
 FP32_LANES_PER_SM = 128  # FP32 FMA units per SM (4 sub-partitions x 32)
 
@@ -830,16 +847,14 @@ def main():
             total_ms, dom_ms = timed_steps_per_product(prods, args.warmup, args.steps, stream, flush, dom_name)
     torch.cuda.synchronize()
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, "cuda")
         torch.distributed.barrier()
     st = tg.tg_stream_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after the timed region: {tg.tg_status_string(st)}")
 
     ms_step = total_ms / args.steps
-    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, step_flops, args.steps, total_ms)
 
     dom_launches = dom["n"] * args.steps
     avg_launch_ms = dom_ms / dom_launches

@@ -1,5 +1,7 @@
 """Host logic of bench.py (no GPU): the kernel identity taken from a call
-record, and the waves of the optional concurrent step."""
+record, the waves of the optional concurrent step, the DRAM traffic taken
+from a committed profile, the FP32 peak, and the replicated (N > 1) timing
+over two gloo ranks."""
 import os
 import sys
 
@@ -79,3 +81,34 @@ def test_profiled_traffic_needs_matching_key_and_sources(tmp_path):
 def test_fp32_peak_from_units_and_clock():
     """152 SMs x 128 FP32 FMA units x 2 flop x 2,070 MHz."""
     assert abs(bench.fp32_peak_tflops(152, 2070.0) - 80.5478) < 1e-3
+
+
+def _two_rank_worker(rank, world, port, out_dir):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took 1.0 + 1.5 r ms: every rank must see the slowest one's time
+        t = bench.max_over_ranks(1.0 + 1.5 * rank, "cpu")
+        with open(os.path.join(out_dir, f"r{rank}.txt"), "w") as f:
+            f.write(repr(t))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_time_is_the_slowest_rank_over_gloo(tmp_path):
+    """The N > 1 path of the benchmark, as two gloo ranks on the CPU: the
+    timed region is the maximum over ranks and the job's throughput counts
+    every replica's work over that time."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.spawn(_two_rank_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        assert float((tmp_path / f"r{r}.txt").read_text()) == 2.5
+    assert bench.max_over_ranks(3.0, "cpu") == 3.0  # no process group: the rank's own time
+    # 2 replicas x 10 steps x 1e12 flop in 4 s
+    assert abs(bench.job_tflops(2, 1e12, 10, 4000.0) - 5.0) < 1e-12
