@@ -5,7 +5,7 @@ kind of kernel launch:
 
     python -m gemms_linear_layers_gb300.probe wgrad 2048 2304 2304 [--plan "256 sk n"] [--reps 20]
 
-`op` is fwd|dgrad|wgrad (dims: T d_in d_out), one of the attention products
+`op` is fwd|dgrad|wgrad (dims: T d_in d_out; --dtype f32 for FP32 operands), one of the attention products
 qk|pv|do_vt|pt_do|ds_k|dst_q (dims: heads s d), or lora_down|lora_up|lora_grad
 (dims: T d_in d_out, rank 16).  --plan "bn splits [raster]"
 writes a one-line tile table for this shape and loads it first.
@@ -32,12 +32,15 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("op")
     ap.add_argument("dims", type=int, nargs=3)
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"])
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16", "f32"],
+                    help="f32: FP32 operands and output (layer products only, CUDA-core kernel)")
     ap.add_argument("--out", default="same", choices=["same", "f32"])
     ap.add_argument("--plan", default=None, help='"bn splits [raster]"; splits may be sk')
     ap.add_argument("--reps", type=int, default=20)
     a = ap.parse_args(argv)
-    dtype = torch.bfloat16 if a.dtype == "bf16" else torch.float16
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[a.dtype]
+    if dtype == torch.float32 and a.op not in ("fwd", "dgrad", "wgrad"):
+        raise SystemExit("--dtype f32 applies to fwd, dgrad and wgrad only")
     out_dtype = dtype if a.out == "same" else torch.float32
     dev = "cuda"
     if a.op in ("fwd", "dgrad", "wgrad"):
