@@ -48,15 +48,16 @@ CSRC_DIR = os.path.join(ROOT, "gemms_linear_layers_gb300", "csrc")
 
 
 def kernel_sources_digest(csrc=None) -> str:
-    """SHA-1 over the sources that decide what a GEMM kernel reads and writes
-    (the kernels, their PTX wrappers and tensor maps; not the host planner,
-    whose changes show up as a different kernel identity, and not the LoRA
-    translation unit, whose kernels are never the step's dominant one), name
-    and bytes in name order."""
+    """SHA-1 over the sources that decide what a kernel of the step reads and
+    writes (the 16-bit GEMM kernels and reductions, their PTX wrappers and
+    tensor maps; not the host planner, whose changes show up as a different
+    kernel identity, and not the LoRA and FP32 CUDA-core translation units,
+    whose kernels are not in the step), name and bytes in name order."""
     csrc = csrc or CSRC_DIR
     h = hashlib.sha1()
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".cpp", ".h")) and name not in ("api.cu", "noalloc.cu", "lora.cu"):
+        if name.endswith((".cu", ".cuh", ".cpp", ".h")) and name not in ("api.cu", "noalloc.cu", "lora.cu",
+                                                                          "gemm_ffma.cu"):
             h.update(name.encode())
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
