@@ -770,6 +770,15 @@ def measure_rows(stream, pk, budget_s=90.0):
                          "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call),
                          "operand_sets": sets})
             del C, Cs
+        # the fused forward, softmax(Q K^T / 8) V without the [s, s] matrices (tensor-bound)
+        Os = [torch.empty(h, s, d, dtype=dt, device="cuda") for _ in range(sets)]
+        ms, call = time_calls(lambda i: (lambda: tg.tg_attn_fwd(ts[i]["Q"], ts[i]["K"], ts[i]["V"], O=Os[i])),
+                              reps=max(5, 2 * sets), sets=sets)
+        fl = 4 * h * s * s * d
+        rows.append({"set": "attention", "s": s, "op": "fused_fwd", "dtype": "bf16", "us": round(ms * 1000, 2),
+                     "tflops": round(fl / ms / 1e9, 1), "frac_of_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 3),
+                     "bound": "tensor", "kernel": call.split(" [")[0][:40], "operand_sets": sets})
+        del Os
         del t, ts
     return rows
 

@@ -9,6 +9,7 @@ the library's kernels.  If libtg.so has not been built the first call raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -46,6 +47,7 @@ SIGNATURES = {
     "tg_lora_up_f32w": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad_f32w": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
                                _vp, _sz, _vp]),
+    "tg_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp]),
     "tg_lora_grad_add": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float,
                               _i, _i, _vp, _sz, _vp]),
     "tg_bmm_attn": (_i, [_i, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -371,6 +373,20 @@ def tg_lora_grad_f32w(X, A, B, H, dY, out_dtype=None, want_dH=False, outs=None, 
     if dH is not None:
         res["dH"] = dH
     return res
+
+
+def tg_attn_fwd(Q, K, V, O=None, scale=None, out_dtype=None, stream=None):
+    """Fused attention forward: O = softmax(scale Q K^T) V per head; Q, K, V [heads, s, 64]."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _need(t, n, 3)
+    heads, s, d = Q.shape
+    if tuple(K.shape) != (heads, s, d) or tuple(V.shape) != (heads, s, d) or K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise ValueError("K and V must match Q")
+    O = _out(O, (heads, s, d), out_dtype or Q.dtype, Q.device, "O")
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    _check(lib().tg_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), heads, s, d, sc, _DT[Q.dtype], _DT[O.dtype],
+                             _stream(stream)), "tg_attn_fwd")
+    return O
 
 
 def tg_bmm_attn(op, A, B, C=None, out_dtype=None, ws=None, stream=None):

@@ -17,6 +17,7 @@
 #include <string>
 #include <unordered_map>
 
+#include "attn.h"
 #include "ptx.cuh"
 #include "tg.h"
 #include "tg_internal.h"
@@ -1316,6 +1317,26 @@ tg_status tg_lora_grad_f32w(const void* X, const float* A, const float* B, const
               "lora_grad_f32w.dX"};
   g4.b_kind_override = EK_F32;
   return run_gemm(g4, ctx);
+}
+
+tg_status tg_attn_fwd(const void* Q, const void* K, const void* V, void* O, int64_t heads, int64_t s, int64_t d,
+                      float scale, tg_dtype in, tg_dtype out, void* stream) {
+  TG_TRY(check_common(in, out, {heads, s, d}));
+  if (d != 64 || !std::isfinite(scale) || heads > 65535) return TG_ERR_INVALID_ARG;
+  const int64_t n = heads * s * d;
+  TG_TRY(check_ptr(Q, n, 2));
+  TG_TRY(check_ptr(K, n, 2));
+  TG_TRY(check_ptr(V, n, 2));
+  TG_TRY(check_ptr(O, n, dt_bytes(out)));
+  if (n > 0 && !(aligned(Q, 16) && aligned(K, 16) && aligned(V, 16) && aligned(O, 16))) return TG_ERR_MISALIGNED;
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  const int ik = in == TG_BF16 ? EK_BF16 : EK_F16;
+  const int ok = out == TG_F32 ? EK_F32 : ik;
+  cudaError_t e = attn_fwd_launch(Q, K, V, O, heads, s, d, scale, ik, ok, static_cast<cudaStream_t>(stream));
+  record(std::string("attn_fwd fused heads=") + std::to_string(heads) + " s=" + std::to_string(s) + " " +
+         (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+  return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
 size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d3, tg_dtype in, tg_dtype out) {

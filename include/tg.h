@@ -222,6 +222,18 @@ tg_status tg_lora_grad_f32w(const void* X, const float* A, const float* B, const
                             int64_t d_out, int64_t r, tg_dtype in, tg_dtype out, void* ws,
                             size_t ws_bytes, void* stream);
 
+/* Fused attention forward (the fused kernel that would replace the two
+ * batched products and the softmax between them):
+ *   O[h] = softmax(scale . Q[h] K[h]^T) V[h]     per head h, softmax over keys
+ * Q, K, V, O are [heads, s, d] contiguous; d must be 64; every pointer
+ * 16-byte aligned (TG_ERR_MISALIGNED otherwise); scale finite (the usual
+ * 1/sqrt(d)).  No mask.  The [s, s] scores never reach memory: each row's
+ * softmax is kept online in FP32 over key blocks, and the probabilities enter
+ * the second product as 16-bit hi + lo parts (to within 2^-18 of FP32).
+ * No workspace. */
+tg_status tg_attn_fwd(const void* Q, const void* K, const void* V, void* O, int64_t heads, int64_t s,
+                      int64_t d, float scale, tg_dtype in, tg_dtype out, void* stream);
+
 /* One of the batched products inside attention ("Tuning the kernels";
  * "Checking the results are right": batched attention), see tg_attn_op. */
 tg_status tg_bmm_attn(tg_attn_op op, const void* A, const void* B, void* C, int64_t batch,

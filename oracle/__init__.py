@@ -237,6 +237,36 @@ def bmm_attn(op, A, B, sample=None, nthreads=None):
     raise ValueError(f"unknown attention product {op!r}")
 
 
+def attn_fwd(Q, K, V, scale, rows=None):
+    """Attention forward with the softmax between the two products, in fp64
+    over the exact input values: O[h,i] = sum_j P[h,i,j] V[h,j] with
+    P[h,i,:] = softmax_j(scale * sum_k Q[h,i,k] K[h,j,k]) (no mask).
+
+    Returns (O, S_O, E): O [h,s,d]; the error scale S_O = sum_j P |V|; and per
+    row E = max_j sum_k |Q K| (the size of the largest logit's terms), from
+    which the FP32 rounding of the logits is bounded.  rows = (heads, row
+    indices) restricts the result to those rows (each a full softmax over all
+    keys); then O, S_O are [n, d] and E [n].
+    Written from the definition: the softmax is exp(x - max) / sum exp(x - max),
+    with NumPy float64 matrix products and exponentials.
+    """
+    q, k, v = decode(Q), decode(K), decode(V)
+    if rows is not None:
+        hh, ii = (np.asarray(x, dtype=np.int64) for x in rows)
+        qs = q[hh, ii]                                  # [n, d]
+        logits = np.einsum("nd,njd->nj", qs, k[hh])     # [n, s]
+        terms = np.einsum("nd,njd->nj", np.abs(qs), np.abs(k[hh]))
+        x = scale * logits
+        p = np.exp(x - x.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        return np.einsum("nj,njd->nd", p, v[hh]), np.einsum("nj,njd->nd", p, np.abs(v[hh])), terms.max(axis=1)
+    x = scale * np.einsum("hid,hjd->hij", q, k)
+    p = np.exp(x - x.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    terms = np.einsum("hid,hjd->hij", np.abs(q), np.abs(k)).max(axis=2)
+    return np.einsum("hij,hjd->hid", p, v), np.einsum("hij,hjd->hid", p, np.abs(v)), terms
+
+
 # --------------------------------------------------------------------------
 # rank-r LoRA products (section "Tuning the kernels": the rank-16 LoRA
 # matrices).  A [r, d_in], B [d_out, r]; no alpha/r scaling (the page gives

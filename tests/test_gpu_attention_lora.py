@@ -259,3 +259,61 @@ def test_lora_fp32_factors_use_the_low_part():
         err = np.abs(got - exact).max()
         err_rounded = np.abs(rounded - exact).max()
         assert err < 0.02 * err_rounded, (err, err_rounded)
+
+
+# ------------------------------------------------------ fused attention forward
+ATTN_SCALE = 0.125  # 1 / sqrt(64)
+
+
+def attn_scale(S, E, scale=ATTN_SCALE):
+    """Error scale of the fused forward: the products' 1e-5 S_O plus the FP32
+    rounding of each logit (64 terms, at most 64 * 2^-24 * E) carried through
+    the exponential, twice over (the row's normaliser too): the bound is
+    (1e-5 + 2 scale 64 2^-24 E) S_O, written as 1e-5 times the value returned."""
+    return S * (1.0 + (2.0 * scale * 64 * 2.0 ** -24 * np.asarray(E))[..., None] / 1e-5)
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("hs", [(2, 256), (3, 200), (1, 65), (1, 1), (2, 130)], ids=lambda t: "x".join(map(str, t)))
+def test_attn_fwd_small(hs, dtype, out_kind):
+    """Fused softmax(scale Q K^T) V against the oracle, full check: whole and
+    ragged key blocks, a single key, rows past the last whole query block."""
+    h, s = hs
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    t = inputs.attn_inputs(h, s, 64, dtype, tag="fused")
+    got = tg.tg_attn_fwd(t["Q"].cuda(), t["K"].cuda(), t["V"].cuda(), out_dtype=out_dtype)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert "attn_fwd fused" in call, call
+    O, S, E = oracle.attn_fwd(t["Q"], t["K"], t["V"], ATTN_SCALE)
+    assert_close(got, O, attn_scale(S, E), f"attn_fwd {hs} [{call}]", out_dtype)
+
+
+@pytest.mark.parametrize("s", workloads.ATTENTION["s"])
+def test_attn_fwd_full_size(s):
+    """36 heads, head_dim 64, bf16: sampled rows (each a full softmax over all
+    keys) against the oracle, and the same bits from a second run."""
+    h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="attn")
+    dev = [t[n].cuda() for n in ("Q", "K", "V")]
+    a = tg.tg_attn_fwd(*dev, out_dtype=torch.float32)
+    b = tg.tg_attn_fwd(*dev, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    rng = np.random.default_rng(s)
+    hh = np.concatenate([rng.integers(0, h, 384), [0, h - 1, 0, h - 1]])
+    ii = np.concatenate([rng.integers(0, s, 384), [0, 0, s - 1, s - 1]])
+    O, S, E = oracle.attn_fwd(t["Q"], t["K"], t["V"], ATTN_SCALE, rows=(hh, ii))
+    got = a[torch.from_numpy(hh).cuda(), torch.from_numpy(ii).cuda()]
+    assert_close(got, O, attn_scale(S, E), f"attn_fwd s={s}", torch.float32)
+
+
+def test_attn_fwd_zero_scale_is_the_mean():
+    """A zero scale weighs every key alike: O is the mean of V's rows."""
+    h, s, d = 2, 300, 64
+    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="fused0")
+    got = tg.tg_attn_fwd(t["Q"].cuda(), t["K"].cuda(), t["V"].cuda(), scale=0.0, out_dtype=torch.float32)
+    mean = t["V"].double().mean(dim=1, keepdim=True).expand(h, s, d).numpy()
+    S = t["V"].double().abs().mean(dim=1, keepdim=True).expand(h, s, d).numpy()
+    assert_close(got, mean, S, "attn_fwd scale 0", torch.float32)

@@ -8,6 +8,7 @@ NumPy's float64 and int64 matmul, hand-worked fixtures, closed forms,
 transpose identities and finite differences.
 """
 import itertools
+import math
 import os
 from fractions import Fraction
 
@@ -418,3 +419,66 @@ def test_pins_catch_planted_mistakes(mutation, tmp_path):
             if not np.all(np.abs(C - ex) <= (K - 1) * U * 1.0001 * exs):
                 caught = True
     assert caught, MUTATIONS[mutation]
+
+
+# ---------------------------------------------------------------------------
+# fused attention forward (softmax between the two products)
+# ---------------------------------------------------------------------------
+def _attn_bruteforce(q, k, v, scale):
+    """softmax(scale q k^T) v with Python loops and math.exp, one row at a time."""
+    import math
+    h, s, d = q.shape
+    out = np.zeros((h, s, d))
+    for b in range(h):
+        for i in range(s):
+            x = [scale * sum(q[b, i, t] * k[b, j, t] for t in range(d)) for j in range(s)]
+            mx = max(x)
+            w = [math.exp(xj - mx) for xj in x]
+            tot = sum(w)
+            for t in range(d):
+                out[b, i, t] = sum(w[j] * v[b, j, t] for j in range(s)) / tot
+    return out
+
+
+@pytest.mark.parametrize("dtype", DT16)
+def test_attn_fwd_bruteforce_tiny(dtype):
+    for h, s, d in ((1, 1, 1), (1, 2, 3), (2, 3, 2), (1, 5, 4)):
+        Q, K, V = (rand16((h, s, d), dtype, 300 + i) for i in range(3))
+        O, S, _ = oracle.attn_fwd(Q, K, V, 0.37)
+        ref = _attn_bruteforce(f64(Q), f64(K), f64(V), 0.37)
+        assert np.all(np.abs(O - ref) <= 1e-13 * S + 1e-300), (h, s, d)
+
+
+def test_attn_fwd_closed_forms():
+    h, s, d = 2, 40, 64
+    V = rand16((h, s, d), torch.bfloat16, 310)
+    K = rand16((h, s, d), torch.bfloat16, 311)
+    # Q = 0: every key weighs 1/s, O is the mean of V's rows
+    O, _, _ = oracle.attn_fwd(torch.zeros(h, s, d, dtype=torch.bfloat16), K, V, 0.125)
+    mean = f64(V).mean(axis=1, keepdims=True)
+    assert np.allclose(O, np.broadcast_to(mean, O.shape), rtol=0, atol=1e-14 * np.abs(f64(V)).max())
+    # V = 1: each row of the softmax sums to one
+    Q = rand16((h, s, d), torch.bfloat16, 312)
+    O, _, _ = oracle.attn_fwd(Q, K, torch.ones(h, s, d, dtype=torch.bfloat16), 0.125)
+    assert np.all(np.abs(O - 1.0) <= 1e-14)
+    # one key far ahead of the others: its row of V comes out
+    Qd = torch.zeros(h, s, d)
+    Qd[:, :, 0] = 4.0
+    Kd = torch.zeros(h, s, d)
+    Kd[:, 7, 0] = 64.0  # logit 0.125 * 256 = 32 for key 7, 0 for the rest
+    O, _, _ = oracle.attn_fwd(Qd.to(torch.bfloat16), Kd.to(torch.bfloat16), V, 0.125)
+    want = np.broadcast_to(f64(V)[:, 7:8, :], O.shape)
+    assert np.all(np.abs(O - want) <= (s * math.exp(-32.0)) * 2 * np.abs(f64(V)).max())
+
+
+def test_attn_fwd_is_the_two_products_with_a_softmax_between():
+    """The same result from the C oracle's batched products and a NumPy softmax."""
+    h, s, d = 3, 50, 64
+    Q, K, V = (rand16((h, s, d), torch.float16, 320 + i, spread=False) for i in range(3))
+    O, S, _ = oracle.attn_fwd(Q, K, V, 0.125)
+    logits, _ = oracle.bmm_attn("qk", Q, K)
+    x = 0.125 * logits
+    p = np.exp(x - x.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    ref = np.einsum("hij,hjd->hid", p, f64(V))
+    assert np.all(np.abs(O - ref) <= 1e-12 * S)
