@@ -124,6 +124,15 @@ def test_fp32_factor_lora_rejects_bad_arguments(lib):
              NULL, 0, NULL) == 1  # no dY
 
 
+def test_fused_attention_rejects_bad_arguments(lib):
+    f = lib.tg_attn_fwd
+    assert f(EVEN, EVEN, EVEN, EVEN, 2, 64, 32, 0.125, B.TG_BF16, B.TG_BF16, NULL) == 1  # head dim must be 64
+    assert f(EVEN, EVEN, EVEN, EVEN, 2, 64, 64, float("nan"), B.TG_BF16, B.TG_BF16, NULL) == 1
+    assert f(EVEN, EVEN, EVEN, EVEN, 2, -1, 64, 0.125, B.TG_BF16, B.TG_BF16, NULL) == 1
+    assert f(EVEN, EVEN, EVEN, EVEN, 2, 64, 64, 0.125, B.TG_F32, B.TG_F32, NULL) == 2
+    assert f(EVEN, ctypes.c_void_p(0x1008), EVEN, EVEN, 2, 64, 64, 0.125, B.TG_BF16, B.TG_BF16, NULL) == 3  # 16 B
+
+
 def test_tile_table_reader(lib, tmp_path):
     good = tmp_path / "t.txt"
     good.write_text("# op in out M N K batch bn splits\n"
