@@ -6,7 +6,7 @@ kind of kernel launch:
     python -m gemms_linear_layers_gb300.probe wgrad 2048 2304 2304 [--plan "256 sk n"] [--reps 20]
 
 `op` is fwd|dgrad|wgrad (dims: T d_in d_out; --dtype f32 for FP32 operands), one of the attention products
-qk|pv|do_vt|pt_do|ds_k|dst_q (dims: heads s d), or lora_down|lora_up|lora_grad
+qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd (dims: heads s d), or lora_down|lora_up|lora_grad
 (dims: T d_in d_out, rank 16).  --plan "bn splits [raster]"
 writes a one-line tile table for this shape and loads it first.
 """
@@ -67,6 +67,12 @@ def main(argv=None):
         nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
                   "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
                   "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
+    elif a.op == "attn_fwd":  # the fused forward (counted as its two products: 4 h s^2 d flops)
+        h, s, d = a.dims
+        t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
+        M, N, K, batch = s, s, 2 * d, h
+        out = torch.empty(h, s, d, dtype=out_dtype, device=dev)
+        fn = lambda ws: tg.tg_attn_fwd(t["Q"], t["K"], t["V"], O=out)  # noqa: E731
     else:
         h, s, d = a.dims
         t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
