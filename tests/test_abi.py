@@ -40,6 +40,17 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
     assert lib.tg_version() == 10000
 
 
+def test_package_exports_every_entry_point():
+    """The package's public names are the binding's, and every C entry point
+    that computes something is among them."""
+    import gemms_linear_layers_gb300 as pkg
+    for n in pkg.__all__:
+        assert hasattr(B, n), n
+    for n in declared_functions():
+        if n.startswith(("tg_gemm", "tg_lora", "tg_bmm", "tg_attn")):
+            assert n in pkg.__all__, n
+
+
 def test_status_strings(lib):
     for code in range(9):
         s = lib.tg_status_string(code)
