@@ -1,5 +1,5 @@
-// floors.cu -- stand-alone measurements of what this GPU allows, used to
-// judge the library's kernels (not linked into libtg.so):
+// floors.cu -- stand-alone measurements of what this GPU allows, the floors
+// the library's kernels are compared with (not linked into libtg.so):
 //   1. the cost of an empty kernel launched back to back;
 //   2. streaming a [T, K] bf16 matrix from HBM with TMA boxes shaped like the
 //      LoRA row-down kernel's ({64, R, 8}, 4 stages), with no arithmetic;
