@@ -482,3 +482,13 @@ def test_attn_fwd_is_the_two_products_with_a_softmax_between():
     p /= p.sum(axis=2, keepdims=True)
     ref = np.einsum("hij,hjd->hid", p, f64(V))
     assert np.all(np.abs(O - ref) <= 1e-12 * S)
+
+
+def test_attn_fwd_sampled_rows_match_the_full_result():
+    h, s, d = 3, 70, 64
+    Q, K, V = (rand16((h, s, d), torch.bfloat16, 330 + i, spread=False) for i in range(3))
+    O, S, E = oracle.attn_fwd(Q, K, V, 0.125)
+    hh, ii = np.array([0, 2, 1, 2]), np.array([0, 69, 33, 5])
+    Or, Sr, Er = oracle.attn_fwd(Q, K, V, 0.125, rows=(hh, ii))
+    assert np.allclose(Or, O[hh, ii], rtol=1e-13, atol=0) and np.allclose(Sr, S[hh, ii], rtol=1e-13, atol=0)
+    assert np.array_equal(Er, E[hh, ii])
