@@ -47,17 +47,22 @@ PROFILES_DIR = os.path.join(ROOT, "profiles")
 CSRC_DIR = os.path.join(ROOT, "gemms_linear_layers_gb300", "csrc")
 
 
+# the sources the step's kernels are built from: the 16-bit GEMM kernels (single
+# CTAs, pairs, cluster split) and their launches, the split and tail
+# reductions, the PTX wrappers, the shared declarations and the tensor maps
+STEP_KERNEL_SOURCES = ("gemm_simt.cu", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_tc_cs.cuh", "gemm_tc_launch.cuh",
+                       "gemm_tc_nn.cu", "gemm_tc_nt.cu", "gemm_tc_tn.cu", "ptx.cuh", "tg_internal.h", "tmap.cpp")
+
+
 def kernel_sources_digest(csrc=None) -> str:
     """SHA-1 over the sources that decide what a kernel of the step reads and
-    writes (the 16-bit GEMM kernels and reductions, their PTX wrappers and
-    tensor maps; not the host planner, whose changes show up as a different
-    kernel identity, and not the LoRA and FP32 CUDA-core translation units,
-    whose kernels are not in the step), name and bytes in name order."""
+    writes (STEP_KERNEL_SOURCES that exist; not the host planner, whose
+    changes show up as a different kernel identity, nor the units whose
+    kernels are not in the step), name and bytes in name order."""
     csrc = csrc or CSRC_DIR
     h = hashlib.sha1()
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".cpp", ".h")) and name not in ("api.cu", "noalloc.cu", "lora.cu",
-                                                                          "gemm_ffma.cu"):
+        if name in STEP_KERNEL_SOURCES:
             h.update(name.encode())
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
