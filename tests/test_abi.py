@@ -251,3 +251,56 @@ def test_cost_model_choices_without_a_table(lib, case):
             assert avoid not in p, p
     finally:
         assert lib.tg_load_table(None) == 0
+
+
+def _plan_fields(p):
+    f = p.split()
+    kv = dict(x.split("=", 1) for x in f if "=" in x)
+    return f, kv
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cost_model_plans_are_well_formed(lib, seed):
+    """Over random shapes (no table), every plan the cost model makes is one
+    the kernels can run: a tile width they offer, CTA pairs only over more
+    than 128 rows, no more K splits than 64-deep K blocks, cluster splits of
+    2-8 CTAs whose clusters all fit on the 152 SMs at once, a persistent
+    stream-K grid no larger than the SMs, and the CUDA-core path exactly when
+    a row pitch is not a multiple of 16 bytes."""
+    import random
+    import torch
+    rng = random.Random(seed)
+    assert lib.tg_load_table(None) == 0
+    sizes = [1, 7, 16, 64, 100, 128, 129, 192, 256, 576, 1000, 1536, 2048, 2304, 4096, 5760, 49152]
+    for _ in range(150):
+        op = rng.randrange(3)
+        M, N, K = (rng.choice(sizes) for _ in range(3))
+        batch = rng.choice([1, 1, 1, 4, 36])
+        dout = rng.choice([torch.bfloat16, torch.float32])
+        p = B.tg_plan_describe(op, M, N, K, batch, torch.bfloat16, dout, 152)
+        layout = ("nt", "nn", "tn")[op]
+        lda, ldb = (M if layout == "tn" else K), (K if layout == "nt" else N)
+        ob = 4 if dout == torch.float32 else 2
+        misaligned = (lda * 2) % 16 or (ldb * 2) % 16 or (N * ob) % 16
+        if misaligned:
+            assert p == f"simt {layout}", (op, M, N, K, batch, p)
+            continue
+        f, kv = _plan_fields(p)
+        assert f[0] == "tc" and f[1] == layout, p
+        bn = int(kv["bn"])
+        assert bn in (64, 128, 144, 192, 256), p
+        kb = -(-K // 64)
+        if "pair" in f:
+            assert M > 128 and bn in (128, 192, 256), p
+        if "sk" in f:
+            assert 1 <= int(kv["grid"]) <= 152, p
+        else:
+            assert 1 <= int(kv["splits"]) <= kb, p
+        if "cs" in f:
+            cs = int(kv["cluster"])
+            tiles = batch * -(-M // 128) * -(-N // bn)
+            assert 2 <= cs <= 8 and cs <= kb and tiles * cs <= 152, p
+        if "tail" in kv:  # the tiles of the last partial wave, each cut into K pieces
+            tail_tiles, pieces = (int(x) for x in kv["tail"].split("x"))
+            tiles = batch * -(-M // (256 if "pair" in f else 128)) * -(-N // bn)
+            assert 1 <= tail_tiles < tiles and 2 <= pieces <= kb, p
