@@ -317,3 +317,20 @@ def test_attn_fwd_zero_scale_is_the_mean():
     mean = t["V"].double().mean(dim=1, keepdim=True).expand(h, s, d).numpy()
     S = t["V"].double().abs().mean(dim=1, keepdim=True).expand(h, s, d).numpy()
     assert_close(got, mean, S, "attn_fwd scale 0", torch.float32)
+
+
+def test_lora_up_fp32_factor_unaligned_takes_the_cuda_cores():
+    """The up product reads an FP32 B with 16-byte loads; a B that starts 4
+    bytes past a 16-byte boundary goes to the CUDA-core path, same result."""
+    T, d_out, r = 256, 192, 16
+    _, _, _, H, _ = inputs.lora_inputs(T, 64, d_out, r, torch.bfloat16, tag="w32u")
+    _, _, B, _, _ = inputs.lora_inputs(T, 64, d_out, r, torch.float32, tag="w32u")
+    buf = torch.empty(d_out * r + 1, dtype=torch.float32, device="cuda")
+    Bu = buf[1:].view(d_out, r)
+    Bu.copy_(B.cuda())
+    y = tg.tg_lora_up_f32w(H.cuda(), Bu, out_dtype=torch.float32)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert "simt" in call, call
+    C, S = oracle.lora_up(H, B)
+    assert_close(y, C, S, f"lora_up_f32w unaligned B [{call}]", torch.float32)
