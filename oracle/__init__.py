@@ -32,6 +32,12 @@ Pins (``tests/test_oracle_pins.py``), each independent of the code it checks:
   the same brute-force/NumPy pins for the individual products.
 * ``bmm_attn``: the six products against NumPy batched matmul, and finite
   differences of <dO, P V> and <dS, Q K^T>.
+* ``attn_fwd`` (softmax between the products): Python-loop brute force with
+  math.exp, closed forms (Q = 0 gives the mean of V; V = 1 gives 1; one
+  dominant key gives its row of V), the C oracle's logits with a NumPy
+  softmax, and sampled rows against the full result.
+* ``attn_bwd``: fp64 finite differences of <dO, attn_fwd(Q, K, V)> for every
+  input element, and dV against P^T dO.
 * ``round16``: hand-derived tie, subnormal and overflow cases
   (``tests/golden/round16_cases.txt``), torch's binary32->bf16/fp16 RNE on
   binary32 inputs and NumPy's float64->float16 conversion on doubles.
@@ -265,6 +271,32 @@ def attn_fwd(Q, K, V, scale, rows=None):
     p /= p.sum(axis=2, keepdims=True)
     terms = np.einsum("hid,hjd->hij", np.abs(q), np.abs(k)).max(axis=2)
     return np.einsum("hij,hjd->hid", p, v), np.einsum("hij,hjd->hid", p, np.abs(v)), terms
+
+
+def attn_bwd(Q, K, V, dO, scale):
+    """Gradients of L = <dO, O> for O = softmax(scale Q K^T) V (the forward of
+    attn_fwd), in fp64 over the exact input values, written from the chain
+    rule: with P the softmax weights,
+        dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(dO * O)),
+        dQ = scale dS K,   dK = scale dS^T Q.
+    Returns a dict of (value, error scale) pairs for dQ, dK, dV; the scales are
+    the same sums with every term replaced by its absolute value.
+    """
+    q, k, v, do = decode(Q), decode(K), decode(V), decode(dO)
+    x = scale * np.einsum("hid,hjd->hij", q, k)
+    p = np.exp(x - x.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    o = np.einsum("hij,hjd->hid", p, v)
+    dv = np.einsum("hij,hid->hjd", p, do)
+    dp = np.einsum("hid,hjd->hij", do, v)
+    delta = np.einsum("hid,hid->hi", do, o)[..., None]
+    ds = p * (dp - delta)
+    dq = scale * np.einsum("hij,hjd->hid", ds, k)
+    dk = scale * np.einsum("hij,hid->hjd", ds, q)
+    ads = p * (np.abs(dp) + np.abs(delta))
+    return {"dQ": (dq, scale * np.einsum("hij,hjd->hid", ads, np.abs(k))),
+            "dK": (dk, scale * np.einsum("hij,hid->hjd", ads, np.abs(q))),
+            "dV": (dv, np.einsum("hij,hid->hjd", p, np.abs(do)))}
 
 
 # --------------------------------------------------------------------------

@@ -492,3 +492,42 @@ def test_attn_fwd_sampled_rows_match_the_full_result():
     Or, Sr, Er = oracle.attn_fwd(Q, K, V, 0.125, rows=(hh, ii))
     assert np.allclose(Or, O[hh, ii], rtol=1e-13, atol=0) and np.allclose(Sr, S[hh, ii], rtol=1e-13, atol=0)
     assert np.array_equal(Er, E[hh, ii])
+
+
+def test_attn_bwd_finite_differences():
+    """The attention gradients are the derivatives of L = <dO, O(Q, K, V)>:
+    fp64 central differences on every input element of a small case."""
+    h, s, d, scale = 2, 5, 3, 0.6
+    Q, K, V, dO = (rand16((h, s, d), torch.float32, 340 + i, spread=False) for i in range(4))
+    g = oracle.attn_bwd(Q, K, V, dO, scale)
+    base = {"Q": f64(Q), "K": f64(K), "V": f64(V)}
+    do = f64(dO)
+
+    def loss(t):
+        O, _, _ = oracle.attn_fwd(torch.from_numpy(t["Q"]), torch.from_numpy(t["K"]), torch.from_numpy(t["V"]),
+                                  scale)
+        return float((O * do).sum())
+
+    eps = 1e-6
+    for name in ("Q", "K", "V"):
+        want = np.zeros_like(base[name])
+        for idx in np.ndindex(*base[name].shape):
+            tp = {k: v.copy() for k, v in base.items()}
+            tm = {k: v.copy() for k, v in base.items()}
+            tp[name][idx] += eps
+            tm[name][idx] -= eps
+            want[idx] = (loss(tp) - loss(tm)) / (2 * eps)
+        got, S = g["d" + name]
+        assert np.all(np.abs(got - want) <= 1e-6 * (S + 1.0)), name
+
+
+def test_attn_bwd_value_gradient_is_p_transposed_times_do():
+    """dV = P^T dO with P from the oracle's own softmax of the C oracle's logits."""
+    h, s, d = 2, 30, 64
+    Q, K, V, dO = (rand16((h, s, d), torch.bfloat16, 350 + i, spread=False) for i in range(4))
+    dV, S = oracle.attn_bwd(Q, K, V, dO, 0.125)["dV"]
+    logits, _ = oracle.bmm_attn("qk", Q, K)
+    x = 0.125 * logits
+    p = np.exp(x - x.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    assert np.all(np.abs(dV - np.einsum("hij,hid->hjd", p, f64(dO))) <= 1e-12 * S)
