@@ -277,8 +277,9 @@ size_t tg_last_call(char* buf, size_t len);
  * for a layer product on a device with `sms` SMs -- tile width, CTA pairs /
  * deep ring / cluster split, split count or stream-K grid, tail split, tile
  * order, and whether the tile table or the cost model chose it -- in the
- * format of tg_last_call, or "simt <layout>" when contiguous operands of
- * these sizes need the CUDA-core path.  op is TG_OP_GEMM_FWD, _DGRAD or
+ * format of tg_last_call, "simt <layout>" when contiguous operands of
+ * these sizes need the CUDA-core path, or "ffma <layout> splits=S" for FP32
+ * operands (the CUDA-core FFMA kernel and its K split).  op is TG_OP_GEMM_FWD, _DGRAD or
  * _WGRAD; M, N, K are the product's output rows, output columns and
  * reduction length (as in the tile table).  Returns the full length, 0 for
  * invalid arguments. */
