@@ -1,25 +1,38 @@
 #!/usr/bin/env python
-"""Benchmark: TFLOP/s of the training products of a linear layer on GB300.
+"""Benchmark: TFLOP/s of the training products of linear layers on GB300.
 
-One step = every product of the 135M-class decoder layer set at T = 2,048
-tokens (q, k, v, o, gate, up, down, head; forward, input gradient and weight
-gradient each; bf16 and fp16 with FP32 accumulation): 48 products.  Inputs
-are seeded synthetic tensors resident in HBM; L2 is flushed (a 256 MiB write)
-before every step, outside the timed events.  Each product is one captured
-CUDA graph of the library call; CUDA events on the launching stream bracket
-every product, so per-kernel times come from the same timed region.
+One step = every product of the 2B-class decoder layer set (q, k, v, o
+2304->2304; gate, up 2304->5760; down 5760->2304) at T = 1,024, 2,048 and
+4,096 tokens, each as forward, input gradient and weight gradient, in bf16 and
+in fp16 with FP32 accumulation: 126 products, 5.25 TFLOP.  Inputs are seeded
+synthetic tensors resident in HBM (3.2 GB, far above the L2); L2 is also
+flushed (a 256 MiB write) before every step, outside the timed events.  The
+step is one captured CUDA graph of the library calls in training order; CUDA
+events inside it mark the step and bracket every launch of the dominant
+launch class (one kernel identity at one product shape), so `value` and the
+roofline entry come from the same timed replays.
 
-Printed: one JSON line (rank 0).  `value` is the whole-job TFLOP/s (all ranks'
-flops / the slowest rank's time).  Also measured: the same step end to end
-through the public API with pinned host inputs and outputs copied each step
-(`e2e`), the oracle's throughput on host cores on a bounded sample
-(`cpu_baseline`), the roofline fraction of the dominant kernel, SM clocks
-sampled during the timed region, and (unless --no-rows) one row per distinct
-product of the other product sets (2B-class layers at 1,024-4,096 tokens,
-rank-16 LoRA at 4,096 tokens, batched attention) against its own roofline.
+Printed on stdout (rank 0): first one `row {...}` line per measured row of the
+other product sets (the 135M-class step, every distinct 2B-class product
+alone with warm and rotated operands, FP32 operands, rank-16 LoRA, batched
+and fused attention in bf16 and fp16), then ONE compact JSON line, the
+headline, last.  `value` is the whole-job TFLOP/s (all ranks' flops / the
+slowest rank's time).  Also in it: the same step end to end through the
+public API with pinned host inputs and outputs copied every step (`e2e`), the
+oracle on the host cores on a bounded sample (`cpu_baseline`), the roofline
+fraction of the dominant launch class and SM clocks sampled during the timed
+region.
 
 `--impl reference` times the fp64 CPU oracle on the same workload instead
 (bounded samples per step, host cores).
+
+`python bench.py probe OP D0 D1 D2 [--dtype bf16|f16|f32] [--out same|f32]
+[--plan "bn splits [raster]"] [--reps R]` times one product alone through the
+public entry points (the command the ncu summaries are captured with): OP is
+fwd|dgrad|wgrad (dims T d_in d_out), one of the attention products
+qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd (dims heads s d), or
+lora_down|lora_up|lora_grad (dims T d_in d_out, rank 16); --plan writes a
+one-line tile table for the shape and loads it first.
 """
 from __future__ import annotations
 
@@ -41,7 +54,14 @@ import torch  # noqa: E402
 from gemms_linear_layers_gb300 import inputs, workloads  # noqa: E402
 
 METRIC = "TFLOPS per training GEMM (fwd/dgrad/wgrad, bf16/fp16) and % of GB300 dense peak"
-WORKLOAD = "135M-class decoder layer set, T=2048, fwd+dgrad+wgrad, bf16 and fp16 (48 products)"
+STEP_SETS = {
+    "2b": (workloads.DECODER_2B,
+           "2B-class decoder layer set (q/k/v/o 2304x2304, gate/up 2304->5760, down 5760->2304) at T=1024, 2048 "
+           "and 4096, fwd+dgrad+wgrad, bf16 and fp16 (126 products)"),
+    "135m": (workloads.DECODER_135M,
+             "135M-class decoder layer set (q/o 576x576, k/v 576->192, gate/up 576->1536, down 1536->576, head "
+             "576->49152) at T=2048, fwd+dgrad+wgrad, bf16 and fp16 (48 products)"),
+}
 L2_FLUSH_BYTES = 256 << 20
 PROFILES_DIR = os.path.join(ROOT, "profiles")
 CSRC_DIR = os.path.join(ROOT, "gemms_linear_layers_gb300", "csrc")
@@ -70,10 +90,10 @@ def kernel_sources_digest(csrc=None) -> str:
 
 
 def profiled_traffic(kernel_key: str, profiles=None, digest=None):
-    """DRAM bytes (read + write) per launch of the kernel identity
-    `kernel_key`, from a committed ncu summary that names it and records the
-    digest of the kernel sources it was captured from; None when no summary
-    matches or the kernels changed since the counters were taken."""
+    """DRAM bytes (read + write) per launch of the launch class `kernel_key`,
+    from a committed ncu summary that names it and records the digest of the
+    kernel sources it was captured from; None when no summary matches or the
+    kernels changed since the counters were taken."""
     profiles = profiles or PROFILES_DIR
     digest = digest or kernel_sources_digest()
     if not os.path.isdir(profiles):
@@ -183,39 +203,52 @@ class Product:
         self.graph = None
         self.call = ""
         self.launches = 1
+        self.kernel = "?"
 
     @property
     def name(self):
-        return f"{self.layer}.{self.op}.{str(self.dtype)[6:]}"
+        return f"{self.layer}.{self.op}.T{self.T}.{str(self.dtype)[6:]}"
+
+    @property
+    def launch_class(self):
+        """The kernel identity at this product's shape: launches of one class
+        do the same work, so a per-launch figure of the class is well defined."""
+        return f"{self.kernel} @ {self.M}x{self.N}x{self.K}"
 
 
-def build_step(device, only=None):
-    """Inputs, outputs and workspaces of every product of the step (or of the
-    products named in `only`), on the device."""
-    from gemms_linear_layers_gb300 import _binding as tg
-    cfg = workloads.DECODER_135M
+def step_token_counts(cfg):
     T = cfg["T"]
-    prods, tensors = [], {}
+    return tuple(T) if isinstance(T, (tuple, list)) else (T,)
+
+
+def build_step(device, only=None, cfg=None):
+    """Inputs, outputs and workspaces of every product of the step (or of the
+    products named in `only`), on the device.  Every layer has its own
+    tensors, as in a training step."""
+    from gemms_linear_layers_gb300 import _binding as tg
+    cfg = cfg or workloads.DECODER_2B
+    prods = []
     for dtype in cfg["dtypes"]:
-        for layer, d_in, d_out in cfg["layers"]:
-            names = [Product(layer, op, dtype, T, d_in, d_out).name for op in ("fwd", "dgrad", "wgrad")]
-            if only and not any(n in only for n in names):
-                continue
-            X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="bench", device=device)
-            tensors[(layer, dtype)] = {
-                "X": X, "W": W, "dY": dY,
-                "Y": torch.empty(T, d_out, dtype=dtype, device=device),
-                "dX": torch.empty(T, d_in, dtype=dtype, device=device),
-                "dW": torch.empty(d_out, d_in, dtype=dtype, device=device)}
-            for op in ("fwd", "dgrad", "wgrad"):
-                p = Product(layer, op, dtype, T, d_in, d_out)
-                if only and p.name not in only:
+        for T in step_token_counts(cfg):
+            for layer, d_in, d_out in cfg["layers"]:
+                names = [Product(layer, op, dtype, T, d_in, d_out).name for op in ("fwd", "dgrad", "wgrad")]
+                if only and not any(n in only for n in names):
                     continue
-                opcode = {"fwd": tg.TG_OP_GEMM_FWD, "dgrad": tg.TG_OP_GEMM_DGRAD, "wgrad": tg.TG_OP_GEMM_WGRAD}[op]
-                n = tg.tg_workspace_size(opcode, T, d_out, d_in, 0, dtype, dtype)
-                p.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
-                p.t = tensors[(layer, dtype)]
-                prods.append(p)
+                X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag=f"bench-{layer}", device=device)
+                t = {"X": X, "W": W, "dY": dY,
+                     "Y": torch.empty(T, d_out, dtype=dtype, device=device),
+                     "dX": torch.empty(T, d_in, dtype=dtype, device=device),
+                     "dW": torch.empty(d_out, d_in, dtype=dtype, device=device)}
+                for op in ("fwd", "dgrad", "wgrad"):
+                    p = Product(layer, op, dtype, T, d_in, d_out)
+                    if only and p.name not in only:
+                        continue
+                    opcode = {"fwd": tg.TG_OP_GEMM_FWD, "dgrad": tg.TG_OP_GEMM_DGRAD,
+                              "wgrad": tg.TG_OP_GEMM_WGRAD}[op]
+                    n = tg.tg_workspace_size(opcode, T, d_out, d_in, 0, dtype, dtype)
+                    p.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
+                    p.t = t
+                    prods.append(p)
     return prods
 
 
@@ -247,13 +280,22 @@ def kernel_key(call: str) -> str:
     return f"tc {f[2]} {bn}{deep}{pair}{sk}" + (" +reduce" if sp != "splits=1" else "") + tail
 
 
+def launches_of(call: str) -> int:
+    """Kernel launches of one call: the product, plus the ordered reduction
+    of split or tail-split partials when the plan has one."""
+    f = call.split()
+    split = any(x.startswith("splits=") and x != "splits=1" for x in f)
+    tail = any(x.startswith("tail=") for x in f)
+    return 2 if (split or tail) else 1
+
+
 def capture(prods, stream):
     from gemms_linear_layers_gb300 import _binding as tg
     for p in prods:  # warm-up call: sets kernel attributes, records the plan
         with torch.cuda.stream(stream):
             run_product(p)
         p.call = tg.tg_last_call()
-        p.launches = 2 if ("splits=" in p.call and "splits=1 " not in p.call) else 1
+        p.launches = launches_of(p.call)
         p.kernel = kernel_key(p.call)
     torch.cuda.synchronize()
     for p in prods:
@@ -265,8 +307,8 @@ def capture(prods, stream):
 
 
 def probe_products(prods, stream, flush, reps=2):
-    """Untimed pass: each product's own graph between events, to find the
-    kernel identity with the largest share of the step."""
+    """Untimed pass: each product's own graph between events, in step order,
+    to find the launch class with the largest share of the step."""
     per_prod = {p.name: 0.0 for p in prods}
     with torch.cuda.stream(stream):
         for _ in range(reps):
@@ -301,16 +343,16 @@ BWD_WAVES = [["head"], ["down"], ["gate", "up"], ["o"], ["q", "k", "v"]]
 
 def step_waves(prods):
     """The step's products as a list of waves (lists of products that may run
-    concurrently), dtype sets one after the other."""
-    by = {(p.layer, p.op, p.dtype): p for p in prods}
+    concurrently); each (dtype, token count) set one after the other."""
+    by = {(p.layer, p.op, p.dtype, p.T): p for p in prods}
     waves = []
-    for dtype in dict.fromkeys(p.dtype for p in prods):
+    for dtype, T in dict.fromkeys((p.dtype, p.T) for p in prods):
         for group in FWD_WAVES:
-            w = [by[(l, "fwd", dtype)] for l in group if (l, "fwd", dtype) in by]
+            w = [by[(l, "fwd", dtype, T)] for l in group if (l, "fwd", dtype, T) in by]
             if w:
                 waves.append(w)
         for group in BWD_WAVES:
-            w = [by[(l, op, dtype)] for l in group for op in ("dgrad", "wgrad") if (l, op, dtype) in by]
+            w = [by[(l, op, dtype, T)] for l in group for op in ("dgrad", "wgrad") if (l, op, dtype, T) in by]
             if w:
                 waves.append(w)
     placed = {id(p) for w in waves for p in w}
@@ -322,11 +364,11 @@ def capture_step(prods, stream, dominant, concurrent=True):
     """One graph for the whole step.  With `concurrent`, the products of a
     wave run on parallel branches (fork/join through events on side
     streams).  External events mark the step's start and end and bracket every
-    launch of the dominant kernel."""
+    launch of the dominant launch class."""
     e0, e1 = external_event(), external_event()
     if e0 is None:
         return None
-    waves = step_waves(prods) if concurrent else [[p] for p in prods]
+    waves = step_waves(prods) if concurrent else [[q] for w in step_waves(prods) for q in w]
     # a stream-K launch waits on its own later CTAs, which need every SM it
     # may occupy: it runs alone in its wave
     split = []
@@ -354,7 +396,7 @@ def capture_step(prods, stream, dominant, concurrent=True):
                     branches.append((side[i], p))
             for st, p in branches:
                 with torch.cuda.stream(st):
-                    if p.kernel == dominant:
+                    if dominant is not None and p.launch_class == dominant:
                         a, b = external_event(), external_event()
                         a.record(st)
                         run_product(p)
@@ -402,8 +444,22 @@ def timed_steps_per_product(prods, n_warm, n_steps, stream, flush, dominant):
             torch.cuda.synchronize()
             if s >= n_warm:
                 total_ms += ev[0].elapsed_time(ev[-1])
-                dom_ms += sum(ev[i].elapsed_time(ev[i + 1]) for i, p in enumerate(prods) if p.kernel == dominant)
+                dom_ms += sum(ev[i].elapsed_time(ev[i + 1]) for i, p in enumerate(prods)
+                              if p.launch_class == dominant)
     return total_ms, dom_ms
+
+
+def by_launch_class(prods, per_prod):
+    """{launch class: {ms, flops, n, products}} from a probe pass."""
+    out = {}
+    for p in prods:
+        k = out.setdefault(p.launch_class, {"ms": 0.0, "flops": 0, "n": 0, "products": [], "launches": 0})
+        k["ms"] += per_prod[p.name]
+        k["flops"] += p.flops
+        k["n"] += 1
+        k["launches"] += p.launches
+        k["products"].append(p.name)
+    return out
 
 
 # ------------------------------------------------------------------ e2e
@@ -412,12 +468,11 @@ def e2e_steps(prods, n_steps, stream):
     copies its inputs host->device and its outputs device->host.  Copies and
     products form a pipeline: every X and W come in first, so each forward
     product starts as soon as its own operands have arrived while the dY
-    tensors (the large ones) follow; each result goes out as soon as the
-    product that writes it is done, on a second copy stream.  Steps do not
-    overlap."""
+    tensors follow; each result goes out as soon as the product that writes
+    it is done, on a second copy stream.  Steps do not overlap."""
     groups = {}
     for p in prods:
-        groups.setdefault((p.layer, p.dtype), []).append(p)
+        groups.setdefault((p.layer, p.dtype, p.T), []).append(p)
     h2d = d2h = 0
     host = {}
     for key, ps in groups.items():
@@ -474,29 +529,31 @@ def e2e_steps(prods, n_steps, stream):
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_sample(target_s):
+def oracle_sample(target_s, cfg=None):
     """The fp64 oracle on the host cores over a bounded sample of the step:
-    the first rows of each of the 48 products (same shapes, same input
-    recipe).  Returns (flops, seconds, rows per product)."""
+    the first output rows of each of its products (same shapes, same input
+    recipe and seeds).  Returns (flops, seconds, rows per product)."""
     import numpy as np
 
     import oracle
-    cfg = workloads.DECODER_135M
-    T = cfg["T"]
-    if not hasattr(oracle_sample, "jobs"):
+    cfg = cfg or workloads.DECODER_2B
+    key = id(cfg)
+    cache = oracle_sample.__dict__.setdefault("cache", {})
+    if key not in cache:
         jobs = []
         for dtype in cfg["dtypes"]:
-            for layer, d_in, d_out in cfg["layers"]:
-                X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="bench")
-                for op in ("fwd", "dgrad", "wgrad"):
-                    jobs.append((op, X, W, dY))
-        oracle_sample.jobs = jobs
-        oracle_sample.sec_per_row = None
+            for T in step_token_counts(cfg):
+                for layer, d_in, d_out in cfg["layers"]:
+                    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag=f"bench-{layer}")
+                    for op in ("fwd", "dgrad", "wgrad"):
+                        jobs.append((op, X, W, dY))
+        cache[key] = {"jobs": jobs, "sec_per_row": None}
+    c = cache[key]
 
     def run(rows):
         flops = 0
         t0 = time.perf_counter()
-        for op, X, W, dY in oracle_sample.jobs:
+        for op, X, W, dY in c["jobs"]:
             if op == "fwd":
                 M, N, K = X.shape[0], W.shape[0], X.shape[1]
             elif op == "dgrad":
@@ -516,19 +573,21 @@ def oracle_sample(target_s):
             flops += 2 * r * N * K
         return flops, time.perf_counter() - t0
 
-    if oracle_sample.sec_per_row is None:
+    if c["sec_per_row"] is None:
         f, t = run(1)  # calibration
-        oracle_sample.sec_per_row = t
-    rows = max(1, int(target_s / max(oracle_sample.sec_per_row, 1e-4)))
+        c["sec_per_row"] = t
+    rows = max(1, int(target_s / max(c["sec_per_row"], 1e-4)))
     f, t = run(rows)
     return f, t, rows
 
 
-def cpu_baseline(target_s=12.0):
+def cpu_baseline(target_s=12.0, cfg=None):
     import oracle
-    f, t, rows = oracle_sample(target_s)
+    cfg = cfg or workloads.DECODER_2B
+    n = len(cfg["dtypes"]) * len(step_token_counts(cfg)) * len(cfg["layers"]) * 3
+    f, t, rows = oracle_sample(target_s, cfg)
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"first {rows} output row(s) of each of the 48 products ({f / 2e9:.2f} GMAC), "
+            "sample": f"first {rows} output row(s) of each of the {n} products ({f / 2e9:.2f} GMAC), "
                       f"fp64 naive loops, {t:.1f} s"}
 
 
@@ -538,6 +597,7 @@ def reference_arm(args):
         return
     import oracle
     oracle.build()
+    cfg, workload = STEP_SETS[args.set]
     steps, warm = args.steps, args.warmup
     t0 = time.perf_counter()
     # each step: a sample of the workload, sized so the whole run takes ~2 minutes
@@ -545,18 +605,19 @@ def reference_arm(args):
     total_f = total_t = 0.0
     rows = 0
     for s in range(warm + steps):
-        f, t, rows = oracle_sample(per_step_s)
+        f, t, rows = oracle_sample(per_step_s, cfg)
         if s >= warm:
             total_f += f
             total_t += t
     value = total_f / total_t / 1e12
+    n = len(cfg["dtypes"]) * len(step_token_counts(cfg)) * len(cfg["layers"]) * 3
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": round(1000 * total_t / steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "host threads"},
+            "data": "synthetic", "config": {"workload": workload, "parallelism": "host threads"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
                              "kind": "oracle",
-                             "sample": f"each step: first {rows} output row(s) of all 48 products"},
+                             "sample": f"each step: first {rows} output row(s) of all {n} products"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": round(time.perf_counter() - t0, 1)}
@@ -599,66 +660,121 @@ def fp32_peak_tflops(sms=None, mhz=None):
     return sms * FP32_LANES_PER_SM * 2 * mhz / 1e6
 
 
-def measure_rows(stream, pk, budget_s=90.0):
+def bars_of(rows):
+    """The spec bars over the 2B-class rows: the smallest tensor
+    fraction (rotated operands) over the 2,048- and 4,096-token products and
+    the smallest weight-gradient / forward ratio."""
+    fr = [r["frac_cold"] for r in rows if r.get("set") == "2B" and r["T"] >= 2048 and r["op"] != "wgrad_acc"]
+    wf = [r["wgrad_over_fwd"] for r in rows if r.get("set") == "2B" and "wgrad_over_fwd" in r]
+    lo = [r["frac_of_hbm"] for r in rows if r.get("set") == "LoRA" and r["op"] in ("down", "up", "grad")]
+    out = {}
+    if fr:
+        out["min_tensor_frac_T2048_4096"] = min(fr)
+    if wf:
+        out["min_wgrad_over_fwd"] = min(wf)
+    if lo:
+        out["min_lora_hbm_frac"] = min(lo)
+    return out
+
+
+def time_calls(stream, make_call, reps=10, sets=1):
+    """Median per-launch ms of one call over 5 replays of a graph of `reps`
+    launches (cycling through `sets` operand sets), and its call record."""
+    from gemms_linear_layers_gb300 import _binding as tg
+    calls = [make_call(i) for i in range(sets)]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    call = tg.tg_last_call()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(reps):
+            calls[r % sets]()
+    res = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b) / reps)
+    del g
+    return statistics.median(res), call
+
+
+def step_row(stream, pk, cfg, workload, steps=10):
+    """A whole layer-set step (as the headline measures it) on its own."""
+    prods = build_step("cuda", cfg=cfg)
+    capture(prods, stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    step = capture_step(prods, stream, None, concurrent=False)
+    flops = sum(p.flops for p in prods)
+    if step:
+        total_ms, _ = timed_steps(step, 3, steps, stream, flush)
+    else:
+        total_ms, _ = timed_steps_per_product(prods, 3, steps, stream, flush, None)
+    tf = flops * steps / (total_ms / 1e3) / 1e12
+    return {"set": "step", "workload": workload, "products": len(prods), "ms_per_step": round(total_ms / steps, 4),
+            "tflops": round(tf, 1), "frac_of_peak": round(tf / pk["bf16_tflops"], 3)}
+
+
+def measure_rows(stream, pk, budget_s=150.0):
     """One timing row per distinct product of the other product sets, each
     alone: CUDA graph of R launches, L2-sized buffer rotation for the
-    HBM-bound ones, median of 5 replays."""
+    HBM-bound ones (and, beside the warm figure, for the 2B-class products),
+    median of 5 replays."""
     from gemms_linear_layers_gb300 import _binding as tg
     rows = []
     t_start = time.perf_counter()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
 
-    def time_calls(make_call, reps=10, sets=1):
-        calls = [make_call(i) for i in range(sets)]
-        for c in calls:
-            c()
-        torch.cuda.synchronize()
-        call = tg.tg_last_call()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for r in range(reps):
-                calls[r % sets]()
-        res = []
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
-            res.append(a.elapsed_time(b) / reps)
-        return statistics.median(res), call
+    # the 135M-class step (the earlier headline) as one row
+    rows.append(step_row(stream, pk, workloads.DECODER_135M, STEP_SETS["135m"][1]))
+    torch.cuda.empty_cache()
 
-    # 2B-class layers
+    # 2B-class layers: each distinct product alone, warm (same operands every
+    # launch) and cold (operand sets rotated so that the bytes between two
+    # uses of a set exceed twice the L2)
     for T in workloads.DECODER_2B["T"]:
         for dtype in workloads.DECODER_2B["dtypes"]:
             for d_in, d_out, names in ((2304, 2304, "q,k,v,o"), (2304, 5760, "gate,up"), (5760, 2304, "down")):
-                X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="rows", device="cuda")
-                outs = {"fwd": torch.empty(T, d_out, dtype=dtype, device="cuda"),
-                        "dgrad": torch.empty(T, d_in, dtype=dtype, device="cuda"),
-                        "wgrad": torch.empty(d_out, d_in, dtype=dtype, device="cuda"),
-                        "wgrad_acc": torch.zeros(d_out, d_in, dtype=torch.float32, device="cuda")}
-                res = {}
+                per_set = (T * d_in + d_out * d_in + T * d_out) * 2  # operand bytes of one set
+                sets = max(1, int(2 * l2 // per_set) + 1)
+                data = [inputs.layer_inputs(T, d_in, d_out, dtype, tag=f"rows{i}", device="cuda")
+                        for i in range(sets)]
+                outs = [{"fwd": torch.empty(T, d_out, dtype=dtype, device="cuda"),
+                         "dgrad": torch.empty(T, d_in, dtype=dtype, device="cuda"),
+                         "wgrad": torch.empty(d_out, d_in, dtype=dtype, device="cuda"),
+                         "wgrad_acc": torch.zeros(d_out, d_in, dtype=torch.float32, device="cuda")}
+                        for _ in range(sets)]
                 ws = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
-                # wgrad_acc: the weight gradient added into an FP32 gradient buffer
+                res = {}
                 for op in ("fwd", "dgrad", "wgrad", "wgrad_acc"):
-                    fn = {"fwd": lambda i: (lambda: tg.tg_gemm_fwd(X, W, Y=outs["fwd"], ws=ws)),
-                          "dgrad": lambda i: (lambda: tg.tg_gemm_dgrad(dY, W, dX=outs["dgrad"], ws=ws)),
-                          "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws)),
-                          "wgrad_acc": lambda i: (lambda: tg.tg_gemm_wgrad_accumulate(dY, X, outs["wgrad_acc"],
-                                                                                      ws=ws))}[op]
-                    ms, call = time_calls(fn)
+                    def fn(i, op=op):
+                        X, W, dY = data[i]
+                        o = outs[i][op]
+                        return {"fwd": lambda: tg.tg_gemm_fwd(X, W, Y=o, ws=ws),
+                                "dgrad": lambda: tg.tg_gemm_dgrad(dY, W, dX=o, ws=ws),
+                                "wgrad": lambda: tg.tg_gemm_wgrad(dY, X, dW=o, ws=ws),
+                                "wgrad_acc": lambda: tg.tg_gemm_wgrad_accumulate(dY, X, o, ws=ws)}[op]
+                    ms_w, call = time_calls(stream, fn, reps=10, sets=1)
+                    ms_c, _ = time_calls(stream, fn, reps=max(10, 2 * sets), sets=sets)
                     M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T),
                                "wgrad_acc": (d_out, d_in, T)}[op]
-                    tf = workloads.flops(M, N, K) / ms / 1e9
-                    res[op] = tf
+                    tf_w = workloads.flops(M, N, K) / ms_w / 1e9
+                    tf_c = workloads.flops(M, N, K) / ms_c / 1e9
+                    res[op] = tf_c
                     rows.append({"set": "2B", "layer": names, "T": T, "op": op, "dtype": str(dtype)[6:],
-                                 "M": M, "N": N, "K": K, "us": round(ms * 1000, 2), "tflops": round(tf, 1),
-                                 "frac_of_peak": round(tf / pk["bf16_tflops"], 3), "bound": "tensor",
-                                 "kernel": kernel_key(call)})
+                                 "M": M, "N": N, "K": K, "us_warm": round(ms_w * 1000, 2),
+                                 "us_cold": round(ms_c * 1000, 2), "tflops_cold": round(tf_c, 1),
+                                 "frac_warm": round(tf_w / pk["bf16_tflops"], 3),
+                                 "frac_cold": round(tf_c / pk["bf16_tflops"], 3), "bound": "tensor",
+                                 "operand_sets": sets, "kernel": kernel_key(call)})
                 rows[-2]["wgrad_over_fwd"] = round(res["wgrad"] / res["fwd"], 3)
                 rows[-1]["acc_over_wgrad"] = round(res["wgrad_acc"] / res["wgrad"], 3)
-                del X, W, dY, outs
+                del data, outs, ws
+                torch.cuda.empty_cache()
     # FP32 operands (the CUDA-core FFMA kernel): the 2B-class layers at T=2048
     # and the 135M-class head, against the FP32 CUDA-core peak
     f32_peak = fp32_peak_tflops()
@@ -674,7 +790,7 @@ def measure_rows(stream, pk, budget_s=90.0):
             fn = {"fwd": lambda i: (lambda: tg.tg_gemm_fwd(X, W, Y=outs["fwd"], ws=ws)),
                   "dgrad": lambda i: (lambda: tg.tg_gemm_dgrad(dY, W, dX=outs["dgrad"], ws=ws)),
                   "wgrad": lambda i: (lambda: tg.tg_gemm_wgrad(dY, X, dW=outs["wgrad"], ws=ws))}[op]
-            ms, call = time_calls(fn, reps=5)
+            ms, call = time_calls(stream, fn, reps=5)
             M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[op]
             tf = workloads.flops(M, N, K) / ms / 1e9
             rows.append({"set": "FP32", "layer": names, "T": T, "op": op, "dtype": "fp32", "M": M, "N": N, "K": K,
@@ -738,54 +854,155 @@ def measure_rows(stream, pk, budget_s=90.0):
              4 * T * r * (d_in + d_out)),
         ]
         for op, fn, nbytes, fl in specs:
-            ms, call = time_calls(fn, reps=max(10, sets * 2), sets=sets)
+            ms, call = time_calls(stream, fn, reps=max(10, sets * 2), sets=sets)
             gbs = nbytes / ms / 1e6
             rows.append({"set": "LoRA", "layer": name, "T": T, "op": op, "dtype": "bf16", "d_in": d_in,
                          "d_out": d_out, "us": round(ms * 1000, 2), "gbs": round(gbs, 1),
                          "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3), "bound": "hbm",
                          "tflops": round(fl / ms / 1e9, 2), "kernel": call.split(" [")[0][:60]})
         del data, Hs, Ys, grads, wss, f32, grads32, wss32
-        if time.perf_counter() - t_start > budget_s:
-            break
-    # attention, s = 1024 / 2048 / 4096, bf16
+        torch.cuda.empty_cache()
+    # attention, s = 1024 / 2048 / 4096, bf16 and fp16
     acfg = workloads.ATTENTION
-    for s in acfg["s"]:
-        if time.perf_counter() - t_start > budget_s:
-            break
-        h, d = acfg["heads"], acfg["d"]
-        dt = torch.bfloat16
-        # operand sets rotated so that the bytes touched between two uses of a
-        # set exceed twice the L2: every launch reads from HBM
-        per_set = 3 * h * s * s * 2 + 6 * h * s * d * 2
-        sets = max(1, int(2 * l2 // per_set) + 1)
-        ts = [inputs.attn_inputs(h, s, d, dt, tag="rows" if i == 0 else f"rows{i}", device="cuda")
-              for i in range(sets)]
-        for op in ("qk", "pv", "do_vt", "pt_do", "ds_k", "dst_q"):
-            a, b = inputs.ATTN_OPERANDS[op]
-            ss_out = op in ("qk", "do_vt")
-            Cs = [torch.empty(h, s, s if ss_out else d, dtype=dt, device="cuda") for _ in range(sets)]
-            ms, call = time_calls(lambda i: (lambda: tg.tg_bmm_attn(op, ts[i][a], ts[i][b], C=Cs[i])),
+    for dt in acfg["dtypes"]:
+        for s in acfg["s"]:
+            if time.perf_counter() - t_start > budget_s:
+                break
+            h, d = acfg["heads"], acfg["d"]
+            # operand sets rotated so that the bytes touched between two uses of a
+            # set exceed twice the L2: every launch reads from HBM
+            per_set = 3 * h * s * s * 2 + 6 * h * s * d * 2
+            sets = max(1, int(2 * l2 // per_set) + 1)
+            ts = [inputs.attn_inputs(h, s, d, dt, tag="rows" if i == 0 else f"rows{i}", device="cuda")
+                  for i in range(sets)]
+            for op in ("qk", "pv", "do_vt", "pt_do", "ds_k", "dst_q"):
+                a, b = inputs.ATTN_OPERANDS[op]
+                ss_out = op in ("qk", "do_vt")
+                Cs = [torch.empty(h, s, s if ss_out else d, dtype=dt, device="cuda") for _ in range(sets)]
+                ms, call = time_calls(stream, lambda i: (lambda: tg.tg_bmm_attn(op, ts[i][a], ts[i][b], C=Cs[i])),
+                                      reps=max(5, 2 * sets), sets=sets)
+                t, C = ts[0], Cs[0]
+                nbytes = (t[a].numel() + t[b].numel() + C.numel()) * 2
+                fl = 2 * h * s * s * d
+                gbs = nbytes / ms / 1e6
+                rows.append({"set": "attention", "s": s, "op": op, "dtype": str(dt)[6:], "us": round(ms * 1000, 2),
+                             "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3),
+                             "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call),
+                             "operand_sets": sets})
+                del C, Cs
+            # the fused forward, softmax(Q K^T / 8) V without the [s, s] matrices (tensor-bound)
+            Os = [torch.empty(h, s, d, dtype=dt, device="cuda") for _ in range(sets)]
+            ms, call = time_calls(stream, lambda i: (lambda: tg.tg_attn_fwd(ts[i]["Q"], ts[i]["K"], ts[i]["V"],
+                                                                            O=Os[i])),
                                   reps=max(5, 2 * sets), sets=sets)
-            t, C = ts[0], Cs[0]
-            nbytes = (t[a].numel() + t[b].numel() + C.numel()) * 2
-            fl = 2 * h * s * s * d
-            gbs = nbytes / ms / 1e6
-            rows.append({"set": "attention", "s": s, "op": op, "dtype": "bf16", "us": round(ms * 1000, 2),
-                         "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 3),
-                         "tflops": round(fl / ms / 1e9, 1), "bound": "hbm", "kernel": kernel_key(call),
-                         "operand_sets": sets})
-            del C, Cs
-        # the fused forward, softmax(Q K^T / 8) V without the [s, s] matrices (tensor-bound)
-        Os = [torch.empty(h, s, d, dtype=dt, device="cuda") for _ in range(sets)]
-        ms, call = time_calls(lambda i: (lambda: tg.tg_attn_fwd(ts[i]["Q"], ts[i]["K"], ts[i]["V"], O=Os[i])),
-                              reps=max(5, 2 * sets), sets=sets)
-        fl = 4 * h * s * s * d
-        rows.append({"set": "attention", "s": s, "op": "fused_fwd", "dtype": "bf16", "us": round(ms * 1000, 2),
-                     "tflops": round(fl / ms / 1e9, 1), "frac_of_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 3),
-                     "bound": "tensor", "kernel": call.split(" [")[0][:40], "operand_sets": sets})
-        del Os
-        del t, ts
+            fl = 4 * h * s * s * d
+            rows.append({"set": "attention", "s": s, "op": "fused_fwd", "dtype": str(dt)[6:],
+                         "us": round(ms * 1000, 2), "tflops": round(fl / ms / 1e9, 1),
+                         "frac_of_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 3),
+                         "bound": "tensor", "kernel": call.split(" [")[0][:40], "operand_sets": sets})
+            del Os, t, ts
+            torch.cuda.empty_cache()
     return rows
+
+
+# ------------------------------------------------------------------ probe
+PROBE_LAYOUT = {"fwd": "nt", "dgrad": "nn", "wgrad": "tn", "qk": "nt", "do_vt": "nt", "pv": "nn", "ds_k": "nn",
+          "pt_do": "tn", "dst_q": "tn"}
+PROBE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+
+
+def probe_main(argv=None):
+    """`bench.py probe OP D0 D1 D2 ...`: one product through the public entry
+    points, alone, optionally with a forced plan (see the module docstring)."""
+    import tempfile
+
+    from gemms_linear_layers_gb300 import _binding as tg
+    ap = argparse.ArgumentParser(prog="bench.py probe")
+    ap.add_argument("op")
+    ap.add_argument("dims", type=int, nargs=3)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16", "f32"],
+                    help="f32: FP32 operands and output (layer products only, CUDA-core kernel)")
+    ap.add_argument("--out", default="same", choices=["same", "f32"])
+    ap.add_argument("--plan", default=None, help='"bn splits [raster]"; splits may be sk')
+    ap.add_argument("--reps", type=int, default=20)
+    a = ap.parse_args(argv)
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[a.dtype]
+    if dtype == torch.float32 and a.op not in ("fwd", "dgrad", "wgrad"):
+        raise SystemExit("--dtype f32 applies to fwd, dgrad and wgrad only")
+    out_dtype = dtype if a.out == "same" else torch.float32
+    dev = "cuda"
+    if a.op in ("fwd", "dgrad", "wgrad"):
+        T, d_in, d_out = a.dims
+        X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="probe", device=dev)
+        M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[a.op]
+        batch = 1
+        out = torch.empty(M, N, dtype=out_dtype, device=dev)
+        fn = {"fwd": lambda ws: tg.tg_gemm_fwd(X, W, Y=out, ws=ws),
+              "dgrad": lambda ws: tg.tg_gemm_dgrad(dY, W, dX=out, ws=ws),
+              "wgrad": lambda ws: tg.tg_gemm_wgrad(dY, X, dW=out, ws=ws)}[a.op]
+    elif a.op.startswith("lora"):
+        T, d_in, d_out = a.dims
+        X, A, B, H, dY = inputs.lora_inputs(T, d_in, d_out, 16, dtype, tag="probe", device=dev)
+        M, N, K, batch = T, 16, d_in, 1
+        outs = {"dA": torch.empty(16, d_in, dtype=out_dtype, device=dev),
+                "dB": torch.empty(d_out, 16, dtype=out_dtype, device=dev),
+                "dX": torch.empty(T, d_in, dtype=out_dtype, device=dev)}
+        Hout = torch.empty(T, 16, dtype=out_dtype, device=dev)
+        Yout = torch.empty(T, d_out, dtype=out_dtype, device=dev)
+        fn = {"lora_down": lambda ws: tg.tg_lora_down(X, A, H=Hout, ws=ws),
+              "lora_up": lambda ws: tg.tg_lora_up(H, B, Y=Yout, ws=ws),
+              "lora_grad": lambda ws: tg.tg_lora_grad(X, A, B, H, dY, outs=outs, ws=ws)}[a.op]
+        nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
+                  "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
+                  "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
+    elif a.op == "attn_fwd":  # the fused forward (counted as its two products: 4 h s^2 d flops)
+        h, s, d = a.dims
+        t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
+        M, N, K, batch = s, s, 2 * d, h
+        out = torch.empty(h, s, d, dtype=out_dtype, device=dev)
+        fn = lambda ws: tg.tg_attn_fwd(t["Q"], t["K"], t["V"], O=out)  # noqa: E731
+    else:
+        h, s, d = a.dims
+        t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
+        x, y = inputs.ATTN_OPERANDS[a.op]
+        ss = a.op in ("qk", "do_vt")
+        M, N, K, batch = (s, s, d, h) if ss else (s, d, s, h)
+        out = torch.empty(h, s, s if ss else d, dtype=out_dtype, device=dev)
+        fn = lambda ws: tg.tg_bmm_attn(a.op, t[x], t[y], C=out, ws=ws)  # noqa: E731
+    if a.plan:
+        f = tempfile.NamedTemporaryFile("w", suffix=".txt", delete=False)
+        f.write(f"{PROBE_LAYOUT[a.op]} {PROBE_NAME[dtype]} {PROBE_NAME[out_dtype]} {M} {N} {K} {batch} {a.plan}\n")
+        f.close()
+        assert tg.tg_load_table(f.name) == 0
+        os.unlink(f.name)
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        fn(ws)
+    torch.cuda.synchronize()
+    plan = tg.tg_last_call()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(a.reps):
+            fn(ws)
+    times = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / a.reps)
+    ms = statistics.median(times)
+    st = tg.tg_stream_status(stream)
+    if a.op.startswith("lora"):
+        print(f"{a.op} T={a.dims[0]} d_in={a.dims[1]} d_out={a.dims[2]}: {ms * 1e3:.2f} us, "
+              f"{nbytes / ms / 1e6:.0f} GB/s, status {st} [{plan}]", flush=True)
+    else:
+        print(f"{a.op} M={M} N={N} K={K} batch={batch}: {ms * 1e3:.2f} us, "
+              f"{workloads.flops(M, N, K, batch) / ms / 1e9:.0f} TFLOP/s, status {st} [{plan}]", flush=True)
+    return 0 if st == 0 else 1
 
 
 # ------------------------------------------------------------------ main
@@ -795,6 +1012,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
+    ap.add_argument("--set", default="2b", choices=sorted(STEP_SETS),
+                    help="layer set of the headline step (default: the 2B-class set at 1,024-4,096 tokens)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-product rows of the other sets")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
@@ -803,7 +1022,7 @@ def main():
     ap.add_argument("--concurrent-step", action="store_true",
                     help="one graph per step with the training step's independent products on parallel branches")
     ap.add_argument("--only", default=None,
-                    help="comma-separated products to run, e.g. head.wgrad.bfloat16 (profiling a single kernel)")
+                    help="comma-separated products to run, e.g. gate.fwd.T4096.bfloat16 (profiling a single kernel)")
     ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -823,32 +1042,30 @@ def main():
     table = os.environ.get("TG_TABLE", tg.DEFAULT_TABLE)
     table = table if table and os.path.exists(table) else None
     pk = peaks()
+    cfg, workload = STEP_SETS[args.set]
     stream = torch.cuda.Stream()
     only = set(args.only.split(",")) if args.only else None
-    prods = build_step("cuda", only)
+    prods = build_step("cuda", only, cfg)
     if not prods:
         raise SystemExit(f"--only {args.only}: no such product")
     capture(prods, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step_flops = sum(p.flops for p in prods)
-
-    # untimed probe: per-product times and the dominant kernel identity
-    per_prod = probe_products(prods, stream, flush)
-    by_kernel = {}
+    seen = {}
     for p in prods:
-        k = by_kernel.setdefault(p.kernel, {"ms": 0.0, "flops": 0, "n": 0, "products": []})
-        k["ms"] += per_prod[p.name]
-        k["flops"] += p.flops
-        k["n"] += 1
-        k["products"].append(p.name)
-    dom_name, dom = max(by_kernel.items(), key=lambda kv: kv[1]["ms"])
+        for n in ("X", "W", "dY"):
+            seen[id(p.t[n])] = p.t[n].numel() * p.t[n].element_size()
+    resident = sum(seen.values())
+
+    # untimed probe: per-product times and the dominant launch class
+    per_prod = probe_products(prods, stream, flush)
+    classes = by_launch_class(prods, per_prod)
+    dom_name, dom = max(classes.items(), key=lambda kv: kv[1]["ms"])
     step = None if args.per_product_graphs else capture_step(prods, stream, dom_name, args.concurrent_step)
     if step and args.concurrent_step:
-        mode = ("one CUDA graph per step with the training step's independent products on parallel branches "
-                "(forward q|k|v and gate|up; backward each layer's dgrad|wgrad, gate|up and q|k|v as groups); "
-                "external events inside it bracket the dominant kernel")
+        mode = "one CUDA graph per step, independent products on parallel branches; events bracket the dominant class"
     elif step:
-        mode = "one CUDA graph per step, products one after another; external events bracket the dominant kernel"
+        mode = "one CUDA graph per step, products in training order; events inside it bracket the dominant class"
     else:
         mode = "one CUDA graph per product; events between them on the launching stream"
 
@@ -877,7 +1094,8 @@ def main():
     achieved = flops_per_launch / (avg_launch_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": profiled_traffic(dom_name),
-                "kernel": dom_name, "products": dom["products"],
+                "kernel": dom_name, "launches_per_step": dom["n"],
+                "gflop_per_launch": round(flops_per_launch / 1e9, 3),
                 "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
                 "share_of_step": round(dom_ms / total_ms, 3)}
 
@@ -885,27 +1103,33 @@ def main():
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": WORKLOAD if not only else f"{WORKLOAD}; only {sorted(only)}", "T": 2048,
-                       "products_per_step": len(prods),
+            "config": {"workload": workload if not only else f"{workload}; only {sorted(only)}",
+                       "T": list(step_token_counts(cfg)), "products_per_step": len(prods),
                        "tile_table": os.path.relpath(table, ROOT) if table else None,
                        "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
-                       "l2": "flushed before every step (256 MiB write, untimed)",
+                       "l2": f"step inputs {resident / 1e9:.2f} GB resident in HBM; L2 flushed before every step "
+                             "(256 MiB write, untimed)",
                        "timing": mode},
-            "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary(),
-            "per_kernel_ms_per_step_probe": {k: round(v["ms"], 4) for k, v in by_kernel.items()}}
+            "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary()}
 
     if rank == 0:
         if not args.no_e2e:
-            e2e_n = min(args.steps, 5)
+            e2e_n = min(args.steps, 3)
             ms, h2d, d2h = e2e_steps(prods, e2e_n, stream)
             line["e2e"] = {"value": round(step_flops * e2e_n / (ms / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "ms_per_step": round(ms / e2e_n, 3)}
         if world == 1 and not args.no_cpu:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(cfg=cfg)
+        classes_ms = {k: round(v["ms"], 4) for k, v in sorted(classes.items(), key=lambda kv: -kv[1]["ms"])}
+        print("row " + json.dumps({"set": "probe", "ms_per_step_by_launch_class": classes_ms}), flush=True)
         if not args.no_rows:
+            del prods, step
+            torch.cuda.empty_cache()
             rows = measure_rows(stream, pk)
-            line["rows"] = rows
+            for r in rows:
+                print("row " + json.dumps(r), flush=True)
+            line["bars"] = bars_of(rows)
             if args.rows_out:
                 with open(args.rows_out, "w") as f:
                     json.dump(rows, f, indent=1)
@@ -916,4 +1140,8 @@ def main():
 
 
 if __name__ == "__main__":
+    if len(sys.argv) > 1 and sys.argv[1] == "probe":
+        import __graft_entry__
+        __graft_entry__.build()
+        sys.exit(probe_main(sys.argv[2:]))
     main()

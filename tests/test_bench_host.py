@@ -50,14 +50,64 @@ def test_step_waves_cover_every_product_once_in_training_order():
     flat = [p for w in waves for p in w]
     assert sorted(map(id, flat)) == sorted(map(id, prods))
     names = [[p.name for p in w] for w in waves]
-    assert names[0] == ["q.fwd.bfloat16", "k.fwd.bfloat16", "v.fwd.bfloat16"]
-    assert names[5] == ["head.dgrad.bfloat16", "head.wgrad.bfloat16"]
+    assert names[0] == ["q.fwd.T2048.bfloat16", "k.fwd.T2048.bfloat16", "v.fwd.T2048.bfloat16"]
+    assert names[5] == ["head.dgrad.T2048.bfloat16", "head.wgrad.T2048.bfloat16"]
     # a wave never mixes dtypes, and forward products come before backward ones per dtype
     for w in waves:
         assert len({p.dtype for p in w}) == 1
     order = [(p.dtype, p.op) for w in waves for p in w]
     bf = [op for dt, op in order if dt == torch.bfloat16]
     assert bf.index("dgrad") > max(i for i, op in enumerate(bf) if op == "fwd")
+
+
+def test_step_waves_of_the_2b_set_keep_token_counts_apart():
+    """The headline step: 7 layers x 3 products x 3 token counts x 2 dtypes,
+    every wave inside one (dtype, token count) set, forwards before
+    backwards within each set."""
+    prods = []
+    cfg = workloads.DECODER_2B
+    for dt in cfg["dtypes"]:
+        for T in cfg["T"]:
+            for layer, d_in, d_out in cfg["layers"]:
+                for op in ("fwd", "dgrad", "wgrad"):
+                    prods.append(bench.Product(layer, op, dt, T, d_in, d_out))
+    assert len(prods) == 126
+    assert abs(sum(p.flops for p in prods) / 1e12 - 5.2510) < 1e-3
+    waves = bench.step_waves(prods)
+    flat = [p for w in waves for p in w]
+    assert sorted(map(id, flat)) == sorted(map(id, prods))
+    for w in waves:
+        assert len({(p.dtype, p.T) for p in w}) == 1
+    assert [p.name for p in waves[0]] == ["q.fwd.T1024.bfloat16", "k.fwd.T1024.bfloat16", "v.fwd.T1024.bfloat16"]
+    assert [p.name for p in waves[4]] == ["down.dgrad.T1024.bfloat16", "down.wgrad.T1024.bfloat16"]
+    p = prods[0]
+    p.kernel = "tc nt bn=256 pair"
+    assert p.launch_class == "tc nt bn=256 pair @ 1024x2304x2304"
+
+
+def test_launches_and_classes():
+    assert bench.launches_of("fwd tc nt M=4096 N=5760 K=2304 batch=1 bn=256 pair splits=1 raster=m table=hit ok") == 1
+    assert bench.launches_of("dgrad tc nn M=2048 N=576 K=49152 batch=1 bn=192 pair splits=3 raster=n ok") == 2
+    assert bench.launches_of("wgrad tc tn M=2304 N=2304 K=2048 batch=1 bn=256 pair splits=1 tail=5x4 ok") == 2
+    prods = [bench.Product("q", "fwd", torch.bfloat16, 2048, 2304, 2304),
+             bench.Product("k", "fwd", torch.bfloat16, 2048, 2304, 2304),
+             bench.Product("gate", "fwd", torch.bfloat16, 2048, 2304, 5760)]
+    for p in prods:
+        p.kernel = "tc nt bn=256 pair"
+    cl = bench.by_launch_class(prods, {prods[0].name: 1.0, prods[1].name: 2.0, prods[2].name: 2.5})
+    k = "tc nt bn=256 pair @ 2048x2304x2304"
+    assert cl[k]["n"] == 2 and cl[k]["ms"] == 3.0 and cl[k]["flops"] == 2 * prods[0].flops
+    assert max(cl.items(), key=lambda kv: kv[1]["ms"])[0] == k
+
+
+def test_bars_from_rows():
+    rows = [{"set": "2B", "T": 1024, "op": "fwd", "frac_cold": 0.4},
+            {"set": "2B", "T": 2048, "op": "fwd", "frac_cold": 0.8},
+            {"set": "2B", "T": 4096, "op": "wgrad", "frac_cold": 0.75, "wgrad_over_fwd": 0.9},
+            {"set": "2B", "T": 4096, "op": "wgrad_acc", "frac_cold": 0.6},
+            {"set": "LoRA", "op": "down", "frac_of_hbm": 0.5}, {"set": "LoRA", "op": "up_add", "frac_of_hbm": 0.3}]
+    assert bench.bars_of(rows) == {"min_tensor_frac_T2048_4096": 0.75, "min_wgrad_over_fwd": 0.9,
+                                   "min_lora_hbm_frac": 0.5}
 
 
 def test_profiled_traffic_needs_matching_key_and_sources(tmp_path):
