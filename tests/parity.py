@@ -73,6 +73,29 @@ def sample_coords(M, N, batch=1, rows=128, cols=128, rand=8192, seed=0):
             np.concatenate(jj).astype(np.int64))
 
 
+def sample_coords_every_batch(M, N, batch, rows=128, cols=128, rand=8192, seed=0):
+    """Like sample_coords, but the full rows and columns are dealt to the
+    batch entries in turn, so every entry (every attention head) has at least
+    one full row and one full column checked when rows, cols >= batch."""
+    rng = np.random.default_rng(seed)
+    bi, ii, jj = [], [], []
+    for t in range(rows):
+        b, i = t % batch, int(rng.integers(0, M))
+        bi.append(np.full(N, b)); ii.append(np.full(N, i)); jj.append(np.arange(N))
+    for t in range(cols):
+        b, j = t % batch, int(rng.integers(0, N))
+        bi.append(np.full(M, b)); ii.append(np.arange(M)); jj.append(np.full(M, j))
+    bi.append(rng.integers(0, batch, rand))
+    ii.append(rng.integers(0, M, rand))
+    jj.append(rng.integers(0, N, rand))
+    for b in (0, batch - 1):
+        for i in (0, M - 1):
+            for j in (0, N - 1):
+                bi.append([b]); ii.append([i]); jj.append([j])
+    return (np.concatenate(bi).astype(np.int64), np.concatenate(ii).astype(np.int64),
+            np.concatenate(jj).astype(np.int64))
+
+
 def gather(t: torch.Tensor, coords):
     """Values of a GPU tensor ([M,N] or [batch,M,N]) at sampled coordinates, as float64."""
     bi, ii, jj = (torch.from_numpy(c).to(t.device) for c in coords)

@@ -14,7 +14,7 @@ import torch
 import oracle
 from gemms_linear_layers_gb300 import _binding as tg
 from gemms_linear_layers_gb300 import inputs, workloads
-from parity import assert_close, gather, sample_coords
+from parity import assert_close, gather, sample_coords, sample_coords_every_batch
 
 pytestmark = pytest.mark.gpu
 DT16 = (torch.bfloat16, torch.float16)
@@ -29,6 +29,8 @@ def _lib():
 
 
 # --------------------------------------------------------------- attention
+ATTN_SEED = {op: i for i, op in enumerate(oracle.ATTN_OPS)}
+
 @pytest.mark.parametrize("out_kind", ["f32", "same"])
 @pytest.mark.parametrize("dtype", DT16)
 @pytest.mark.parametrize("op", oracle.ATTN_OPS)
@@ -46,9 +48,9 @@ def test_attention_small(hsd, op, dtype, out_kind):
 @pytest.mark.parametrize("dtype", DT16)
 @pytest.mark.parametrize("s", workloads.ATTENTION["s"])
 def test_attention_full_size(s, dtype):
-    """36 heads, head_dim 64: all six products, sampled against the oracle."""
-    if s == 4096 and dtype == torch.float16:
-        pytest.skip("s=4096 checked in bf16")
+    """36 heads, head_dim 64: all six products, sampled against the oracle:
+    128 full rows and 128 full columns dealt over the heads (each head has
+    at least three of each) plus 8,192 random elements."""
     h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
     t = inputs.attn_inputs(h, s, d, dtype, tag="attn")
     dev = {k: v.cuda() for k, v in t.items()}
@@ -56,7 +58,7 @@ def test_attention_full_size(s, dtype):
         a, b = inputs.ATTN_OPERANDS[op]
         got = tg.tg_bmm_attn(op, dev[a], dev[b])
         M, N = (s, s) if op in ("qk", "do_vt") else (s, d)
-        co = sample_coords(M, N, batch=h, rows=16, cols=16, rand=2048, seed=s)
+        co = sample_coords_every_batch(M, N, h, seed=s + ATTN_SEED[op])
         C, S = oracle.bmm_attn(op, t[a], t[b], sample=co)
         assert_close(gather(got, co), C, S, f"attn {op} s={s} [{tg.tg_last_call()}]", dtype)
         del got
