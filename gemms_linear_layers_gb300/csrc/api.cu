@@ -405,50 +405,13 @@ static Plan heuristic_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int o
       }
     }
   }
-  // stream-K: every CTA gets an equal share of the tile x K-block iterations;
-  // a cut tile costs its pieces' FP32 write and the owner's read-back
-  for (int bn : bns) {
-    if (bn % 64 != 0) continue;  // stream-K partial tiles are 64-column multiples
-    const int64_t tiles = batch * cdiv(M, 128) * cdiv(N, bn);
-    const int64_t iters = tiles * kb;
-    if (iters < sms || tiles * 4 < sms) continue;
-    const double kb_cyc = kb_cycles(bn);
-    const double per_cta = static_cast<double>(cdiv(iters, sms));
-    // + the fix-up: flag waits, then the partial tile written and read back
-    // (measured: ~3 us more than the MMAs on small weight gradients)
-    double t = per_cta * kb_cyc + (600.0 + 128.0 * bn * out_bytes / 48.0) * cdiv(tiles, sms) + 6000.0 +
-               2.0 * 128.0 * bn * 4 / 16.0;
-    if (t < best_t * 0.95) {
-      best_t = t;
-      best.bn = bn;
-      best.splits = 1;
-      best.sk = true;
-      best.tail = 0;
-      best.pair = false;
-      best.csplit = 0;
-    }
-  }
-  // stream-K on CTA pairs (256 x 256 tiles, ranges per pair)
-  if (M > 128) {
-    const int bn = 256, pairs = sms / 2;
-    const int64_t tiles = batch * cdiv(M, 256) * cdiv(N, bn);
-    const int64_t iters = tiles * kb;
-    if (pairs > 0 && iters >= pairs && tiles * 4 >= pairs) {
-      const double kb_cyc = 4.0 * fmax(125.0, 0.525 * bn);
-      const double per_pair = static_cast<double>(cdiv(iters, pairs));
-      const double t = per_pair * kb_cyc + (600.0 + 128.0 * bn * out_bytes / 48.0) * cdiv(tiles, pairs) + 6000.0 +
-                       2.0 * 128.0 * bn * 4 / 16.0;
-      if (t < best_t * 0.95) {
-        best_t = t;
-        best.bn = bn;
-        best.splits = 1;
-        best.sk = true;
-        best.tail = 0;
-        best.pair = true;
-        best.csplit = 0;
-      }
-    }
-  }
+  // Stream-K is never proposed here, only taken from a table entry: its
+  // owners wait for partial tiles from later CTAs of the same launch, which
+  // assumes the whole persistent grid is resident at once.  A launch that
+  // shares the GPU with work on another stream may have CTAs waiting for SMs
+  // that its own waiting owners hold, until the bounded wait gives up.  The
+  // tail split and the cluster split cover the shapes where it was measured
+  // to help, without any wait between CTAs of different clusters.
   return best;
 }
 

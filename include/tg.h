@@ -38,7 +38,14 @@
  *     takes a slower CUDA-core GPU path with identical semantics.
  *   - Errors are return codes; nothing aborts, exits or throws across the ABI.
  *   - Calls on different streams may run concurrently if they do not share a
- *     workspace or an output.
+ *     workspace or an output.  One exception: a layer product whose tile-table
+ *     entry selects the stream-K schedule (token "sk", see tg_load_table)
+ *     needs every CTA of its launch resident at once, because CTAs wait for
+ *     partial tiles of later CTAs of the same launch; run it with the GPU to
+ *     itself (nothing else in flight on other streams), or a wait may run out
+ *     and tg_stream_status report TG_ERR_DEVICE_TIMEOUT.  Only a table entry
+ *     selects stream-K; the shipped table has none and the library never
+ *     picks it by itself.
  */
 #ifndef TG_H
 #define TG_H

@@ -264,8 +264,8 @@ def test_cost_model_plans_are_well_formed(lib, seed):
     """Over random shapes (no table), every plan the cost model makes is one
     the kernels can run: a tile width they offer, CTA pairs only over more
     than 128 rows, no more K splits than 64-deep K blocks, cluster splits of
-    2-8 CTAs whose clusters all fit on the 152 SMs at once, a persistent
-    stream-K grid no larger than the SMs, and the CUDA-core path exactly when
+    2-8 CTAs whose clusters all fit on the 152 SMs at once, never stream-K
+    (whose waits need the whole grid resident), and the CUDA-core path exactly when
     a row pitch is not a multiple of 16 bytes."""
     import random
     import torch
@@ -292,10 +292,9 @@ def test_cost_model_plans_are_well_formed(lib, seed):
         kb = -(-K // 64)
         if "pair" in f:
             assert M > 128 and bn in (128, 192, 256), p
-        if "sk" in f:
-            assert 1 <= int(kv["grid"]) <= 152, p
-        else:
-            assert 1 <= int(kv["splits"]) <= kb, p
+        # stream-K needs its whole grid resident; only a table entry may pick it
+        assert "sk" not in f, p
+        assert 1 <= int(kv["splits"]) <= kb, p
         if "cs" in f:
             cs = int(kv["cluster"])
             tiles = batch * -(-M // 128) * -(-N // bn)
