@@ -5,7 +5,7 @@ One step = every product of the 2B-class decoder layer set (q, k, v, o
 2304->2304; gate, up 2304->5760; down 5760->2304) at T = 1,024, 2,048 and
 4,096 tokens, each as forward, input gradient and weight gradient, in bf16 and
 in fp16 with FP32 accumulation: 126 products, 5.25 TFLOP.  Inputs are seeded
-synthetic tensors resident in HBM (3.2 GB, far above the L2); L2 is also
+synthetic tensors resident in HBM (1.95 GB, far above the L2); L2 is also
 flushed (a 256 MiB write) before every step, outside the timed events.  The
 step is one captured CUDA graph of the library calls in training order; CUDA
 events inside it mark the step and bracket every launch of the dominant
