@@ -294,8 +294,9 @@ def attn_bwd(Q, K, V, dO, scale):
     dq = scale * np.einsum("hij,hjd->hid", ds, k)
     dk = scale * np.einsum("hij,hid->hjd", ds, q)
     ads = p * (np.abs(dp) + np.abs(delta))
-    return {"dQ": (dq, scale * np.einsum("hij,hjd->hid", ads, np.abs(k))),
-            "dK": (dk, scale * np.einsum("hij,hid->hjd", ads, np.abs(q))),
+    asc = abs(scale)
+    return {"dQ": (dq, asc * np.einsum("hij,hjd->hid", ads, np.abs(k))),
+            "dK": (dk, asc * np.einsum("hij,hid->hjd", ads, np.abs(q))),
             "dV": (dv, np.einsum("hij,hid->hjd", p, np.abs(do)))}
 
 

@@ -531,3 +531,19 @@ def test_attn_bwd_value_gradient_is_p_transposed_times_do():
     p = np.exp(x - x.max(axis=2, keepdims=True))
     p /= p.sum(axis=2, keepdims=True)
     assert np.all(np.abs(dV - np.einsum("hij,hid->hjd", p, f64(dO))) <= 1e-12 * S)
+
+
+@pytest.mark.parametrize("scale", [0.6, -0.6])
+def test_attn_bwd_error_scales_bound_the_values(scale):
+    """Each error scale is a sum of magnitudes of the terms the gradient sums
+    (for dQ and dK the terms carry the factor scale, so their magnitudes carry
+    |scale|): it is non-negative and at least the magnitude of the value, for
+    a negative scale too.  The finite differences of the same case pin the
+    values."""
+    h, s, d = 2, 5, 3
+    Q, K, V, dO = (rand16((h, s, d), torch.float32, 360 + i, spread=False) for i in range(4))
+    g = oracle.attn_bwd(Q, K, V, dO, scale)
+    for name in ("dQ", "dK", "dV"):
+        val, S = g[name]
+        assert np.all(S >= 0), name
+        assert np.all(np.abs(val) <= S * (1 + 1e-12)), name
