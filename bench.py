@@ -30,7 +30,7 @@ region.
 [--plan "bn splits [raster]"] [--reps R]` times one product alone through the
 public entry points (the command the ncu summaries are captured with): OP is
 fwd|dgrad|wgrad (dims T d_in d_out), one of the attention products
-qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd (dims heads s d), or
+qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd / attn_bwd (dims heads s d), or
 lora_down|lora_up|lora_grad (dims T d_in d_out, rank 16); --plan writes a
 one-line tile table for the shape and loads it first.
 """
@@ -955,6 +955,12 @@ def probe_main(argv=None):
         nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
                   "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
                   "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
+    elif a.op == "attn_bwd":  # the fused backward (counted as its four products dV, dP, dQ, dK: 8 h s^2 d flops)
+        h, s, d = a.dims
+        t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)
+        M, N, K, batch = s, s, 4 * d, h
+        outs = {k: torch.empty(h, s, d, dtype=out_dtype, device=dev) for k in ("dQ", "dK", "dV")}
+        fn = lambda ws: tg.tg_attn_bwd(t["Q"], t["K"], t["V"], t["dO"], outs=outs, ws=ws)  # noqa: E731
     elif a.op == "attn_fwd":  # the fused forward (counted as its two products: 4 h s^2 d flops)
         h, s, d = a.dims
         t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)

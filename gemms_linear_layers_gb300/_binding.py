@@ -27,6 +27,7 @@ _DT = {torch.bfloat16: TG_BF16, torch.float16: TG_F16, torch.float32: TG_F32}
 TG_OP_GEMM_FWD, TG_OP_GEMM_DGRAD, TG_OP_GEMM_WGRAD = 0, 1, 2
 TG_OP_LORA_DOWN, TG_OP_LORA_UP, TG_OP_LORA_GRAD, TG_OP_BMM_ATTN = 3, 4, 5, 6
 TG_OP_LORA_DOWN_F32W, TG_OP_LORA_UP_F32W, TG_OP_LORA_GRAD_F32W = 7, 8, 9
+TG_OP_ATTN_BWD = 10
 ATTN_OPS = {"qk": 0, "pv": 1, "do_vt": 2, "pt_do": 3, "ds_k": 4, "dst_q": 5}
 SIZE_MAX = (1 << 64) - 1
 
@@ -48,6 +49,7 @@ SIGNATURES = {
     "tg_lora_grad_f32w": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i, _i,
                                _vp, _sz, _vp]),
     "tg_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp]),
+    "tg_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz, _vp]),
     "tg_lora_grad_add": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float,
                               _i, _i, _vp, _sz, _vp]),
     "tg_bmm_attn": (_i, [_i, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -387,6 +389,26 @@ def tg_attn_fwd(Q, K, V, O=None, scale=None, out_dtype=None, stream=None):
     _check(lib().tg_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), heads, s, d, sc, _DT[Q.dtype], _DT[O.dtype],
                              _stream(stream)), "tg_attn_fwd")
     return O
+
+
+def tg_attn_bwd(Q, K, V, dO, scale=None, out_dtype=None, outs=None, ws=None, stream=None):
+    """Fused attention backward: {"dQ", "dK", "dV"} of the forward of tg_attn_fwd given dO; all [heads, s, 64]."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (dO, "dO")):
+        _need(t, n, 3)
+    heads, s, d = Q.shape
+    for t in (K, V, dO):
+        if tuple(t.shape) != (heads, s, d) or t.dtype != Q.dtype:
+            raise ValueError("K, V and dO must match Q")
+    outs = dict(outs or {})
+    dt = out_dtype or (next(iter(outs.values())).dtype if outs else Q.dtype)
+    res = {k: _out(outs.get(k), (heads, s, d), dt, Q.device, k) for k in ("dQ", "dK", "dV")}
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    wptr, wbytes, buf = _workspace(TG_OP_ATTN_BWD, (heads, s, d, 0), _DT[Q.dtype], _DT[dt], ws, Q.device)
+    _check(lib().tg_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(res["dQ"]), _ptr(res["dK"]), _ptr(res["dV"]),
+                             heads, s, d, sc, _DT[Q.dtype], _DT[dt], wptr, wbytes, _stream(stream)), "tg_attn_bwd")
+    if buf is not ws:
+        _keep(buf, stream)
+    return res
 
 
 def tg_bmm_attn(op, A, B, C=None, out_dtype=None, ws=None, stream=None):

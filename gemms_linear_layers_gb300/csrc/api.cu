@@ -1296,8 +1296,39 @@ tg_status tg_attn_fwd(const void* Q, const void* K, const void* V, void* O, int6
   TG_TRY(device_ctx(&ctx));
   const int ik = in == TG_BF16 ? EK_BF16 : EK_F16;
   const int ok = out == TG_F32 ? EK_F32 : ik;
-  cudaError_t e = attn_fwd_launch(Q, K, V, O, heads, s, d, scale, ik, ok, static_cast<cudaStream_t>(stream));
-  record(std::string("attn_fwd fused heads=") + std::to_string(heads) + " s=" + std::to_string(s) + " " +
+  cudaError_t e = attn_fwd_tc_launch(Q, K, V, O, heads, s, d, scale, ik, ok, ctx->status, ctx->timeout_ns,
+                                     static_cast<cudaStream_t>(stream));
+  record(std::string("attn_fwd fused tc heads=") + std::to_string(heads) + " s=" + std::to_string(s) + " " +
+         (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+  return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status tg_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,
+                      int64_t heads, int64_t s, int64_t d, float scale, tg_dtype in, tg_dtype out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {heads, s, d}));
+  if (d != 64 || !std::isfinite(scale) || heads > 65535) return TG_ERR_INVALID_ARG;
+  const int64_t n = heads * s * d;
+  TG_TRY(check_ptr(Q, n, 2));
+  TG_TRY(check_ptr(K, n, 2));
+  TG_TRY(check_ptr(V, n, 2));
+  TG_TRY(check_ptr(dO, n, 2));
+  TG_TRY(check_ptr(dQ, n, dt_bytes(out)));
+  TG_TRY(check_ptr(dK, n, dt_bytes(out)));
+  TG_TRY(check_ptr(dV, n, dt_bytes(out)));
+  if (n > 0 && !(aligned(Q, 16) && aligned(K, 16) && aligned(V, 16) && aligned(dO, 16) && aligned(dQ, 16) &&
+                 aligned(dK, 16) && aligned(dV, 16)))
+    return TG_ERR_MISALIGNED;
+  const size_t need = n > 0 ? attn_bwd_ws_bytes(heads, s) : 0;
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return TG_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned(ws, 16)) return TG_ERR_MISALIGNED;
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  const int ik = in == TG_BF16 ? EK_BF16 : EK_F16;
+  const int ok = out == TG_F32 ? EK_F32 : ik;
+  cudaError_t e = attn_bwd_tc_launch(Q, K, V, dO, dQ, dK, dV, heads, s, d, scale, ik, ok, ws, ctx->status,
+                                     ctx->timeout_ns, static_cast<cudaStream_t>(stream));
+  record(std::string("attn_bwd fused tc heads=") + std::to_string(heads) + " s=" + std::to_string(s) + " " +
          (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
   return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
@@ -1324,6 +1355,7 @@ size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d
     case TG_OP_LORA_DOWN_F32W: return w32_ws(0, d0, d1, 0, d2, in, ctx->sms);
     case TG_OP_LORA_UP_F32W: return w32_ws(1, d0, 0, d1, d2, in, ctx->sms);
     case TG_OP_LORA_GRAD_F32W: return w32_ws(2, d0, d1, d2, d3, in, ctx->sms);
+    case TG_OP_ATTN_BWD: return d2 == 64 ? attn_bwd_ws_bytes(d0, d1) : SIZE_MAX;
     case TG_OP_BMM_ATTN: {
       GemmCall g;
       if (!attn_call(static_cast<tg_attn_op>(d0), nullptr, nullptr, nullptr, d1, d2, d3, in, out, nullptr, 0,

@@ -94,7 +94,8 @@ typedef enum {
   TG_OP_BMM_ATTN = 6,   /* d0=tg_attn_op, d1=batch, d2=s, d3=d */
   TG_OP_LORA_DOWN_F32W = 7,  /* d0=T, d1=d_in, d2=r */
   TG_OP_LORA_UP_F32W = 8,    /* d0=T, d1=d_out, d2=r */
-  TG_OP_LORA_GRAD_F32W = 9   /* d0=T, d1=d_in, d2=d_out, d3=r */
+  TG_OP_LORA_GRAD_F32W = 9,  /* d0=T, d1=d_in, d2=d_out, d3=r */
+  TG_OP_ATTN_BWD = 10        /* d0=heads, d1=s, d2=d */
 } tg_op;
 
 /* Forward product of a linear layer ("Where the time went"):
@@ -236,10 +237,30 @@ tg_status tg_lora_grad_f32w(const void* X, const float* A, const float* B, const
  * 16-byte aligned (TG_ERR_MISALIGNED otherwise); scale finite (the usual
  * 1/sqrt(d)).  No mask.  The [s, s] scores never reach memory: each row's
  * softmax is kept online in FP32 over key blocks, and the probabilities enter
- * the second product as 16-bit hi + lo parts (to within 2^-18 of FP32).
+ * the second product as 16-bit hi + lo parts (to within 2^-17 of FP32), on
+ * the tensor cores (tcgen05, with S, P and O in tensor memory).
  * No workspace. */
 tg_status tg_attn_fwd(const void* Q, const void* K, const void* V, void* O, int64_t heads, int64_t s,
                       int64_t d, float scale, tg_dtype in, tg_dtype out, void* stream);
+
+/* Fused attention backward: the gradients of L = <dO, O> for the forward of
+ * tg_attn_fwd, O[h] = softmax(scale . Q[h] K[h]^T) V[h], given Q, K, V and dO:
+ *   P = softmax(scale . Q K^T),  D_i = sum_j P_ij (dO V^T)_ij,
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale . dS K,  dK = scale . dS^T Q
+ * Q, K, V, dO are [heads, s, d] of type `in` (bf16 or fp16); dQ, dK, dV are
+ * [heads, s, d] of type `out` (FP32 or `in`), overwritten.  d must be 64;
+ * every pointer 16-byte aligned (TG_ERR_MISALIGNED otherwise); scale finite.
+ * No mask.  The [s, s] matrices never reach memory: three launches on the
+ * tensor cores recompute them per 128 x 128 block (row statistics, then dK
+ * and dV per key block, then dQ per query block); P and dS enter the
+ * products as 16-bit hi + lo parts, each scaled by a power of two that is
+ * taken off in FP32, so fp16 neither overflows nor loses small values.
+ * Workspace: tg_workspace_size(TG_OP_ATTN_BWD, heads, s, d, 0, in, out)
+ * bytes (three FP32 values per row), 16-byte aligned.  Results are bitwise
+ * reproducible run to run (no atomics). */
+tg_status tg_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,
+                      int64_t heads, int64_t s, int64_t d, float scale, tg_dtype in, tg_dtype out, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /* One of the batched products inside attention ("Tuning the kernels";
  * "Checking the results are right": batched attention), see tg_attn_op. */

@@ -124,7 +124,7 @@ def test_profiled_traffic_needs_matching_key_and_sources(tmp_path):
                                f"- traffic_bytes_per_launch: `275000000`\n- kernel_sources_sha1: `{digest}`\n")
     assert bench.profiled_traffic("tc nn bn=192 pair +reduce", str(prof), digest) == 275000000
     assert bench.profiled_traffic("tc nt bn=256 pair", str(prof), digest) is None
-    (csrc / "attn_fused.cu").write_text("another unit\n")  # a unit with no kernel of the step
+    (csrc / "attn_tc.cu").write_text("another unit\n")  # a unit with no kernel of the step
     assert bench.kernel_sources_digest(str(csrc)) == digest
     (csrc / "gemm_tc.cuh").write_text("kernel v2\n")  # the kernel changed since the capture
     assert bench.profiled_traffic("tc nn bn=192 pair +reduce", str(prof), bench.kernel_sources_digest(str(csrc))) is None

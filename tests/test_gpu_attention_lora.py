@@ -292,12 +292,13 @@ def test_attn_fwd_small(hs, dtype, out_kind):
     assert_close(got, O, attn_scale(S, E), f"attn_fwd {hs} [{call}]", out_dtype)
 
 
+@pytest.mark.parametrize("dtype", DT16)
 @pytest.mark.parametrize("s", workloads.ATTENTION["s"])
-def test_attn_fwd_full_size(s):
-    """36 heads, head_dim 64, bf16: sampled rows (each a full softmax over all
-    keys) against the oracle, and the same bits from a second run."""
+def test_attn_fwd_full_size(s, dtype):
+    """36 heads, head_dim 64, bf16 and fp16: sampled rows (each a full softmax
+    over all keys) against the oracle, and the same bits from a second run."""
     h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
-    t = inputs.attn_inputs(h, s, d, torch.bfloat16, tag="attn")
+    t = inputs.attn_inputs(h, s, d, dtype, tag="attn")
     dev = [t[n].cuda() for n in ("Q", "K", "V")]
     a = tg.tg_attn_fwd(*dev, out_dtype=torch.float32)
     b = tg.tg_attn_fwd(*dev, out_dtype=torch.float32)
@@ -309,6 +310,116 @@ def test_attn_fwd_full_size(s):
     O, S, E = oracle.attn_fwd(t["Q"], t["K"], t["V"], ATTN_SCALE, rows=(hh, ii))
     got = a[torch.from_numpy(hh).cuda(), torch.from_numpy(ii).cuda()]
     assert_close(got, O, attn_scale(S, E), f"attn_fwd s={s}", torch.float32)
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("scale", [1.0, -0.5, 3.0])
+def test_attn_fwd_running_maximum_refreshed(scale, dtype):
+    """Logits with a spread of tens (scale 1 to 3 on N(0,1) inputs, and keys
+    whose size grows along the sequence): the running maximum of a row is
+    overtaken block after block, so the partial output and sum are rescaled
+    many times, and most weights are far below the row's largest (fp16 keeps
+    their low parts).  Full check against the oracle."""
+    h, s, d = 2, 1000, 64
+    t = inputs.attn_inputs(h, s, d, dtype, tag="refresh")
+    grow = torch.linspace(0.25, 2.0, s).reshape(1, s, 1)
+    K = (t["K"].float() * grow).to(dtype)
+    got = tg.tg_attn_fwd(t["Q"].cuda(), K.cuda(), t["V"].cuda(), scale=scale, out_dtype=torch.float32)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    O, S, E = oracle.attn_fwd(t["Q"], K, t["V"], scale)
+    assert_close(got, O, attn_scale(S, E, abs(scale)), f"attn_fwd scale={scale} [{call}]", torch.float32)
+
+
+def logit_terms_max(Q, K):
+    """Per head, the largest sum_k |q_ik k_jk| over query i and key j (the
+    size of the largest logit's terms)."""
+    q, k = np.abs(oracle.decode(Q)), np.abs(oracle.decode(K))
+    return np.array([(q[h] @ k[h].T).max() for h in range(q.shape[0])])
+
+
+def attn_bwd_scale(S, E, scale):
+    """Error scale of the fused backward: the products' 1e-5 times the
+    oracle's sums of absolute terms, plus the FP32 rounding of the logits
+    (at most 64 2^-24 E each) carried through the probabilities into dV, dS
+    and D (four times over, generously); E per head, broadcast over rows."""
+    E = np.asarray(E, dtype=np.float64).reshape(-1, 1, 1)
+    return S * (1.0 + 4.0 * abs(scale) * 64 * 2.0 ** -24 * E / 1e-5)
+
+
+def check_attn_bwd(t, scale, out_dtype, what, heads=None, dO=None):
+    Q, K, V = t["Q"], t["K"], t["V"]
+    dO = t["dO"] if dO is None else dO
+    got = tg.tg_attn_bwd(Q.cuda(), K.cuda(), V.cuda(), dO.cuda(), scale=scale, out_dtype=out_dtype)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    assert "attn_bwd fused" in call, call
+    for h in (range(Q.shape[0]) if heads is None else heads):
+        sl = slice(h, h + 1)
+        ref = oracle.attn_bwd(Q[sl], K[sl], V[sl], dO[sl], scale)
+        E = logit_terms_max(Q[sl], K[sl])
+        for name in ("dQ", "dK", "dV"):
+            C, S = ref[name]
+            assert_close(got[name][sl], C, attn_bwd_scale(S, E, scale), f"{what} {name} head {h} [{call}]",
+                         out_dtype)
+    return got
+
+
+@pytest.mark.parametrize("out_kind", ["f32", "same"])
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("hs", [(2, 256), (3, 200), (1, 65), (1, 1), (2, 130), (1, 384)],
+                         ids=lambda t: "x".join(map(str, t)))
+def test_attn_bwd_small(hs, dtype, out_kind):
+    """Fused backward (dQ, dK, dV of <dO, softmax(scale Q K^T) V>) against the
+    oracle's chain rule in fp64, every element: whole and ragged blocks of
+    queries and keys, a single position."""
+    h, s = hs
+    out_dtype = torch.float32 if out_kind == "f32" else dtype
+    t = inputs.attn_inputs(h, s, 64, dtype, tag="fusedbwd")
+    check_attn_bwd(t, ATTN_SCALE, out_dtype, f"attn_bwd {hs}")
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("s", workloads.ATTENTION["s"])
+def test_attn_bwd_full_size(s, dtype):
+    """36 heads, head_dim 64: every element of dQ, dK and dV of three heads
+    (first, middle, last) against the oracle, and the same bits from a
+    second run."""
+    h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
+    t = inputs.attn_inputs(h, s, d, dtype, tag="attn")
+    a = check_attn_bwd(t, ATTN_SCALE, torch.float32, f"attn_bwd s={s}", heads=(0, h // 2, h - 1))
+    b = tg.tg_attn_bwd(t["Q"].cuda(), t["K"].cuda(), t["V"].cuda(), t["dO"].cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("scale", [1.0, -0.5, 3.0])
+def test_attn_bwd_wide_logits(scale, dtype):
+    """Logits with a spread of tens and keys growing along the sequence (as
+    in the forward's refresh test): the row statistics' running maximum is
+    overtaken block after block and most probabilities are far below the
+    row's largest.  Full check."""
+    h, s, d = 2, 1000, 64
+    t = dict(inputs.attn_inputs(h, s, d, dtype, tag="refreshbwd"))
+    grow = torch.linspace(0.25, 2.0, s).reshape(1, s, 1)
+    t["K"] = (t["K"].float() * grow).to(dtype)
+    check_attn_bwd(t, scale, torch.float32, f"attn_bwd scale={scale}")
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("g", [1e-4, 1e-7, 30.0])
+def test_attn_bwd_gradient_magnitudes(g, dtype):
+    """Output gradients far smaller and far larger than the config's N(0, 1e-2):
+    the power-of-two scaling of dS keeps fp16's hi + lo parts out of its
+    subnormal range and below its overflow, so the bound holds at every size."""
+    h, s, d = 2, 300, 64
+    t = inputs.attn_inputs(h, s, d, dtype, tag="gscale")
+    dO = inputs.normal((h, s, d), g, dtype, inputs.seed_for("gscale", g, str(dtype), "dO"))
+    check_attn_bwd(t, ATTN_SCALE, torch.float32, f"attn_bwd dO~N(0,{g})", dO=dO)
 
 
 def test_attn_fwd_zero_scale_is_the_mean():
