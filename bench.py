@@ -29,7 +29,8 @@ region.
 `python bench.py probe OP D0 D1 D2 [--dtype bf16|f16|f32] [--out same|f32]
 [--plan "bn splits [raster]"] [--reps R]` times one product alone through the
 public entry points (the command the ncu summaries are captured with): OP is
-fwd|dgrad|wgrad (dims T d_in d_out), one of the attention products
+fwd|dgrad|wgrad or fwd_lora|dgrad_lora (dims T d_in d_out; rank 16, scale 2),
+one of the attention products
 qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd / attn_bwd (dims heads s d), or
 lora_down|lora_up|lora_grad (dims T d_in d_out, rank 16); --plan writes a
 one-line tile table for the shape and loads it first.
@@ -775,6 +776,37 @@ def measure_rows(stream, pk, budget_s=150.0):
                 rows[-1]["acc_over_wgrad"] = round(res["wgrad_acc"] / res["wgrad"], 3)
                 del data, outs, ws
                 torch.cuda.empty_cache()
+    # the LoRA branch added inside the layer product (one pass over the output)
+    # against the product followed by the branch's read-modify-write pass
+    for name, d_in, d_out in (("q", 2304, 2304), ("gate", 2304, 5760), ("down", 5760, 2304)):
+        T, r, dt = 4096, 16, torch.bfloat16
+        X, W, dY = inputs.layer_inputs(T, d_in, d_out, dt, tag="rowsf", device="cuda")
+        _, A, B, H, _ = inputs.lora_inputs(T, d_in, d_out, r, dt, tag="rowsf", device="cuda")
+        dH = inputs.normal((T, r), 0.01, torch.float32, 7, device="cuda")
+        dH16, At = dH.to(dt), A.t().contiguous()
+        Y = torch.empty(T, d_out, dtype=dt, device="cuda")
+        dX = torch.empty(T, d_in, dtype=dt, device="cuda")
+        ws = torch.empty(1 << 28, dtype=torch.uint8, device="cuda")
+        pairs = {
+            "fwd_lora": (lambda i: (lambda: tg.tg_gemm_fwd_lora(X, W, H, B, 2.0, Y=Y, ws=ws)),
+                         lambda i: (lambda: (tg.tg_gemm_fwd(X, W, Y=Y, ws=ws), tg.tg_lora_up_add(H, B, Y, 2.0))),
+                         workloads.flops(T, d_out, d_in) + workloads.flops(T, d_out, r)),
+            "dgrad_lora": (lambda i: (lambda: tg.tg_gemm_dgrad_lora(dY, W, dH, A, 2.0, dX=dX, ws=ws)),
+                           lambda i: (lambda: (tg.tg_gemm_dgrad(dY, W, dX=dX, ws=ws),
+                                               tg.tg_lora_up_add(dH16, At, dX, 2.0))),
+                           workloads.flops(T, d_in, d_out) + workloads.flops(T, d_in, r)),
+        }
+        for op, (fused, separate, fl) in pairs.items():
+            ms_f, call = time_calls(stream, fused, reps=10)
+            ms_s, _ = time_calls(stream, separate, reps=10)
+            tf = fl / ms_f / 1e9
+            rows.append({"set": "LoRA-fused", "layer": name, "T": T, "op": op, "dtype": "bf16", "r": r,
+                         "us_fused": round(ms_f * 1000, 2), "us_product_then_add": round(ms_s * 1000, 2),
+                         "speedup": round(ms_s / ms_f, 3), "tflops": round(tf, 1),
+                         "frac_of_peak": round(tf / pk["bf16_tflops"], 3), "bound": "tensor",
+                         "kernel": call.split(" [")[0][:80]})
+        del X, W, dY, A, B, H, dH, dH16, At, Y, dX, ws
+        torch.cuda.empty_cache()
     # FP32 operands (the CUDA-core FFMA kernel): the 2B-class layers at T=2048
     # and the 135M-class head, against the FP32 CUDA-core peak
     f32_peak = fp32_peak_tflops()
@@ -900,7 +932,20 @@ def measure_rows(stream, pk, budget_s=150.0):
                          "us": round(ms * 1000, 2), "tflops": round(fl / ms / 1e9, 1),
                          "frac_of_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 3),
                          "bound": "tensor", "kernel": call.split(" [")[0][:40], "operand_sets": sets})
-            del Os, t, ts
+            # the fused backward: dQ, dK, dV without the [s, s] matrices (counted as its
+            # four products dV, dP, dQ, dK: 8 h s^2 d flops)
+            gs = [{k: torch.empty(h, s, d, dtype=dt, device="cuda") for k in ("dQ", "dK", "dV")} for _ in range(sets)]
+            wsb = torch.empty(max(16, tg.tg_workspace_size(tg.TG_OP_ATTN_BWD, h, s, d, 0, dt, dt)), dtype=torch.uint8,
+                              device="cuda")
+            ms, call = time_calls(stream, lambda i: (lambda: tg.tg_attn_bwd(ts[i]["Q"], ts[i]["K"], ts[i]["V"],
+                                                                            ts[i]["dO"], outs=gs[i], ws=wsb)),
+                                  reps=max(3, 2 * sets), sets=sets)
+            fl = 8 * h * s * s * d
+            rows.append({"set": "attention", "s": s, "op": "fused_bwd", "dtype": str(dt)[6:],
+                         "us": round(ms * 1000, 2), "tflops": round(fl / ms / 1e9, 1),
+                         "frac_of_peak": round(fl / ms / 1e9 / pk["bf16_tflops"], 3),
+                         "bound": "tensor", "kernel": call.split(" [")[0][:40], "operand_sets": sets})
+            del Os, gs, wsb, t, ts
             torch.cuda.empty_cache()
     return rows
 
@@ -955,6 +1000,15 @@ def probe_main(argv=None):
         nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
                   "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
                   "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
+    elif a.op in ("fwd_lora", "dgrad_lora"):  # the layer product with a rank-16 LoRA branch inside it
+        T, d_in, d_out = a.dims
+        X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="probe", device=dev)
+        _, A, B, H, _ = inputs.lora_inputs(T, d_in, d_out, 16, dtype, tag="probe", device=dev)
+        dH = inputs.normal((T, 16), 0.01, torch.float32, 7, device=dev)
+        M, N, K, batch = (T, d_out, d_in + 16, 1) if a.op == "fwd_lora" else (T, d_in, d_out + 16, 1)
+        out = torch.empty(M, N, dtype=out_dtype, device=dev)
+        fn = ((lambda ws: tg.tg_gemm_fwd_lora(X, W, H, B, 2.0, Y=out, ws=ws)) if a.op == "fwd_lora"
+              else (lambda ws: tg.tg_gemm_dgrad_lora(dY, W, dH, A, 2.0, dX=out, ws=ws)))
     elif a.op == "attn_bwd":  # the fused backward (counted as its four products dV, dP, dQ, dK: 8 h s^2 d flops)
         h, s, d = a.dims
         t = inputs.attn_inputs(h, s, d, dtype, tag="probe", device=dev)

@@ -9,7 +9,8 @@ library; the first call does, and fails loudly if it has not been built.
 from __future__ import annotations
 
 __all__ = [
-    "tg_gemm_fwd", "tg_gemm_dgrad", "tg_gemm_wgrad", "tg_gemm_wgrad_noalloc", "tg_gemm_wgrad_accumulate",
+    "tg_gemm_fwd", "tg_gemm_dgrad", "tg_gemm_wgrad", "tg_gemm_fwd_lora", "tg_gemm_dgrad_lora",
+    "tg_gemm_wgrad_noalloc", "tg_gemm_wgrad_accumulate",
     "tg_lora_down", "tg_lora_up", "tg_lora_grad", "tg_lora_up_add", "tg_lora_grad_add",
     "tg_lora_down_f32w", "tg_lora_up_f32w", "tg_lora_grad_f32w", "tg_bmm_attn", "tg_attn_fwd", "tg_attn_bwd",
     "tg_workspace_size", "tg_plan_describe", "tg_stream_status",

@@ -28,6 +28,7 @@ TG_OP_GEMM_FWD, TG_OP_GEMM_DGRAD, TG_OP_GEMM_WGRAD = 0, 1, 2
 TG_OP_LORA_DOWN, TG_OP_LORA_UP, TG_OP_LORA_GRAD, TG_OP_BMM_ATTN = 3, 4, 5, 6
 TG_OP_LORA_DOWN_F32W, TG_OP_LORA_UP_F32W, TG_OP_LORA_GRAD_F32W = 7, 8, 9
 TG_OP_ATTN_BWD = 10
+TG_OP_GEMM_FWD_LORA, TG_OP_GEMM_DGRAD_LORA = 11, 12
 ATTN_OPS = {"qk": 0, "pv": 1, "do_vt": 2, "pt_do": 3, "ds_k": 4, "dst_q": 5}
 SIZE_MAX = (1 << 64) - 1
 
@@ -37,6 +38,9 @@ SIGNATURES = {
     "tg_gemm_fwd": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_dgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
     "tg_gemm_wgrad": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
+    "tg_gemm_fwd_lora": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz, _vp]),
+    "tg_gemm_dgrad_lora": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_float, _i, _i, _vp, _sz,
+                                _vp]),
     "tg_gemm_wgrad_accumulate": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _vp, _sz, _vp]),
     "tg_gemm_wgrad_noalloc": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
     "tg_lora_down": (_i, [_vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _vp, _sz, _vp]),
@@ -182,6 +186,47 @@ def tg_gemm_wgrad(dY, X, dW=None, out_dtype=None, ws=None, stream=None):
     _keep(keep, stream)
     return dW
 
+
+
+def tg_gemm_fwd_lora(X, W, H, B, scale, Y=None, out_dtype=None, ws=None, stream=None):
+    """Y = X W^T + scale H B^T in one product: X [T, d_in], W [d_out, d_in], H [T, r], B [d_out, r]."""
+    _need(X, "X", 2)
+    _need(W, "W", 2)
+    _need(H, "H", 2)
+    _need(B, "B", 2)
+    T, d_in = X.shape
+    d_out, r = W.shape[0], H.shape[1]
+    if W.shape[1] != d_in or H.shape[0] != T or tuple(B.shape) != (d_out, r):
+        raise ValueError("shapes do not match")
+    if not (W.dtype == H.dtype == B.dtype == X.dtype):
+        raise ValueError("X, W, H, B must share a dtype")
+    Y = _out(Y, (T, d_out), out_dtype or X.dtype, X.device, "Y")
+    wp, wn, keep = _workspace(TG_OP_GEMM_FWD_LORA, (T, d_out, d_in, r), _DT[X.dtype], _DT[Y.dtype], ws, X.device)
+    _check(lib().tg_gemm_fwd_lora(_ptr(X), _ptr(W), _ptr(H), _ptr(B), _ptr(Y), T, d_out, d_in, r, float(scale),
+                                  _DT[X.dtype], _DT[Y.dtype], wp, wn, _stream(stream)), "tg_gemm_fwd_lora")
+    _keep(keep, stream)
+    return Y
+
+
+def tg_gemm_dgrad_lora(dY, W, dH, A, scale, dX=None, out_dtype=None, ws=None, stream=None):
+    """dX = dY W + scale dH A in one product: dY [T, d_out], W [d_out, d_in], dH [T, r] FP32, A [r, d_in]."""
+    _need(dY, "dY", 2)
+    _need(W, "W", 2)
+    _need(A, "A", 2)
+    T, d_out = dY.shape
+    d_in, r = W.shape[1], A.shape[0]
+    if W.shape[0] != d_out or A.shape[1] != d_in or tuple(dH.shape) != (T, r):
+        raise ValueError("shapes do not match")
+    if dH.dtype != torch.float32 or not dH.is_contiguous() or dH.device != dY.device:
+        raise ValueError("dH must be a contiguous FP32 tensor on the device of dY")
+    if not (W.dtype == A.dtype == dY.dtype):
+        raise ValueError("dY, W, A must share a dtype")
+    dX = _out(dX, (T, d_in), out_dtype or dY.dtype, dY.device, "dX")
+    wp, wn, keep = _workspace(TG_OP_GEMM_DGRAD_LORA, (T, d_out, d_in, r), _DT[dY.dtype], _DT[dX.dtype], ws, dY.device)
+    _check(lib().tg_gemm_dgrad_lora(_ptr(dY), _ptr(W), _ptr(dH), _ptr(A), _ptr(dX), T, d_out, d_in, r, float(scale),
+                                    _DT[dY.dtype], _DT[dX.dtype], wp, wn, _stream(stream)), "tg_gemm_dgrad_lora")
+    _keep(keep, stream)
+    return dX
 
 
 def tg_gemm_wgrad_accumulate(dY, X, dW, ws=None, stream=None):

@@ -599,7 +599,7 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
       record(buf);
       return TG_ERR_WORKSPACE_TOO_SMALL;
     }
-    TcGemm t;
+    TcGemm t{};
     t.layout = g.layout;
     t.A = g.A;
     t.B = g.B;
@@ -822,6 +822,191 @@ tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int6
   GemmCall g{LAYOUT_NN, dY, W, dX, 1, T, d_in, d_out, d_out, d_in, T * d_out, d_out * d_in, in, out, -1, ws,
              ws_bytes, static_cast<cudaStream_t>(stream), "dgrad"};
   return run_gemm(g, ctx);
+}
+
+// ------------------------------------------------ layer product + LoRA branch
+// Workspace of a layer product with its LoRA branch added inside the
+// product: the staged LoRA block on the tensor-core path; on the CUDA-core
+// path an FP32 copy of the output when the output is 16-bit (both products
+// are added in FP32 there and the sum rounded once).
+static size_t layer_lora_ws(int layout, int64_t M, int64_t N, int64_t K, int64_t r, tg_dtype in, tg_dtype out,
+                            int sms) {
+  if (r == 0) return gemm_ws_bytes(layout, M, N, K, 1, in, out, sms);  // the plain product
+  const size_t tc = lora_block_ws_bytes(M, N);
+  const size_t simt = out == TG_F32 ? 0 : static_cast<size_t>(M) * N * 4;
+  return tc > simt ? tc : simt;
+}
+
+// C[M, N] = A B (layout NT: forward; NN: input gradient) + scale H F, H [M, r]
+// (16-bit, or FP32 when h_f32), F: forward B [N, r]; input gradient A [r, N]
+static tg_status run_layer_lora(const GemmCall& base, const void* H, int h_f32, const void* F, int64_t r, float scale,
+                                DevCtx* ctx) {
+  const bool dgrad = base.layout == LAYOUT_NN;
+  const int64_t M = base.M, N = base.N;
+  if (M == 0 || N == 0) {
+    record(std::string(base.name) + " empty output: nothing to do");
+    return TG_OK;
+  }
+  if (r == 0) return run_gemm(base, ctx);
+  const int ik = base.in == TG_BF16 ? EK_BF16 : EK_F16;
+  const int ok_kind = base.out == TG_F32 ? EK_F32 : ik;
+  char buf[320];
+  if (tc_eligible(base) && base.K > 0 && r <= 32 && aligned(H, h_f32 ? 4 : 2) && aligned(F, 2)) {
+    const size_t need = lora_block_ws_bytes(M, N);
+    if (base.ws == nullptr || base.ws_bytes < need || !aligned(base.ws, 16)) {
+      snprintf(buf, sizeof buf, "%s: workspace %zu bytes needed, %zu given", base.name, need,
+               base.ws ? base.ws_bytes : static_cast<size_t>(0));
+      record(buf);
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    // the product's own plan, with every K split undone: the LoRA block is
+    // the last K block of each whole tile
+    Plan p = make_plan(base.layout, M, N, base.K, 1, base.in, base.out, ctx->sms);
+    p.splits = 1;
+    p.tail = 0;
+    p.sk = false;
+    p.csplit = 0;
+    const void* A2 = nullptr;
+    const void* B2 = nullptr;
+    cudaError_t e = lora_block_prep_launch(H, h_f32, F, M, N, r, scale, ik, dgrad ? 1 : 0, base.ws, &A2, &B2, ctx->sms,
+                                           base.stream);
+    if (e == cudaSuccess) {
+      TcGemm t{};
+      t.layout = base.layout;
+      t.A = base.A;
+      t.B = base.B;
+      t.C = base.C;
+      t.in_kind = ik;
+      t.out_kind = ok_kind;
+      t.batch = 1;
+      t.M = M;
+      t.N = N;
+      t.K = base.K;
+      t.lda = base.lda;
+      t.ldb = base.ldb;
+      t.a_bstride = base.a_bs;
+      t.b_bstride = base.b_bs;
+      t.bn = p.bn;
+      t.splits = 1;
+      t.raster_n = p.raster_n;
+      t.pair = p.pair ? 1 : 0;
+      t.deep = plan_deep(p, M, N, base.K, 1, ctx->sms) ? 1 : 0;
+      t.lora_A2 = A2;
+      t.lora_B2 = B2;
+      t.grid = ctx->sms;
+      t.stream = base.stream;
+      t.status = ctx->status;
+      t.timeout_ns = ctx->timeout_ns;
+      e = dgrad ? tc_gemm_launch_nn(t) : tc_gemm_launch_nt(t);
+    }
+    record(std::string(base.name) + " " + plan_text(p, base.layout, M, N, base.K, 1, ctx->sms) + " lora r=" +
+           std::to_string(r) + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  // CUDA-core path: both products added in an FP32 buffer (the output itself
+  // when it is FP32), then rounded once
+  const size_t need = base.out == TG_F32 ? 0 : static_cast<size_t>(M) * N * 4;
+  if (need > 0 && (base.ws == nullptr || base.ws_bytes < need || !aligned(base.ws, 16))) {
+    snprintf(buf, sizeof buf, "%s simt lora: workspace %zu bytes needed, %zu given", base.name, need,
+             base.ws ? base.ws_bytes : static_cast<size_t>(0));
+    record(buf);
+    return TG_ERR_WORKSPACE_TOO_SMALL;
+  }
+  void* acc = base.out == TG_F32 ? base.C : base.ws;
+  SimtGemm s{};
+  s.A = base.A;
+  s.B = base.B;
+  s.C = acc;
+  s.a_kind = ik;
+  s.b_kind = ik;
+  s.out_kind = EK_F32;
+  s.batch = 1;
+  s.M = M;
+  s.N = N;
+  s.K = base.K;
+  s.a_bs = base.a_bs;
+  s.b_bs = base.b_bs;
+  s.a_rs = base.lda;
+  s.a_cs = 1;
+  if (dgrad) {
+    s.b_rs = base.ldb;
+    s.b_cs = 1;
+  } else {
+    s.b_rs = 1;
+    s.b_cs = base.ldb;
+  }
+  s.scale = 1.f;
+  s.stream = base.stream;
+  cudaError_t e = simt_gemm_launch(s);
+  if (e == cudaSuccess) {
+    SimtGemm l{};
+    l.A = H;
+    l.B = F;
+    l.C = acc;
+    l.a_kind = h_f32 ? EK_F32 : ik;
+    l.b_kind = ik;
+    l.out_kind = EK_F32;
+    l.batch = 1;
+    l.M = M;
+    l.N = N;
+    l.K = r;
+    l.a_bs = M * r;
+    l.b_bs = N * r;
+    l.a_rs = r;
+    l.a_cs = 1;
+    if (dgrad) {  // F = A [r][N]
+      l.b_rs = N;
+      l.b_cs = 1;
+    } else {  // F = B [N][r]
+      l.b_rs = 1;
+      l.b_cs = r;
+    }
+    l.accumulate = 1;
+    l.scale = scale;
+    l.stream = base.stream;
+    e = simt_gemm_launch(l);
+  }
+  if (e == cudaSuccess && base.out != TG_F32)
+    e = splitk_reduce_launch(static_cast<const float*>(acc), base.C, ok_kind, 1, 1, M * N, base.stream, 0);
+  snprintf(buf, sizeof buf, "%s simt %s lora M=%lld N=%lld K=%lld r=%lld %s", base.name, layout_name(base.layout),
+           (long long)M, (long long)N, (long long)base.K, (long long)r,
+           e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+  record(buf);
+  return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status tg_gemm_fwd_lora(const void* X, const void* W, const void* H, const void* B, void* Y, int64_t T,
+                           int64_t d_out, int64_t d_in, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, d_in, r}));
+  if (!std::isfinite(scale)) return TG_ERR_INVALID_ARG;
+  TG_TRY(check_ptr(X, T * d_in, 2));
+  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_ptr(H, T * r, 2));
+  TG_TRY(check_ptr(B, d_out * r, 2));
+  TG_TRY(check_ptr(Y, T * d_out, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NT, X, W, Y, 1, T, d_out, d_in, d_in, d_in, T * d_in, d_out * d_in, in, out, -1, ws, ws_bytes,
+             static_cast<cudaStream_t>(stream), "fwd_lora"};
+  return run_layer_lora(g, H, 0, B, r, scale, ctx);
+}
+
+tg_status tg_gemm_dgrad_lora(const void* dY, const void* W, const float* dH, const void* A, void* dX, int64_t T,
+                             int64_t d_out, int64_t d_in, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  TG_TRY(check_common(in, out, {T, d_out, d_in, r}));
+  if (!std::isfinite(scale)) return TG_ERR_INVALID_ARG;
+  TG_TRY(check_ptr(dY, T * d_out, 2));
+  TG_TRY(check_ptr(W, d_out * d_in, 2));
+  TG_TRY(check_ptr(dH, T * r, 4));
+  TG_TRY(check_ptr(A, r * d_in, 2));
+  TG_TRY(check_ptr(dX, T * d_in, dt_bytes(out)));
+  DevCtx* ctx = nullptr;
+  TG_TRY(device_ctx(&ctx));
+  GemmCall g{LAYOUT_NN, dY, W, dX, 1, T, d_in, d_out, d_out, d_in, T * d_out, d_out * d_in, in, out, -1, ws,
+             ws_bytes, static_cast<cudaStream_t>(stream), "dgrad_lora"};
+  return run_layer_lora(g, dH, 1, A, r, scale, ctx);
 }
 
 tg_status tg_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t d_out, int64_t d_in,
@@ -1356,6 +1541,8 @@ size_t tg_workspace_size(tg_op op, int64_t d0, int64_t d1, int64_t d2, int64_t d
     case TG_OP_LORA_UP_F32W: return w32_ws(1, d0, 0, d1, d2, in, ctx->sms);
     case TG_OP_LORA_GRAD_F32W: return w32_ws(2, d0, d1, d2, d3, in, ctx->sms);
     case TG_OP_ATTN_BWD: return d2 == 64 ? attn_bwd_ws_bytes(d0, d1) : SIZE_MAX;
+    case TG_OP_GEMM_FWD_LORA: return layer_lora_ws(LAYOUT_NT, d0, d1, d2, d3, in, out, ctx->sms);
+    case TG_OP_GEMM_DGRAD_LORA: return layer_lora_ws(LAYOUT_NN, d0, d2, d1, d3, in, out, ctx->sms);
     case TG_OP_BMM_ATTN: {
       GemmCall g;
       if (!attn_call(static_cast<tg_attn_op>(d0), nullptr, nullptr, nullptr, d1, d2, d3, in, out, nullptr, 0,

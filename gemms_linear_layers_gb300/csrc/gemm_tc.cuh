@@ -95,6 +95,8 @@ struct TcArgs {
   unsigned int* status;
   unsigned long long* trace;  // event timestamps per CTA (only in -DTG_TRACE builds)
   int accumulate;             // FP32 output: the tile writer adds its tile into C (C += A B)
+  int kb_lora;                // >= 0: K block kb_lora comes from tmA2 / tmB2 at K offset 0 (a LoRA
+                              // branch appended to the reduction); -1: none
 };
 
 #ifdef TG_TRACE
@@ -328,7 +330,8 @@ template <bool A_MN, bool B_MN, int BN, bool OUT16, bool DEEP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
-                   const __grid_constant__ CUtensorMap tmP, const TcArgs args) {
+                   const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB2, const TcArgs args) {
   using Cfg = TcCfg<BN, DEEP>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -368,6 +371,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmC);
     if (BN % 64 != 0) prefetch_tmap(&tmC2);
     if (args.tail_splits > 1) prefetch_tmap(&tmP);
+    if (args.kb_lora >= 0) {
+      prefetch_tmap(&tmA2);
+      prefetch_tmap(&tmB2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -404,27 +411,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           mbar_arrive_expect_tx(fb, TC_A_STAGE + (B_MN ? Cfg::B_BYTES_MN : Cfg::B_BYTES_K));
           const uint32_t a_dst = smem_u32(sA + stage * TC_A_STAGE);
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_STAGE);
-          const int k0 = kb * TC_BK;
+          // the appended LoRA block: the same boxes from the second pair of maps
+          const bool lx = kb == args.kb_lora;
+          const CUtensorMap* mA = lx ? &tmA2 : &tmA;
+          const CUtensorMap* mB = lx ? &tmB2 : &tmB;
+          const int k0 = lx ? 0 : kb * TC_BK;
           if (A_MN) {
             if (args.a_chunked) {  // one box: 2 chunks of 64 columns x 64 k-rows
-              tma_load_4d(a_dst, &tmA, fb, 0, k0, c.m0 / 64, c.b);
+              tma_load_4d(a_dst, mA, fb, 0, k0, c.m0 / 64, c.b);
             } else {
-              tma_load_3d(a_dst, &tmA, fb, c.m0, k0, c.b);
-              tma_load_3d(a_dst + 8192, &tmA, fb, c.m0 + 64, k0, c.b);
+              tma_load_3d(a_dst, mA, fb, c.m0, k0, c.b);
+              tma_load_3d(a_dst + 8192, mA, fb, c.m0 + 64, k0, c.b);
             }
           } else {
-            tma_load_3d(a_dst, &tmA, fb, k0, c.m0, c.b);
+            tma_load_3d(a_dst, mA, fb, k0, c.m0, c.b);
           }
           if (B_MN) {
             if (args.b_chunked) {
-              tma_load_4d(b_dst, &tmB, fb, 0, k0, c.n0 / 64, c.b);
+              tma_load_4d(b_dst, mB, fb, 0, k0, c.n0 / 64, c.b);
             } else {
 #pragma unroll
               for (int j = 0; j < Cfg::B_CHUNKS; ++j)
-                tma_load_3d(b_dst + j * 8192, &tmB, fb, c.n0 + 64 * j, k0, c.b);
+                tma_load_3d(b_dst + j * 8192, mB, fb, c.n0 + 64 * j, k0, c.b);
             }
           } else {
-            tma_load_3d(b_dst, &tmB, fb, k0, c.n0, c.b);
+            tma_load_3d(b_dst, mB, fb, k0, c.n0, c.b);
           }
           issued[stage] = static_cast<int>(phase);
           if (++stage == S) {

@@ -174,6 +174,7 @@ template <bool A_MN, bool B_MN, int BN, bool OUT16>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                     const TcArgs args) {
   using Cfg = Tc2Cfg<BN, B_MN>;
   constexpr int S = Cfg::STAGES;
@@ -214,6 +215,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
     if (args.tail_splits > 1) prefetch_tmap(&tmP);
+    if (args.kb_lora >= 0) {
+      prefetch_tmap(&tmA2);
+      prefetch_tmap(&tmB2);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -258,28 +263,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t fb = mapa_shared(fb_local, 0);
           const uint32_t a_dst = smem_u32(sA + stage * TC_A_STAGE);
           const uint32_t b_dst = smem_u32(sB + stage * Cfg::B_BYTES);
-          const int k0 = kb * TC_BK;
+          // the appended LoRA block: the same boxes from the second pair of maps
+          const bool lx = kb == args.kb_lora;
+          const CUtensorMap* mA = lx ? &tmA2 : &tmA;
+          const CUtensorMap* mB = lx ? &tmB2 : &tmB;
+          const int k0 = lx ? 0 : kb * TC_BK;
           const int m = c.m0 + a_row;
           if (A_MN) {
             if (args.a_chunked) {
-              tma_load_4d_pair(a_dst, &tmA, fb, 0, k0, m / 64, c.b);
+              tma_load_4d_pair(a_dst, mA, fb, 0, k0, m / 64, c.b);
             } else {
-              tma_load_3d_pair(a_dst, &tmA, fb, m, k0, c.b);
-              tma_load_3d_pair(a_dst + 8192, &tmA, fb, m + 64, k0, c.b);
+              tma_load_3d_pair(a_dst, mA, fb, m, k0, c.b);
+              tma_load_3d_pair(a_dst + 8192, mA, fb, m + 64, k0, c.b);
             }
           } else {
-            tma_load_3d_pair(a_dst, &tmA, fb, k0, m, c.b);
+            tma_load_3d_pair(a_dst, mA, fb, k0, m, c.b);
           }
           const int n = c.n0 + b_off;
           if (B_MN) {
             if (args.b_chunked) {
-              tma_load_4d_pair(b_dst, &tmB, fb, 0, k0, n / 64, c.b);
+              tma_load_4d_pair(b_dst, mB, fb, 0, k0, n / 64, c.b);
             } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d_pair(b_dst + j * 8192, &tmB, fb, n + 64 * j, k0, c.b);
+              for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d_pair(b_dst + j * 8192, mB, fb, n + 64 * j, k0, c.b);
             }
           } else {
-            tma_load_3d_pair(b_dst, &tmB, fb, k0, n, c.b);
+            tma_load_3d_pair(b_dst, mB, fb, k0, n, c.b);
           }
           if (issued[stage] < 0 && stage == 0) TG_EVENT(1);
           issued[stage] = static_cast<int>(phase);

@@ -13,6 +13,28 @@
 
 namespace tg {
 
+// Tensor maps of the LoRA block appended to the reduction (same boxes as the
+// main operands' maps, K = 64): A2 [M][64] K-major; B2 [N][64] K-major or
+// [64][N] MN-major (chunked like the main B when that is chunked).  Without a
+// LoRA block the main maps are copied (never read).
+static bool lora_maps(const TcGemm& g, bool b_mn, bool b4, uint32_t b_box_rows, int b_chunks, const CUtensorMap& tmA,
+                      const CUtensorMap& tmB, CUtensorMap* tmA2, CUtensorMap* tmB2) {
+  if (g.lora_A2 == nullptr) {
+    *tmA2 = tmA;
+    *tmB2 = tmB;
+    return true;
+  }
+  const uint64_t M = g.M, N = g.N;
+  if (!encode_tmap_3d(tmA2, g.lora_A2, g.in_kind, 64, M, 1, 128, M * 128, 64, TC_BM, 128)) return false;
+  if (b4) {
+    const uint64_t d[4] = {64, 64, N / 64, 1}, st[3] = {N * 2, 128, 64 * N * 2};
+    const uint32_t b[4] = {64, 64, static_cast<uint32_t>(b_chunks), 1};
+    return encode_tmap_nd(tmB2, g.lora_B2, g.in_kind, 4, d, st, b, 128);
+  }
+  if (b_mn) return encode_tmap_3d(tmB2, g.lora_B2, g.in_kind, N, 64, 1, N * 2, 64 * N * 2, 64, 64, 128);
+  return encode_tmap_3d(tmB2, g.lora_B2, g.in_kind, 64, N, 1, 128, N * 128, 64, b_box_rows, 128);
+}
+
 template <bool A_MN, bool B_MN, int BN, bool OUT16, bool DEEP = false>
 static cudaError_t tc_launch_one(const TcGemm& g) {
   using Cfg = TcCfg<BN, DEEP>;
@@ -61,6 +83,8 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
     ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap tmA2, tmB2;
+  if (!lora_maps(g, B_MN, b4, BN, Cfg::B_CHUNKS, tmA, tmB, &tmA2, &tmB2)) return cudaErrorInvalidValue;
 
   // output (or FP32 split partials): [batch * splits][M][N], dense
   const bool split_parts = !g.sk && g.splits > 1;
@@ -81,6 +105,11 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
   a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.kb_lora = -1;
+  if (g.lora_A2 != nullptr) {  // one more K block, after the product's own
+    a.kb_lora = a.kb_total;
+    a.kb_total += 1;
+  }
   a.splits = g.sk ? 1 : g.splits;
   a.kps = (a.kb_total + a.splits - 1) / a.splits;
   a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * a.splits;
@@ -91,7 +120,8 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.a_chunked = a4 ? 1 : 0;
   a.b_chunked = b4 ? 1 : 0;
   // tail split (never with stream-K or split partials)
-  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid, (g.sk || g.splits > 1) ? 1 : g.tail_splits, g.raster_n);
+  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid, (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits,
+                              g.raster_n);
   a.dp_tiles = tg.dp_tiles;
   a.tail_splits = tg.splits;
   a.tail_kps = tg.kps;
@@ -121,7 +151,8 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
     a.sk_flags = reinterpret_cast<unsigned long long*>(static_cast<char*>(g.ws) +
                                                        static_cast<size_t>(grid) * TC_BM * BN * 4);
   }
-  cudaError_t e2 = launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, tmC2, tmP, a);
+  cudaError_t e2 =
+      launch_k(kern, dim3(grid), dim3(TC_THREADS), Cfg::SMEM, g.stream, tmA, tmB, tmC, tmC2, tmP, tmA2, tmB2, a);
   if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
   return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream, g.accumulate);
 }
@@ -192,6 +223,8 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
     ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, Cfg::BH, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap tmA2, tmB2;
+  if (!lora_maps(g, B_MN, b4, Cfg::BH, Cfg::B_CHUNKS, tmA, tmB, &tmA2, &tmB2)) return cudaErrorInvalidValue;
   const bool split_parts = !g.sk && g.splits > 1;
   const int ck = split_parts ? EK_F32 : g.out_kind;
   const uint64_t esz = elem_bytes(ck);
@@ -204,6 +237,11 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.m_tiles = static_cast<int>((M + TC2_BM - 1) / TC2_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
   a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.kb_lora = -1;
+  if (g.lora_A2 != nullptr) {  // one more K block, after the product's own
+    a.kb_lora = a.kb_total;
+    a.kb_total += 1;
+  }
   a.splits = g.sk ? 1 : g.splits;
   a.kps = (a.kb_total + a.splits - 1) / a.splits;
   a.units = static_cast<int>(nb) * a.m_tiles * a.n_tiles * a.splits;
@@ -214,8 +252,8 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.b_chunked = b4 ? 1 : 0;
   // tail split (never with stream-K or split partials); the geometry is that
   // of a full wave of grid / 2 pairs, whatever number of pairs runs
-  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid / 2, (g.sk || g.splits > 1) ? 1 : g.tail_splits, g.raster_n,
-                              TC2_BM);
+  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid / 2, (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits,
+                              g.raster_n, TC2_BM);
   a.dp_tiles = tg.dp_tiles;
   a.tail_splits = tg.splits;
   a.tail_kps = tg.kps;
@@ -248,7 +286,7 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   }
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  cudaError_t e2 = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmP, a);
+  cudaError_t e2 = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmP, tmA2, tmB2, a);
   if (e2 != cudaSuccess || tg.tail_tiles == 0) return e2;
   return tail_reduce_launch(static_cast<const float*>(g.ws), g.C, g.out_kind, tg, g.stream, g.accumulate);
 }

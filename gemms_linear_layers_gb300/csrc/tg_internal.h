@@ -78,6 +78,11 @@ struct TcGemm {
   int pair;                   // 1: CTA-pair kernel, 256 x bn tiles (bn 128, 192 or 256)
   int csplit;                 // > 1: split-K across the CTAs of a cluster, added on chip (bn 64..256)
   int accumulate;             // FP32 C only: C += the product (gradient accumulation)
+  // a LoRA branch appended to the reduction as one more 64-deep K block:
+  // A2 [M][64] (K-major) and B2 laid out as B with K = 64 ([N][64] K-major,
+  // [64][N] MN-major); both nullptr when absent
+  const void* lora_A2;
+  const void* lora_B2;
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
@@ -235,6 +240,16 @@ cudaError_t lora_grad_launch(const LoraArgs& a);
 // workspace of the FP32-factor calls (op 0 down, 1 up, 2 gradient): the
 // factors' hi/lo parts, after the gradient's own workspace
 size_t lora_w32_ws_bytes(int op, int64_t T, int64_t d_in, int64_t d_out, int sms);
+
+// A rank-r LoRA branch (r <= 32) staged as the 64-deep K block a layer product
+// appends to its reduction (lora_block.cu): A2 = [hi(scale h) | lo(scale h) | 0]
+// [T][64] from H [T][r] (16-bit, or FP32 when h_f32), B2 from F: forward
+// F = B [N][r] -> [N][64]; input gradient (dgrad) F = A [r][N] -> [64][N].
+// ws holds lora_block_ws_bytes(T, N) bytes; *A2, *B2 receive the two arrays.
+size_t lora_block_ws_bytes(int64_t T, int64_t N);
+cudaError_t lora_block_prep_launch(const void* H, int h_f32, const void* F, int64_t T, int64_t N, int64_t r, float scale,
+                                   int in_kind, int dgrad, void* ws, const void** A2, const void** B2, int sms,
+                                   cudaStream_t stream);
 
 // wait-timeout probe kernel (api.cu)
 cudaError_t wait_probe_launch(unsigned long long timeout_ns, unsigned int* status,

@@ -95,7 +95,9 @@ typedef enum {
   TG_OP_LORA_DOWN_F32W = 7,  /* d0=T, d1=d_in, d2=r */
   TG_OP_LORA_UP_F32W = 8,    /* d0=T, d1=d_out, d2=r */
   TG_OP_LORA_GRAD_F32W = 9,  /* d0=T, d1=d_in, d2=d_out, d3=r */
-  TG_OP_ATTN_BWD = 10        /* d0=heads, d1=s, d2=d */
+  TG_OP_ATTN_BWD = 10,       /* d0=heads, d1=s, d2=d */
+  TG_OP_GEMM_FWD_LORA = 11,  /* d0=T, d1=d_out, d2=d_in, d3=r */
+  TG_OP_GEMM_DGRAD_LORA = 12 /* d0=T, d1=d_out, d2=d_in, d3=r */
 } tg_op;
 
 /* Forward product of a linear layer ("Where the time went"):
@@ -110,6 +112,35 @@ tg_status tg_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t 
 tg_status tg_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t d_out,
                         int64_t d_in, tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes,
                         void* stream);
+
+/* Forward product with a rank-r LoRA branch added inside it (section "What's
+ * left": fusing the small element-wise operations):
+ *   Y[T, d_out] = X[T, d_in] . W[d_out, d_in]^T + scale . H[T, r] . B[d_out, r]^T
+ * X, W, H, B have type `in` (bf16 or fp16); Y has type `out` (FP32 or `in`)
+ * and is overwritten with one rounding of the FP32 sum.  On the tensor-core
+ * path (the alignment rules of the layer products, r <= 32) one small launch
+ * stages the branch as a 64-deep K block -- scale . H as 16-bit hi + lo
+ * parts beside two copies of B -- that the product appends to its own
+ * reduction, so Y is written once and never read (the product runs whole
+ * tiles: no K split); otherwise both products are added in an FP32 buffer on
+ * the CUDA cores and rounded once.  scale must be finite; r = 0 is
+ * tg_gemm_fwd.  Workspace: tg_workspace_size(TG_OP_GEMM_FWD_LORA, T, d_out,
+ * d_in, r, in, out) bytes (the larger of the two paths' needs). */
+tg_status tg_gemm_fwd_lora(const void* X, const void* W, const void* H, const void* B, void* Y, int64_t T,
+                           int64_t d_out, int64_t d_in, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Input-gradient product with the LoRA branch's part added inside it, for
+ * Y = X W^T + scale . (X A^T) B^T:
+ *   dX[T, d_in] = dY[T, d_out] . W[d_out, d_in] + scale . dH[T, r] . A[r, d_in]
+ * with dH = dY . B in FP32 (tg_lora_grad's optional output).  dY, W, A have
+ * type `in`; dX has type `out`, overwritten with one rounding.  The same two
+ * paths and rules as tg_gemm_fwd_lora (scale . dH staged as hi + lo parts
+ * beside two copies of A).  Workspace: tg_workspace_size(
+ * TG_OP_GEMM_DGRAD_LORA, T, d_out, d_in, r, in, out). */
+tg_status tg_gemm_dgrad_lora(const void* dY, const void* W, const float* dH, const void* A, void* dX, int64_t T,
+                             int64_t d_out, int64_t d_in, int64_t r, float scale, tg_dtype in, tg_dtype out, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /* Weight-gradient product ("Where the time went"), reduced over tokens:
  *   dW[d_out, d_in] = dY[T, d_out]^T . X[T, d_in]
