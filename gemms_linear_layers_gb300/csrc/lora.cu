@@ -30,9 +30,14 @@
 //   row-up     OUT[t, j] = sum_r Hm[t, r] S2(j, r)      (Y = H B^T)
 //              writes a [T, d] tensor from the small factors, all from
 //              registers (16-byte stores).
-// FP32 operands (the gradient dH) enter the 16-bit MMA as hi + lo, both
-// rounded to the input type (hi = rn(x), lo = rn(x - hi)); both parts are
-// multiplied, so dH keeps about 16 significant bits instead of 8.
+// FP32 operands (the gradient dH, FP32 LoRA factors) enter the 16-bit MMA as
+// hi + lo parts, hi = rn(x) and lo = rn((x - hi) 2^11): the lo part is stored
+// scaled by 2^11, its products go to their own FP32 sums and those are scaled
+// back by 2^-11 at the end (exact: powers of two).  Both parts are
+// multiplied, so x keeps about 16 (bf16) or 22 (fp16) significant bits; the
+// scaling keeps fp16's lo part out of its subnormal range (without it, a lo
+// part below 2^-14 would keep only the bits above 2^-24, a fixed absolute
+// precision that fails the relative bound for small gradients or factors).
 //
 // Every result is a fixed-order sum: a warp adds its chunks in K order, the
 // warps' partial tiles are added in warp order, the CTAs' partials of a column
@@ -53,6 +58,8 @@
 namespace tg {
 
 constexpr int LR = 16;                    // the rank these kernels are written for
+constexpr float LO_SCALE = 2048.f;        // lo parts are stored times 2^11 ...
+constexpr float LO_UNSCALE = 1.f / 2048.f;  // ... and their products' sums scaled back
 constexpr int LCW = 8;                    // consumer warps of a TMA-fed role
 constexpr int LGROUP = (LCW + 1) * 32;    // one role: consumers + one producer warp
 constexpr int LGROUP_UP = (2 * LCW + 1) * 32;  // col-red + row-up warps + one producer warp
@@ -355,13 +362,13 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
   const int cw = warp % a.CH;                     // chunk of each stage this warp takes
   const int rgs = LCW / a.CH, rg0 = warp / a.CH;  // row groups rg with rg % rgs == rg0
   const int nrg = R16 / 16;
-  float acc[2][2][4];
+  float acc[2][2][4], accl[SLO ? 2 : 1][2][4];  // SLO: the factor's lo-part products apart
 #pragma unroll
   for (int rg = 0; rg < 2; ++rg)
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[rg][nb][q] = 0.f;
+      for (int q = 0; q < 4; ++q) acc[rg][nb][q] = accl[SLO ? rg : 0][nb][q] = 0.f;
   for (int s = 0; s < nst; ++s) {
     const int slot = s % a.stages;
     const uint32_t ph = static_cast<uint32_t>((s / a.stages) & 1);
@@ -394,9 +401,9 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
             ldsm_x4(sw128s(xb, seg0 + rg * 16 + (m & 1) * 8 + i, 2 * kk + (m >> 1)), af);
             mma_16816<BF16>(acc[rg][0], af, b);
             mma_16816<BF16>(acc[rg][1], af, b + 2);
-            if (SLO) {
-              mma_16816<BF16>(acc[rg][0], af, bl);
-              mma_16816<BF16>(acc[rg][1], af, bl + 2);
+            if (SLO) {  // the factor's lo part (stored times 2^11): its own sums
+              mma_16816<BF16>(accl[rg][0], af, bl);
+              mma_16816<BF16>(accl[rg][1], af, bl + 2);
             }
           }
         }
@@ -404,6 +411,14 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&rb.empty[slot]));
+  }
+  if (SLO) {  // the lo products' sums, scaled back
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[rg][nb][q] += accl[SLO ? rg : 0][nb][q] * LO_UNSCALE;
   }
   // this warp's partial tile -> red[warp]; rows rg*16 + g (+8), columns nb*8 + 2c (+1)
   float* rw = red + warp * (32 * 17);
@@ -431,7 +446,7 @@ __device__ void rowdown_run(int tile, const RdMaps* mp, const RdArgs& a, uint8_t
       if (a.hi != nullptr) {
         const float h = round16<BF16>(v);
         a.hi[e] = bits16<BF16>(h);
-        a.lo[e] = bits16<BF16>(v - h);
+        a.lo[e] = bits16<BF16>((v - h) * LO_SCALE);
       }
     }
   }
@@ -662,9 +677,12 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         float d[4][4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
+          // the lo parts (of Hm, and of an FP32 S2) are stored times 2^11: their
+          // products have their own sum, scaled back before it joins d
+          float dl[4] = {0.f, 0.f, 0.f, 0.f};
           d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
           mma_16816<BF16>(d[t], ah, bup[q][t]);
-          if (HILO) mma_16816<BF16>(d[t], al, bup[q][t]);
+          if (HILO) mma_16816<BF16>(dl, al, bup[q][t]);
           if (SLO) {
             // the lo fragment, read from this stage as bup was (the lo part times
             // the lo part of Hm is below FP32 resolution and is left out)
@@ -679,7 +697,11 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
               v[u] = x;
             }
             const uint32_t bl[2] = {v[0] | (v[1] << 16), v[2] | (v[3] << 16)};
-            mma_16816<BF16>(d[t], ah, bl);
+            mma_16816<BF16>(dl, ah, bl);
+          }
+          if (HILO || SLO) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[t][e] += dl[e] * LO_UNSCALE;
           }
         }
         const int j = jb * CR_CB + 32 * q + 8 * c;  // this thread's 8 consecutive columns
@@ -768,9 +790,11 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) {
           const int r = nb * 8 + 2 * c;
-          *reinterpret_cast<float2*>(dst + jl * LR + r) = make_float2(acc[nb][0] + accl[nb][0], acc[nb][1] + accl[nb][1]);
+          // the lo parts were stored times 2^11: their sums scaled back
+          *reinterpret_cast<float2*>(dst + jl * LR + r) =
+              make_float2(acc[nb][0] + accl[nb][0] * LO_UNSCALE, acc[nb][1] + accl[nb][1] * LO_UNSCALE);
           *reinterpret_cast<float2*>(dst + (jl + 8) * LR + r) =
-              make_float2(acc[nb][2] + accl[nb][2], acc[nb][3] + accl[nb][3]);
+              make_float2(acc[nb][2] + accl[nb][2] * LO_UNSCALE, acc[nb][3] + accl[nb][3] * LO_UNSCALE);
         }
       }
 #pragma unroll
@@ -867,7 +891,7 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
       for (int e = 0; e < 4; ++e) {
         const float h = round16<BF16>(wv[e]);
         hb[e] = bits16<BF16>(h);
-        lb[e] = bits16<BF16>(wv[e] - h);
+        lb[e] = bits16<BF16>((wv[e] - h) * LO_SCALE);
       }
       bfr[jb][0] = hb[0] | (hb[1] << 16);
       bfr[jb][1] = hb[2] | (hb[3] << 16);
@@ -907,7 +931,12 @@ __device__ void rowup_role(int cta_j, int cta_t, const RuArgs& a) {
 #pragma unroll
       for (int jb = 0; jb < 4; ++jb) {
         mma_16816<BF16>(acc[jb], ah, bfr[jb]);
-        if (SLO) mma_16816<BF16>(acc[jb], ah, bfl[SLO ? jb : 0]);
+        if (SLO) {  // the factor's lo part (stored times 2^11): its own sum, scaled back
+          float l[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_16816<BF16>(l, ah, bfl[SLO ? jb : 0]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[jb][e] += l[e] * LO_UNSCALE;
+        }
       }
       // thread (g, c): rows ra / rb, columns j0 + 8c + 2*jb + {0,1}
       if (colv) {
@@ -1169,7 +1198,7 @@ __global__ void __launch_bounds__(256)
     const float v = (first ? w1 : w2)[k];
     const float h = round16<BF16>(v);
     hi[k] = bits16<BF16>(h);
-    hi[n + k] = bits16<BF16>(v - h);
+    hi[n + k] = bits16<BF16>((v - h) * LO_SCALE);
   }
 }
 

@@ -207,7 +207,10 @@ tg_status tg_lora_up_add(const void* H, const void* B, void* Y, int64_t T, int64
                          tg_dtype in, tg_dtype out, void* ws, size_t ws_bytes, void* stream);
 
 /* Gradients of the LoRA branch Y = (X A^T) B^T given dY:
- *   dH[T, r]     = dY . B          (kept in FP32; written to dH_f32 when non-NULL)
+ *   dH[T, r]     = dY . B          (kept in FP32; written to dH_f32 when non-NULL;
+ *                                    enters the products below as 16-bit hi + lo
+ *                                    parts, lo stored times 2^11, as for the FP32
+ *                                    factors of tg_lora_grad_f32w)
  *   dB[d_out, r] = dY^T . H
  *   dA[r, d_in]  = dH^T . X        (uses the FP32 dH)
  *   dX[T, d_in]  = dH . A          (uses the FP32 dH)
@@ -245,11 +248,14 @@ tg_status tg_lora_grad_add(const void* X, const void* A, const void* B, const vo
  *                       dA = dH^T . X, dX = dH . A;  dA and dB FP32
  * X, H, dY have type `in` (bf16 or fp16); A, B are FP32 and are not rounded
  * to `in`: r = 16 splits each factor into 16-bit parts hi = RNE(w) and
- * lo = RNE(w - hi) (in `ws` by one small launch, or in registers for the up
- * product, whose B must then be 16-byte aligned) and the streaming
- * kernels multiply both parts into the same FP32 sums, so hi + lo stands for
- * w to within 2^-18 |w| (bf16); other ranks run on the CUDA cores with the
- * FP32 factors as they are.  H, Y, dX have type `out`.  Workspace:
+ * lo = RNE((w - hi) 2^11) (in `ws` by one small launch, or in registers for
+ * the up product, whose B must then be 16-byte aligned) and the streaming
+ * kernels multiply both parts, the lo products in FP32 sums of their own that
+ * are scaled back by 2^-11, so the parts stand for w to within 2^-17 |w|
+ * (bf16) or 2^-22 |w| (fp16, for |w| >= 2^-14; below that, to within 2^-36
+ * absolutely, so fp16 factors below about 1.5e-6 in magnitude lose the 1e-5
+ * relative bound); other ranks run on the CUDA cores with the FP32 factors
+ * as they are.  H, Y, dX have type `out`.  Workspace:
  * tg_workspace_size(TG_OP_LORA_*_F32W, ...); arguments and errors otherwise
  * as tg_lora_down / _up / _grad. */
 tg_status tg_lora_down_f32w(const void* X, const float* A, void* H, int64_t T, int64_t d_in, int64_t r,

@@ -248,6 +248,54 @@ def test_lora_fp32_factors(shape, dtype, out_kind):
         assert torch.equal(g[k], g2[k]), k
 
 
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("g", [1e-4, 1e-6])
+def test_lora_grad_small_output_gradients(g, dtype):
+    """Output gradients far below the config's N(0, 1e-2): the FP32 dH = dY B
+    enters the 16-bit MMAs of dA and dX as hi + lo parts with the lo part
+    stored times 2^11, which keeps fp16's lo part out of its subnormal range,
+    so the relative bound holds at every gradient size (and bf16 is
+    unchanged).  Full check at a 2B-class width."""
+    T, d_in, d_out, r = 1024, 2304, 2304, 16
+    X, A, B, H, _ = inputs.lora_inputs(T, d_in, d_out, r, dtype, tag="smallg")
+    dY = inputs.normal((T, d_out), g, dtype, inputs.seed_for("smallg", g, str(dtype)))
+    got = tg.tg_lora_grad(*(t.cuda() for t in (X, A, B, H, dY)), out_dtype=torch.float32, want_dH=True)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    ref = oracle.lora_grad(X, A, B, H, dY)
+    for name in ("dH", "dB", "dA", "dX"):
+        assert_close(got[name], *ref[name], f"lora_grad dY~N(0,{g}) {name} [{call}]", None)
+
+
+@pytest.mark.parametrize("dtype", DT16)
+@pytest.mark.parametrize("w", [1e-4, 1e-5])
+def test_lora_fp32_factors_small(w, dtype):
+    """FP32 factors far smaller than N(0, 0.02): their lo parts (stored times
+    2^11) keep their precision in fp16 down to the range the header states
+    (|w| above about 1.5e-6: a hi part in fp16's subnormal range carries 2^-25
+    absolutely, the scaled lo part 2^-36), so down, up and the gradient hold
+    the relative bound."""
+    T, d_in, d_out, r = 1024, 2304, 2304, 16
+    X, _, _, H, dY = inputs.lora_inputs(T, d_in, d_out, r, dtype, tag="w32s")
+    A = inputs.normal((r, d_in), w, torch.float32, inputs.seed_for("w32s", w, "A"))
+    B = inputs.normal((d_out, r), w, torch.float32, inputs.seed_for("w32s", w, "B"))
+    Xc, Ac, Bc, Hc, dYc = (t.cuda() for t in (X, A, B, H, dY))
+    h = tg.tg_lora_down_f32w(Xc, Ac, out_dtype=torch.float32)
+    C, S = oracle.lora_down(X, A)
+    assert_close(h, C, S, f"lora_down_f32w A~N(0,{w}) [{tg.tg_last_call()}]", None)
+    y = tg.tg_lora_up_f32w(Hc, Bc, out_dtype=torch.float32)
+    C, S = oracle.lora_up(H, B)
+    assert_close(y, C, S, f"lora_up_f32w B~N(0,{w}) [{tg.tg_last_call()}]", None)
+    got = tg.tg_lora_grad_f32w(Xc, Ac, Bc, Hc, dYc, out_dtype=torch.float32, want_dH=True)
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert tg.tg_stream_status() == 0
+    ref = oracle.lora_grad(X, A, B, H, dY)
+    for name in ("dH", "dB", "dA", "dX"):
+        assert_close(got[name], *ref[name], f"lora_grad_f32w factors~N(0,{w}) {name} [{call}]", None)
+
+
 def test_lora_fp32_factors_use_the_low_part():
     """With FP32 outputs the error against the FP32 factors is far below what
     rounding the factors to bf16 first would give: the lo parts are used."""
