@@ -270,7 +270,7 @@ def kernel_key(call: str) -> str:
     path = f[1] if len(f) > 1 else "?"
     if path == "ffma":
         return f"ffma {f[2]}" + (" +reduce" if any(x.startswith("splits=") and x != "splits=1" for x in f) else "")
-    if path != "tc":
+    if path not in ("tc", "tc3"):
         return f"{path} {f[2] if len(f) > 2 else ''}".strip()
     bn = next((x for x in f if x.startswith("bn=")), "bn=?")
     sp = next((x for x in f if x.startswith("splits=")), "splits=1")
@@ -278,7 +278,7 @@ def kernel_key(call: str) -> str:
     pair = " pair" if "pair" in f else (" cs" if "cs" in f else "")
     tail = " +tail" if any(x.startswith("tail=") for x in f) else ""
     sk = " sk" if "sk" in f else ""
-    return f"tc {f[2]} {bn}{deep}{pair}{sk}" + (" +reduce" if sp != "splits=1" else "") + tail
+    return f"{path} {f[2]} {bn}{deep}{pair}{sk}" + (" +reduce" if sp != "splits=1" else "") + tail
 
 
 def launches_of(call: str) -> int:
@@ -825,10 +825,18 @@ def measure_rows(stream, pk, budget_s=150.0):
             ms, call = time_calls(stream, fn, reps=5)
             M, N, K = {"fwd": (T, d_out, d_in), "dgrad": (T, d_in, d_out), "wgrad": (d_out, d_in, T)}[op]
             tf = workloads.flops(M, N, K) / ms / 1e9
-            rows.append({"set": "FP32", "layer": names, "T": T, "op": op, "dtype": "fp32", "M": M, "N": N, "K": K,
-                         "us": round(ms * 1000, 2), "tflops": round(tf, 2),
-                         "frac_of_peak": round(tf / f32_peak, 3), "bound": "alu",
-                         "peak_tflops": round(f32_peak, 1), "kernel": kernel_key(call)})
+            key = kernel_key(call)
+            row = {"set": "FP32", "layer": names, "T": T, "op": op, "dtype": "fp32", "M": M, "N": N, "K": K,
+                   "us": round(ms * 1000, 2), "tflops": round(tf, 2), "kernel": key,
+                   "frac_of_fp32_alu": round(tf / f32_peak, 3)}
+            if key.startswith("tc3"):
+                # three bf16 parts per operand: six 16-bit MMAs per product term, so
+                # the ceiling is a sixth of the 16-bit tensor peak
+                row.update({"bound": "tensor (three-part split)", "peak_tflops": round(pk["bf16_tflops"] / 6, 1),
+                            "frac_of_peak": round(6 * tf / pk["bf16_tflops"], 3)})
+            else:
+                row.update({"bound": "alu", "peak_tflops": round(f32_peak, 1), "frac_of_peak": round(tf / f32_peak, 3)})
+            rows.append(row)
         del X, W, dY, outs, ws
     # rank-16 LoRA, bf16, T=4096: effective HBM bandwidth
     cfg = workloads.LORA_2B

@@ -545,6 +545,34 @@ static bool tc_eligible(const GemmCall& g) {
          g.batch <= 65535;
 }
 
+// FP32 operands on the tensor cores: each operand cut into three bf16 parts
+// in the workspace ([3][elements], parts 8-element aligned), the product run
+// over the six part products (reduction 6 K long) on the single-CTA or pair
+// kernel (split-K, tail split allowed; a cluster split becomes a split-K).
+static bool split3_eligible(const GemmCall& g) {
+  return g.in == TG_F32 && g.out == TG_F32 && g.batch == 1 && g.lda % 8 == 0 && g.ldb % 8 == 0 &&
+         (g.N * 4) % 16 == 0 && aligned(g.C, 16) && g.M <= kMaxDim && g.N <= kMaxDim && g.K <= kMaxDim / 6 &&
+         g.a_kind_override < 0 && g.b_kind_override < 0 && g.scale == 1.f;
+}
+static int64_t up8(int64_t n) { return (n + 7) / 8 * 8; }
+static Plan split3_plan(int layout, int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t kb = (K + 63) / 64;
+  Plan p = make_plan(layout, M, N, 6 * kb * 64, 1, TG_F32, TG_F32, sms);
+  if (p.csplit > 1) {
+    p.splits = p.csplit;
+    p.csplit = 0;
+  }
+  p.sk = false;
+  return p;
+}
+static size_t split3_parts_bytes(int64_t M, int64_t N, int64_t K) {
+  return (static_cast<size_t>(3) * (up8(M * K) + up8(N * K)) * 2 + 255) / 256 * 256;
+}
+static size_t split3_ws_bytes(int layout, int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t kb = (K + 63) / 64;
+  return split3_parts_bytes(M, N, K) + plan_ws_bytes(split3_plan(layout, M, N, K, sms), M, N, 6 * kb * 64, 1, sms);
+}
+
 static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
   if (g.M == 0 || g.N == 0 || g.batch == 0) {
     record(std::string(g.name) + " empty output: nothing to do");
@@ -562,7 +590,63 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
                : TG_ERR_CUDA;
   }
   char buf[320];
-  if (g.in == TG_F32) {  // FP32 operands: the CUDA-core FFMA kernel
+  if (split3_eligible(g)) {  // FP32 operands: three bf16 parts each, on the tensor cores
+    const int64_t na = g.M * g.K, nbb = g.N * g.K, pa = up8(na), pb = up8(nbb);
+    const int64_t kb = (g.K + 63) / 64;
+    const Plan p = split3_plan(g.layout, g.M, g.N, g.K, ctx->sms);
+    const size_t parts = split3_parts_bytes(g.M, g.N, g.K);
+    const size_t need = split3_ws_bytes(g.layout, g.M, g.N, g.K, ctx->sms);
+    if (g.ws == nullptr || g.ws_bytes < need || !aligned(g.ws, 256)) {
+      snprintf(buf, sizeof buf, "%s tc3 %s: workspace %zu bytes needed (256-byte aligned), %zu given", g.name,
+               layout_name(g.layout), need, g.ws ? g.ws_bytes : static_cast<size_t>(0));
+      record(buf);
+      return TG_ERR_WORKSPACE_TOO_SMALL;
+    }
+    uint16_t* partsA = static_cast<uint16_t*>(g.ws);
+    uint16_t* partsB = partsA + 3 * pa;
+    void* pws = static_cast<char*>(g.ws) + parts;
+    cudaError_t e = split3_launch(static_cast<const float*>(g.A), na, pa, partsA, g.stream);
+    if (e == cudaSuccess) e = split3_launch(static_cast<const float*>(g.B), nbb, pb, partsB, g.stream);
+    if (e == cudaSuccess) {
+      TcGemm t{};
+      t.layout = g.layout;
+      t.A = partsA;
+      t.B = partsB;
+      t.C = g.C;
+      t.in_kind = EK_BF16;
+      t.out_kind = EK_F32;
+      t.batch = 1;
+      t.M = g.M;
+      t.N = g.N;
+      t.K = g.K;
+      t.lda = g.lda;
+      t.ldb = g.ldb;
+      t.a_bstride = pa;
+      t.b_bstride = pb;
+      t.split3 = 1;
+      t.bn = p.bn;
+      t.splits = p.splits;
+      t.raster_n = p.raster_n;
+      t.tail_splits = p.tail;
+      t.pair = p.pair ? 1 : 0;
+      t.accumulate = g.accumulate;
+      t.deep = plan_deep(p, g.M, g.N, 6 * kb * 64, 1, ctx->sms) ? 1 : 0;
+      t.ws = pws;
+      t.grid = ctx->sms;
+      t.stream = g.stream;
+      t.status = ctx->status;
+      t.timeout_ns = ctx->timeout_ns;
+      e = g.layout == LAYOUT_NT ? tc_gemm_launch_nt(t) : g.layout == LAYOUT_NN ? tc_gemm_launch_nn(t) : tc_gemm_launch_tn(t);
+      if (e == cudaSuccess && p.splits > 1)
+        e = splitk_reduce_launch(static_cast<const float*>(pws), g.C, EK_F32, 1, p.splits, g.M * g.N, g.stream,
+                                 g.accumulate);
+    }
+    std::string txt = plan_text(p, g.layout, g.M, g.N, 6 * kb * 64, 1, ctx->sms);
+    if (txt.compare(0, 3, "tc ") == 0) txt = "tc3 " + txt.substr(3);
+    record(std::string(g.name) + " " + txt + " " + (e == cudaSuccess ? "ok" : cudaGetErrorString(e)));
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+  if (g.in == TG_F32) {  // FP32 operands the tensor-core path cannot take: the CUDA-core FFMA kernel
     FfmaGemm f;
     f.layout = g.layout;
     f.A = static_cast<const float*>(g.A);
@@ -681,7 +765,11 @@ static tg_status run_gemm(GemmCall g, DevCtx* ctx) {
 static size_t gemm_ws_bytes(int layout, int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in, tg_dtype out,
                             int sms) {
   if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
-  if (in == TG_F32) return batch == 1 ? ffma_ws_bytes(M, N, K, sms) : 0;
+  if (in == TG_F32) {  // the larger of the tensor-core split's and the FFMA kernel's needs
+    if (batch != 1) return 0;
+    const size_t a = ffma_ws_bytes(M, N, K, sms), b = K <= kMaxDim / 6 ? split3_ws_bytes(layout, M, N, K, sms) : 0;
+    return a > b ? a : b;
+  }
   return plan_ws_bytes(make_plan(layout, M, N, K, batch, in, out, sms), M, N, K, batch, sms);
 }
 
@@ -757,7 +845,14 @@ size_t tg_plan_describe(tg_op op, int64_t M, int64_t N, int64_t K, int64_t batch
   const int64_t lda = layout == LAYOUT_TN ? M : K, ldb = layout == LAYOUT_NT ? K : N;
   std::string s;
   if (in == TG_F32) {
-    s = std::string("ffma ") + layout_name(layout) + " splits=" + std::to_string(ffma_splits(M, N, K, sms));
+    if (batch == 1 && lda % 8 == 0 && ldb % 8 == 0 && (N * 4) % 16 == 0 && K <= kMaxDim / 6) {
+      // the three-part split on the tensor cores: a reduction six times as long
+      const int64_t kb = (K + 63) / 64;
+      s = plan_text(split3_plan(layout, M, N, K, sms), layout, M, N, 6 * kb * 64, 1, sms);
+      s = "tc3 " + s.substr(3);
+    } else {
+      s = std::string("ffma ") + layout_name(layout) + " splits=" + std::to_string(ffma_splits(M, N, K, sms));
+    }
   } else if ((lda * 2) % 16 || (ldb * 2) % 16 || (N * static_cast<int64_t>(dt_bytes(out))) % 16 || batch > 65535) {
     s = std::string("simt ") + layout_name(layout);
   } else {

@@ -19,6 +19,13 @@
 // MN-major one is copied as it is.  Long reductions over few tiles are split
 // along K into FP32 partials that the ordered split-K reduction adds up
 // (bitwise reproducible).
+//
+// The same products also run on the tensor cores (api.cu chooses when the
+// operand pitches allow TMA): split3_kernel below cuts each FP32 operand into
+// three bf16 parts, and the layer-product kernels form the six part products
+// a_i b_j with i + j <= 2 in FP32 sums.
+#include <cuda_bf16.h>
+
 #include "tg_internal.h"
 
 namespace tg {
@@ -204,6 +211,39 @@ cudaError_t ffma_gemm_launch(const FfmaGemm& g) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || s == 1) return e;
   return splitk_reduce_launch(g.ws, g.C, EK_F32, 1, s, g.M * g.N, g.stream, g.accumulate);
+}
+
+// ---------------------------------------------------------------------------
+// FP32 operands on the tensor cores: each operand split into three bf16 parts
+// (8 significant bits each; FP32 has 24) so that the 16-bit MMA, which
+// multiplies exactly and adds in FP32, can form the six part products that
+// carry the product to within 2^-24 of its magnitude.
+namespace {
+__global__ void split3_kernel(const float* __restrict__ src, int64_t n, int64_t pstride, uint16_t* __restrict__ dst) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // src may be the previous kernel's output
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = src[i];
+    // v - p0 and its remainder are exact in FP32 (each part takes the leading
+    // 8 bits of what is left, rounded to nearest)
+    const __nv_bfloat16 p0 = __float2bfloat16_rn(v);
+    const float r1 = isfinite(v) ? v - __bfloat162float(p0) : 0.f;
+    const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(p1);
+    const __nv_bfloat16 p2 = __float2bfloat16_rn(r2);
+    dst[i] = __bfloat16_as_ushort(p0);
+    dst[pstride + i] = __bfloat16_as_ushort(p1);
+    dst[2 * pstride + i] = __bfloat16_as_ushort(p2);
+  }
+}
+}  // namespace
+
+cudaError_t split3_launch(const float* src, int64_t n, int64_t pstride, uint16_t* dst, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return launch_k(split3_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, src, n, pstride, dst);
 }
 
 }  // namespace tg

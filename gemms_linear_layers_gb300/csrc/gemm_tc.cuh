@@ -97,7 +97,22 @@ struct TcArgs {
   int accumulate;             // FP32 output: the tile writer adds its tile into C (C += A B)
   int kb_lora;                // >= 0: K block kb_lora comes from tmA2 / tmB2 at K offset 0 (a LoRA
                               // branch appended to the reduction); -1: none
+  int split3;                 // 1: FP32 operands as three 16-bit parts each (the maps' batch index is
+                              // the part); the reduction runs over 6 segments of kbs K blocks
+  int kbs;
 };
+
+// FP32 operands split into three bf16 parts a = a0 + a1 + a2 (exactly, for
+// normal values): a b is the sum of the six part products a_i b_j with
+// i + j <= 2 (the three left out are below 2^-24 |a b|).  Segment s of the
+// reduction multiplies part PA(s) of A by part PB(s) of B, the largest terms
+// first: (0,0) (0,1) (1,0) (0,2) (1,1) (2,0).
+__device__ __forceinline__ void split3_block(int kb, int kbs, int* k0, int* za, int* zb) {
+  const int seg = kb / kbs;
+  *k0 = (kb - seg * kbs) * TC_BK;
+  *za = (0x210100 >> (4 * seg)) & 0xF;
+  *zb = (0x012010 >> (4 * seg)) & 0xF;
+}
 
 #ifdef TG_TRACE
 #define TG_EVENT(ev)                                                                    \
@@ -415,27 +430,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const bool lx = kb == args.kb_lora;
           const CUtensorMap* mA = lx ? &tmA2 : &tmA;
           const CUtensorMap* mB = lx ? &tmB2 : &tmB;
-          const int k0 = lx ? 0 : kb * TC_BK;
+          int k0 = lx ? 0 : kb * TC_BK, za = c.b, zb = c.b;
+          if (args.split3) split3_block(kb, args.kbs, &k0, &za, &zb);
           if (A_MN) {
             if (args.a_chunked) {  // one box: 2 chunks of 64 columns x 64 k-rows
-              tma_load_4d(a_dst, mA, fb, 0, k0, c.m0 / 64, c.b);
+              tma_load_4d(a_dst, mA, fb, 0, k0, c.m0 / 64, za);
             } else {
-              tma_load_3d(a_dst, mA, fb, c.m0, k0, c.b);
-              tma_load_3d(a_dst + 8192, mA, fb, c.m0 + 64, k0, c.b);
+              tma_load_3d(a_dst, mA, fb, c.m0, k0, za);
+              tma_load_3d(a_dst + 8192, mA, fb, c.m0 + 64, k0, za);
             }
           } else {
-            tma_load_3d(a_dst, mA, fb, k0, c.m0, c.b);
+            tma_load_3d(a_dst, mA, fb, k0, c.m0, za);
           }
           if (B_MN) {
             if (args.b_chunked) {
-              tma_load_4d(b_dst, mB, fb, 0, k0, c.n0 / 64, c.b);
+              tma_load_4d(b_dst, mB, fb, 0, k0, c.n0 / 64, zb);
             } else {
 #pragma unroll
               for (int j = 0; j < Cfg::B_CHUNKS; ++j)
-                tma_load_3d(b_dst + j * 8192, mB, fb, c.n0 + 64 * j, k0, c.b);
+                tma_load_3d(b_dst + j * 8192, mB, fb, c.n0 + 64 * j, k0, zb);
             }
           } else {
-            tma_load_3d(b_dst, mB, fb, k0, c.n0, c.b);
+            tma_load_3d(b_dst, mB, fb, k0, c.n0, zb);
           }
           issued[stage] = static_cast<int>(phase);
           if (++stage == S) {

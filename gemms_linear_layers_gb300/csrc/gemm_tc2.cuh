@@ -267,28 +267,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const bool lx = kb == args.kb_lora;
           const CUtensorMap* mA = lx ? &tmA2 : &tmA;
           const CUtensorMap* mB = lx ? &tmB2 : &tmB;
-          const int k0 = lx ? 0 : kb * TC_BK;
+          int k0 = lx ? 0 : kb * TC_BK, za = c.b, zb = c.b;
+          if (args.split3) split3_block(kb, args.kbs, &k0, &za, &zb);
           const int m = c.m0 + a_row;
           if (A_MN) {
             if (args.a_chunked) {
-              tma_load_4d_pair(a_dst, mA, fb, 0, k0, m / 64, c.b);
+              tma_load_4d_pair(a_dst, mA, fb, 0, k0, m / 64, za);
             } else {
-              tma_load_3d_pair(a_dst, mA, fb, m, k0, c.b);
-              tma_load_3d_pair(a_dst + 8192, mA, fb, m + 64, k0, c.b);
+              tma_load_3d_pair(a_dst, mA, fb, m, k0, za);
+              tma_load_3d_pair(a_dst + 8192, mA, fb, m + 64, k0, za);
             }
           } else {
-            tma_load_3d_pair(a_dst, mA, fb, k0, m, c.b);
+            tma_load_3d_pair(a_dst, mA, fb, k0, m, za);
           }
           const int n = c.n0 + b_off;
           if (B_MN) {
             if (args.b_chunked) {
-              tma_load_4d_pair(b_dst, mB, fb, 0, k0, n / 64, c.b);
+              tma_load_4d_pair(b_dst, mB, fb, 0, k0, n / 64, zb);
             } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d_pair(b_dst + j * 8192, mB, fb, n + 64 * j, k0, c.b);
+              for (int j = 0; j < Cfg::B_CHUNKS; ++j) tma_load_3d_pair(b_dst + j * 8192, mB, fb, n + 64 * j, k0, zb);
             }
           } else {
-            tma_load_3d_pair(b_dst, mB, fb, k0, n, c.b);
+            tma_load_3d_pair(b_dst, mB, fb, k0, n, zb);
           }
           if (issued[stage] < 0 && stage == 0) TG_EVENT(1);
           issued[stage] = static_cast<int>(phase);

@@ -54,6 +54,7 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmC2, tmP;
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
+  const uint64_t nbm = g.split3 ? 3 : nb;  // the operand maps' batch: the three parts of a split
   bool ok;
   // An MN-major operand whose width is a multiple of 64 is viewed as
   // [batch][width/64 chunks][K][64], so one box loads all of a stage's chunks
@@ -62,25 +63,25 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
   const bool b4 = B_MN && N % 64 == 0 && BN % 64 == 0 && chunked_mn_enabled();
   if (a4) {
-    const uint64_t d[4] = {64, K, M / 64, nb}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
+    const uint64_t d[4] = {64, K, M / 64, nbm}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
                                                       static_cast<uint64_t>(g.a_bstride) * 2};
     const uint32_t b[4] = {64, 64, TC_BM / 64, 1};
     ok = encode_tmap_nd(&tmA, g.A, g.in_kind, 4, d, st, b, 128);
   } else if (A_MN) {  // stored [batch][K][M]
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nbm, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
   } else {  // stored [batch][M][K]
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nbm, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
   if (b4) {
-    const uint64_t d[4] = {64, K, N / 64, nb}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
+    const uint64_t d[4] = {64, K, N / 64, nbm}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
                                                       static_cast<uint64_t>(g.b_bstride) * 2};
     const uint32_t b[4] = {64, 64, static_cast<uint32_t>(Cfg::B_CHUNKS), 1};
     ok = encode_tmap_nd(&tmB, g.B, g.in_kind, 4, d, st, b, 128);
   } else if (B_MN) {  // stored [batch][K][N]
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nbm, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
   } else {  // stored [batch][N][K]
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nbm, g.ldb * 2, g.b_bstride * 2, 64, BN, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap tmA2, tmB2;
@@ -104,7 +105,9 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   TcArgs a;
   a.m_tiles = static_cast<int>((M + TC_BM - 1) / TC_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
-  a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.kbs = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.split3 = g.split3 ? 1 : 0;
+  a.kb_total = g.split3 ? 6 * a.kbs : a.kbs;
   a.kb_lora = -1;
   if (g.lora_A2 != nullptr) {  // one more K block, after the product's own
     a.kb_lora = a.kb_total;
@@ -120,8 +123,8 @@ static cudaError_t tc_launch_one(const TcGemm& g) {
   a.a_chunked = a4 ? 1 : 0;
   a.b_chunked = b4 ? 1 : 0;
   // tail split (never with stream-K or split partials)
-  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid, (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits,
-                              g.raster_n);
+  const TailGeo tg = tail_geo(M, N, static_cast<uint64_t>(a.kb_total) * TC_BK, nb, BN, g.grid,
+                              (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits, g.raster_n);
   a.dp_tiles = tg.dp_tiles;
   a.tail_splits = tg.splits;
   a.tail_kps = tg.kps;
@@ -198,29 +201,30 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmP;
   const uint64_t M = g.M, N = g.N, K = g.K, nb = g.batch;
+  const uint64_t nbm = g.split3 ? 3 : nb;  // the operand maps' batch: the three parts of a split
   bool ok;
   const bool a4 = A_MN && M % 64 == 0 && chunked_mn_enabled();
   const bool b4 = B_MN && N % 64 == 0 && Cfg::BH % 64 == 0 && chunked_mn_enabled();
   if (a4) {
-    const uint64_t d[4] = {64, K, M / 64, nb}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
+    const uint64_t d[4] = {64, K, M / 64, nbm}, st[3] = {static_cast<uint64_t>(g.lda) * 2, 128,
                                                       static_cast<uint64_t>(g.a_bstride) * 2};
     const uint32_t b[4] = {64, 64, TC_BM / 64, 1};
     ok = encode_tmap_nd(&tmA, g.A, g.in_kind, 4, d, st, b, 128);
   } else if (A_MN) {
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nb, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, M, K, nbm, g.lda * 2, g.a_bstride * 2, 64, 64, 128);
   } else {
-    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nb, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
+    ok = encode_tmap_3d(&tmA, g.A, g.in_kind, K, M, nbm, g.lda * 2, g.a_bstride * 2, 64, TC_BM, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
   if (b4) {
-    const uint64_t d[4] = {64, K, N / 64, nb}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
+    const uint64_t d[4] = {64, K, N / 64, nbm}, st[3] = {static_cast<uint64_t>(g.ldb) * 2, 128,
                                                       static_cast<uint64_t>(g.b_bstride) * 2};
     const uint32_t b[4] = {64, 64, static_cast<uint32_t>(Cfg::B_CHUNKS), 1};
     ok = encode_tmap_nd(&tmB, g.B, g.in_kind, 4, d, st, b, 128);
   } else if (B_MN) {
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nb, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, N, K, nbm, g.ldb * 2, g.b_bstride * 2, 64, 64, 128);
   } else {
-    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nb, g.ldb * 2, g.b_bstride * 2, 64, Cfg::BH, 128);
+    ok = encode_tmap_3d(&tmB, g.B, g.in_kind, K, N, nbm, g.ldb * 2, g.b_bstride * 2, 64, Cfg::BH, 128);
   }
   if (!ok) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap tmA2, tmB2;
@@ -236,7 +240,9 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   TcArgs a = {};
   a.m_tiles = static_cast<int>((M + TC2_BM - 1) / TC2_BM);
   a.n_tiles = static_cast<int>((N + BN - 1) / BN);
-  a.kb_total = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.kbs = static_cast<int>((K + TC_BK - 1) / TC_BK);
+  a.split3 = g.split3 ? 1 : 0;
+  a.kb_total = g.split3 ? 6 * a.kbs : a.kbs;
   a.kb_lora = -1;
   if (g.lora_A2 != nullptr) {  // one more K block, after the product's own
     a.kb_lora = a.kb_total;
@@ -252,8 +258,8 @@ static cudaError_t tc2_launch_one(const TcGemm& g) {
   a.b_chunked = b4 ? 1 : 0;
   // tail split (never with stream-K or split partials); the geometry is that
   // of a full wave of grid / 2 pairs, whatever number of pairs runs
-  const TailGeo tg = tail_geo(M, N, K, nb, BN, g.grid / 2, (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits,
-                              g.raster_n, TC2_BM);
+  const TailGeo tg = tail_geo(M, N, static_cast<uint64_t>(a.kb_total) * TC_BK, nb, BN, g.grid / 2,
+                              (g.sk || g.splits > 1 || g.lora_A2) ? 1 : g.tail_splits, g.raster_n, TC2_BM);
   a.dp_tiles = tg.dp_tiles;
   a.tail_splits = tg.splits;
   a.tail_kps = tg.kps;

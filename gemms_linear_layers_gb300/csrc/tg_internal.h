@@ -83,6 +83,10 @@ struct TcGemm {
   // [64][N] MN-major); both nullptr when absent
   const void* lora_A2;
   const void* lora_B2;
+  // 1: A and B are FP32 operands given as three bf16 parts each, stored
+  // [3][...] with the parts a_bstride / b_bstride elements apart (batch 1);
+  // the reduction runs over the six part products (gemm_tc.cuh, split3_block)
+  int split3;
   void* ws;
   int grid;                   // persistent CTAs
   cudaStream_t stream;
@@ -208,6 +212,11 @@ bool encode_tmap_3d(void* tmap_out, const void* base, int elem_kind, uint64_t d0
                     uint32_t box1, int swizzle_bytes);
 bool encode_tmap_nd(void* tmap_out, const void* base, int elem_kind, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box, int swizzle_bytes);
+
+// FP32 [n] -> three bf16 parts at dst, dst + pstride and dst + 2 pstride, with
+// v = p0 + p1 + p2 exactly for normal v (gemm_ffma.cu); non-finite v keeps
+// only p0.
+cudaError_t split3_launch(const float* src, int64_t n, int64_t pstride, uint16_t* dst, cudaStream_t stream);
 
 // rank-r LoRA streaming kernels (lora.cu)
 struct LoraArgs {

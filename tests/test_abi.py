@@ -220,11 +220,15 @@ def test_plan_describe_reports_table_entries_and_the_cuda_core_path(lib):
         assert _plan(B.TG_OP_GEMM_FWD, 3000, 1000, 700) == "simt nt"  # K = 700: rows of 1,400 bytes
         assert _plan(B.TG_OP_GEMM_WGRAD, 0, 576, 2048) == ""
         assert _plan(B.TG_OP_LORA_DOWN, 2048, 576, 16) == ""
-        # FP32 operands: the FFMA kernel, split along K when few tiles would occupy the SMs
+        # FP32 operands: three bf16 parts each on the tensor cores (a reduction six
+        # times as long) when the pitches allow TMA, else the FFMA kernel, split
+        # along K when few tiles would occupy the SMs
         f32 = lambda op, M, N, K: B.tg_plan_describe(op, M, N, K, 1, torch.float32, torch.float32, 152)
-        assert f32(B.TG_OP_GEMM_FWD, 4096, 5760, 2304) == "ffma nt splits=1"
-        assert f32(B.TG_OP_GEMM_DGRAD, 2048, 576, 49152) == "ffma nn splits=3"
-        assert f32(B.TG_OP_GEMM_WGRAD, 576, 576, 2048) == "ffma tn splits=4"
+        assert f32(B.TG_OP_GEMM_FWD, 4096, 5760, 2304).startswith("tc3 nt M=4096 N=5760 K=13824 batch=1 bn=")
+        assert f32(B.TG_OP_GEMM_DGRAD, 2048, 576, 49152).startswith("tc3 nn M=2048 N=576 K=294912 ")
+        assert " cs " not in f32(B.TG_OP_GEMM_WGRAD, 576, 576, 2048)  # no cluster split for the parts
+        assert f32(B.TG_OP_GEMM_FWD, 1000, 1001, 999) == "ffma nt splits=1"  # rows of 999 floats
+        assert f32(B.TG_OP_GEMM_DGRAD, 2048, 578, 49152) == "ffma nn splits=3"
         assert B.tg_plan_describe(B.TG_OP_GEMM_FWD, 64, 64, 64, 1, torch.float32, torch.bfloat16, 152) == ""
     finally:
         assert lib.tg_load_table(None) == 0

@@ -31,6 +31,8 @@ def test_kernel_key():
     assert k("fwd tc nt M=2048 N=576 K=1536 batch=1 bn=192 cs splits=1 cluster=3 raster=m table=hit ok") == \
         "tc nt bn=192 cs"
     assert k("wgrad simt tn M=200 N=300 K=520 batch=1 ok") == "simt tn"
+    assert k("fwd tc3 nt M=2048 N=2304 K=13824 batch=1 bn=256 pair splits=1 raster=m table=miss ok") == \
+        "tc3 nt bn=256 pair"
 
 
 def _products():

@@ -50,6 +50,13 @@ LADDER = [(1, 1, 1), (7, 5, 13), (16, 16, 16), (64, 64, 64), (129, 65, 257), (10
           (256, 4096, 128), (3000, 64, 40)]
 
 
+def fp32_path(op, T, d_in, d_out):
+    """'tc3' (three bf16 parts on the tensor cores) when the row pitches of both
+    operands are multiples of 8 elements and the output's of 4, else 'ffma'."""
+    lda, ldb, N = {"fwd": (d_in, d_in, d_out), "dgrad": (d_out, d_in, d_in), "wgrad": (d_out, d_in, d_in)}[op]
+    return "tc3" if lda % 8 == 0 and ldb % 8 == 0 and N % 4 == 0 else "ffma"
+
+
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("shape", LADDER, ids=lambda s: "x".join(map(str, s)))
 def test_fp32_ladder(shape, op):
@@ -59,7 +66,7 @@ def test_fp32_ladder(shape, op):
     call = tg.tg_last_call()
     torch.cuda.synchronize()
     assert tg.tg_stream_status() == 0
-    assert " ffma " in call, call
+    assert f" {fp32_path(op, *shape)} " in call, call
     C, S = ref(op, X, W, dY)
     assert got.dtype == F32 and tuple(got.shape) == C.shape
     assert_close(got, C, S, f"fp32 {op} {shape} [{call}]", F32)
@@ -101,9 +108,11 @@ def test_fp32_small_integers_exact(op):
     assert np.array_equal(got.cpu().double().numpy(), C), tg.tg_last_call()
 
 
-@pytest.mark.parametrize("shape", [(1000, 300, 200), (8192, 576, 192)], ids=("one-pass", "split"))
+@pytest.mark.parametrize("shape", [(1000, 300, 200), (8192, 576, 192), (1000, 296, 200)],
+                         ids=("ffma", "tensor-cores", "tensor-cores-small"))
 def test_fp32_weight_gradient_accumulates(shape):
-    """dW += dY^T X with FP32 operands, unsplit (added in the kernel) and split
+    """dW += dY^T X with FP32 operands, on the CUDA cores (a row pitch of 300
+    floats) and on the tensor cores (three-part split), unsplit and split
     (added by the ordered reduction)."""
     T, d_in, d_out = shape
     X, _, dY = inputs.layer_inputs(T, d_in, d_out, F32, tag="f32acc")
@@ -112,7 +121,7 @@ def test_fp32_weight_gradient_accumulates(shape):
     tg.tg_gemm_wgrad_accumulate(dY.cuda(), X.cuda(), dW)
     call = tg.tg_last_call()
     torch.cuda.synchronize()
-    assert "ffma" in call, call
+    assert f" {fp32_path('wgrad', T, d_in, d_out)} " in call, call
     C, S = oracle.gemm_wgrad(dY, X)
     base = dW0.double().numpy()
     assert_close(dW, base + C, np.abs(base) + S, f"fp32 wgrad accumulate {shape} [{call}]", F32)
@@ -126,3 +135,20 @@ def test_fp32_empty_reduction_and_sizes():
     dW = tg.tg_gemm_wgrad(dY, X)  # K = T = 0: an empty sum is zero
     torch.cuda.synchronize()
     assert torch.count_nonzero(dW) == 0
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_fp32_wide_exponents_on_the_tensor_cores(op):
+    """FP32 operands whose magnitudes span twelve decades, with all 24
+    significand bits in use: the three bf16 parts carry each value exactly, so
+    the tensor-core path holds the bound wherever the magnitudes fall."""
+    T, d_in, d_out = 512, 384, 256
+    X, W, dY = inputs.layer_inputs(T, d_in, d_out, F32, tag="f32wide")
+    spread = lambda shape, seed: torch.pow(10.0, inputs.normal(shape, 2.0, F32, seed).clamp(-6, 6))
+    X, W, dY = X * spread(X.shape, 51), W * spread(W.shape, 52), dY * spread(dY.shape, 53)
+    got = run(op, X.cuda(), W.cuda(), dY.cuda())
+    call = tg.tg_last_call()
+    torch.cuda.synchronize()
+    assert " tc3 " in call, call
+    C, S = ref(op, X, W, dY)
+    assert_close(got, C, S, f"fp32 wide {op} [{call}]", F32)
