@@ -64,6 +64,16 @@ bool chunked_mn_enabled() {
   return on;
 }
 
+// FP32 operands on the tensor cores (three-part split) when the pitches allow
+// (default), or always on the CUDA cores ($TG_FP32_PATH=ffma).
+static bool fp32_tc_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("TG_FP32_PATH");
+    return !(e && strcmp(e, "ffma") == 0);
+  }();
+  return on;
+}
+
 struct DevCtx {
   bool ready = false;
   tg_status init_status = TG_OK;
@@ -550,7 +560,7 @@ static bool tc_eligible(const GemmCall& g) {
 // over the six part products (reduction 6 K long) on the single-CTA or pair
 // kernel (split-K, tail split allowed; a cluster split becomes a split-K).
 static bool split3_eligible(const GemmCall& g) {
-  return g.in == TG_F32 && g.out == TG_F32 && g.batch == 1 && g.lda % 8 == 0 && g.ldb % 8 == 0 &&
+  return fp32_tc_enabled() && g.in == TG_F32 && g.out == TG_F32 && g.batch == 1 && g.lda % 8 == 0 && g.ldb % 8 == 0 &&
          (g.N * 4) % 16 == 0 && aligned(g.C, 16) && g.M <= kMaxDim && g.N <= kMaxDim && g.K <= kMaxDim / 6 &&
          g.a_kind_override < 0 && g.b_kind_override < 0 && g.scale == 1.f;
 }
@@ -845,7 +855,7 @@ size_t tg_plan_describe(tg_op op, int64_t M, int64_t N, int64_t K, int64_t batch
   const int64_t lda = layout == LAYOUT_TN ? M : K, ldb = layout == LAYOUT_NT ? K : N;
   std::string s;
   if (in == TG_F32) {
-    if (batch == 1 && lda % 8 == 0 && ldb % 8 == 0 && (N * 4) % 16 == 0 && K <= kMaxDim / 6) {
+    if (fp32_tc_enabled() && batch == 1 && lda % 8 == 0 && ldb % 8 == 0 && (N * 4) % 16 == 0 && K <= kMaxDim / 6) {
       // the three-part split on the tensor cores: a reduction six times as long
       const int64_t kb = (K + 63) / 64;
       s = plan_text(split3_plan(layout, M, N, K, sms), layout, M, N, 6 * kb * 64, 1, sms);

@@ -27,8 +27,13 @@
  *     `out` is TG_F32 or the input type.  16-bit outputs are the FP32 result
  *     rounded to nearest even.  The layer products (tg_gemm_fwd, _dgrad,
  *     _wgrad and their _noalloc / _accumulate forms) also take in = TG_F32
- *     with out = TG_F32: FP32 operands, every product fused into its FP32 sum
- *     on the CUDA cores (FFMA), no tensor-core rounding of the operands.
+ *     with out = TG_F32: FP32 operands, held to the same bound.  When every
+ *     row pitch is a multiple of 8 elements (the output's of 4) they run on
+ *     the tensor cores: each operand is cut into three bf16 parts that carry
+ *     it exactly (staged in `ws`), and the product sums the six part products
+ *     a_i b_j with i + j <= 2 in FP32; otherwise every product is fused into
+ *     its FP32 sum on the CUDA cores (FFMA; also for every FP32 product when
+ *     the environment sets TG_FP32_PATH=ffma).  No TF32 rounding either way.
  *   - Sizes: a negative size is TG_ERR_INVALID_ARG; an empty output (a zero
  *     row or column count) is TG_OK with nothing done; an empty reduction
  *     writes zeros.  Every size must be below 2^31.
