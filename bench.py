@@ -32,7 +32,7 @@ public entry points (the command the ncu summaries are captured with): OP is
 fwd|dgrad|wgrad or fwd_lora|dgrad_lora (dims T d_in d_out; rank 16, scale 2),
 one of the attention products
 qk|pv|do_vt|pt_do|ds_k|dst_q or the fused attn_fwd / attn_bwd (dims heads s d), or
-lora_down|lora_up|lora_grad (dims T d_in d_out, rank 16); --plan writes a
+lora_down|lora_up|lora_grad and their _f32w forms (dims T d_in d_out, rank 16); --plan writes a
 one-line tile table for the shape and loads it first.
 """
 from __future__ import annotations
@@ -993,7 +993,7 @@ def probe_main(argv=None):
         fn = {"fwd": lambda ws: tg.tg_gemm_fwd(X, W, Y=out, ws=ws),
               "dgrad": lambda ws: tg.tg_gemm_dgrad(dY, W, dX=out, ws=ws),
               "wgrad": lambda ws: tg.tg_gemm_wgrad(dY, X, dW=out, ws=ws)}[a.op]
-    elif a.op.startswith("lora"):
+    elif a.op.startswith("lora"):  # rank 16; --dtype applies to the activations
         T, d_in, d_out = a.dims
         X, A, B, H, dY = inputs.lora_inputs(T, d_in, d_out, 16, dtype, tag="probe", device=dev)
         M, N, K, batch = T, 16, d_in, 1
@@ -1002,12 +1002,22 @@ def probe_main(argv=None):
                 "dX": torch.empty(T, d_in, dtype=out_dtype, device=dev)}
         Hout = torch.empty(T, 16, dtype=out_dtype, device=dev)
         Yout = torch.empty(T, d_out, dtype=out_dtype, device=dev)
+        # FP32 factors (the *_f32w forms): A, B drawn in fp32, dA, dB FP32
+        _, A32, B32, _, _ = inputs.lora_inputs(T, d_in, d_out, 16, torch.float32, tag="probe", device=dev)
+        outs32 = {"dA": torch.empty(16, d_in, dtype=torch.float32, device=dev),
+                  "dB": torch.empty(d_out, 16, dtype=torch.float32, device=dev),
+                  "dX": torch.empty(T, d_in, dtype=out_dtype, device=dev)}
         fn = {"lora_down": lambda ws: tg.tg_lora_down(X, A, H=Hout, ws=ws),
               "lora_up": lambda ws: tg.tg_lora_up(H, B, Y=Yout, ws=ws),
-              "lora_grad": lambda ws: tg.tg_lora_grad(X, A, B, H, dY, outs=outs, ws=ws)}[a.op]
-        nbytes = {"lora_down": (T * d_in + 16 * d_in + T * 16) * 2,
-                  "lora_up": (T * 16 + 16 * d_out + T * d_out) * 2,
-                  "lora_grad": (T * d_out + 2 * T * d_in + T * 16 + 2 * 16 * d_in + 2 * 16 * d_out) * 2}[a.op]
+              "lora_grad": lambda ws: tg.tg_lora_grad(X, A, B, H, dY, outs=outs, ws=ws),
+              "lora_down_f32w": lambda ws: tg.tg_lora_down_f32w(X, A32, H=Hout, ws=ws),
+              "lora_up_f32w": lambda ws: tg.tg_lora_up_f32w(H, B32, Y=Yout, ws=ws),
+              "lora_grad_f32w": lambda ws: tg.tg_lora_grad_f32w(X, A32, B32, H, dY, outs=outs32, ws=ws)}[a.op]
+        base = a.op.replace("_f32w", "")
+        wb = 4 if a.op.endswith("_f32w") else 2  # bytes of a factor element
+        nbytes = {"lora_down": (T * d_in + T * 16) * 2 + 16 * d_in * wb,
+                  "lora_up": (T * 16 + T * d_out) * 2 + 16 * d_out * wb,
+                  "lora_grad": (T * d_out + 2 * T * d_in + T * 16) * 2 + (2 * 16 * d_in + 2 * 16 * d_out) * wb}[base]
     elif a.op in ("fwd_lora", "dgrad_lora"):  # the layer product with a rank-16 LoRA branch inside it
         T, d_in, d_out = a.dims
         X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="probe", device=dev)

@@ -219,31 +219,62 @@ cudaError_t ffma_gemm_launch(const FfmaGemm& g) {
 // multiplies exactly and adds in FP32, can form the six part products that
 // carry the product to within 2^-24 of its magnitude.
 namespace {
+// the three parts of one value: v - p0 and its remainder are exact in FP32
+// (each part takes the leading 8 bits of what is left, rounded to nearest)
+__device__ __forceinline__ void split3_one(float v, uint16_t* p) {
+  const __nv_bfloat16 p0 = __float2bfloat16_rn(v);
+  const float r1 = isfinite(v) ? v - __bfloat162float(p0) : 0.f;
+  const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+  p[0] = __bfloat16_as_ushort(p0);
+  p[1] = __bfloat16_as_ushort(p1);
+  p[2] = __bfloat16_as_ushort(p2);
+}
+
+// vec4: four values per step (16-byte loads, 8-byte stores of each part)
+template <bool VEC4>
 __global__ void split3_kernel(const float* __restrict__ src, int64_t n, int64_t pstride, uint16_t* __restrict__ dst) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // src may be the previous kernel's output
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float v = src[i];
-    // v - p0 and its remainder are exact in FP32 (each part takes the leading
-    // 8 bits of what is left, rounded to nearest)
-    const __nv_bfloat16 p0 = __float2bfloat16_rn(v);
-    const float r1 = isfinite(v) ? v - __bfloat162float(p0) : 0.f;
-    const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(p1);
-    const __nv_bfloat16 p2 = __float2bfloat16_rn(r2);
-    dst[i] = __bfloat16_as_ushort(p0);
-    dst[pstride + i] = __bfloat16_as_ushort(p1);
-    dst[2 * pstride + i] = __bfloat16_as_ushort(p2);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (VEC4) {
+    for (int64_t q = i0; q < n / 4; q += stride) {
+      const float4 v = reinterpret_cast<const float4*>(src)[q];
+      uint16_t a[3], b[3], c[3], d[3];
+      split3_one(v.x, a);
+      split3_one(v.y, b);
+      split3_one(v.z, c);
+      split3_one(v.w, d);
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+        *reinterpret_cast<uint2*>(dst + p * pstride + 4 * q) =
+            make_uint2(a[p] | (static_cast<uint32_t>(b[p]) << 16), c[p] | (static_cast<uint32_t>(d[p]) << 16));
+    }
+  } else {
+    for (int64_t i = i0; i < n; i += stride) {
+      uint16_t a[3];
+      split3_one(src[i], a);
+      dst[i] = a[0];
+      dst[pstride + i] = a[1];
+      dst[2 * pstride + i] = a[2];
+    }
   }
 }
 }  // namespace
 
 cudaError_t split3_launch(const float* src, int64_t n, int64_t pstride, uint16_t* dst, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  int64_t blocks = (n + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_k(split3_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, src, n, pstride, dst);
+  // whole float4 groups when the source and every part start 16 / 8 bytes aligned
+  const bool vec = n % 4 == 0 && pstride % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(dst) % 8 == 0;
+  const int64_t work = vec ? n / 4 : n;
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  return vec ? launch_k(split3_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, src, n, pstride,
+                        dst)
+             : launch_k(split3_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, src, n,
+                        pstride, dst);
 }
 
 }  // namespace tg

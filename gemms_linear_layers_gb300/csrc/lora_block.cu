@@ -36,38 +36,54 @@ __device__ __forceinline__ uint16_t to_16(float x, int bf16) {
   return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
+// one 8-element (16-byte) group of A2 or B2 per step
 __global__ void lora_block_prep_kernel(const BlockPrep p) {
   pdl_wait();  // H may be the previous kernel's output
   pdl_trigger();
-  const long long na = p.T * 64, nb = p.N * 64;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < na + nb;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    if (i < na) {
-      const long long t = i >> 6;
-      const int c = static_cast<int>(i & 63);
-      uint16_t out = 0;
-      if (c < 2 * p.r) {
-        const int k = c < p.r ? c : c - p.r;
-        const long long e = t * p.r + k;
-        const float h = p.h_f32 ? static_cast<const float*>(p.H)[e] : to_f32(static_cast<const uint16_t*>(p.H)[e], p.bf16);
-        const float v = p.scale * h;
-        const uint16_t hi = to_16(v, p.bf16);
-        out = c < p.r ? hi : to_16(v - to_f32(hi, p.bf16), p.bf16);
+  const long long ga = p.T * 8, gb = p.N * 8;  // 8 groups per 64-column row; B2 of the dgrad: 64 rows of N / 8
+  const long long nb8 = p.N / 8;
+  for (long long gi = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; gi < ga + gb;
+       gi += static_cast<long long>(gridDim.x) * blockDim.x) {
+    uint16_t v[8];
+    uint16_t* dst;
+    if (gi < ga) {  // A2 row t, columns c0 .. c0 + 7: hi / lo parts of scale h
+      const long long t = gi >> 3;
+      const int c0 = static_cast<int>(gi & 7) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = c0 + e;
+        uint16_t out = 0;
+        if (c < 2 * p.r) {
+          const long long el = t * p.r + (c < p.r ? c : c - p.r);
+          const float h =
+              p.h_f32 ? static_cast<const float*>(p.H)[el] : to_f32(static_cast<const uint16_t*>(p.H)[el], p.bf16);
+          const float x = p.scale * h;
+          const uint16_t hi = to_16(x, p.bf16);
+          out = c < p.r ? hi : to_16(x - to_f32(hi, p.bf16), p.bf16);
+        }
+        v[e] = out;
       }
-      p.A2[i] = out;
-    } else {
-      const long long j = i - na;
-      uint16_t out = 0;
-      if (!p.dgrad) {  // B' [N][64]: B[n][k] in columns k and r + k
-        const long long n = j >> 6;
-        const int c = static_cast<int>(j & 63);
-        if (c < 2 * p.r) out = static_cast<const uint16_t*>(p.F)[n * p.r + (c < p.r ? c : c - p.r)];
-      } else {  // A' [64][N]: A[k][n] in rows k and r + k
-        const long long k = j / p.N, n = j - k * p.N;
-        if (k < 2 * p.r) out = static_cast<const uint16_t*>(p.F)[(k < p.r ? k : k - p.r) * p.N + n];
+      dst = p.A2 + gi * 8;
+    } else if (!p.dgrad) {  // B' [N][64]: B[n][k] in columns k and r + k
+      const long long j = gi - ga, n = j >> 3;
+      const int c0 = static_cast<int>(j & 7) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = c0 + e;
+        v[e] = c < 2 * p.r ? static_cast<const uint16_t*>(p.F)[n * p.r + (c < p.r ? c : c - p.r)] : uint16_t(0);
       }
-      p.B2[j] = out;
+      dst = p.B2 + j * 8;
+    } else {  // A' [64][N]: A[k][n] in rows k and r + k
+      const long long j = gi - ga, k = j / nb8, n0 = (j - k * nb8) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        v[e] = k < 2 * p.r ? static_cast<const uint16_t*>(p.F)[(k < p.r ? k : k - p.r) * p.N + n0 + e] : uint16_t(0);
+      dst = p.B2 + j * 8;
     }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16),
+                                                v[2] | (static_cast<uint32_t>(v[3]) << 16),
+                                                v[4] | (static_cast<uint32_t>(v[5]) << 16),
+                                                v[6] | (static_cast<uint32_t>(v[7]) << 16));
   }
 }
 
@@ -95,7 +111,9 @@ cudaError_t lora_block_prep_launch(const void* H, int h_f32, const void* F, int6
   p.scale = scale;
   *A2 = p.A2;
   *B2 = p.B2;
-  const long long total = (T + N) * 64;
+  // the input gradient's A' is 64 rows of N: N is a multiple of 8 on the tensor-core path
+  if (dgrad && N % 8 != 0) return cudaErrorInvalidValue;
+  const long long total = (T + N) * 8;  // 16-byte groups
   long long blocks = (total + 255) / 256;
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
