@@ -10,6 +10,10 @@ single CTA or CTA pair, split count or schedule, raster order) of the
 tensor-core kernel; each candidate is timed
 through the public entry point with a one-line table that forces it, and the
 fastest per shape is written with the same key the library looks up.
+Each candidate is timed as a training step meets it: by default every call
+reads operands that are not in L2 (operand sets rotated beyond twice the L2
+size, the state a step's products find after the previous ones streamed
+their own); `--warm` times one operand set over and over instead.
 
 Usage (on the GPU): python -m gemms_linear_layers_gb300.sweep [--out PATH] [--sets 2b,135m,attn]
 """
@@ -34,7 +38,32 @@ PAIR_BNS = (128, 192, 256)
 SPLITS = (1, 2, 3, 4, 6, 8, 12, 16)
 
 
-def shapes(sets):
+def cold_sets(set_bytes: int, warm: bool) -> int:
+    """Operand sets to rotate through so that no call finds its operands in L2."""
+    if warm:
+        return 1
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    return max(1, min(24, 2 * l2 // max(set_bytes, 1) + 1))
+
+
+class Rotating:
+    """A call over `len(calls)` operand sets, taking the next set each time."""
+
+    def __init__(self, calls):
+        self.calls = calls
+        self.i = 0
+
+    @property
+    def sets(self) -> int:
+        return len(self.calls)
+
+    def __call__(self):
+        c = self.calls[self.i % len(self.calls)]
+        self.i += 1
+        return c()
+
+
+def shapes(sets, warm=False):
     """(layout, M, N, K, batch, make_call) for every distinct product."""
     out = []
     seen = set()
@@ -53,37 +82,48 @@ def shapes(sets):
                 groups.append((T, workloads.LAYERS_2B))
         for T, layers in groups:
             for _, d_in, d_out in layers:
-                add(("nt", T, d_out, d_in, 1), lambda T=T, a=d_in, b=d_out: layer_call("fwd", T, a, b))
-                add(("nn", T, d_in, d_out, 1), lambda T=T, a=d_in, b=d_out: layer_call("dgrad", T, a, b))
-                add(("tn", d_out, d_in, T, 1), lambda T=T, a=d_in, b=d_out: layer_call("wgrad", T, a, b))
+                for lay, op, key in (("nt", "fwd", (T, d_out, d_in)), ("nn", "dgrad", (T, d_in, d_out)),
+                                     ("tn", "wgrad", (d_out, d_in, T))):
+                    add((lay, *key, 1), lambda T=T, a=d_in, b=d_out, op=op: layer_call(op, T, a, b, warm=warm))
     if "attn" in sets:
         h, d = workloads.ATTENTION["heads"], workloads.ATTENTION["d"]
         for s in workloads.ATTENTION["s"]:
-            add(("nt", s, s, d, h), lambda s=s: attn_call("qk", h, s, d))
-            add(("nn", s, d, s, h), lambda s=s: attn_call("pv", h, s, d))
-            add(("tn", s, d, s, h), lambda s=s: attn_call("pt_do", h, s, d))
+            add(("nt", s, s, d, h), lambda s=s: attn_call("qk", h, s, d, warm=warm))
+            add(("nn", s, d, s, h), lambda s=s: attn_call("pv", h, s, d, warm=warm))
+            add(("tn", s, d, s, h), lambda s=s: attn_call("pt_do", h, s, d, warm=warm))
     return out
 
 
-def layer_call(op, T, d_in, d_out, dtype=torch.bfloat16):
-    X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag="sweep", device="cuda")
+def layer_call(op, T, d_in, d_out, dtype=torch.bfloat16, warm=False):
+    n = cold_sets((T * d_in + d_out * d_in + T * d_out) * dtype.itemsize, warm)
     ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
-    if op == "fwd":
-        Y = torch.empty(T, d_out, dtype=dtype, device="cuda")
-        return lambda: tg.tg_gemm_fwd(X, W, Y=Y, ws=ws)
-    if op == "dgrad":
-        dX = torch.empty(T, d_in, dtype=dtype, device="cuda")
-        return lambda: tg.tg_gemm_dgrad(dY, W, dX=dX, ws=ws)
-    dW = torch.empty(d_out, d_in, dtype=dtype, device="cuda")
-    return lambda: tg.tg_gemm_wgrad(dY, X, dW=dW, ws=ws)
+    calls = []
+    for i in range(n):
+        X, W, dY = inputs.layer_inputs(T, d_in, d_out, dtype, tag=f"sweep{i}", device="cuda")
+        if op == "fwd":
+            Y = torch.empty(T, d_out, dtype=dtype, device="cuda")
+            calls.append(lambda X=X, W=W, Y=Y: tg.tg_gemm_fwd(X, W, Y=Y, ws=ws))
+        elif op == "dgrad":
+            dX = torch.empty(T, d_in, dtype=dtype, device="cuda")
+            calls.append(lambda dY=dY, W=W, dX=dX: tg.tg_gemm_dgrad(dY, W, dX=dX, ws=ws))
+        else:
+            dW = torch.empty(d_out, d_in, dtype=dtype, device="cuda")
+            calls.append(lambda dY=dY, X=X, dW=dW: tg.tg_gemm_wgrad(dY, X, dW=dW, ws=ws))
+    return Rotating(calls)
 
 
-def attn_call(op, h, s, d, dtype=torch.bfloat16):
-    t = inputs.attn_inputs(h, s, d, dtype, tag="sweep", device="cuda")
+def attn_call(op, h, s, d, dtype=torch.bfloat16, warm=False):
     a, b = inputs.ATTN_OPERANDS[op]
-    C = torch.empty(h, s, s if op in ("qk", "do_vt") else d, dtype=dtype, device="cuda")
+    out_cols = s if op in ("qk", "do_vt") else d
+    elems = {"Q": s * d, "K": s * d, "V": s * d, "dO": s * d, "P": s * s, "dS": s * s}
+    n = cold_sets(h * (elems[a] + elems[b] + s * out_cols) * dtype.itemsize, warm)
     ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
-    return lambda: tg.tg_bmm_attn(op, t[a], t[b], C=C, ws=ws)
+    calls = []
+    for i in range(n):
+        t = inputs.attn_inputs(h, s, d, dtype, tag=f"sweep{i}", device="cuda")
+        C = torch.empty(h, s, out_cols, dtype=dtype, device="cuda")
+        calls.append(lambda t=t, C=C: tg.tg_bmm_attn(op, t[a], t[b], C=C, ws=ws))
+    return Rotating(calls)
 
 
 def time_call(call, stream, reps):
@@ -106,7 +146,7 @@ def time_call(call, stream, reps):
     return statistics.median(res)
 
 
-def candidates(M, N, K, batch, sms):
+def candidates(M, N, K, batch, sms, stream_k=False):
     kb = -(-K // 64)
     for bn in BNS:
         tiles = batch * -(-M // 128) * -(-N // bn)
@@ -135,7 +175,9 @@ def candidates(M, N, K, batch, sms):
                     yield bn, f"c{cs}", raster
         # stream-K: an equal share of tile x K-block iterations per CTA
         # (its partial tiles are 64-column multiples)
-        if bn % 64 == 0 and tiles * kb >= sms and tiles * 4 >= sms:
+        # (offered only on request: its CTAs wait for each other, so a table
+        # entry that selects it needs the GPU to itself)
+        if stream_k and bn % 64 == 0 and tiles * kb >= sms and tiles * 4 >= sms:
             for raster in ("m", "n"):
                 yield bn, "sk", raster
     # CTA pairs: 256-row tiles on two SMs, data-parallel or split
@@ -152,7 +194,7 @@ def candidates(M, N, K, batch, sms):
                     continue
                 for raster in ("m", "n"):
                     yield f"{bn}p", s, raster
-            if tiles * kb >= sms // 2 and tiles * 4 >= sms // 2:
+            if stream_k and tiles * kb >= sms // 2 and tiles * 4 >= sms // 2:
                 for raster in ("m", "n"):
                     yield f"{bn}p", "sk", raster
             # tail split over the pairs' last partial wave
@@ -171,6 +213,9 @@ def main(argv=None):
     ap.add_argument("--budget-s", type=float, default=900.0)
     ap.add_argument("--only", default=None, help="comma-separated layouts or MxNxKxbatch keys to sweep")
     ap.add_argument("-v", "--verbose", action="store_true", help="print every candidate's time")
+    ap.add_argument("--warm", action="store_true", help="time one operand set repeatedly (operands in L2)")
+    ap.add_argument("--stream-k", action="store_true",
+                    help="also offer stream-K plans (their CTAs wait for each other: the GPU must be otherwise idle)")
     args = ap.parse_args(argv)
     sets = set(args.sets.split(","))
     stream = torch.cuda.Stream()
@@ -180,7 +225,7 @@ def main(argv=None):
     lines = []
     tmpdir = tempfile.mkdtemp()
     only = set(args.only.split(",")) if args.only else None
-    for layout, M, N, K, batch, make in shapes(sets):
+    for layout, M, N, K, batch, make in shapes(sets, warm=args.warm):
         if only and layout not in only and f"{M}x{N}x{K}x{batch}" not in only:
             continue
         if time.time() - t0 > args.budget_s:
@@ -188,13 +233,13 @@ def main(argv=None):
             break
         call = make()
         flops = 2 * M * N * K * batch
-        reps = max(3, min(50, int(2e13 / max(flops, 1))))
+        reps = max(3, min(50, int(2e13 / max(flops, 1))), call.sets)
         # the heuristic's own choice, for the record
         tg.tg_load_table(None)
         base_ms = time_call(call, stream, reps)
         base_plan = tg.tg_last_call()
         best = None
-        for bn, s, raster in candidates(M, N, K, batch, sms):
+        for bn, s, raster in candidates(M, N, K, batch, sms, stream_k=args.stream_k):
             path = os.path.join(tmpdir, "one.txt")
             with open(path, "w") as f:
                 f.write(f"{layout} bf16 bf16 {M} {N} {K} {batch} {bn} {s} {raster}\n")
@@ -213,17 +258,19 @@ def main(argv=None):
         tg.tg_load_table(None)
         ms, bn, s, raster = best
         tf = flops / ms / 1e9
+        temp = "warm" if call.sets == 1 and args.warm else f"cold, {call.sets} operand sets"
         print(f"{layout} {M}x{N}x{K}x{batch}: best bn={bn} splits={s} raster={raster} {ms * 1e3:.1f} us "
-              f"{tf:.0f} TFLOP/s (heuristic {base_ms * 1e3:.1f} us: {base_plan})", flush=True)
+              f"{tf:.0f} TFLOP/s ({temp}; heuristic {base_ms * 1e3:.1f} us: {base_plan})", flush=True)
         for din in ("bf16", "f16"):
             for dout in (din, "f32"):
                 lines.append(f"{layout} {din} {dout} {M} {N} {K} {batch} {bn} {s} {raster}"
-                             f"   # {ms * 1e3:.1f} us, {tf:.0f} TFLOP/s")
+                             f"   # {ms * 1e3:.1f} us {'warm' if args.warm else 'cold'}, {tf:.0f} TFLOP/s")
         del call
         torch.cuda.empty_cache()
     os.makedirs(os.path.dirname(args.out), exist_ok=True)
-    if only and os.path.exists(args.out):
-        # a partial sweep updates its entries and keeps every other line
+    if os.path.exists(args.out):
+        # a sweep updates its entries and keeps every other line (shapes of
+        # other sets, or left out by --only)
         swept = {" ".join(l.split()[:7]) for l in lines}
         kept = []
         for l in open(args.out):
@@ -233,8 +280,10 @@ def main(argv=None):
         lines = kept + lines
     with open(args.out, "w") as f:
         f.write("# tile table for the tensor-core kernel: op in out M N K batch bn splits raster\n")
-        f.write(f"# written by `python -m gemms_linear_layers_gb300.sweep --sets {args.sets}` on {name} "
-                f"({sms} SMs); timings are bf16 and apply to fp16 and FP32 outputs too\n")
+        f.write(f"# last written by `python -m gemms_linear_layers_gb300.sweep --sets {args.sets}"
+                f"{' --warm' if args.warm else ''}` on {name} ({sms} SMs), which kept the entries of shapes it did "
+                f"not time; timings are bf16 and apply to fp16 and FP32 outputs too; cold = operand sets rotated "
+                f"beyond 2 x L2\n")
         for l in lines:
             f.write(l + "\n")
     print(f"wrote {len(lines)} entries to {args.out} in {time.time() - t0:.0f} s", flush=True)
