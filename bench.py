@@ -7,10 +7,13 @@ One step = every product of the 2B-class decoder layer set (q, k, v, o
 in fp16 with FP32 accumulation: 126 products, 5.25 TFLOP.  Inputs are seeded
 synthetic tensors resident in HBM (1.95 GB, far above the L2); L2 is also
 flushed (a 256 MiB write) before every step, outside the timed events.  The
-step is one captured CUDA graph of the library calls in training order; CUDA
-events inside it mark the step and bracket every launch of the dominant
-launch class (one kernel identity at one product shape), so `value` and the
-roofline entry come from the same timed replays.
+step is one captured CUDA graph of the library calls in training order, the
+products that a training step may run side by side (the q, k and v
+projections, gate and up, a layer's input and weight gradients) on parallel
+branches; CUDA events inside it mark the step and bracket every launch of
+the dominant launch class (one kernel identity at one product shape), which
+runs alone, so `value` and the roofline entry come from the same timed
+replays (`--serial-step`: one product at a time).
 
 Printed on stdout (rank 0): first one `row {...}` line per measured row of the
 other product sets (the 135M-class step, every distinct 2B-class product
@@ -361,24 +364,33 @@ def step_waves(prods):
     return waves
 
 
+def graph_waves(prods, concurrent=True):
+    """The waves of the step graph: with `concurrent`, the step's waves, a
+    stream-K launch taken out to run alone after the rest of its wave (it
+    waits on its own later CTAs, which need every SM it may occupy); without,
+    one product per wave in training order."""
+    if not concurrent:
+        return [[q] for w in step_waves(prods) for q in w]
+    out = []
+    for w in step_waves(prods):
+        alone = [p for p in w if " sk" in p.kernel]
+        rest = [p for p in w if not any(p is q for q in alone)]
+        if rest:
+            out.append(rest)
+        out += [[p] for p in alone]
+    return out
+
+
 def capture_step(prods, stream, dominant, concurrent=True):
-    """One graph for the whole step.  With `concurrent`, the products of a
-    wave run on parallel branches (fork/join through events on side
+    """One graph for the whole step: the waves of `graph_waves`, the products
+    of a wave on parallel branches (fork/join through events on side
     streams).  External events mark the step's start and end and bracket every
-    launch of the dominant launch class."""
+    launch of the dominant launch class (time it in a serial step: beside
+    other products its bracketed time is not the kernel's)."""
     e0, e1 = external_event(), external_event()
     if e0 is None:
         return None
-    waves = step_waves(prods) if concurrent else [[q] for w in step_waves(prods) for q in w]
-    # a stream-K launch waits on its own later CTAs, which need every SM it
-    # may occupy: it runs alone in its wave
-    split = []
-    for w in waves:
-        split += [[p] for p in w if " sk" in p.kernel]
-        rest = [p for p in w if " sk" not in p.kernel]
-        if rest:
-            split.append(rest)
-    waves = split
+    waves = graph_waves(prods, concurrent)
     width = max(len(w) for w in waves)
     side = [torch.cuda.Stream() for _ in range(width)]
     marks = []
@@ -709,7 +721,7 @@ def step_row(stream, pk, cfg, workload, steps=10):
     prods = build_step("cuda", cfg=cfg)
     capture(prods, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    step = capture_step(prods, stream, None, concurrent=False)
+    step = capture_step(prods, stream, None)
     flops = sum(p.flops for p in prods)
     if step:
         total_ms, _ = timed_steps(step, 3, steps, stream, flush)
@@ -1097,8 +1109,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--per-product-graphs", action="store_true",
                     help="time with one graph per product instead of one graph per step")
-    ap.add_argument("--concurrent-step", action="store_true",
-                    help="one graph per step with the training step's independent products on parallel branches")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="one product at a time in training order (default: the step's independent products on "
+                         "parallel graph branches)")
     ap.add_argument("--only", default=None,
                     help="comma-separated products to run, e.g. gate.fwd.T4096.bfloat16 (profiling a single kernel)")
     ap.add_argument("--rows-out", default=None, help="also write the rows to this JSON file")
@@ -1139,9 +1152,20 @@ def main():
     per_prod = probe_products(prods, stream, flush)
     classes = by_launch_class(prods, per_prod)
     dom_name, dom = max(classes.items(), key=lambda kv: kv[1]["ms"])
-    step = None if args.per_product_graphs else capture_step(prods, stream, dom_name, args.concurrent_step)
-    if step and args.concurrent_step:
-        mode = "one CUDA graph per step, independent products on parallel branches; events bracket the dominant class"
+    # the headline step runs the independent products side by side; the
+    # dominant class is timed in the same step run one product at a time
+    # (beside other products its bracketed time would not be the kernel's)
+    step = dstep = None
+    if not args.per_product_graphs:
+        if args.serial_step:
+            step = dstep = capture_step(prods, stream, dom_name, concurrent=False)
+        else:
+            step = capture_step(prods, stream, None, concurrent=True)
+            dstep = capture_step(prods, stream, dom_name, concurrent=False) if step else None
+    if step and not args.serial_step:
+        mode = ("one CUDA graph per step, independent products (q/k/v, gate/up, a layer's input and weight "
+                "gradients) on parallel branches; the dominant class timed by events around its launches in the "
+                "same step run one product at a time (as many steps again)")
     elif step:
         mode = "one CUDA graph per step, products in training order; events inside it bracket the dominant class"
     else:
@@ -1153,8 +1177,12 @@ def main():
     with ClockSampler(local) as clk:
         if step:
             total_ms, dom_ms = timed_steps(step, args.warmup, args.steps, stream, flush)
+            ser_ms = total_ms
+            if dstep is not step:
+                ser_ms, dom_ms = timed_steps(dstep, args.warmup, args.steps, stream, flush)
         else:
             total_ms, dom_ms = timed_steps_per_product(prods, args.warmup, args.steps, stream, flush, dom_name)
+            ser_ms = total_ms
     torch.cuda.synchronize()
     if world > 1:
         total_ms = max_over_ranks(total_ms, "cuda")
@@ -1175,7 +1203,8 @@ def main():
                 "kernel": dom_name, "launches_per_step": dom["n"],
                 "gflop_per_launch": round(flops_per_launch / 1e9, 3),
                 "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
-                "share_of_step": round(dom_ms / total_ms, 3)}
+                "share_of_step": round(dom_ms / ser_ms, 3),
+                "timed_in_ms_per_step": round(ser_ms / args.steps, 4)}
 
     launches = sum(p.launches for p in prods) * args.steps
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -1202,7 +1231,7 @@ def main():
         classes_ms = {k: round(v["ms"], 4) for k, v in sorted(classes.items(), key=lambda kv: -kv[1]["ms"])}
         print("row " + json.dumps({"set": "probe", "ms_per_step_by_launch_class": classes_ms}), flush=True)
         if not args.no_rows:
-            del prods, step
+            del prods, step, dstep
             torch.cuda.empty_cache()
             rows = measure_rows(stream, pk)
             for r in rows:

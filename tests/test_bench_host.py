@@ -1,5 +1,5 @@
 """Host logic of bench.py (no GPU): the kernel identity taken from a call
-record, the waves of the optional concurrent step, the DRAM traffic taken
+record, the waves of the step graph, the DRAM traffic taken
 from a committed profile, the FP32 peak, and the replicated (N > 1) timing
 over two gloo ranks."""
 import os
@@ -85,6 +85,32 @@ def test_step_waves_of_the_2b_set_keep_token_counts_apart():
     p = prods[0]
     p.kernel = "tc nt bn=256 pair"
     assert p.launch_class == "tc nt bn=256 pair @ 1024x2304x2304"
+
+
+def test_graph_waves_run_stream_k_alone():
+    """The step graph: each wave's products side by side, except stream-K
+    launches, which follow their wave one by one; serial: one product per
+    wave in training order."""
+    prods = []
+    for T in (1024, 4096):
+        for layer, d_in, d_out in workloads.DECODER_2B["layers"]:
+            for op in ("fwd", "dgrad", "wgrad"):
+                p = bench.Product(layer, op, torch.bfloat16, T, d_in, d_out)
+                p.kernel = "tc tn bn=256 pair +tail" if op == "wgrad" else "tc nt bn=256 pair"
+                prods.append(p)
+    prods[-1].kernel = "tc tn bn=256 pair sk"  # down.wgrad.T4096: stream-K
+    waves = bench.graph_waves(prods)
+    flat = [p for w in waves for p in w]
+    assert sorted(map(id, flat)) == sorted(map(id, prods))
+    names = [[p.name for p in w] for w in waves]
+    i = names.index(["down.dgrad.T4096.bfloat16"])
+    assert names[i + 1] == ["down.wgrad.T4096.bfloat16"]
+    assert ["q.dgrad.T4096.bfloat16", "q.wgrad.T4096.bfloat16", "k.dgrad.T4096.bfloat16", "k.wgrad.T4096.bfloat16",
+            "v.dgrad.T4096.bfloat16", "v.wgrad.T4096.bfloat16"] in names
+    assert ["q.fwd.T1024.bfloat16", "k.fwd.T1024.bfloat16", "v.fwd.T1024.bfloat16"] in names
+    serial = bench.graph_waves(prods, concurrent=False)
+    assert all(len(w) == 1 for w in serial) and len(serial) == len(prods)
+    assert [w[0] for w in serial] == [p for w in bench.step_waves(prods) for p in w]
 
 
 def test_launches_and_classes():
