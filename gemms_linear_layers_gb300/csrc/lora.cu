@@ -218,7 +218,7 @@ __device__ __forceinline__ void drain_issued(const uint64_t* full, const int* is
 struct RoleBars {
   uint64_t* full;
   uint64_t* empty;
-  volatile int* flags;  // [0] abort, [1] shared decision, [2] last-contributor
+  volatile int* flags;  // [0] abort, [1] shared decision, [2] last-contributor, [3] last CTA of a column block
   __device__ RoleBars(uint8_t* p)
       : full(reinterpret_cast<uint64_t*>(p)),
         empty(reinterpret_cast<uint64_t*>(p) + LMAX_STAGES),
@@ -491,6 +491,18 @@ struct CrArgs {
   unsigned long long timeout_ns;
   unsigned int* status;
   unsigned long long* trace;
+  unsigned int* cnt;  // pass 2: arrival counters, one per column block (the last CTA of a block adds its
+                      // partials); pass 1 clears cnt_n of them for it
+  int cnt_n;
+};
+
+// What pass 2 of the gradient finishes besides its own column reduction:
+// dB from pass 1's partials (complete when pass 2 starts) and dA from its own.
+struct FinArgs {
+  CrArgs crb;  // pass 1's column reduction
+  void* dB;    // [d_out][16]
+  void* dA;    // [16][d_in]
+  int kind;    // element kind of dA and dB
 };
 
 __host__ __device__ inline long long cr_start(long long c, const CrArgs& a) { return c * a.N / a.G; }
@@ -525,6 +537,73 @@ __device__ __forceinline__ RoleBars cr_bars(const CrArgs& a, int nh, bool up, ui
   return RoleBars(smem + a.stages * cr_stage_bytes(nh, up, a.s2parts == 2));
 }
 
+// Finish of a column reduction: out element (j, r) = sum over the CTAs that
+// worked on column block j / 128, in CTA order, of their partials.
+//   transposed = 0: out is [J][16] (dB);  1: out is [16][J] (dA)
+__device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, int transposed, int jb, int e) {
+  const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
+  const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
+  const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);  // slot of c0; every later one uses slot 0
+  constexpr int CB = 8;  // contributors whose loads are in flight together
+  float v = 0.f;
+  for (int cb = c0; cb <= c1; cb += CB) {
+    float x[CB];
+#pragma unroll
+    for (int q = 0; q < CB; ++q) {
+      const int cc = cb + q;
+      x[q] = cc <= c1 ? __ldcg(a.P + (static_cast<size_t>(cc) * a.max_segs + (cc == c0 ? k0 : 0)) * (CR_CB * LR) + e)
+                      : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < CB; ++q) v += x[q];
+  }
+  v *= a.scale;  // exact for scale 1
+  const int j = jb * CR_CB + (e >> 4), r = e & 15;
+  if (j < a.J) store_out(out, kind, transposed ? static_cast<size_t>(r) * a.J + j : static_cast<size_t>(j) * LR + r, v);
+}
+
+// The same for 8 consecutive elements e0..e0+7 (one output column, ranks
+// 0..7 or 8..15) per thread: two 16-byte loads per contributor, the loads of
+// CB contributors in flight together, and the same order of the sum.
+__device__ __forceinline__ void cr_finish8(const CrArgs& a, void* out, int kind, int transposed, int jb, int e0) {
+  const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
+  const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
+  const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);
+  constexpr int CB = 8;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int cb = c0; cb <= c1; cb += CB) {
+    float4 x[CB][2];
+#pragma unroll
+    for (int q = 0; q < CB; ++q) {
+      const int cc = cb + q;
+      if (cc <= c1) {
+        const float* src = a.P + (static_cast<size_t>(cc) * a.max_segs + (cc == c0 ? k0 : 0)) * (CR_CB * LR) + e0;
+        x[q][0] = __ldcg(reinterpret_cast<const float4*>(src));
+        x[q][1] = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+      } else {
+        x[q][0] = x[q][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < CB; ++q) {
+      v[0] += x[q][0].x;
+      v[1] += x[q][0].y;
+      v[2] += x[q][0].z;
+      v[3] += x[q][0].w;
+      v[4] += x[q][1].x;
+      v[5] += x[q][1].y;
+      v[6] += x[q][1].z;
+      v[7] += x[q][1].w;
+    }
+  }
+  const int j = jb * CR_CB + (e0 >> 4), r0 = e0 & 15;
+  if (j >= a.J) return;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    store_out(out, kind, transposed ? static_cast<size_t>(r0 + k) * a.J + j : static_cast<size_t>(j) * LR + r0 + k,
+              v[k] * a.scale);
+}
+
 template <bool HILO, bool UP>
 __device__ __forceinline__ void colred_init(const CrArgs& a, const CrMaps* m, uint8_t* smem, int tid) {
   if (tid == 0) cr_bars(a, HILO ? 2 : 1, UP, smem).init(a.stages, UP ? 2 * LCW : LCW);
@@ -546,8 +625,15 @@ __host__ __device__ inline int ru_old_bytes(int out_kind) { return LCW * 2 * ru_
 
 // SLO (with UP): S2 is an FP32 factor given as hi + lo 16-bit parts; the lo
 // tile follows the hi one in each stage and the row-up adds its products too.
-template <bool BF16, bool HILO, bool UP, bool ADD = false, bool SLO = false>
-__device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid) {
+//
+// FIN (pass 2 of the gradient): the consumers first add up their share of
+// dB from pass 1's partials; at the end of its part of a column block each
+// CTA counts itself in, and the last of the block's CTAs adds the block's
+// partials (in CTA order, as every other column reduction) into dA.  No CTA
+// waits for another: the last one to arrive does the sum.
+template <bool BF16, bool HILO, bool UP, bool ADD = false, bool SLO = false, bool FIN = false>
+__device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int tid,
+                           const FinArgs* fin = nullptr) {
   constexpr int NH = HILO ? 2 : 1;
   constexpr int SB = 32768 + NH * 4096 + (UP ? 4096 : 0) + (UP && SLO ? 4096 : 0);
   constexpr int HOFF = 32768, S2OFF = 32768 + NH * 4096;
@@ -748,6 +834,12 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
   }
 
   // ------------------------------------------------------ col-red consumers
+  if (FIN) {
+    // this CTA's share of dB (pass 1's partials are complete and visible)
+    const int per = CR_CB * LR, total = fin->crb.nj * per;
+    for (int i = cta * LCW * 32 + tid; i < total; i += a.G * LCW * 32)
+      cr_finish(fin->crb, fin->dB, fin->kind, 0, i / per, i - (i / per) * per);
+  }
   // warp w: columns 16w..16w+15 of the block = chunks 2(w%4), 2(w%4)+1 of IN tile w/4
   float acc[2][4], accl[2][4];  // hi and lo products: two independent chains
 #pragma unroll
@@ -802,34 +894,30 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nb][e] = accl[nb][e] = 0.f;
       ++seg;
+      if (FIN) {
+        const int jb = static_cast<int>(p / a.nsteps);
+        __threadfence();  // this thread's partial, visible device-wide before the CTA counts itself in
+        group_bar(1);     // every consumer warp has stored its columns of the partial
+        if (tid == 0) {
+          int last = 0;
+          if (ok) {
+            const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
+            const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
+            last = atomicAdd(&a.cnt[jb], 1u) == static_cast<unsigned int>(c1 - c0);
+          }
+          rb.flags[3] = last;
+        }
+        group_bar(1);
+        if (rb.flags[3]) {
+          __threadfence();  // the other CTAs' partials, seen after their arrivals
+          static_assert(CR_CB * LR == LCW * 32 * 8, "eight elements of a column block per consumer thread");
+          cr_finish8(a, fin->dA, fin->kind, 1, jb, tid * 8);
+          if (tid == 0) a.cnt[jb] = 0u;  // ready for the next call (pass 1 clears them too)
+        }
+      }
     }
   }
   if (tid == 0) LORA_EVENT(a.trace, 4);
-}
-
-// Finish of a column reduction: out element (j, r) = sum over the CTAs that
-// worked on column block j / 128, in CTA order, of their partials.
-//   transposed = 0: out is [J][16] (dB);  1: out is [16][J] (dA)
-__device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, int transposed, int jb, int e) {
-  const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
-  const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
-  const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);  // slot of c0; every later one uses slot 0
-  constexpr int CB = 8;  // contributors whose loads are in flight together
-  float v = 0.f;
-  for (int cb = c0; cb <= c1; cb += CB) {
-    float x[CB];
-#pragma unroll
-    for (int q = 0; q < CB; ++q) {
-      const int cc = cb + q;
-      x[q] = cc <= c1 ? __ldcg(a.P + (static_cast<size_t>(cc) * a.max_segs + (cc == c0 ? k0 : 0)) * (CR_CB * LR) + e)
-                      : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < CB; ++q) v += x[q];
-  }
-  v *= a.scale;  // exact for scale 1
-  const int j = jb * CR_CB + (e >> 4), r = e & 15;
-  if (j < a.J) store_out(out, kind, transposed ? static_cast<size_t>(r) * a.J + j : static_cast<size_t>(j) * LR + r, v);
 }
 
 // ===================================================================
@@ -1010,6 +1098,9 @@ __global__ void __launch_bounds__(2 * LGROUP, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  // pass 2's arrival counters start at zero (whatever an earlier call left)
+  if (blockIdx.x == 0)
+    for (int i = tid; i < cr.cnt_n; i += blockDim.x) cr.cnt[i] = 0u;
   if (tid < LGROUP) {
     if (static_cast<int>(blockIdx.x) * rd.R < rd.T) rowdown_run<BF16, true, SLO>(blockIdx.x, &rmaps, rd, smem, tid, 1);
   } else {
@@ -1018,11 +1109,12 @@ __global__ void __launch_bounds__(2 * LGROUP, 1)
 }
 
 // Pass 2 over X: each step reads an X tile with its dH hi/lo tiles and the
-// matching columns of A; one warp group accumulates dA^T = X^T dH (partials),
-// the other writes the dX = dH A tile.
+// matching columns of A; one warp group accumulates dA^T = X^T dH (partials,
+// then dA by the last CTA of each column block; first, dB from pass 1's
+// partials), the other writes the dX = dH A tile.
 template <bool BF16, bool ADD, bool SLO>
 __global__ void __launch_bounds__(LGROUP_UP, 1)
-    lora_grad2_kernel(const __grid_constant__ CrMaps cmaps, const CrArgs cr) {
+    lora_grad2_kernel(const __grid_constant__ CrMaps cmaps, const CrArgs cr, const __grid_constant__ FinArgs fin) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = aligned_smem(smem_raw);
   const int tid = threadIdx.x;
@@ -1032,21 +1124,7 @@ __global__ void __launch_bounds__(LGROUP_UP, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  colred_run<BF16, true, true, ADD, SLO>(&cmaps, cr, smem, tid);
-}
-
-// Pass 3: dB and dA from the partials of passes 1 and 2.  CTA b takes
-// 256 elements (one per thread) of one column block; blocks of dB first.
-constexpr int FIN_SPLIT = CR_CB * LR / 256;  // CTAs per column block
-__global__ void __launch_bounds__(256) lora_grad3_kernel(const CrArgs crb, const CrArgs cra, void* dB, void* dA,
-                                                         int kind) {
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.x / FIN_SPLIT, e = (blockIdx.x % FIN_SPLIT) * 256 + threadIdx.x;
-  if (b < crb.nj)
-    cr_finish(crb, dB, kind, 0, b, e);
-  else
-    cr_finish(cra, dA, kind, 1, b - crb.nj, e);
+  colred_run<BF16, true, true, ADD, SLO, true>(&cmaps, cr, smem, tid, &fin);
 }
 
 // ===================================================================
@@ -1287,7 +1365,7 @@ struct GradPlan {
   CrArgs crb;  // pass 1 column reduction (dB)
   CrArgs cra;  // pass 2 column reduction + row-up (dA, dX)
   int g1;
-  size_t dh, hi, lo, pb, pa, total;  // workspace layout
+  size_t dh, hi, lo, pb, pa, cnt, total;  // workspace layout
 };
 static size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -1303,7 +1381,8 @@ static GradPlan grad_plan(int64_t T, int64_t d_in, int64_t d_out, int sms, int o
   g.lo = g.hi + up256(static_cast<size_t>(T) * LR * 2);
   g.pb = g.lo + up256(static_cast<size_t>(T) * LR * 2);
   g.pa = g.pb + up256(static_cast<size_t>(g.crb.G) * g.crb.max_segs * CR_CB * LR * 4);
-  g.total = g.pa + up256(static_cast<size_t>(g.cra.G) * g.cra.max_segs * CR_CB * LR * 4);
+  g.cnt = g.pa + up256(static_cast<size_t>(g.cra.G) * g.cra.max_segs * CR_CB * LR * 4);
+  g.total = g.cnt + up256(static_cast<size_t>(g.cra.nj) * 4);
   return g;
 }
 
@@ -1350,6 +1429,8 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   rd.trace = trace_ptr(0);
   CrArgs& crb = gp.crb;
   crb.P = reinterpret_cast<float*>(base + gp.pb);
+  crb.cnt = reinterpret_cast<unsigned int*>(base + gp.cnt);  // cleared by pass 1 for pass 2
+  crb.cnt_n = gp.cra.nj;
   crb.scale = a.add ? a.scale : 1.f;
   crb.timeout_ns = a.timeout_ns;
   crb.status = a.status;
@@ -1374,6 +1455,7 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   // ---- pass 2: dA partials (col-red over X with dH hi/lo) and dX (row-up of the same tiles)
   CrArgs& cra = gp.cra;
   cra.P = reinterpret_cast<float*>(base + gp.pa);
+  cra.cnt = reinterpret_cast<unsigned int*>(base + gp.cnt);
   cra.out = a.out3;  // dX
   cra.add = a.add;   // dX += scale * dH A
   cra.scale = a.add ? a.scale : 1.f;
@@ -1393,14 +1475,14 @@ cudaError_t lora_grad_launch(const LoraArgs& a) {
   if (a.add) cra.stages = G2_CR_STAGES - (a.out_kind == EK_F32 ? 2 : 1);
   const int smem2 =
       1024 + cr_region_bytes(cra.stages, 2, true, a.w32 != 0) + (a.add ? ru_old_bytes(a.out_kind) : 0);
-  e = launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), smem2, a.stream, cmaps2,
-               cra);
-  if (e != cudaSuccess) return e;
-
-  // ---- pass 3: dB and dA from the partials
-  // dA and dB: FP32 for FP32 factors (the gradients of FP32 weights), else the output type
-  return launch_k(lora_grad3_kernel, dim3((crb.nj + cra.nj) * FIN_SPLIT), dim3(256), 0, a.stream, crb, cra, a.out2,
-                  a.out, a.w32 ? static_cast<int>(EK_F32) : a.out_kind);
+  // and the sums of the partials: dB (pass 1's) and dA (its own), FP32 for
+  // FP32 factors (the gradients of FP32 weights), else the output type
+  FinArgs fin{};
+  fin.crb = crb;
+  fin.dB = a.out2;
+  fin.dA = a.out;
+  fin.kind = a.w32 ? static_cast<int>(EK_F32) : a.out_kind;
+  return launch_k(k2, dim3(cra.G), dim3(LGROUP_UP), smem2, a.stream, cmaps2, cra, fin);
 }
 
 }  // namespace tg

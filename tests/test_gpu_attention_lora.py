@@ -112,6 +112,36 @@ def test_lora_grad_deterministic():
         assert torch.equal(a[k], b[k]), k
 
 
+def test_lora_grad_counters_from_any_workspace_and_in_a_replayed_graph():
+    """The gradient's second pass adds each column block's partials in the
+    CTA that arrives last, counted on per-block counters in the workspace:
+    a workspace full of garbage, and the same call replayed in a CUDA graph,
+    give the same bits as the first call (the first pass clears the
+    counters, the last CTA resets its block's)."""
+    T, d_in, d_out, r = 4096, 2304, 2304, 16
+    t = [x.cuda() for x in inputs.lora_inputs(T, d_in, d_out, r, torch.bfloat16, tag="cnt")]
+    ref = tg.tg_lora_grad(*t, out_dtype=torch.float32)
+    n = tg.tg_workspace_size(tg.TG_OP_LORA_GRAD, T, d_in, d_out, r, torch.bfloat16, torch.float32)
+    ws = torch.full((n,), 0xA5, dtype=torch.uint8, device="cuda")
+    outs = {k: torch.full_like(v, float("nan")) for k, v in ref.items()}
+    got = tg.tg_lora_grad(*t, out_dtype=torch.float32, outs=outs, ws=ws)
+    for k in ref:
+        assert torch.equal(got[k], ref[k]), k
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            tg.tg_lora_grad(*t, out_dtype=torch.float32, outs=outs, ws=ws, stream=s)
+    for _ in range(2):
+        for v in outs.values():
+            v.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(outs[k], ref[k]), k
+    assert tg.tg_stream_status() == 0 and tg.tg_stream_status(s) == 0
+
+
 @pytest.mark.parametrize("out_kind", ["f32", "same"])
 @pytest.mark.parametrize("dtype", DT16)
 @pytest.mark.parametrize("case", [(256, 192, 16, 2.0), (130, 136, 16, -0.5), (4096, 2304, 16, 0.125),
