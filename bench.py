@@ -479,13 +479,15 @@ def by_launch_class(prods, per_prod):
 def e2e_steps(prods, n_steps, stream):
     """The step through the public API with pinned host buffers: every step
     copies its inputs host->device and its outputs device->host.  Copies and
-    products form a pipeline: every X and W come in first, so each forward
-    product starts as soon as its own operands have arrived while the dY
-    tensors follow; each result goes out as soon as the product that writes
-    it is done, on a second copy stream.  Steps do not overlap."""
+    products form a pipeline over the step's (dtype, token count) sets, in
+    step order: a set's X and W come in, then its dY, while the set before it
+    computes; each product starts as soon as its own operands have arrived,
+    and each result goes out on a second copy stream as soon as the product
+    that writes it is done, while later sets come in.  Steps do not overlap."""
     groups = {}
     for p in prods:
         groups.setdefault((p.layer, p.dtype, p.T), []).append(p)
+    sets = list(dict.fromkeys((p.dtype, p.T) for p in prods))
     h2d = d2h = 0
     host = {}
     for key, ps in groups.items():
@@ -507,29 +509,33 @@ def e2e_steps(prods, n_steps, stream):
         s_in.wait_event(a)
         s_out.wait_event(a)
         arrived = {}
-        for names in (("X", "W"), ("dY",)):  # operands in: X and W of every layer, then dY
-            for key in groups:
-                with torch.cuda.stream(s_in):
-                    for n in names:
-                        dev, h = host[(key, n)]
-                        dev.copy_(h, non_blocking=True)
-                        arrived[(key, n)] = torch.cuda.Event()
-                        arrived[(key, n)].record(s_in)
-        for ops in (("fwd",), ("dgrad", "wgrad")):  # forward products first, as their operands arrive
-            for key, ps in groups.items():
-                for p in ps:
-                    if p.op not in ops:
-                        continue
-                    for n in needs[p.op]:
-                        stream.wait_event(arrived[(key, n)])
-                    with torch.cuda.stream(stream):
-                        run_product(p)
-                    done = torch.cuda.Event()
-                    done.record(stream)
-                    s_out.wait_event(done)
-                    with torch.cuda.stream(s_out):  # its result out
-                        dev, h = host[(key, writes[p.op])]
-                        h.copy_(dev, non_blocking=True)
+        for dt, T in sets:  # operands in, set by set: X and W of every layer of the set, then its dY
+            keys = [k for k in groups if k[1] == dt and k[2] == T]
+            for names in (("X", "W"), ("dY",)):
+                for key in keys:
+                    with torch.cuda.stream(s_in):
+                        for n in names:
+                            dev, h = host[(key, n)]
+                            dev.copy_(h, non_blocking=True)
+                            arrived[(key, n)] = torch.cuda.Event()
+                            arrived[(key, n)].record(s_in)
+        for dt, T in sets:  # products set by set, forwards first, as their operands arrive
+            keys = [k for k in groups if k[1] == dt and k[2] == T]
+            for ops in (("fwd",), ("dgrad", "wgrad")):
+                for key in keys:
+                    for p in groups[key]:
+                        if p.op not in ops:
+                            continue
+                        for n in needs[p.op]:
+                            stream.wait_event(arrived[(key, n)])
+                        with torch.cuda.stream(stream):
+                            run_product(p)
+                        done = torch.cuda.Event()
+                        done.record(stream)
+                        s_out.wait_event(done)
+                        with torch.cuda.stream(s_out):  # its result out
+                            dev, h = host[(key, writes[p.op])]
+                            h.copy_(dev, non_blocking=True)
         out_done = torch.cuda.Event()
         out_done.record(s_out)
         stream.wait_event(out_done)
