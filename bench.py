@@ -10,10 +10,11 @@ flushed (a 256 MiB write) before every step, outside the timed events.  The
 step is one captured CUDA graph of the library calls in training order, the
 products that a training step may run side by side (the q, k and v
 projections, gate and up, a layer's input and weight gradients) on parallel
-branches; CUDA events inside it mark the step and bracket every launch of
-the dominant launch class (one kernel identity at one product shape), which
-runs alone, so `value` and the roofline entry come from the same timed
-replays (`--serial-step`: one product at a time).
+branches; CUDA events inside it mark the step (`value`).  The roofline entry
+times the dominant launch class (one kernel identity at one product shape)
+with events around each of its launches in a second timed replay of the
+same step with one product at a time, where the bracket times the kernel
+alone (`--serial-step`: the headline that way too).
 
 Printed on stdout (rank 0): first one `row {...}` line per measured row of the
 other product sets (the 135M-class step, every distinct 2B-class product
