@@ -538,38 +538,17 @@ __device__ __forceinline__ RoleBars cr_bars(const CrArgs& a, int nh, bool up, ui
 }
 
 // Finish of a column reduction: out element (j, r) = sum over the CTAs that
-// worked on column block j / 128, in CTA order, of their partials.
+// worked on column block j / 128, in CTA order, of their partials, times
+// a.scale (exact for scale 1).  One call takes 8 consecutive elements
+// e0..e0+7 of the block (one output column j, ranks 0..7 or 8..15): two
+// 16-byte loads per contributor, the loads of CB contributors in flight
+// together.
 //   transposed = 0: out is [J][16] (dB);  1: out is [16][J] (dA)
-__device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, int transposed, int jb, int e) {
+__device__ __forceinline__ void cr_finish(const CrArgs& a, void* out, int kind, int transposed, int jb, int e0) {
   const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
   const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
   const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);  // slot of c0; every later one uses slot 0
   constexpr int CB = 8;  // contributors whose loads are in flight together
-  float v = 0.f;
-  for (int cb = c0; cb <= c1; cb += CB) {
-    float x[CB];
-#pragma unroll
-    for (int q = 0; q < CB; ++q) {
-      const int cc = cb + q;
-      x[q] = cc <= c1 ? __ldcg(a.P + (static_cast<size_t>(cc) * a.max_segs + (cc == c0 ? k0 : 0)) * (CR_CB * LR) + e)
-                      : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < CB; ++q) v += x[q];
-  }
-  v *= a.scale;  // exact for scale 1
-  const int j = jb * CR_CB + (e >> 4), r = e & 15;
-  if (j < a.J) store_out(out, kind, transposed ? static_cast<size_t>(r) * a.J + j : static_cast<size_t>(j) * LR + r, v);
-}
-
-// The same for 8 consecutive elements e0..e0+7 (one output column, ranks
-// 0..7 or 8..15) per thread: two 16-byte loads per contributor, the loads of
-// CB contributors in flight together, and the same order of the sum.
-__device__ __forceinline__ void cr_finish8(const CrArgs& a, void* out, int kind, int transposed, int jb, int e0) {
-  const int c0 = cr_cta_of(static_cast<long long>(jb) * a.nsteps, a);
-  const int c1 = cr_cta_of(static_cast<long long>(jb + 1) * a.nsteps - 1, a);
-  const int k0 = jb - static_cast<int>(cr_start(c0, a) / a.nsteps);
-  constexpr int CB = 8;
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int cb = c0; cb <= c1; cb += CB) {
     float4 x[CB][2];
@@ -835,10 +814,11 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
 
   // ------------------------------------------------------ col-red consumers
   if (FIN) {
-    // this CTA's share of dB (pass 1's partials are complete and visible)
-    const int per = CR_CB * LR, total = fin->crb.nj * per;
+    // this CTA's share of dB (pass 1's partials are complete and visible),
+    // eight elements of a column block per task
+    const int per = CR_CB * LR / 8, total = fin->crb.nj * per;
     for (int i = cta * LCW * 32 + tid; i < total; i += a.G * LCW * 32)
-      cr_finish(fin->crb, fin->dB, fin->kind, 0, i / per, i - (i / per) * per);
+      cr_finish(fin->crb, fin->dB, fin->kind, 0, i / per, (i - (i / per) * per) * 8);
   }
   // warp w: columns 16w..16w+15 of the block = chunks 2(w%4), 2(w%4)+1 of IN tile w/4
   float acc[2][4], accl[2][4];  // hi and lo products: two independent chains
@@ -911,7 +891,7 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         if (rb.flags[3]) {
           __threadfence();  // the other CTAs' partials, seen after their arrivals
           static_assert(CR_CB * LR == LCW * 32 * 8, "eight elements of a column block per consumer thread");
-          cr_finish8(a, fin->dA, fin->kind, 1, jb, tid * 8);
+          cr_finish(a, fin->dA, fin->kind, 1, jb, tid * 8);
           if (tid == 0) a.cnt[jb] = 0u;  // ready for the next call (pass 1 clears them too)
         }
       }
