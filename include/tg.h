@@ -219,7 +219,10 @@ tg_status tg_lora_up_add(const void* H, const void* B, void* Y, int64_t T, int64
  *   dB[d_out, r] = dY^T . H
  *   dA[r, d_in]  = dH^T . X        (uses the FP32 dH)
  *   dX[T, d_in]  = dH . A          (uses the FP32 dH)
- * X, A, B, H, dY have type `in`; dA, dB, dX have type `out`; dH_f32 is float. */
+ * X, A, B, H, dY have type `in`; dA, dB, dX have type `out`; dH_f32 is float.
+ * The sums over tokens are FP32 partials added in a fixed order, so results
+ * are bitwise reproducible; `ws` may hold anything on entry (the call clears
+ * the counters it keeps there). */
 tg_status tg_lora_grad(const void* X, const void* A, const void* B, const void* H, const void* dY,
                        void* dA, void* dB, void* dX, float* dH_f32, int64_t T, int64_t d_in,
                        int64_t d_out, int64_t r, tg_dtype in, tg_dtype out, void* ws,
