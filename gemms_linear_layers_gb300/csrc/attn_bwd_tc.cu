@@ -313,9 +313,11 @@ __global__ void __launch_bounds__(THREADS, BwdCfg<MODE>::MIN_BLOCKS)
       } else {
         const float* slse = reinterpret_cast<const float*>(sY + (j % BSTAGES) * Cfg::STAGE + 2 * TILE);
         const float* sdd = slse + BT;
-        // pass A: P (DKDV: over S) and dS (over dP) in FP32, with their largest magnitudes
+        // pass A: P (DKDV: over S, in FP32 back to its columns) and dS (this
+        // thread's 64 values kept in registers), with their largest magnitudes
         float mp = 0.f, mds = 0.f;
-#pragma unroll 1
+        float dv[64];
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32], g[32];
           tmem_ld_32x32b_x32(cS + c * 32, r);
@@ -334,10 +336,9 @@ __global__ void __launch_bounds__(THREADS, BwdCfg<MODE>::MIN_BLOCKS)
             mp = fmaxf(mp, p);
             mds = fmaxf(mds, fabsf(dsv));
             r[e] = __float_as_uint(p);
-            g[e] = __float_as_uint(dsv);
+            dv[c * 32 + e] = dsv;
           }
           if (MODE == DKDV) tmem_st_32x32b_x32(cS + c * 32, r);
-          tmem_st_32x32b_x32(cP + c * 32, g);
         }
         // the rows' exponents: lowered when this block's largest value would
         // reach 2^14 at the current one, the accumulator rescaled with it
@@ -358,21 +359,26 @@ __global__ void __launch_bounds__(THREADS, BwdCfg<MODE>::MIN_BLOCKS)
         // DKDV: dV [256, 320), dK [320, 384); DQ: dQ [256, 320)
         if (__any_sync(0xffffffffu, fs != 1.f)) rescale32(t_row + T_ACC + (MODE == DKDV ? 64 : 0) + half * 32, fs);
         if (MODE == DKDV && __any_sync(0xffffffffu, fp != 1.f)) rescale32(t_row + T_ACC + half * 32, fp);
-        // pass B: v 2^sigma as hi + lo over the same columns
+        // pass B: v 2^sigma as hi + lo, written over the block's S and dP columns
         const float ss = sigma == NO_SIGMA ? 1.f : pow2i(sigma);
         const float sp = sigma_p == NO_SIGMA ? 1.f : pow2i(sigma_p);
-        tmem_st_wait();
-#pragma unroll 1
+        if (MODE == DKDV) tmem_st_wait();  // P's FP32 stores, read back below
+#pragma unroll
         for (int c = 0; c < (MODE == DKDV ? 4 : 2); ++c) {
           const bool isp = MODE == DKDV && c >= 2;  // DKDV: dS chunks, then P chunks
           const uint32_t col = (isp ? cS : cP) + (c & 1) * 32;
           const float sc = isp ? sp : ss;
-          uint32_t g[32];
-          tmem_ld_32x32b_x32(col, g);
-          tmem_ld_wait();
           float v[32];
+          if (isp) {
+            uint32_t g[32];
+            tmem_ld_32x32b_x32(col, g);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(g[e]) * sc;
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(g[e]) * sc;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = dv[(c & 1) * 32 + e] * sc;
+          }
           uint32_t w[32];
           split32<BF16>(v, w);
           tmem_st_32x32b_x32(col, w);
