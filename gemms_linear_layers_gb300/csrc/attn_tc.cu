@@ -207,18 +207,18 @@ __global__ void __launch_bounds__(THREADS, 2)
       const int kvalid = min(BT, a.s - j * BT) - half * 64;  // keys of this warp's half inside the sequence
       // pass 1: the largest (or smallest, for a negative scale) score of the row's half block
       float vm = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + T_S + half * 64 + c * 32, r);
+      {
+        uint32_t r[64];  // both 32-column chunks in flight together
+        tmem_ld_32x32b_x32(t_row + T_S + half * 64, r);
+        tmem_ld_32x32b_x32(t_row + T_S + half * 64 + 32, r + 32);
         tmem_ld_wait();
         if (kvalid >= 64) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) vm = fmaxf(vm, neg ? -__uint_as_float(r[e]) : __uint_as_float(r[e]));
+          for (int e = 0; e < 64; ++e) vm = fmaxf(vm, neg ? -__uint_as_float(r[e]) : __uint_as_float(r[e]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < kvalid) vm = fmaxf(vm, neg ? -__uint_as_float(r[e]) : __uint_as_float(r[e]));
+          for (int e = 0; e < 64; ++e)
+            if (e < kvalid) vm = fmaxf(vm, neg ? -__uint_as_float(r[e]) : __uint_as_float(r[e]));
         }
       }
       vm = fmaxf(vm, pair_exchange(xch, j & 1, q, half, lane, vm));
@@ -232,18 +232,20 @@ __global__ void __launch_bounds__(THREADS, 2)
       const float mc = m_used - CP;
       // pass 2: P = 2^(x - m + C) as hi + lo 16-bit pairs over the same columns
       float sum = 0.f;
-#pragma unroll 1
+      uint32_t r[64];  // both chunks in flight together again
+      tmem_ld_32x32b_x32(t_row + T_S + half * 64, r);
+      tmem_ld_32x32b_x32(t_row + T_S + half * 64 + 32, r + 32);
+      tmem_ld_wait();
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + T_S + half * 64 + c * 32, r);
-        tmem_ld_wait();
         float p[32];
         if (kvalid >= 64) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) p[e] = ex2(fmaf(__uint_as_float(r[e]), sl, -mc));
+          for (int e = 0; e < 32; ++e) p[e] = ex2(fmaf(__uint_as_float(r[c * 32 + e]), sl, -mc));
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) p[e] = c * 32 + e < kvalid ? ex2(fmaf(__uint_as_float(r[e]), sl, -mc)) : 0.f;
+          for (int e = 0; e < 32; ++e)
+            p[e] = c * 32 + e < kvalid ? ex2(fmaf(__uint_as_float(r[c * 32 + e]), sl, -mc)) : 0.f;
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) sum += p[e];
