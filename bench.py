@@ -10,11 +10,11 @@ flushed (a 256 MiB write) before every step, outside the timed events.  The
 step is one captured CUDA graph of the library calls in training order, the
 products that a training step may run side by side (the q, k and v
 projections, gate and up, a layer's input and weight gradients) on parallel
-branches; CUDA events inside it mark the step (`value`).  The roofline entry
-times the dominant launch class (one kernel identity at one product shape)
-with events around each of its launches in a second timed replay of the
-same step with one product at a time, where the bracket times the kernel
-alone (`--serial-step`: the headline that way too).
+branches (`--serial-step`: one product at a time); CUDA events inside it
+mark the step (`value`).  The roofline entry times the dominant launch class
+(one kernel identity at one product shape): its launches of the step, with
+the same tensors and plans, replayed back to back in a graph of their own
+(L2 flushed before each replay), events around each replay.
 
 Printed on stdout (rank 0): first one `row {...}` line per measured row of the
 other product sets (the 135M-class step, every distinct 2B-class product
@@ -382,19 +382,16 @@ def graph_waves(prods, concurrent=True):
     return out
 
 
-def capture_step(prods, stream, dominant, concurrent=True):
+def capture_step(prods, stream, concurrent=True):
     """One graph for the whole step: the waves of `graph_waves`, the products
     of a wave on parallel branches (fork/join through events on side
-    streams).  External events mark the step's start and end and bracket every
-    launch of the dominant launch class (time it in a serial step: beside
-    other products its bracketed time is not the kernel's)."""
+    streams).  External events mark the step's start and end."""
     e0, e1 = external_event(), external_event()
     if e0 is None:
         return None
     waves = graph_waves(prods, concurrent)
     width = max(len(w) for w in waves)
     side = [torch.cuda.Stream() for _ in range(width)]
-    marks = []
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         e0.record()
@@ -410,14 +407,7 @@ def capture_step(prods, stream, dominant, concurrent=True):
                     branches.append((side[i], p))
             for st, p in branches:
                 with torch.cuda.stream(st):
-                    if dominant is not None and p.launch_class == dominant:
-                        a, b = external_event(), external_event()
-                        a.record(st)
-                        run_product(p)
-                        b.record(st)
-                        marks.append((p, a, b))
-                    else:
-                        run_product(p)
+                    run_product(p)
             if len(w) > 1:
                 for st, _ in branches:
                     j = torch.cuda.Event()
@@ -425,13 +415,14 @@ def capture_step(prods, stream, dominant, concurrent=True):
                     stream.wait_event(j)
         e1.record()
     torch.cuda.synchronize()
-    return g, e0, e1, marks
+    return g, e0, e1
 
 
 def timed_steps(step, n_warm, n_steps, stream, flush):
-    """Per step: flush L2 (untimed), replay the step graph, read its events."""
-    g, e0, e1, marks = step
-    total_ms, dom_ms = 0.0, 0.0
+    """Per step: flush L2 (untimed), replay the step graph, read its events;
+    the total ms of the timed steps."""
+    g, e0, e1 = step
+    total_ms = 0.0
     for s in range(n_warm + n_steps):
         with torch.cuda.stream(stream):
             flush.add_(1)
@@ -439,8 +430,43 @@ def timed_steps(step, n_warm, n_steps, stream, flush):
         torch.cuda.synchronize()
         if s >= n_warm:
             total_ms += e0.elapsed_time(e1)
-            dom_ms += sum(a.elapsed_time(b) for _, a, b in marks)
-    return total_ms, dom_ms
+    return total_ms
+
+
+def capture_dominant(dprods, stream, rounds=3):
+    """One graph of the dominant launch class's products of the step (same
+    tensors, workspaces and plans as in the step), `rounds` passes back to
+    back between two events: inside a graph, events around each launch would
+    cut it off from the launch before it (measured: 37.6 us bracketed against
+    32.0 us per launch back to back for the 4,096-token q/k/v/o weight
+    gradient), so the class is timed as a run of its own launches."""
+    e0, e1 = external_event(), external_event()
+    if e0 is None:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        e0.record()
+        for _ in range(rounds):
+            for p in dprods:
+                run_product(p)
+        e1.record()
+    torch.cuda.synchronize()
+    return g, e0, e1, rounds * len(dprods)
+
+
+def timed_dominant(dg, n_warm, n_steps, stream, flush):
+    """Per replay: flush L2 (untimed), replay the dominant-class graph; the
+    average ms per launch of the class."""
+    g, e0, e1, n = dg
+    total = 0.0
+    for s in range(n_warm + n_steps):
+        with torch.cuda.stream(stream):
+            flush.add_(1)
+            g.replay()
+        torch.cuda.synchronize()
+        if s >= n_warm:
+            total += e0.elapsed_time(e1)
+    return total / (n_steps * n)
 
 
 def timed_steps_per_product(prods, n_warm, n_steps, stream, flush, dominant):
@@ -728,10 +754,10 @@ def step_row(stream, pk, cfg, workload, steps=10):
     prods = build_step("cuda", cfg=cfg)
     capture(prods, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    step = capture_step(prods, stream, None)
+    step = capture_step(prods, stream)
     flops = sum(p.flops for p in prods)
     if step:
-        total_ms, _ = timed_steps(step, 3, steps, stream, flush)
+        total_ms = timed_steps(step, 3, steps, stream, flush)
     else:
         total_ms, _ = timed_steps_per_product(prods, 3, steps, stream, flush, None)
     tf = flops * steps / (total_ms / 1e3) / 1e12
@@ -1159,22 +1185,20 @@ def main():
     per_prod = probe_products(prods, stream, flush)
     classes = by_launch_class(prods, per_prod)
     dom_name, dom = max(classes.items(), key=lambda kv: kv[1]["ms"])
-    # the headline step runs the independent products side by side; the
-    # dominant class is timed in the same step run one product at a time
-    # (beside other products its bracketed time would not be the kernel's)
-    step = dstep = None
+    # the headline step (the independent products side by side unless
+    # --serial-step); the dominant class timed as a run of its own launches
+    step = dg = None
     if not args.per_product_graphs:
-        if args.serial_step:
-            step = dstep = capture_step(prods, stream, dom_name, concurrent=False)
-        else:
-            step = capture_step(prods, stream, None, concurrent=True)
-            dstep = capture_step(prods, stream, dom_name, concurrent=False) if step else None
+        step = capture_step(prods, stream, concurrent=not args.serial_step)
+        if step:
+            dg = capture_dominant([p for p in prods if p.launch_class == dom_name], stream)
     if step and not args.serial_step:
         mode = ("one CUDA graph per step, independent products (q/k/v, gate/up, a layer's input and weight "
-                "gradients) on parallel branches; the dominant class timed by events around its launches in the "
-                "same step run one product at a time (as many steps again)")
+                "gradients) on parallel branches; the dominant class's launches of the step replayed back to "
+                "back (3 rounds per replay, L2 flushed before each), events around each replay")
     elif step:
-        mode = "one CUDA graph per step, products in training order; events inside it bracket the dominant class"
+        mode = ("one CUDA graph per step, products in training order; the dominant class's launches of the step "
+                "replayed back to back (3 rounds per replay, L2 flushed before each), events around each replay")
     else:
         mode = "one CUDA graph per product; events between them on the launching stream"
 
@@ -1183,13 +1207,11 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         if step:
-            total_ms, dom_ms = timed_steps(step, args.warmup, args.steps, stream, flush)
-            ser_ms = total_ms
-            if dstep is not step:
-                ser_ms, dom_ms = timed_steps(dstep, args.warmup, args.steps, stream, flush)
+            total_ms = timed_steps(step, args.warmup, args.steps, stream, flush)
+            avg_launch_ms = timed_dominant(dg, args.warmup, args.steps, stream, flush)
         else:
             total_ms, dom_ms = timed_steps_per_product(prods, args.warmup, args.steps, stream, flush, dom_name)
-            ser_ms = total_ms
+            avg_launch_ms = dom_ms / (dom["n"] * args.steps)
     torch.cuda.synchronize()
     if world > 1:
         total_ms = max_over_ranks(total_ms, "cuda")
@@ -1201,8 +1223,6 @@ def main():
     ms_step = total_ms / args.steps
     value = job_tflops(world, step_flops, args.steps, total_ms)
 
-    dom_launches = dom["n"] * args.steps
-    avg_launch_ms = dom_ms / dom_launches
     flops_per_launch = dom["flops"] / dom["n"]
     achieved = flops_per_launch / (avg_launch_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
@@ -1210,10 +1230,13 @@ def main():
                 "kernel": dom_name, "launches_per_step": dom["n"],
                 "gflop_per_launch": round(flops_per_launch / 1e9, 3),
                 "peak_source": f"{pk['source']} bf16 burst (fp16 same nominal rate)",
-                "share_of_step": round(dom_ms / ser_ms, 3),
-                "timed_in_ms_per_step": round(ser_ms / args.steps, 4)}
+                "ms_per_launch": round(avg_launch_ms, 5),
+                "share_of_step": round(avg_launch_ms * dom["n"] / ms_step, 3)}
 
-    launches = sum(p.launches for p in prods) * args.steps
+    launches = sum(p.launches for p in prods) * args.steps  # the step's timed region
+    if dg is not None:  # and the dominant class's
+        launches += dg[3] // len([p for p in prods if p.launch_class == dom_name]) * args.steps * sum(
+            p.launches for p in prods if p.launch_class == dom_name)
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
@@ -1238,7 +1261,7 @@ def main():
         classes_ms = {k: round(v["ms"], 4) for k, v in sorted(classes.items(), key=lambda kv: -kv[1]["ms"])}
         print("row " + json.dumps({"set": "probe", "ms_per_step_by_launch_class": classes_ms}), flush=True)
         if not args.no_rows:
-            del prods, step, dstep
+            del prods, step, dg
             torch.cuda.empty_cache()
             rows = measure_rows(stream, pk)
             for r in rows:
