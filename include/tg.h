@@ -295,13 +295,13 @@ tg_status tg_attn_fwd(const void* Q, const void* K, const void* V, void* O, int6
  * Q, K, V, dO are [heads, s, d] of type `in` (bf16 or fp16); dQ, dK, dV are
  * [heads, s, d] of type `out` (FP32 or `in`), overwritten.  d must be 64;
  * every pointer 16-byte aligned (TG_ERR_MISALIGNED otherwise); scale finite.
- * No mask.  The [s, s] matrices never reach memory: three launches on the
- * tensor cores recompute them per 128 x 128 block (row statistics, then dK
- * and dV per key block, then dQ per query block); P and dS enter the
+ * No mask.  The [s, s] matrices never reach memory: two launches on the
+ * tensor cores recompute them per 128 x 64 block (per query tile the row
+ * statistics, then dQ; per key tile dK and dV); P and dS enter the
  * products as 16-bit hi + lo parts, each scaled by a power of two that is
  * taken off in FP32, so fp16 neither overflows nor loses small values.
  * Workspace: tg_workspace_size(TG_OP_ATTN_BWD, heads, s, d, 0, in, out)
- * bytes (three FP32 values per row), 16-byte aligned.  Results are bitwise
+ * bytes (two FP32 values per row, s rounded up to 128), 16-byte aligned.  Results are bitwise
  * reproducible run to run (no atomics). */
 tg_status tg_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK, void* dV,
                       int64_t heads, int64_t s, int64_t d, float scale, tg_dtype in, tg_dtype out, void* ws,
