@@ -1,8 +1,8 @@
 // attn_common.cuh -- pieces shared by the fused attention kernels (forward
 // attn_tc.cu, backward attn_bwd_tc.cu): the tensor-memory A-operand MMA, a
-// bulk copy, the base-2 exponential, the hi + lo 16-bit split and the
-// exchange of per-row values between the two warps that share a TMEM lane
-// quadrant.
+// bulk copy, the base-2 exponential, the hi + lo 16-bit split, the rescale
+// of accumulator columns, and (forward) the exchange of per-row values
+// between the two warps that share a TMEM lane quadrant.
 //
 // Every tcgen05.ld / tcgen05.st is a warp-collective (.sync.aligned)
 // instruction: the row code around them keeps whole warps together and
@@ -80,13 +80,6 @@ __device__ __forceinline__ void split32(const float* v, uint32_t* w) {
 // value per row: each writes its own, both wait on the pair's named barrier
 // (ids 1..4), each reads the other's.  buf: [2 slots][4 quadrants][2 halves][32].
 __device__ __forceinline__ float pair_exchange(float* buf, int slot, int q, int half, int lane, float v) {
-  buf[((slot * 4 + q) * 2 + half) * 32 + lane] = v;
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
-  return buf[((slot * 4 + q) * 2 + (half ^ 1)) * 32 + lane];
-}
-
-// The same for two values per row at once: buf [2 slots][4][2][32] float2.
-__device__ __forceinline__ float2 pair_exchange2(float2* buf, int slot, int q, int half, int lane, float2 v) {
   buf[((slot * 4 + q) * 2 + half) * 32 + lane] = v;
   asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
   return buf[((slot * 4 + q) * 2 + (half ^ 1)) * 32 + lane];
