@@ -1129,6 +1129,28 @@ def probe_main(argv=None):
 
 
 # ------------------------------------------------------------------ main
+MODE_CONCURRENT = ("one CUDA graph per step, independent products on parallel branches; dominant class: its "
+                   "launches replayed back to back, 3 rounds per replay, L2 flushed per replay")
+MODE_SERIAL = ("one CUDA graph per step, products in training order; dominant class: its launches replayed "
+               "back to back, 3 rounds per replay, L2 flushed per replay")
+MODE_PER_PRODUCT = "one CUDA graph per product; events between them on the launching stream"
+
+
+def headline(value, ms_step, world, steps, warmup, workload, token_counts, products, table, step_flops, resident,
+             mode, roofline, launches, clocks):
+    """The headline JSON object (e2e, cpu_baseline and bars are added to it
+    afterwards); printed as the last stdout line, kept under 2 KB."""
+    return {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": workload, "T": token_counts, "products_per_step": products, "tile_table": table,
+                       "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
+                       "l2": f"step inputs {resident / 1e9:.2f} GB resident in HBM; L2 flushed before every step "
+                             "(256 MiB write, untimed)",
+                       "timing": mode},
+            "roofline": roofline, "gpu_launches": launches, "clocks": clocks}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1192,15 +1214,7 @@ def main():
         step = capture_step(prods, stream, concurrent=not args.serial_step)
         if step:
             dg = capture_dominant([p for p in prods if p.launch_class == dom_name], stream)
-    if step and not args.serial_step:
-        mode = ("one CUDA graph per step, independent products (q/k/v, gate/up, a layer's input and weight "
-                "gradients) on parallel branches; the dominant class's launches of the step replayed back to "
-                "back (3 rounds per replay, L2 flushed before each), events around each replay")
-    elif step:
-        mode = ("one CUDA graph per step, products in training order; the dominant class's launches of the step "
-                "replayed back to back (3 rounds per replay, L2 flushed before each), events around each replay")
-    else:
-        mode = "one CUDA graph per product; events between them on the launching stream"
+    mode = (MODE_PER_PRODUCT if not step else MODE_SERIAL if args.serial_step else MODE_CONCURRENT)
 
     if world > 1:
         torch.distributed.barrier()
@@ -1237,17 +1251,10 @@ def main():
     if dg is not None:  # and the dominant class's
         launches += dg[3] // len([p for p in prods if p.launch_class == dom_name]) * args.steps * sum(
             p.launches for p in prods if p.launch_class == dom_name)
-    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16,fp16 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": workload if not only else f"{workload}; only {sorted(only)}",
-                       "T": list(step_token_counts(cfg)), "products_per_step": len(prods),
-                       "tile_table": os.path.relpath(table, ROOT) if table else None,
-                       "gflop_per_step": round(step_flops / 1e9, 2), "parallelism": f"replicas x{world}",
-                       "l2": f"step inputs {resident / 1e9:.2f} GB resident in HBM; L2 flushed before every step "
-                             "(256 MiB write, untimed)",
-                       "timing": mode},
-            "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary()}
+    line = headline(value, ms_step, world, args.steps, args.warmup,
+                    workload if not only else f"{workload}; only {sorted(only)}", list(step_token_counts(cfg)),
+                    len(prods), os.path.relpath(table, ROOT) if table else None, step_flops, resident, mode,
+                    roofline, launches, clk.summary())
 
     if rank == 0:
         if not args.no_e2e:

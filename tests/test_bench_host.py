@@ -192,3 +192,29 @@ def test_replicas_time_is_the_slowest_rank_over_gloo(tmp_path):
     assert bench.max_over_ranks(3.0, "cpu") == 3.0  # no process group: the rank's own time
     # 2 replicas x 10 steps x 1e12 flop in 4 s
     assert abs(bench.job_tflops(2, 1e12, 10, 4000.0) - 5.0) < 1e-12
+
+
+def test_headline_line_stays_compact():
+    """The last stdout line carries every key the contract asks for and stays
+    under 2 KB even with the longest strings the bench can put in it."""
+    import json
+    roofline = {"bound": "tensor", "achieved": 1295.7, "peak": 1908.0, "unit": "TFLOP/s", "frac": 0.6791,
+                "traffic": 48533248, "kernel": "tc tn bn=256 pair +tail @ 2304x2304x4096", "launches_per_step": 8,
+                "gflop_per_launch": 43.487, "peak_source": "measured bf16 burst (fp16 same nominal rate)",
+                "ms_per_launch": 0.03366, "share_of_step": 0.074}
+    workload = bench.STEP_SETS["2b"][1]
+    for mode in (bench.MODE_CONCURRENT, bench.MODE_SERIAL, bench.MODE_PER_PRODUCT):
+        line = bench.headline(1437.53, 3.6528, 1, 20, 5, workload, [1024, 2048, 4096], 126,
+                              "gemms_linear_layers_gb300/tables/gb300.txt", 5.251e12, 1.954e9, mode, roofline, 4040,
+                              {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 4})
+        line["e2e"] = {"value": 402.94, "unit": "TFLOP/s", "h2d_bytes_per_step": 1954676736,
+                       "d2h_bytes_per_step": 1954676736, "ms_per_step": 13.032}
+        line["cpu_baseline"] = {"value": 0.006108, "unit": "TFLOP/s", "cores": 16, "kind": "oracle",
+                                "sample": "first 32 output row(s) of each of the 126 products (32.43 GMAC), fp64 "
+                                          "naive loops, 10.6 s"}
+        line["bars"] = {"min_tensor_frac_T2048_4096": 0.519, "min_wgrad_over_fwd": 0.752, "min_lora_hbm_frac": 0.304}
+        text = json.dumps(line)
+        assert len(text) < 2000, len(text)
+        for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                  "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks"):
+            assert k in line, k
