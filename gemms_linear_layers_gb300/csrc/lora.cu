@@ -809,16 +809,19 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
       }
     }
     if (ADD) cp_async_wait_all();  // no copy outlives the kernel (a step given up after a failed wait)
+    if (w == 0 && lane == 0) LORA_EVENT(a.trace, 9);
     return;
   }
 
   // ------------------------------------------------------ col-red consumers
   if (FIN) {
     // this CTA's share of dB (pass 1's partials are complete and visible),
-    // eight elements of a column block per task
+    // eight elements of a column block per task, dealt out across the CTAs
+    // (task i to CTA i % G) so that no CTA starts its own steps late
     const int per = CR_CB * LR / 8, total = fin->crb.nj * per;
-    for (int i = cta * LCW * 32 + tid; i < total; i += a.G * LCW * 32)
+    for (int i = tid * a.G + cta; i < total; i += a.G * LCW * 32)
       cr_finish(fin->crb, fin->dB, fin->kind, 0, i / per, (i - (i / per) * per) * 8);
+    if (tid == 0) LORA_EVENT(a.trace, 6);
   }
   // warp w: columns 16w..16w+15 of the block = chunks 2(w%4), 2(w%4)+1 of IN tile w/4
   float acc[2][4], accl[2][4];  // hi and lo products: two independent chains
@@ -891,8 +894,10 @@ __device__ void colred_run(const CrMaps* mp, const CrArgs& a, uint8_t* smem, int
         if (rb.flags[3]) {
           __threadfence();  // the other CTAs' partials, seen after their arrivals
           static_assert(CR_CB * LR == LCW * 32 * 8, "eight elements of a column block per consumer thread");
+          if (tid == 0) LORA_EVENT(a.trace, 7);
           cr_finish(a, fin->dA, fin->kind, 1, jb, tid * 8);
           if (tid == 0) a.cnt[jb] = 0u;  // ready for the next call (pass 1 clears them too)
+          if (tid == 0) LORA_EVENT(a.trace, 8);
         }
       }
     }
@@ -1210,7 +1215,10 @@ static CrArgs cr_plan(int64_t T, int64_t J, int G, int stages) {
   c.nj = static_cast<int>((J + CR_CB - 1) / CR_CB);
   c.nsteps = static_cast<int>((T + CR_RS - 1) / CR_RS);
   c.N = static_cast<long long>(c.nj) * c.nsteps;
-  c.G = static_cast<int>(G < c.N ? G : c.N);
+  // the fewest CTAs with the same largest share as G of them: ranges of equal
+  // length, so fewer CTAs share a column block (their partials are summed)
+  const long long per = (c.N > 0 && G > 0) ? (c.N + G - 1) / G : 1;
+  c.G = static_cast<int>((c.N + per - 1) / per);
   c.stages = stages;
   c.scale = 1.f;
   c.max_segs = 1;
