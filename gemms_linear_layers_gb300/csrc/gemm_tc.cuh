@@ -555,6 +555,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
+      const int row = q * 32 + lane;  // row of the tile this thread holds
       if (!c.owner) {
         // ---- stream-K contributor: FP32 partial tile to this CTA's slot, then publish
         sk_put_part<BN>(args, blockIdx.x, q, lane, t_row, [&] { mbar_arrive(smem_u32(&tempty[acc])); });
