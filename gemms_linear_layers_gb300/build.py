@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtg.so")
 
 SOURCES = ["api.cu", "gemm_tc_nt.cu", "gemm_tc_nn.cu", "gemm_tc_tn.cu", "gemm_simt.cu", "gemm_ffma.cu", "lora.cu", "lora_block.cu",
-           "attn_tc.cu", "attn_bwd_tc.cu", "noalloc.cu", "tmap.cpp"]
+           "attn_tc.cu", "attn_bwd_tc.cu", "noalloc.cu", "tmap.cpp", "smem_attr.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC,-O2",
          f"-I{INCLUDE}", f"-I{CSRC}"]

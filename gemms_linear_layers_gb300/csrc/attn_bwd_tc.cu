@@ -34,6 +34,7 @@
 // precision).  The powers of two come off in FP32 at the end.
 #include "attn.h"
 #include "attn_common.cuh"
+#include "smem_attr.h"
 
 namespace tg {
 namespace {
@@ -443,12 +444,8 @@ template <int MODE, bool BF16>
 cudaError_t launch_mode2(const CUtensorMap& x0, const CUtensorMap& x1, const CUtensorMap& y0, const CUtensorMap& y1,
                          const BwdArgs& a, int heads, cudaStream_t stream) {
   auto kern = attn_bwd2_kernel<MODE, BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Bwd2Cfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), Bwd2Cfg::SMEM);
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.nblk), static_cast<unsigned>(heads));
   return launch_k(kern, grid, dim3(THREADS2), Bwd2Cfg::SMEM, stream, x0, x1, y0, y1, a);
 }

@@ -30,6 +30,7 @@
 // every weight above 2^-10 of the row's largest (the scale cancels in O / l).
 #include "attn.h"
 #include "attn_common.cuh"
+#include "smem_attr.h"
 
 namespace tg {
 namespace {
@@ -312,12 +313,8 @@ cudaError_t attn_fwd_tc_launch(const void* Q, const void* K, const void* V, void
   a.timeout_ns = timeout_ns;
   a.status = status;
   auto kern = bf ? attn_fwd_tc_kernel<true> : attn_fwd_tc_kernel<false>;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[bf ? 1 : 0]) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FSMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[bf ? 1 : 0] = true;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), FSMEM);
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((s + BT - 1) / BT), static_cast<unsigned>(heads));
   return launch_k(kern, grid, dim3(THREADS), FSMEM, stream, tmQ, tmK, tmV, a);
 }

@@ -48,11 +48,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
-#include <mutex>
-#include <set>
-#include <utility>
-
 #include "ptx.cuh"
+#include "smem_attr.h"
 #include "tg_internal.h"
 
 namespace tg {
@@ -1117,20 +1114,8 @@ __global__ void __launch_bounds__(LGROUP_UP, 1)
 // ===================================================================
 static int clampi(int64_t v, int lo, int hi) { return static_cast<int>(v < lo ? lo : (v > hi ? hi : v)); }
 
-// Raise a kernel's dynamic shared-memory limit once per device (on first use,
-// so that calls under stream capture make no such call).
-static cudaError_t allow_smem(const void* kern) {
-  static std::mutex mu;
-  static std::set<std::pair<int, const void*>> done;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lk(mu);
-  if (done.count({dev, kern})) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
-  if (e == cudaSuccess) done.insert({dev, kern});
-  return e;
-}
+// Raise a kernel's dynamic shared-memory limit (once per device and kernel).
+static cudaError_t allow_smem(const void* kern) { return raise_smem_limit(kern, SMEM_LIMIT); }
 
 static unsigned long long* trace_ptr(int which) {
 #ifdef TG_TRACE
