@@ -707,9 +707,11 @@ def fp32_peak_tflops(sms=None, mhz=None):
 
 
 def bars_of(rows):
-    """The spec bars over the 2B-class rows: the smallest tensor
-    fraction (rotated operands) over the 2,048- and 4,096-token products and
-    the smallest weight-gradient / forward ratio."""
+    """The rows against the targets they are held to: the smallest tensor
+    fraction (rotated operands) over the 2,048- and 4,096-token products of
+    the 2B-class set (target 0.70), the smallest weight-gradient / forward
+    ratio (target 0.85) and the smallest HBM fraction of the rank-16 LoRA
+    down, up and gradient products (target 0.70)."""
     fr = [r["frac_cold"] for r in rows if r.get("set") == "2B" and r["T"] >= 2048 and r["op"] != "wgrad_acc"]
     wf = [r["wgrad_over_fwd"] for r in rows if r.get("set") == "2B" and "wgrad_over_fwd" in r]
     lo = [r["frac_of_hbm"] for r in rows if r.get("set") == "LoRA" and r["op"] in ("down", "up", "grad")]
