@@ -506,15 +506,23 @@ def by_launch_class(prods, per_prod):
 def e2e_steps(prods, n_steps, stream):
     """The step through the public API with pinned host buffers: every step
     copies its inputs host->device and its outputs device->host.  Copies and
-    products form a pipeline over the step's (dtype, token count) sets, in
-    step order: a set's X and W come in, then its dY, while the set before it
-    computes; each product starts as soon as its own operands have arrived,
+    products form a pipeline over the step's (dtype, token count) sets (the
+    smallest first, the next smallest last): a set's X and W come in, then
+    its dY, while the set before it computes; each product starts as soon as its own operands have arrived,
     and each result goes out on a second copy stream as soon as the product
     that writes it is done, while later sets come in.  Steps do not overlap."""
     groups = {}
     for p in prods:
         groups.setdefault((p.layer, p.dtype, p.T), []).append(p)
-    sets = list(dict.fromkeys((p.dtype, p.T) for p in prods))
+    # the smallest set first (the first products wait for it alone) and the
+    # next smallest last (its outputs are what still crosses the link after
+    # the last product): the large sets in between, while both directions of
+    # the link are busy
+    size = {}
+    for p in prods:
+        size[(p.dtype, p.T)] = size.get((p.dtype, p.T), 0) + p.M * p.N
+    by_size = sorted(dict.fromkeys((p.dtype, p.T) for p in prods), key=lambda k: size[k])
+    sets = by_size[:1] + by_size[:1:-1] + by_size[1:2] if len(by_size) > 2 else by_size
     h2d = d2h = 0
     host = {}
     for key, ps in groups.items():
