@@ -1,7 +1,7 @@
 """Host logic of bench.py (no GPU): the kernel identity taken from a call
 record, the waves of the step graph, the DRAM traffic taken
-from a committed profile, the FP32 peak, and the replicated (N > 1) timing
-over two gloo ranks."""
+from a committed profile, the FP32 peak, the replicated (N > 1) timing
+over two gloo ranks, the headline line and the reference arm's line."""
 import os
 import sys
 
@@ -218,3 +218,24 @@ def test_headline_line_stays_compact():
         for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                   "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks"):
             assert k in line, k
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys, the arm's own cpu_baseline and an
+    e2e of the same value without host-device traffic; the oracle's sample
+    is cut short here (135M-class set) to keep the test quick."""
+    import argparse
+    import json
+    orig = bench.oracle_sample
+    monkeypatch.setattr(bench, "oracle_sample", lambda target_s, cfg=None: orig(0.2, cfg))
+    bench.reference_arm(argparse.Namespace(set="135m", steps=1, warmup=0, gpus=1))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    for k in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling", "vs_baseline",
+              "dtype", "data", "config"):
+        assert k in line, k
