@@ -1304,9 +1304,12 @@ cudaError_t lora_down_launch(const LoraArgs& a) {
                   maps, rd);
 }
 
+// Row-block CTAs per 256-column slab: at most `ctas` CTAs in all (rounded
+// down, so that the grid is one wave of resident CTAs, with no straggler
+// CTAs left for a second one)
 static int rowup_nt(int64_t T, int64_t J, int ctas) {
   const int64_t nj = (J + 255) / 256, nblk = (T + 15) / 16;
-  return clampi((ctas + nj - 1) / nj, 1, static_cast<int>(nblk));
+  return clampi(ctas / nj, 1, static_cast<int>(nblk));
 }
 
 cudaError_t lora_up_launch(const LoraArgs& a) {
