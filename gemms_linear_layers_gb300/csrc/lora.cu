@@ -18,15 +18,16 @@
 //              CTA = R consecutive rows (R <= 32: about one CTA per SM), all
 //              of K; a warp owns one 64-column chunk of each stage.
 //   col-red    P[j, r] = sum_t IN[t, j] Hm[t, r]        (dB = dY^T H, dA^T = X^T dH)
-//              the (64-column block, 128-token step) space is cut into equal
-//              contiguous ranges, one per CTA (so every CTA streams the same
-//              number of bytes); a column block cut by range boundaries gets
-//              one FP32 partial per CTA, and the last CTA to publish one adds
-//              them in CTA order.  The tiles are read transposed by
-//              ldmatrix.trans, so there is no transposition pass.
-//              Optionally fused with the row-up of the same tile (dX = dH A):
-//              the dH tile in the stage also feeds the [128 x 64] dX tile,
-//              which leaves through a TMA store.
+//              the (128-column block, 128-token step) space is cut into
+//              contiguous ranges of equal length on the fewest CTAs that keep
+//              the largest share (every CTA streams about the same number of
+//              bytes, and few CTAs share a column block); a column block cut
+//              by range boundaries gets one FP32 partial per CTA, and the last
+//              CTA to publish one adds them in CTA order.  The tiles are read
+//              transposed by ldmatrix.trans, so there is no transposition
+//              pass.  Optionally fused with the row-up of the same tile
+//              (dX = dH A): the dH tile in the stage also feeds the
+//              [128 x 128] dX tile, written straight from registers.
 //   row-up     OUT[t, j] = sum_r Hm[t, r] S2(j, r)      (Y = H B^T)
 //              writes a [T, d] tensor from the small factors, all from
 //              registers (16-byte stores).
